@@ -1,0 +1,397 @@
+"""Benchmark one decode step of the DSpark hot path: the K-step Markov drafting
+loop plus rejection-sampling verification, on the MiniMax-like drafter
+workload (vocab 200064, K = 7, markov_rank 256, fp32 logits and cache,
+batch 32 by default), synthetic seeded data.
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on
+the host cores instead (the slow, obviously-correct restatement), on a
+bounded sample of the same workload.
+
+Timing: CUDA graphs of the two library calls, replayed once per step; CUDA
+events on the launching stream bracket the Markov loop and the verifier in
+every timed step; L2 is flushed (a 512 MiB write) before every step, outside
+the timed events. For N > 1 (torchrun) every rank runs an independent replica
+(no collectives on the data path); the barrier and the max over ranks use the
+process group only for timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs per decode step (K-step Markov loop + verify) and % of HBM roofline, 1×GB300"
+PAGES_ROOFLINE_GBS = 8000.0  # the "8 TB/s" the workload's roofline is quoted against
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+def _dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(w):
+    """Bytes the path must move at least once (the roofline's numerator):
+    Markov loop per step: markov_w2 once, the base row and the cache row of
+    every request, the Markov embeddings; verification: every target row and
+    every draft-cache row once."""
+    s_base = 2 if w.base_bf16 else 4
+    s_cache = 2 if w.cache_bf16 else 4
+    s_t = 2 if w.target_bf16 else 4
+    per_markov_launch = 2 * w.V * w.R + w.B * w.V * (s_base + s_cache) + 2 * w.B * w.R
+    verify = w.B * (w.K + 1) * w.V * s_t + w.B * w.K * w.V * s_cache
+    return per_markov_launch, verify
+
+
+def _subset(w, idx):
+    import copy
+    idx = np.asarray(idx)
+    v = copy.copy(w)
+    v.B = len(idx)
+    v.base = np.ascontiguousarray(w.base[idx])
+    v.anchor = np.ascontiguousarray(w.anchor[idx])
+    v.req_state_idx = np.ascontiguousarray(w.req_state_idx[idx])
+    v.positions = np.ascontiguousarray(w.positions[idx])
+    v.target = np.ascontiguousarray(w.target[idx])
+    return v
+
+
+def time_oracle(w, n_req: int):
+    """Seconds of the CPU oracle for n_req requests of w (loop + verify)."""
+    import oracle
+    oracle.build()
+    sub = _subset(w, list(range(n_req)))
+    t0 = time.perf_counter()
+    tok, cache, _ = oracle.markov_sample(sub.base, sub.w1, sub.w2, sub.anchor,
+                                         sub.req_state_idx, sub.positions, sub.temperature,
+                                         sub.seeds, cache_rows=w.C, cache_bf16=w.cache_bf16,
+                                         row_map=w.row_map)
+    t1 = time.perf_counter()
+    oracle.rejection_sample(tok, cache, sub.target, sub.req_state_idx, sub.positions,
+                            sub.temperature, sub.top_p, sub.seeds, row_map=w.row_map)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def build_workload(args):
+    from verify_dspark_markov_step_gb300 import workloads as wl
+    return wl.make(args.config, batch=args.batch)
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle on the host cores."""
+    if rank != 0:
+        return
+    w = build_workload(args)
+    n_req = max(1, min(w.B, args.cpu_requests))
+    loops, vers = [], []
+    for _ in range(max(1, args.steps)):
+        a, b = time_oracle(w, n_req)
+        loops.append(a)
+        vers.append(b)
+    loop_us = statistics.median(loops) / n_req * w.B * 1e6
+    ver_us = statistics.median(vers) / n_req * w.B * 1e6
+    val = loop_us + ver_us
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 1), "unit": "us",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(val / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w, args),
+        "loop_us": round(loop_us, 1), "verify_us": round(ver_us, 1),
+        "cpu_baseline": {"value": round(val, 1), "unit": "us", "cores": 1, "kind": "oracle",
+                         "sample": f"{n_req} of {w.B} requests per step (whole K-step loop "
+                                   f"+ verification), scaled by {w.B}/{n_req}"},
+        "e2e": {"value": round(val, 1), "unit": "us", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w, args):
+    return {"workload": f"{w.name}-like drafter: batch {w.B}, K={w.K}, vocab {w.V}, "
+                        f"markov_rank {w.R}, {'bf16' if w.base_bf16 else 'fp32'} logits, "
+                        f"{'bf16' if w.cache_bf16 else 'fp32'} draft cache",
+            "batch": w.B, "K": w.K, "vocab": w.V, "markov_rank": w.R,
+            "l2": "flushed (512 MiB write) before every timed step",
+            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from verify_dspark_markov_step_gb300 import build
+    from verify_dspark_markov_step_gb300.step import DecodeStep, to_device
+    from verify_dspark_markov_step_gb300 import _lib
+
+    torch.cuda.set_device(local)
+    build.build()
+    w = build_workload(args)
+    st = DecodeStep(w)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    # capture the Markov loop and the verifier as two graphs on one stream
+    with torch.cuda.stream(stream):
+        st.run(stream=stream)
+    stream.synchronize()
+    g_markov = torch.cuda.CUDAGraph()
+    g_verify = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_markov, stream=stream):
+        st.markov(stream=stream)
+    with torch.cuda.graph(g_verify, stream=stream):
+        st.verify(stream=stream)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def one_step(ev):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            ev[0].record(stream)
+            g_markov.replay()
+            ev[1].record(stream)
+            g_verify.replay()
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        one_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one_step(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    loop_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    ver_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = [a + b for a, b in zip(loop_ms, ver_ms)]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = st.status_code()
+    nacc = st.num_accepted.float().mean().item()
+    tokens = (st.num_accepted + 1).sum().item()
+
+    # end to end through the public API with host buffers
+    base_h = torch.from_numpy(np.ascontiguousarray(w.base)).pin_memory()
+    tgt_h = torch.from_numpy(np.ascontiguousarray(w.target)).pin_memory()
+    small_h = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+               for a in (w.anchor, w.req_state_idx, w.positions)]
+    small_d = [st.anchor, st.rsi, st.pos]
+    out_h = torch.empty((w.B, w.K + 1), dtype=torch.int32).pin_memory()
+    nacc_h = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h2d = base_h.numel() * base_h.element_size() + tgt_h.numel() * tgt_h.element_size() + \
+        sum(t.numel() * t.element_size() for t in small_h)
+    d2h = out_h.numel() * 4 + nacc_h.numel() * 4
+
+    def e2e_step(ev):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            ev[0].record(stream)
+            st.base.copy_(base_h, non_blocking=True)
+            st.target.copy_(tgt_h, non_blocking=True)
+            for h, d in zip(small_h, small_d):
+                d.copy_(h, non_blocking=True)
+            st.run(stream=stream)
+            out_h.copy_(st.out, non_blocking=True)
+            nacc_h.copy_(st.num_accepted, non_blocking=True)
+            ev[1].record(stream)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(3):
+        e2e_step([torch.cuda.Event(enable_timing=True) for _ in range(2)])
+    torch.cuda.synchronize()
+    eev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        e2e_step(eev[i])
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in eev)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peak, peak_kind = _peaks()
+    per_launch, ver_bytes = algorithmic_bytes(w)
+    loop_us = statistics.mean(loop_ms) * 1e3
+    ver_us = statistics.mean(ver_ms) * 1e3
+    launch_us = loop_us / w.K
+    achieved = per_launch / (launch_us * 1e-6) / 1e9
+    traffic = _traffic_from_profile(args)
+    line = {
+        "metric": METRIC, "value": round(ms * 1e3, 2), "unit": "us", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": _config(w, args),
+        "loop_us": round(loop_us, 2), "verify_us": round(ver_us, 2),
+        "loop_us_p10_p90": [round(float(np.percentile(loop_ms, 10)) * 1e3, 2),
+                            round(float(np.percentile(loop_ms, 90)) * 1e3, 2)],
+        "verify_us_p10_p90": [round(float(np.percentile(ver_ms, 10)) * 1e3, 2),
+                              round(float(np.percentile(ver_ms, 90)) * 1e3, 2)],
+        "tokens_per_s": round(tokens * world / (ms * 1e-3), 1),
+        "mean_accepted": round(nacc, 3),
+        "hbm_frac_8tbs": {
+            "loop": round(per_launch * w.K / (loop_us * 1e-6) / 1e9 / PAGES_ROOFLINE_GBS, 3),
+            "verify": round(ver_bytes / (ver_us * 1e-6) / 1e9 / PAGES_ROOFLINE_GBS, 3)},
+        "roofline": {"bound": "hbm", "kernel": "markov_step (one launch = one Markov step)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "peak_kind": peak_kind,
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": per_launch,
+                     "verify_achieved": round(ver_bytes / (ver_us * 1e-6) / 1e9, 1),
+                     "verify_frac": round(ver_bytes / (ver_us * 1e-6) / 1e9 / peak, 3)},
+        "e2e": {"value": round(e2e_ms * 1e3, 1), "unit": "us", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps * (w.K + 2),
+        "clocks": clk, "status": status, "wall_s_timed_region": round(wall, 4),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        n_req = max(1, min(w.B, args.cpu_requests))
+        a, b = time_oracle(w, n_req)
+        v = (a + b) / n_req * w.B * 1e6
+        line["cpu_baseline"] = {"value": round(v, 1), "unit": "us", "cores": 1, "kind": "oracle",
+                                "sample": f"{n_req} of {w.B} requests (whole K-step loop + "
+                                          f"verification), scaled by {w.B}/{n_req}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _traffic_from_profile(args):
+    """DRAM bytes per Markov-step launch from the committed ncu summary, if it
+    was taken on the current kernel; else None."""
+    p = os.path.join(ROOT, "profiles", "markov_step_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("batch") == args.batch and d.get("config") == args.config:
+            return d.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="minimax")
+    ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--cpu-requests", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = _dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

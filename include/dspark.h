@@ -1,0 +1,211 @@
+/*
+ * dspark.h -- C ABI of the DSpark Markov drafting step and rejection-sampling
+ * verifier for one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow these pages (cited by title and section):
+ *   - "DSparkSpeculator" API page (vllm/v1/worker/gpu/spec_decode/dspark/
+ *     speculator.py): _sample_markov_chain (the K sequential steps: Markov
+ *     embedding of the previous token, Markov bias, bias add, sampling) and
+ *     _sample_logits (gumbel_sample with temperature, per-request seeds, the
+ *     position before the sampled token, the draft-logits cache and its row
+ *     mapping).
+ *   - vLLM PR #65007 "vocab-parallel DSpark Markov sampling", Part 1 (per-step
+ *     list: Gumbel-noised argmax over 1024-column blocks, the first NaN block
+ *     wins, otherwise the first maximum) and Part 2 (temperature, exact top-p
+ *     by logit then token id with 64-bit fixed-point masses, and the
+ *     rejection sampler).
+ *   - vLLM PR #63554 "batch-sharded draft logits cache" (cache rows addressed
+ *     through a row mapping; greedy rows never read the cache).
+ *
+ * Conventions shared by every entry point
+ *   Memory.  Every pointer argument is DEVICE memory owned by the caller,
+ *            except `status`, which may also be pinned (mapped) host memory.
+ *            The library allocates nothing and keeps no state between calls;
+ *            scratch space is the caller's `workspace`.
+ *   Layout.  Row-major and contiguous. fp32 tensors are IEEE binary32; bf16
+ *            tensors are passed as uint16 bit patterns.
+ *   Streams. All work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *            legacy default stream). Calls return before the work finishes.
+ *            Two calls in flight at once must not share a workspace.
+ *   Errors.  Argument errors (null pointers, sizes, dtypes, alignment, a
+ *            workspace that is too small) are detected on the host before
+ *            anything is launched: a negative dspark_status is returned and
+ *            nothing runs. A failed launch returns DSPARK_ERR_CUDA. Errors
+ *            found on the device (a token, slot or cache row out of range; a
+ *            bounded wait that ran out) never fault: the kernel stores the
+ *            first error code into *status (if `status` is not NULL, with an
+ *            atomic compare-and-swap from 0) and the affected request is
+ *            treated as padding. The caller reads *status after the stream
+ *            has been synchronised; it should be 0 before the call.
+ *   Noise.   Random draws use the Philox4x32-10 counter-based generator
+ *            (Salmon, Moraes, Dror, Shaw, SC'11): key = (seed low word, seed
+ *            high word), counter = (column / 4, position low word, position
+ *            high word, stream), output word = column mod 4; u = ((w >> 9) +
+ *            1/2) * 2^-23; Gumbel g = -log(-log u). Streams: 2^30 for draft
+ *            noise (the pages' draft-noise salt), 0 for the verifier's
+ *            categorical draws, 2^29 for its accept uniforms.
+ */
+#ifndef DSPARK_H_
+#define DSPARK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* dspark_stream_t;
+
+typedef enum {
+  DSPARK_F32 = 0,  /* IEEE binary32                     */
+  DSPARK_BF16 = 1  /* bfloat16, passed as uint16 bits    */
+} dspark_dtype;
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID_ARG = -1, /* null pointer, bad size or dtype          */
+  DSPARK_ERR_UNSUPPORTED = -2, /* valid but not implemented (e.g. R % 64)  */
+  DSPARK_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed     */
+  DSPARK_ERR_TIMEOUT = -4,     /* device: a bounded wait ran out           */
+  DSPARK_ERR_BOUNDS = -5,      /* device: token, slot or row out of range  */
+  DSPARK_ERR_WORKSPACE = -6,   /* workspace null or smaller than required  */
+  DSPARK_ERR_ALIGNMENT = -7    /* a pointer is not 16-byte aligned         */
+} dspark_status;
+
+/* Limits checked on the host. */
+#define DSPARK_MAX_VOCAB (1 << 23)  /* keeps V * 2^40 < 2^63 (fixed point) */
+#define DSPARK_MAX_BATCH 256
+#define DSPARK_MAX_STEPS 16
+
+/* ------------------------------------------------------------------------
+ * dspark_markov_sample -- the drafter's K-step Markov sampling loop.
+ * (DSparkSpeculator page, _sample_markov_chain / _sample_logits; PR #65007
+ *  Part 1, per-step list.)
+ *
+ * For every request b with slot s = req_state_idx[b] >= 0, starting from
+ * prev = anchor_tokens[b], for i = 0..K-1:
+ *   e      = markov_w1[prev, :]                        (Markov embedding)
+ *   bias_v = sum_r markov_w2[v, r] * e[r]              (fp32 accumulation)
+ *   z_v    = base_logits[b, i, v] + bias_v             (fp32)
+ *   T = temperature[s] > 0:  x_v = z_v / T (IEEE), y_v = x_v + g_v with g the
+ *       Gumbel noise of (seeds[s], positions[b] + i - 1, v, draft stream)
+ *   otherwise (greedy):      x_v = y_v = z_v
+ *   out_tokens[b, i] = lowest-index NaN of y if any, else the lowest index of
+ *       max(y) (the "first NaN block, else first maximum" rule over
+ *       1024-column blocks, which does not depend on the blocking);
+ *   cache[row, i, :] = x (fp32, or bf16 rounded to nearest even), row =
+ *       cache_row_map ? cache_row_map[s] : s;
+ *   prev = out_tokens[b, i].
+ * Requests with req_state_idx[b] < 0 are padding: out_tokens[b, :] = -1 and
+ * nothing else is read or written for them.
+ *
+ * Arguments
+ *   base_logits   [B, K, V] base_dtype (fp32 or bf16)
+ *   markov_w1     [V, R] bf16    Markov embedding table (indexed by token)
+ *   markov_w2     [V, R] bf16    Markov bias projection
+ *   anchor_tokens [B] int32      first `prev` of each request, in [0, V)
+ *   req_state_idx [B] int32      slot in [0, S), or < 0 for padding
+ *   positions     [B] int64      position P0 of each request's first draft token
+ *   temperature   [S] fp32       per slot; <= 0 (or NaN) = greedy
+ *   seeds         [S] uint64     per slot
+ *   cache         [C, K, V] cache_dtype, or NULL for no cache write
+ *   cache_row_map [S] int32 in [0, C), or NULL for row = slot
+ *   out_tokens    [B, K] int32   (written)
+ *   B in [0, 256], K in [1, 16], V in [1, 2^23), R a multiple of 64 up to
+ *   512, S >= 1, C >= 1 if cache != NULL.
+ *   workspace     device scratch of at least dspark_markov_workspace_bytes()
+ *                 bytes, 256-byte aligned. Its contents need no
+ *                 initialisation; the call leaves it ready for the next call.
+ *   status        see the conventions above; may be NULL.
+ * Alignment: base_logits, markov_w2 and cache must be 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t dspark_markov_workspace_bytes(int B, int K, int V, int R);
+
+dspark_status dspark_markov_sample(
+    const void* base_logits, dspark_dtype base_dtype,
+    const uint16_t* markov_w1, const uint16_t* markov_w2,
+    const int32_t* anchor_tokens, const int32_t* req_state_idx,
+    const int64_t* positions, const float* temperature, const uint64_t* seeds,
+    void* cache, dspark_dtype cache_dtype, const int32_t* cache_row_map,
+    int32_t* out_tokens, int B, int K, int V, int R, int S, int C,
+    void* workspace, size_t workspace_bytes, int32_t* status,
+    dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dspark_rejection_sample -- probabilistic rejection-sampling verification.
+ * (PR #65007 Part 2: temperature, exact top-p, the rejection sampler;
+ *  PR #63554: greedy rows compare with the target argmax.)
+ *
+ * For every request b with slot s >= 0, T = temperature[s]:
+ *   target row k (k = 0..K): xt = target[b,k,:] / T, NaN read as -inf;
+ *     m = max xt; e_v = exp(xt_v - m) (fp32); f_v = rint(e_v * 2^40) (uint64);
+ *     if top_p[s] < 1 keep the shortest prefix of the (xt desc, id asc) order
+ *     with (sum of f over the prefix) * 2^32 >= rint(top_p * 2^32) * (sum of
+ *     all f), else keep all; p_v = e_v / (fp32(sum of kept f) * 2^-40) on the
+ *     kept set, 0 elsewhere. A row with no value above -inf is one-hot at 0.
+ *   draft row k (k < K): q = the same normalisation of cache[row, k, :] with
+ *     no temperature and no top-p (the cache holds scaled logits); a row with
+ *     no value above -inf gives q = 0.
+ *   for k = 0..K-1, d = draft_tokens[b, k]:
+ *     d = -1: emit a draw from p_k and stop;
+ *     u = uniform(seeds[s], positions[b] + k - 1, column 0, accept stream);
+ *     accept iff fp32(u * q_k(d)) < p_k(d)  (probability min(1, p/q));
+ *     on reject emit the Gumbel-max draw (target stream, same position) from
+ *     r = max(0, p_k - q_k) (from p_k if r is all zero) and stop.
+ *   all K accepted: emit a draw from p_K (position positions[b] + K - 1).
+ *   A "draw from w" is argmax_v fp32(log w_v) + g_v, same winner rule as
+ *   the drafter.
+ *   Greedy slots (T <= 0 or NaN): accept d iff d equals the winner of the
+ *   raw target row k; emit that winner on mismatch or d = -1; the bonus is
+ *   the winner of row K. The cache is not read.
+ * Outputs: out_tokens[b, :] = the accepted drafts, then the one emitted
+ * token, then -1; num_accepted[b] = number of accepted drafts. Padding
+ * requests (slot < 0) get all -1 and 0.
+ *
+ * Arguments
+ *   draft_tokens  [B, K] int32 in [0, V) or -1
+ *   draft_cache   [C, K, V] cache_dtype (may be NULL if every slot is greedy)
+ *   cache_row_map [S] int32 or NULL (row = slot)
+ *   target_logits [B, K+1, V] target_dtype
+ *   req_state_idx [B], positions [B], temperature [S], top_p [S] fp32,
+ *   seeds [S] as for dspark_markov_sample
+ *   out_tokens    [B, K+1] int32, num_accepted [B] int32 (written)
+ *   workspace     at least dspark_verify_workspace_bytes() bytes
+ * Alignment: draft_cache and target_logits must be 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t dspark_verify_workspace_bytes(int B, int K, int V);
+
+dspark_status dspark_rejection_sample(
+    const int32_t* draft_tokens, const void* draft_cache,
+    dspark_dtype cache_dtype, const int32_t* cache_row_map,
+    const void* target_logits, dspark_dtype target_dtype,
+    const int32_t* req_state_idx, const int64_t* positions,
+    const float* temperature, const float* top_p, const uint64_t* seeds,
+    int32_t* out_tokens, int32_t* num_accepted, int B, int K, int V, int S,
+    int C, void* workspace, size_t workspace_bytes, int32_t* status,
+    dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dspark_noise -- the device noise generator on its own, for checking it
+ * against other implementations: for i < n, word[i] = Philox output of
+ * (seed[i], pos[i], col[i], stream[i]) as described above, u[i] its uniform
+ * and g[i] its Gumbel variate. Any of word, u, g may be NULL. Device arrays.
+ * ------------------------------------------------------------------------ */
+dspark_status dspark_noise(const uint64_t* seed, const int64_t* pos,
+                           const uint32_t* col, const uint32_t* stream,
+                           uint32_t* word, float* u, float* g, int64_t n,
+                           dspark_stream_t stream_handle);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* dspark_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dspark_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H_ */

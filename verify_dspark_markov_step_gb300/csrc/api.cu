@@ -1,0 +1,225 @@
+// api.cu -- the C ABI declared in include/dspark.h: host-side argument
+// checks, workspace carving and kernel launches. No allocation, no host
+// synchronisation, no state kept between calls.
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dspark.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(int d) { return d == DSPARK_F32 || d == DSPARK_BF16; }
+
+int num_sms_of_current_device(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  return 0;
+}
+
+struct MarkovWs {
+  size_t counter, partials, total;
+  MarkovWs(int B, int V) {
+    counter = 0;
+    partials = align_up(counter + sizeof(unsigned int));
+    total = align_up(partials + static_cast<size_t>(B) *
+                                    dspark::markov_simt_max_grid(V) * sizeof(unsigned long long));
+  }
+};
+
+struct VerifyWs {
+  size_t counters, tstats, dstats, keys, anypos, total;
+  VerifyWs(int B, int K, int V) {
+    const int mc = dspark::verify_max_chunks(V);
+    counters = 0;
+    tstats = align_up(counters + static_cast<size_t>(B) * sizeof(unsigned int));
+    dstats = align_up(tstats + dspark::verify_tstats_bytes(B, K));
+    keys = align_up(dstats + dspark::verify_dstats_bytes(B, K));
+    anypos = align_up(keys + static_cast<size_t>(B) * mc * sizeof(unsigned long long));
+    total = align_up(anypos + static_cast<size_t>(B) * mc * sizeof(unsigned int));
+  }
+};
+
+bool sizes_ok(int B, int K, int V, int S) {
+  return B >= 0 && B <= DSPARK_MAX_BATCH && K >= 1 && K <= DSPARK_MAX_STEPS && V >= 1 &&
+         V < DSPARK_MAX_VOCAB && S >= 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dspark_markov_workspace_bytes(int B, int K, int V, int R) {
+  (void)K;
+  (void)R;
+  if (B < 0 || V < 1) return 0;
+  return MarkovWs(B, V).total;
+}
+
+dspark_status dspark_markov_sample(
+    const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
+    const uint16_t* markov_w2, const int32_t* anchor_tokens, const int32_t* req_state_idx,
+    const int64_t* positions, const float* temperature, const uint64_t* seeds, void* cache,
+    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens, int B, int K,
+    int V, int R, int S, int C, void* workspace, size_t workspace_bytes, int32_t* status,
+    dspark_stream_t stream) {
+  if (!sizes_ok(B, K, V, S) || R < 1) return DSPARK_ERR_INVALID_ARG;
+  if (!valid_dtype(base_dtype) || !valid_dtype(cache_dtype)) return DSPARK_ERR_INVALID_ARG;
+  if (R % 64 != 0 || R > 512) return DSPARK_ERR_UNSUPPORTED;
+  if (dspark::markov_simt_smem_bytes(B, R) > 227u * 1024u) return DSPARK_ERR_UNSUPPORTED;
+  if (B == 0) return DSPARK_OK;
+  if (!base_logits || !markov_w1 || !markov_w2 || !anchor_tokens || !req_state_idx ||
+      !positions || !temperature || !seeds || !out_tokens)
+    return DSPARK_ERR_INVALID_ARG;
+  if (cache && C < 1) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(base_logits) || !aligned16(markov_w1) || !aligned16(markov_w2) ||
+      (cache && !aligned16(cache)))
+    return DSPARK_ERR_ALIGNMENT;
+  const MarkovWs ws(B, V);
+  if (!workspace || workspace_bytes < ws.total || !aligned16(workspace))
+    return DSPARK_ERR_WORKSPACE;
+  int sms = 0;
+  if (num_sms_of_current_device(&sms) != 0) return DSPARK_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  dspark::MarkovStepParams p;
+  p.base = base_logits;
+  p.base_bf16 = base_dtype == DSPARK_BF16;
+  p.w1 = markov_w1;
+  p.w2 = markov_w2;
+  p.anchor = anchor_tokens;
+  p.rsi = req_state_idx;
+  p.pos = positions;
+  p.temperature = temperature;
+  p.seeds = seeds;
+  p.cache = cache;
+  p.cache_bf16 = cache_dtype == DSPARK_BF16;
+  p.row_map = cache_row_map;
+  p.out_tokens = out_tokens;
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.R = R;
+  p.S = S;
+  p.C = C;
+  p.partials = reinterpret_cast<unsigned long long*>(w + ws.partials);
+  p.counter = reinterpret_cast<unsigned int*>(w + ws.counter);
+  p.status = status;
+  if (cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), st) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  const int grid = dspark::markov_simt_grid(B, V, R, sms);
+  for (int i = 0; i < K; ++i) {
+    p.step = i;
+    if (dspark::launch_markov_step_simt(p, grid, st) != cudaSuccess) return DSPARK_ERR_CUDA;
+  }
+  return DSPARK_OK;
+}
+
+size_t dspark_verify_workspace_bytes(int B, int K, int V) {
+  if (B < 0 || K < 1 || V < 1) return 0;
+  return VerifyWs(B, K, V).total;
+}
+
+dspark_status dspark_rejection_sample(
+    const int32_t* draft_tokens, const void* draft_cache, dspark_dtype cache_dtype,
+    const int32_t* cache_row_map, const void* target_logits, dspark_dtype target_dtype,
+    const int32_t* req_state_idx, const int64_t* positions, const float* temperature,
+    const float* top_p, const uint64_t* seeds, int32_t* out_tokens, int32_t* num_accepted,
+    int B, int K, int V, int S, int C, void* workspace, size_t workspace_bytes,
+    int32_t* status, dspark_stream_t stream) {
+  if (!sizes_ok(B, K, V, S)) return DSPARK_ERR_INVALID_ARG;
+  if (!valid_dtype(cache_dtype) || !valid_dtype(target_dtype)) return DSPARK_ERR_INVALID_ARG;
+  if (B == 0) return DSPARK_OK;
+  if (!draft_tokens || !target_logits || !req_state_idx || !positions || !temperature ||
+      !top_p || !seeds || !out_tokens || !num_accepted)
+    return DSPARK_ERR_INVALID_ARG;
+  if (draft_cache && C < 1) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(target_logits) || (draft_cache && !aligned16(draft_cache)))
+    return DSPARK_ERR_ALIGNMENT;
+  const VerifyWs ws(B, K, V);
+  if (!workspace || workspace_bytes < ws.total || !aligned16(workspace))
+    return DSPARK_ERR_WORKSPACE;
+  int sms = 0;
+  if (num_sms_of_current_device(&sms) != 0) return DSPARK_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  dspark::VerifyParams p;
+  p.draft = draft_tokens;
+  p.cache = draft_cache;
+  p.cache_bf16 = cache_dtype == DSPARK_BF16;
+  p.row_map = cache_row_map;
+  p.target = target_logits;
+  p.target_bf16 = target_dtype == DSPARK_BF16;
+  p.rsi = req_state_idx;
+  p.pos = positions;
+  p.temperature = temperature;
+  p.top_p = top_p;
+  p.seeds = seeds;
+  p.out_tokens = out_tokens;
+  p.num_accepted = num_accepted;
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.S = S;
+  p.C = C;
+  p.counters = reinterpret_cast<unsigned int*>(w + ws.counters);
+  p.tstats = w + ws.tstats;
+  p.dstats = w + ws.dstats;
+  p.keys = reinterpret_cast<unsigned long long*>(w + ws.keys);
+  p.anypos = reinterpret_cast<unsigned int*>(w + ws.anypos);
+  p.nchunk = dspark::verify_chunks(B, V, sms);
+  p.status = status;
+  if (cudaMemsetAsync(p.counters, 0, static_cast<size_t>(B) * sizeof(unsigned int), st) !=
+      cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (dspark::launch_verify(p, st) != cudaSuccess) return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_noise(const uint64_t* seed, const int64_t* pos, const uint32_t* col,
+                           const uint32_t* stream, uint32_t* word, float* u, float* g,
+                           int64_t n, dspark_stream_t stream_handle) {
+  if (n < 0) return DSPARK_ERR_INVALID_ARG;
+  if (n == 0) return DSPARK_OK;
+  if (!seed || !pos || !col || !stream) return DSPARK_ERR_INVALID_ARG;
+  if (dspark::launch_noise(seed, pos, col, stream, word, u, g, n,
+                           reinterpret_cast<cudaStream_t>(stream_handle)) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+const char* dspark_status_string(int status) {
+  switch (status) {
+    case DSPARK_OK:
+      return "ok";
+    case DSPARK_ERR_INVALID_ARG:
+      return "invalid argument";
+    case DSPARK_ERR_UNSUPPORTED:
+      return "unsupported configuration";
+    case DSPARK_ERR_CUDA:
+      return "CUDA error";
+    case DSPARK_ERR_TIMEOUT:
+      return "device wait timed out";
+    case DSPARK_ERR_BOUNDS:
+      return "token, slot or cache row out of range";
+    case DSPARK_ERR_WORKSPACE:
+      return "workspace missing or too small";
+    case DSPARK_ERR_ALIGNMENT:
+      return "pointer not 16-byte aligned";
+    default:
+      return "unknown status";
+  }
+}
+
+int dspark_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,277 @@
+// common.cuh -- device helpers shared by the Markov-step and verify kernels:
+// the Philox4x32-10 noise generator, the winner key, fixed-point masses,
+// mbarrier / bulk-copy wrappers with bounded waits, and the status word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+// Noise streams (the header's "draft", "verifier categorical", "accept").
+constexpr uint32_t kStreamDraft = 1u << 30;
+constexpr uint32_t kStreamTarget = 0u;
+constexpr uint32_t kStreamAccept = 1u << 29;
+
+// One unit of exp-mass in the 64-bit fixed point of the top-p select.
+constexpr int kFixShift = 40;
+
+// Upper bound of any spin on an mbarrier or flag, in nanoseconds of
+// %globaltimer (about 2 s, like the pages' exchange timeout).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies with the
+// round multipliers, a half swap and a key xor; the key advances by the two
+// Weyl increments between rounds.
+// ---------------------------------------------------------------------------
+struct U4 {
+  uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ U4 philox4x32_10(U4 c, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t kMul0 = 0xD2511F53u, kMul1 = 0xCD9E8D57u;
+  constexpr uint32_t kWeyl0 = 0x9E3779B9u, kWeyl1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = kMul0 * c.x, hi0 = __umulhi(kMul0, c.x);
+    const uint32_t lo1 = kMul1 * c.z, hi1 = __umulhi(kMul1, c.z);
+    U4 n;
+    n.x = hi1 ^ c.y ^ k0;
+    n.y = lo1;
+    n.z = hi0 ^ c.w ^ k1;
+    n.w = lo0;
+    c = n;
+    k0 += kWeyl0;
+    k1 += kWeyl1;
+  }
+  return c;
+}
+
+// All four words of the counter block holding `col` (cols 4j..4j+3).
+__device__ __forceinline__ U4 noise_block(uint64_t seed, int64_t pos,
+                                          uint32_t col, uint32_t stream) {
+  const uint64_t upos = static_cast<uint64_t>(pos);
+  U4 c{col >> 2, static_cast<uint32_t>(upos), static_cast<uint32_t>(upos >> 32),
+       stream};
+  return philox4x32_10(c, static_cast<uint32_t>(seed),
+                       static_cast<uint32_t>(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t pick_word(const U4& r, uint32_t j) {
+  return j == 0 ? r.x : (j == 1 ? r.y : (j == 2 ? r.z : r.w));
+}
+
+// u = ((w >> 9) + 1/2) * 2^-23: every step is exact in fp32.
+__device__ __forceinline__ float uniform_of(uint32_t w) {
+  return __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 0x1p-23f);
+}
+
+// Standard Gumbel variate; accurate logf (never __logf / fast math).
+__device__ __forceinline__ float gumbel_of(uint32_t w) {
+  return -logf(-logf(uniform_of(w)));
+}
+
+// ---------------------------------------------------------------------------
+// Winner key. Larger key = better: NaN above everything, then larger values,
+// then lower column index. -0 and +0 map to the same value bits.
+// 0 is below every real key ("no candidate").
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ordered_bits(float y) {
+  if (y != y) return 0xFFFFFFFFu;
+  uint32_t b = __float_as_uint(y);
+  if (b == 0x80000000u) b = 0u;  // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned long long winner_key(float y, uint32_t col) {
+  return (static_cast<unsigned long long>(ordered_bits(y)) << 32) |
+         static_cast<unsigned long long>(0xFFFFFFFFu - col);
+}
+
+__device__ __forceinline__ int32_t key_index(unsigned long long key) {
+  return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a,
+                                                     unsigned long long b) {
+  return a > b ? a : b;
+}
+
+__device__ __forceinline__ unsigned long long warp_max64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = umax64(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_maxf(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Element access.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__device__ __forceinline__ float load_logit(const void* p, bool bf16, int64_t i) {
+  return bf16 ? bf16_bits_to_float(__ldg(static_cast<const unsigned short*>(p) + i))
+              : __ldg(static_cast<const float*>(p) + i);
+}
+
+// fp32 -> bf16, round to nearest even (NaN stays NaN).
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// rint(e * 2^40) as uint64 for a finite e >= 0, round half to even, in
+// integer arithmetic (GB300's fp64 rate is far too low for a per-element
+// conversion). e = mant * 2^(E - 23), so e * 2^40 = mant * 2^(E + 17).
+__device__ __forceinline__ unsigned long long to_fixed(float e) {
+  const uint32_t bits = __float_as_uint(e);
+  const int ex = static_cast<int>((bits >> 23) & 0xFFu);
+  if (ex == 0) return 0ull;  // zero or subnormal (< 2^-126): far below 2^-41
+  const uint32_t mant = (bits & 0x7FFFFFu) | 0x800000u;
+  const int sh = ex - 127 + 17;
+  if (sh >= 0) return static_cast<unsigned long long>(mant) << sh;
+  const int rs = -sh;
+  if (rs > 24) return 0ull;  // mant * 2^-rs < 1/2
+  const uint32_t q = mant >> rs;
+  const uint32_t rem = mant & ((1u << rs) - 1u);
+  const uint32_t half = 1u << (rs - 1);
+  const uint32_t up = (rem > half) || (rem == half && (q & 1u));
+  return static_cast<unsigned long long>(q + up);
+}
+
+// ---------------------------------------------------------------------------
+// Status word: the first error wins.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier and bulk async copies (sm_90+ PTX), all waits bounded.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with parity `phase` to complete. Returns false (and
+// records DSPARK_ERR_TIMEOUT) if it has not completed within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase,
+                                          int32_t* status) {
+  if (mbar_try_wait(bar, phase)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, phase)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      report(status, DSPARK_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes and
+// both addresses multiples of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Streaming 16-byte load: no L1 allocation, L2 eviction priority from
+// `policy` (data read exactly once).
+__device__ __forceinline__ float4 ld_stream_f4(const float* p, uint64_t policy) {
+  float4 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(p), "l"(policy));
+  return v;
+}
+
+// Streaming 16-byte store (evict-first in L1 and L2).
+__device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+}  // namespace dspark

@@ -1,0 +1,77 @@
+// kernels.h -- launch interface between the C-ABI layer (api.cu) and the
+// kernels (markov_step.cu, markov_tc.cu, verify.cu). Internal to the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dspark {
+
+// One Markov step: parameters shared by both Markov-step variants.
+struct MarkovStepParams {
+  const void* base;
+  int base_bf16;
+  const uint16_t* w1;
+  const uint16_t* w2;
+  const int32_t* anchor;
+  const int32_t* rsi;
+  const int64_t* pos;
+  const float* temperature;
+  const uint64_t* seeds;
+  void* cache;
+  int cache_bf16;
+  const int32_t* row_map;
+  int32_t* out_tokens;
+  int B, K, V, R, S, C;
+  int step;
+  unsigned long long* partials;  // [B][grid] winner keys of each CTA
+  unsigned int* counter;         // CTAs finished in this step (self-resetting)
+  int32_t* status;
+};
+
+// CUDA-core variant (markov_step.cu).
+size_t markov_simt_smem_bytes(int B, int R);
+int markov_simt_grid(int B, int V, int R, int num_sms);
+int markov_simt_max_grid(int V);
+cudaError_t launch_markov_step_simt(const MarkovStepParams& p, int grid,
+                                    cudaStream_t stream);
+
+// Verification (verify.cu).
+struct VerifyParams {
+  const int32_t* draft;
+  const void* cache;
+  int cache_bf16;
+  const int32_t* row_map;
+  const void* target;
+  int target_bf16;
+  const int32_t* rsi;
+  const int64_t* pos;
+  const float* temperature;
+  const float* top_p;
+  const uint64_t* seeds;
+  int32_t* out_tokens;
+  int32_t* num_accepted;
+  int B, K, V, S, C;
+  void* tstats;                  // [B][K+1] target-row statistics
+  void* dstats;                  // [B][K] draft-row statistics
+  unsigned long long* keys;      // [B][nchunk] chunk winner keys
+  unsigned int* anypos;          // [B][nchunk] residual had a positive entry
+  unsigned int* counters;        // [B] finished chunks (self-resetting)
+  int nchunk;
+  int32_t* status;
+};
+
+size_t verify_tstats_bytes(int B, int K);
+size_t verify_dstats_bytes(int B, int K);
+int verify_max_chunks(int V);
+int verify_chunks(int B, int V, int num_sms);
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
+
+// Noise generator on its own (api.cu / verify.cu).
+cudaError_t launch_noise(const uint64_t* seed, const int64_t* pos,
+                         const uint32_t* col, const uint32_t* stream_word,
+                         uint32_t* word, float* u, float* g, int64_t n,
+                         cudaStream_t stream);
+
+}  // namespace dspark
