@@ -75,7 +75,7 @@ typedef enum {
 } dspark_status;
 
 /* Limits checked on the host. */
-#define DSPARK_MAX_VOCAB (1 << 23)  /* keeps V * 2^40 < 2^63 (fixed point) */
+#define DSPARK_MAX_VOCAB (1 << 22)  /* token ids fit 22 bits; V * 2^40 < 2^63 */
 #define DSPARK_MAX_BATCH 256
 #define DSPARK_MAX_STEPS 16
 
@@ -113,7 +113,7 @@ typedef enum {
  *   cache         [C, K, V] cache_dtype, or NULL for no cache write
  *   cache_row_map [S] int32 in [0, C), or NULL for row = slot
  *   out_tokens    [B, K] int32   (written)
- *   B in [0, 256], K in [1, 16], V in [1, 2^23), R a multiple of 64 up to
+ *   B in [0, 256], K in [1, 16], V in [1, 2^22), R a multiple of 64 up to
  *   512, S >= 1, C >= 1 if cache != NULL.
  *   workspace     device scratch of at least dspark_markov_workspace_bytes()
  *                 bytes, 256-byte aligned. Its contents need no

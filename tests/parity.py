@@ -5,7 +5,7 @@ the oracle's top-two noised-value gap (drafter draws, resample, bonus) or its
 accept margin |u - p/q| is below 1e-5, or where the top-p boundary mass is
 within 1e-6 of p (the pages' own exception for the kept set); such cases are
 counted. fp32 cache values agree within abs 1e-4 + rel 1e-5 with NaN matching
-NaN; a bf16 cache within one bf16 ulp.
+NaN; a bf16 cache within abs 1e-4 + one bf16 ulp (rel 2^-8).
 """
 from __future__ import annotations
 
@@ -18,6 +18,7 @@ MARGIN_TOL = 1e-5
 SLACK_TOL = 1e-6
 CACHE_ATOL = 1e-4
 CACHE_RTOL = 1e-5
+BF16_RTOL = 2.0 ** -8
 
 
 def subset(w, idx):
@@ -38,18 +39,16 @@ def subset(w, idx):
 def check_cache(gpu, ora, bf16, mask_rows=None):
     """Compare cache tensors ([C,K,V]); returns the max abs deviation."""
     if bf16:
-        g = gpu.astype(np.int32)
-        o = ora.astype(np.int32)
         gf = (gpu.astype(np.uint32) << 16).view(np.float32)
         of = (ora.astype(np.uint32) << 16).view(np.float32)
         nan_g, nan_o = np.isnan(gf), np.isnan(of)
         assert (nan_g == nan_o).all(), "NaN positions differ in the bf16 cache"
         fin = ~nan_g
-        # one bf16 ulp: the bit patterns differ by at most 1 (same sign)
-        diff = np.abs(g[fin] - o[fin])
-        same_sign = (np.signbit(gf[fin]) == np.signbit(of[fin])) | (gf[fin] == of[fin])
-        assert ((diff <= 1) & same_sign).all(), f"bf16 cache differs by > 1 ulp: {diff.max()}"
-        return float(np.abs(gf[fin] - of[fin]).max()) if fin.any() else 0.0
+        # bf16 rounding of the fp32 value: within abs 1e-4 + one bf16 ulp
+        np.testing.assert_allclose(gf[fin], of[fin], atol=CACHE_ATOL, rtol=BF16_RTOL)
+        d = np.abs(gf[fin].astype(np.float64) - of[fin].astype(np.float64))
+        d = d[np.isfinite(d)]
+        return float(d.max()) if d.size else 0.0
     nan_g, nan_o = np.isnan(gpu), np.isnan(ora)
     assert (nan_g == nan_o).all(), "NaN positions differ in the cache"
     fin = ~nan_g

@@ -1,6 +1,7 @@
 """The device noise generator against the oracle's: Philox words and
 uniforms bit-exact (pure integer and exact fp32 arithmetic), Gumbel variates
-within a few fp32 ulps (accurate fp32 logf on the device, fp64 on the host)."""
+within a few fp32 ulps of max(1, |g|) (accurate fp32 logf on the device, fp64
+on the host)."""
 import numpy as np
 import pytest
 
@@ -30,10 +31,9 @@ def test_noise_matches_oracle():
     torch.cuda.synchronize()
     np.testing.assert_array_equal(word.cpu().numpy().view(np.uint32), w_o)
     np.testing.assert_array_equal(u.cpu().numpy(), u_o)
-    gg = g.cpu().numpy()
-    ulps = np.abs(gg.view(np.int32).astype(np.int64) - g_o.view(np.int32).astype(np.int64))
-    same_sign = np.signbit(gg) == np.signbit(g_o)
-    small = np.abs(g_o) < 1e-3   # near the zero of g, compare absolutely
-    assert (np.abs(gg - g_o)[small] < 1e-6).all()
-    assert (ulps[~small & same_sign] <= 4).all(), ulps[~small].max()
-    assert (np.abs(gg - g_o) <= 4e-6).all()
+    gg = g.cpu().numpy().astype(np.float64)
+    go = g_o.astype(np.float64)
+    # fp32 logf twice against fp64 log rounded once: a few ulps of max(1, |g|)
+    # (near g = 0 the inner log's rounding dominates, so the bound is absolute)
+    err = np.abs(gg - go)
+    assert (err <= 4 * 2.0 ** -23 * np.maximum(1.0, np.abs(go))).all(), err.max()

@@ -12,6 +12,9 @@ namespace {
 
 constexpr size_t kAlign = 256;
 
+// Batches from this size on run the bias projection on the tensor cores.
+constexpr int kTensorCoreMinBatch = 8;
+
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -75,7 +78,6 @@ dspark_status dspark_markov_sample(
   if (!sizes_ok(B, K, V, S) || R < 1) return DSPARK_ERR_INVALID_ARG;
   if (!valid_dtype(base_dtype) || !valid_dtype(cache_dtype)) return DSPARK_ERR_INVALID_ARG;
   if (R % 64 != 0 || R > 512) return DSPARK_ERR_UNSUPPORTED;
-  if (dspark::markov_simt_smem_bytes(B, R) > 227u * 1024u) return DSPARK_ERR_UNSUPPORTED;
   if (B == 0) return DSPARK_OK;
   if (!base_logits || !markov_w1 || !markov_w2 || !anchor_tokens || !req_state_idx ||
       !positions || !temperature || !seeds || !out_tokens)
@@ -116,6 +118,21 @@ dspark_status dspark_markov_sample(
   p.status = status;
   if (cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), st) != cudaSuccess)
     return DSPARK_ERR_CUDA;
+  // Tensor cores once the batch makes the bias projection a real contraction.
+  dspark::MarkovTcPlan plan;
+  alignas(64) unsigned char tmap[128];
+  const bool use_tc = B >= kTensorCoreMinBatch && dspark::markov_tc_plan(B, R, &plan) &&
+                      dspark::markov_tc_make_tmap(tmap, markov_w2, V, R) == 0;
+  if (use_tc) {
+    const int grid = dspark::markov_tc_grid(V, sms);
+    for (int i = 0; i < K; ++i) {
+      p.step = i;
+      if (dspark::launch_markov_step_tc(p, tmap, plan, grid, st) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    }
+    return DSPARK_OK;
+  }
+  if (dspark::markov_simt_smem_bytes(B, R) > 227u * 1024u) return DSPARK_ERR_UNSUPPORTED;
   const int grid = dspark::markov_simt_grid(B, V, R, sms);
   for (int i = 0; i < K; ++i) {
     p.step = i;
@@ -145,6 +162,8 @@ dspark_status dspark_rejection_sample(
   if (draft_cache && C < 1) return DSPARK_ERR_INVALID_ARG;
   if (!aligned16(target_logits) || (draft_cache && !aligned16(draft_cache)))
     return DSPARK_ERR_ALIGNMENT;
+  int cluster = 0, slice = 0;
+  if (!dspark::verify_rows_plan(V, &cluster, &slice)) return DSPARK_ERR_UNSUPPORTED;
   const VerifyWs ws(B, K, V);
   if (!workspace || workspace_bytes < ws.total || !aligned16(workspace))
     return DSPARK_ERR_WORKSPACE;
@@ -181,7 +200,7 @@ dspark_status dspark_rejection_sample(
   if (cudaMemsetAsync(p.counters, 0, static_cast<size_t>(B) * sizeof(unsigned int), st) !=
       cudaSuccess)
     return DSPARK_ERR_CUDA;
-  if (dspark::launch_verify(p, st) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (dspark::launch_verify(p, cluster, slice, st) != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
 

@@ -37,6 +37,19 @@ int markov_simt_max_grid(int V);
 cudaError_t launch_markov_step_simt(const MarkovStepParams& p, int grid,
                                     cudaStream_t stream);
 
+// Tensor-core variant (markov_tc.cu).
+struct MarkovTcPlan {
+  int Npad;            // batch padded to a multiple of 16 (UMMA N)
+  int stages;          // shared-memory ring stages of 16 KB
+  unsigned tmem_cols;  // TMEM columns allocated (two accumulator buffers)
+  size_t smem;         // dynamic shared memory bytes
+};
+bool markov_tc_plan(int B, int R, MarkovTcPlan* plan);
+int markov_tc_make_tmap(void* tmap_out /* 128-byte CUtensorMap */, const void* w2, int V, int R);
+int markov_tc_grid(int V, int num_sms);
+cudaError_t launch_markov_step_tc(const MarkovStepParams& p, const void* tmap,
+                                  const MarkovTcPlan& plan, int grid, cudaStream_t stream);
+
 // Verification (verify.cu).
 struct VerifyParams {
   const int32_t* draft;
@@ -66,7 +79,10 @@ size_t verify_tstats_bytes(int B, int K);
 size_t verify_dstats_bytes(int B, int K);
 int verify_max_chunks(int V);
 int verify_chunks(int B, int V, int num_sms);
-cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
+size_t verify_rows_smem_bytes(int W);
+bool verify_rows_plan(int V, int* CL, int* W);
+cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_t stream);
+cudaError_t launch_verify(const VerifyParams& p, int CL, int W, cudaStream_t stream);
 
 // Noise generator on its own (api.cu / verify.cu).
 cudaError_t launch_noise(const uint64_t* seed, const int64_t* pos,

@@ -201,7 +201,7 @@ markov_step_simt_kernel(MarkovStepParams P) {
       }
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
       const ReqInfo ri = info[b];
-      unsigned long long key = 0ull;
+      uint32_t ord = 0u;
       // the pair's two threads share the row; the even one runs the epilogue
       if (half == 0 && in_range && ri.valid) {
         const int64_t boff = (static_cast<int64_t>(b) * K + step) * V + v;
@@ -220,10 +220,14 @@ markov_step_simt_kernel(MarkovStepParams P) {
           else
             static_cast<float*>(P.cache)[ri.cache_off + v] = x;
         }
-        key = winner_key(y, static_cast<uint32_t>(v));
+        ord = ordered_bits(y);  // every real value maps above 0
       }
-      key = warp_max64(key);
-      if ((tid & 31) == 0 && key != 0ull) atomicMax(&best[b], key);
+      // winner over the warp's rows: largest value, then lowest column
+      const uint32_t omax = __reduce_max_sync(0xFFFFFFFFu, ord);
+      const uint32_t cand = (ord == omax && ord != 0u) ? static_cast<uint32_t>(v) : 0xFFFFFFFFu;
+      const uint32_t vmin = __reduce_min_sync(0xFFFFFFFFu, cand);
+      if ((tid & 31) == 0 && omax != 0u)
+        atomicMax(&best[b], (static_cast<unsigned long long>(omax) << 32) | (0xFFFFFFFFu - vmin));
     }
     __syncthreads();  // every thread is done reading this stage
     if (tid == 0) {

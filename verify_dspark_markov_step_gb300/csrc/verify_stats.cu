@@ -1,0 +1,725 @@
+// verify_stats.cu -- per-row statistics of the verifier, one thread-block
+// cluster per row.
+//
+// vLLM PR #65007 Part 2 ("Temperature and top-p"): the target row after
+// temperature, its maximum and total exp-mass in 64-bit fixed point, and the
+// exact top-p keep set -- the smallest prefix by (logit desc, token id asc)
+// whose mass reaches p, plus the row max. Draft rows (the cache) get their
+// maximum and fixed-point mass. Greedy target rows get their winner key.
+//
+// A row is split over the CL CTAs of a cluster (CL up to 16). Each CTA reads
+// its slice from HBM exactly once into shared memory and every later pass
+// (fixed-point mass, the radix stages of the top-p select) runs on the
+// shared-memory copy. Reductions across the cluster go through distributed
+// shared memory: scalars by each CTA reading the others' slots, histograms
+// by each CTA reducing its own range of bins over the cluster.
+//
+// Top-p select: a radix select on the ordered bits kd of the scaled logits,
+// most significant first (11 + 11 + 10 bits), with histograms of fixed-point
+// mass; each stage finds the first bin (in descending kd order) at which the
+// running mass reaches P32 * F / 2^32. Exact ties at the boundary value are
+// resolved by two more stages on the token id (ascending, 11 + 11 bits).
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "verify_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace dspark {
+
+namespace {
+
+constexpr int kRowThreads = 512;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowBins = 2048;
+constexpr int kMaxCluster = 16;
+constexpr size_t kRowSmemLimit = 227u * 1024u;
+
+struct RowSmem {
+  unsigned long long hmass[kRowBins];
+  unsigned int hcnt[kRowBins];
+  unsigned int hid[kRowBins];
+  unsigned long long red64[kRowWarps];
+  float redf[kRowWarps];
+  // slots read by the other CTAs of the cluster
+  float x_max;
+  int x_pos;
+  unsigned long long x_key;
+  unsigned long long x_sum;
+  unsigned long long x_range;
+  unsigned long long x_before;
+  unsigned long long x_mass;
+  unsigned int x_cnt;
+  unsigned int x_id;
+  // block-local scratch
+  int found_pos;
+  int bcast_i;
+  unsigned long long found_before;
+  unsigned long long bcast_u;
+  float bcast_f;
+  int pad_[3];
+};
+
+struct Found {
+  int bin;
+  unsigned long long before;  // running mass before the bin
+  unsigned int cnt;
+  unsigned long long mass;
+  unsigned int id;
+};
+
+__device__ float block_max_f(float v, RowSmem& sm) {
+  v = warp_maxf(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sm.redf[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    float x = l < kRowWarps ? sm.redf[l] : -INFINITY;
+    x = warp_maxf(x);
+    if (l == 0) sm.redf[0] = x;
+  }
+  __syncthreads();
+  return sm.redf[0];
+}
+
+__device__ unsigned long long block_sum_u64(unsigned long long v, RowSmem& sm) {
+  v = warp_sum64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sm.red64[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    unsigned long long x = l < kRowWarps ? sm.red64[l] : 0ull;
+    x = warp_sum64(x);
+    if (l == 0) sm.red64[0] = x;
+  }
+  __syncthreads();
+  return sm.red64[0];
+}
+
+__device__ unsigned long long block_max_u64(unsigned long long v, RowSmem& sm) {
+  v = warp_max64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) sm.red64[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    unsigned long long x = l < kRowWarps ? sm.red64[l] : 0ull;
+    x = warp_max64(x);
+    if (l == 0) sm.red64[0] = x;
+  }
+  __syncthreads();
+  return sm.red64[0];
+}
+
+// ---- cluster reductions of one value per CTA ---------------------------------
+__device__ float cluster_max_f(cg::cluster_group& cl, RowSmem& sm, float v, int CL) {
+  if (threadIdx.x == 0) sm.x_max = v;
+  cl.sync();
+  if (threadIdx.x < 32) {
+    float m = -INFINITY;
+    if (static_cast<int>(threadIdx.x) < CL) m = *cl.map_shared_rank(&sm.x_max, threadIdx.x);
+    m = warp_maxf(m);
+    if (threadIdx.x == 0) sm.bcast_f = m;
+  }
+  __syncthreads();
+  return sm.bcast_f;
+}
+
+__device__ unsigned long long cluster_sum_u64(cg::cluster_group& cl, RowSmem& sm,
+                                              unsigned long long v, int CL) {
+  if (threadIdx.x == 0) sm.x_sum = v;
+  cl.sync();
+  if (threadIdx.x < 32) {
+    unsigned long long s = 0ull;
+    if (static_cast<int>(threadIdx.x) < CL) s = *cl.map_shared_rank(&sm.x_sum, threadIdx.x);
+    s = warp_sum64(s);
+    if (threadIdx.x == 0) sm.bcast_u = s;
+  }
+  __syncthreads();
+  return sm.bcast_u;
+}
+
+__device__ unsigned long long cluster_max_u64(cg::cluster_group& cl, RowSmem& sm,
+                                              unsigned long long v, int CL) {
+  if (threadIdx.x == 0) sm.x_key = v;
+  cl.sync();
+  if (threadIdx.x < 32) {
+    unsigned long long s = 0ull;
+    if (static_cast<int>(threadIdx.x) < CL) s = *cl.map_shared_rank(&sm.x_key, threadIdx.x);
+    s = warp_max64(s);
+    if (threadIdx.x == 0) sm.bcast_u = s;
+  }
+  __syncthreads();
+  return sm.bcast_u;
+}
+
+// ---- slice loader: fn(local index, value) over [v0, v0 + n) of a row -----
+template <class Fn>
+__device__ __forceinline__ void slice_load(const void* row, bool bf16, int v0, int n,
+                                           uint64_t policy, Fn&& fn) {
+  const int tid = threadIdx.x;
+  if (!bf16) {
+    const float* r = static_cast<const float*>(row) + v0;
+    if ((reinterpret_cast<uintptr_t>(r) & 15u) == 0) {
+      const int n4 = n >> 2;
+      int i = tid;
+      for (; i + 3 * kRowThreads < n4; i += 4 * kRowThreads) {
+        float4 a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = ld_stream_f4(r + 4 * (i + u * kRowThreads), policy);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = 4 * (i + u * kRowThreads);
+          fn(j, a[u].x);
+          fn(j + 1, a[u].y);
+          fn(j + 2, a[u].z);
+          fn(j + 3, a[u].w);
+        }
+      }
+      for (; i < n4; i += kRowThreads) {
+        const float4 a = ld_stream_f4(r + 4 * i, policy);
+        fn(4 * i, a.x);
+        fn(4 * i + 1, a.y);
+        fn(4 * i + 2, a.z);
+        fn(4 * i + 3, a.w);
+      }
+      for (int j = 4 * n4 + tid; j < n; j += kRowThreads) fn(j, __ldg(r + j));
+    } else {
+      int j = tid;
+      for (; j + 3 * kRowThreads < n; j += 4 * kRowThreads) {
+        float a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = __ldg(r + j + u * kRowThreads);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) fn(j + u * kRowThreads, a[u]);
+      }
+      for (; j < n; j += kRowThreads) fn(j, __ldg(r + j));
+    }
+  } else {
+    const unsigned short* r = static_cast<const unsigned short*>(row) + v0;
+    if ((reinterpret_cast<uintptr_t>(r) & 15u) == 0) {
+      const int n8 = n >> 3;
+      int i = tid;
+      for (; i + kRowThreads < n8; i += 2 * kRowThreads) {
+        uint4 a[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) a[u] = __ldg(reinterpret_cast<const uint4*>(r) + i + u * kRowThreads);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = 8 * (i + u * kRowThreads);
+          const uint32_t w4[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            fn(j + 2 * q, __uint_as_float(w4[q] << 16));
+            fn(j + 2 * q + 1, __uint_as_float(w4[q] & 0xFFFF0000u));
+          }
+        }
+      }
+      for (; i < n8; i += kRowThreads) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(r) + i);
+        const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          fn(8 * i + 2 * q, __uint_as_float(w4[q] << 16));
+          fn(8 * i + 2 * q + 1, __uint_as_float(w4[q] & 0xFFFF0000u));
+        }
+      }
+      for (int j = 8 * n8 + tid; j < n; j += kRowThreads) fn(j, bf16_bits_to_float(__ldg(r + j)));
+    } else {
+      for (int j = tid; j < n; j += kRowThreads) fn(j, bf16_bits_to_float(__ldg(r + j)));
+    }
+  }
+}
+
+// ---- histograms -------------------------------------------------------------
+__device__ void hist_clear(RowSmem& sm, int nb) {
+  for (int i = threadIdx.x; i < nb; i += kRowThreads) {
+    sm.hmass[i] = 0ull;
+    sm.hcnt[i] = 0u;
+    sm.hid[i] = 0u;
+  }
+}
+
+// Adds (mass f, one count, id) to bin `bin`, aggregated over the lanes of the
+// warp sharing the bin. Every lane of the warp calls it; inactive lanes add
+// nothing.
+__device__ __forceinline__ void hist_add(RowSmem& sm, bool active, int bin,
+                                         unsigned long long f, uint32_t id) {
+  unsigned int todo = __ballot_sync(0xFFFFFFFFu, active);
+  const int lane = threadIdx.x & 31;
+  while (todo) {
+    const int leader = __ffs(todo) - 1;
+    const int lb = __shfl_sync(0xFFFFFFFFu, bin, leader);
+    const bool mine = active && bin == lb;
+    const unsigned int peers = __ballot_sync(0xFFFFFFFFu, mine);
+    // f <= 2^40: two 20-bit halves keep the 32-bit warp sums exact
+    const unsigned int hi =
+        __reduce_add_sync(0xFFFFFFFFu, mine ? static_cast<unsigned int>(f >> 20) : 0u);
+    const unsigned int lo =
+        __reduce_add_sync(0xFFFFFFFFu, mine ? static_cast<unsigned int>(f & 0xFFFFFu) : 0u);
+    const unsigned int idm = __reduce_max_sync(0xFFFFFFFFu, mine ? id : 0u);
+    if (lane == leader) {
+      atomicAdd(&sm.hmass[lb], (static_cast<unsigned long long>(hi) << 20) + lo);
+      atomicAdd(&sm.hcnt[lb], static_cast<unsigned int>(__popc(peers)));
+      atomicMax(&sm.hid[lb], idm);
+    }
+    todo &= ~peers;
+  }
+}
+
+// Reduces the local histograms over the cluster and finds the first
+// non-empty bin, in scan order (descending bin index if desc), at which the
+// running mass (starting from `above`) reaches the target (t_hi:t_lo).
+__device__ Found cluster_find(cg::cluster_group& cl, RowSmem& sm, int nb, bool desc,
+                              unsigned long long above, unsigned long long t_hi,
+                              unsigned long long t_lo, int CL, int rank) {
+  const int tid = threadIdx.x;
+  const int w = nb / CL;
+  const int b0 = rank * w;
+  __syncthreads();
+  cl.sync();  // every local histogram is complete
+  // 1. reduce the bins this CTA owns over the cluster
+  constexpr int kPer = kRowBins / kRowThreads;  // at most 4 owned bins per thread
+  unsigned long long rm[kPer];
+  unsigned int rc[kPer], ri[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    rm[j] = 0ull;
+    rc[j] = 0u;
+    ri[j] = 0u;
+    const int bi = tid + j * kRowThreads;
+    if (bi < w) {
+      for (int r = 0; r < CL; ++r) {
+        RowSmem* o = cl.map_shared_rank(&sm, r);
+        rm[j] += o->hmass[b0 + bi];
+        rc[j] += o->hcnt[b0 + bi];
+        ri[j] = max(ri[j], o->hid[b0 + bi]);
+      }
+    }
+  }
+  cl.sync();  // every remote read is done; owned bins may be overwritten
+  unsigned long long mine = 0ull;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int bi = tid + j * kRowThreads;
+    if (bi < w) {
+      sm.hmass[b0 + bi] = rm[j];
+      sm.hcnt[b0 + bi] = rc[j];
+      sm.hid[b0 + bi] = ri[j];
+      mine += rm[j];
+    }
+  }
+  const unsigned long long range_mass = block_sum_u64(mine, sm);
+  if (tid == 0) sm.x_range = range_mass;
+  cl.sync();
+  // 2. running mass before this CTA's range, in scan order
+  if (tid < 32) {
+    unsigned long long s = 0ull;
+    const int r = tid;
+    if (r < CL && (desc ? r > rank : r < rank)) s = *cl.map_shared_rank(&sm.x_range, r);
+    s = warp_sum64(s);
+    if (tid == 0) sm.bcast_u = s;
+  }
+  __syncthreads();
+  const unsigned long long range_before = above + sm.bcast_u;
+  // 3. scan the owned range: thread t takes positions [t*per, t*per+per)
+  const int per = (w + kRowThreads - 1) / kRowThreads;
+  const int p0 = tid * per;
+  unsigned long long tsum = 0ull;
+  for (int i = 0; i < per; ++i) {
+    const int pos = p0 + i;
+    if (pos < w) tsum += sm.hmass[desc ? b0 + w - 1 - pos : b0 + pos];
+  }
+  const int lane = tid & 31, wp = tid >> 5;
+  unsigned long long incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long nv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += nv;
+  }
+  __syncthreads();
+  if (lane == 31) sm.red64[wp] = incl;
+  if (tid == 0) sm.found_pos = 0x7FFFFFFF;
+  __syncthreads();
+  unsigned long long woff = 0ull;
+  for (int i = 0; i < wp; ++i) woff += sm.red64[i];
+  unsigned long long run = range_before + woff + incl - tsum;
+  int found = 0x7FFFFFFF;
+  unsigned long long fbefore = 0ull;
+  for (int i = 0; i < per; ++i) {
+    const int pos = p0 + i;
+    if (pos >= w) break;
+    const int bin = desc ? b0 + w - 1 - pos : b0 + pos;
+    const unsigned long long mb = sm.hmass[bin];
+    if (sm.hcnt[bin] > 0u && reaches(run + mb, t_hi, t_lo)) {
+      found = pos;
+      fbefore = run;
+      break;
+    }
+    run += mb;
+  }
+  atomicMin(&sm.found_pos, found);
+  __syncthreads();
+  if (found != 0x7FFFFFFF && found == sm.found_pos) {
+    const int bin = desc ? b0 + w - 1 - found : b0 + found;
+    sm.x_pos = desc ? nb - 1 - bin : bin;  // global scan position
+    sm.x_before = fbefore;
+    sm.x_cnt = sm.hcnt[bin];
+    sm.x_mass = sm.hmass[bin];
+    sm.x_id = sm.hid[bin];
+  }
+  if (tid == 0 && sm.found_pos == 0x7FFFFFFF) sm.x_pos = 0x7FFFFFFF;
+  cl.sync();
+  // 4. the first qualifying bin over the cluster
+  if (tid == 0) {
+    int best_r = -1, best_pos = 0x7FFFFFFF;
+    for (int r = 0; r < CL; ++r) {
+      const int p = cl.map_shared_rank(&sm, r)->x_pos;
+      if (p < best_pos) {
+        best_pos = p;
+        best_r = r;
+      }
+    }
+    sm.bcast_i = best_r;
+  }
+  __syncthreads();
+  Found f;
+  const int br = sm.bcast_i;
+  if (br < 0) {  // cannot happen: the stage's set always holds the boundary
+    f.bin = 0;
+    f.before = above;
+    f.cnt = 1u;
+    f.mass = 0ull;
+    f.id = 0u;
+  } else {
+    const RowSmem* o = cl.map_shared_rank(&sm, br);
+    const int pos = o->x_pos;
+    f.bin = desc ? nb - 1 - pos : pos;
+    f.before = o->x_before;
+    f.cnt = o->x_cnt;
+    f.mass = o->x_mass;
+    f.id = o->x_id;
+  }
+  cl.sync();  // slots may be rewritten by the next stage
+  return f;
+}
+
+// One local histogram pass over the shared-memory slice: elements whose kd
+// and id pass `match` add their fixed-point mass to bin digit(kd, id).
+template <class Match, class Digit>
+__device__ void hist_pass(RowSmem& sm, const float* xs, int n, int v0, float m, int nb,
+                          Match match, Digit digit) {
+  hist_clear(sm, nb);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  for (int base = threadIdx.x & ~31; base < n; base += kRowThreads) {
+    const int i = base + lane;
+    const bool valid = i < n;
+    const float x = valid ? xs[i] : -INFINITY;
+    const uint32_t kd = kd_of(x);
+    const uint32_t id = static_cast<uint32_t>(v0 + i);
+    const bool act = valid && match(kd, id);
+    const unsigned long long f = act ? fixed_mass(exp_rel(x, m)) : 0ull;
+    hist_add(sm, act, act ? digit(kd, id) : 0, f, id);
+  }
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParams P, int W) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int CL = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
+  float* xs = reinterpret_cast<float*>(smem_raw + ((sizeof(RowSmem) + 15) & ~size_t(15)));
+  const int tid = threadIdx.x;
+  const int K = P.K, V = P.V;
+  const int row_id = blockIdx.x / CL;
+  const int nT = P.B * (K + 1);
+  int b, k;
+  bool is_target;
+  if (row_id < nT) {
+    b = row_id / (K + 1);
+    k = row_id % (K + 1);
+    is_target = true;
+  } else {
+    const int r = row_id - nT;
+    b = r / K;
+    k = r % K;
+    is_target = false;
+  }
+  // Decisions below depend only on the row, so a whole cluster returns
+  // together, before touching distributed shared memory.
+  const int32_t s = P.rsi[b];
+  if (s < 0 || s >= P.S) return;
+  const float T = P.temperature[s];
+  const bool greedy = !(T > 0.0f);
+  int64_t crow = 0;
+  if (!is_target) {
+    if (greedy || P.cache == nullptr) return;
+    crow = P.row_map ? P.row_map[s] : s;
+    if (crow < 0 || crow >= P.C) return;
+  }
+  const int v0 = rank * W;
+  const int n = max(0, min(W, V - v0));
+  const void* row;
+  bool bf16;
+  if (is_target) {
+    const int64_t off = (static_cast<int64_t>(b) * (K + 1) + k) * V;
+    bf16 = P.target_bf16 != 0;
+    row = bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(P.target) + off)
+               : static_cast<const void*>(static_cast<const float*>(P.target) + off);
+  } else {
+    const int64_t off = (crow * K + k) * V;
+    bf16 = P.cache_bf16 != 0;
+    row = bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(P.cache) + off)
+               : static_cast<const void*>(static_cast<const float*>(P.cache) + off);
+  }
+  const uint64_t pol = policy_evict_first();
+  const int32_t d = k < K ? P.draft[static_cast<int64_t>(b) * K + k] : -1;
+  TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(b) * (K + 1) + k;
+  DrfStats* ds = static_cast<DrfStats*>(P.dstats) + static_cast<int64_t>(b) * K + (k < K ? k : 0);
+
+  // ---- greedy target row: winner key of the raw row ----------------------------
+  if (is_target && greedy) {
+    unsigned long long key = 0ull;
+    slice_load(row, bf16, v0, n, pol, [&](int i, float t) {
+      key = umax64(key, winner_key(t, static_cast<uint32_t>(v0 + i)));
+    });
+    key = block_max_u64(key, sm);
+    key = cluster_max_u64(cl, sm, key, CL);
+    if (rank == 0 && tid == 0) {
+      ts->m = 0.f;
+      ts->D = 1.f;
+      ts->kd_thr = 0u;
+      ts->id_thr = 0;
+      ts->p_d = 0.f;
+      ts->mode = kModeGreedy;
+      ts->amax_key = key;
+    }
+    cl.sync();
+    return;
+  }
+
+  // ---- pass 1: HBM -> shared memory, maximum --------------------------------------
+  float lmax = -INFINITY;
+  if (is_target) {
+    slice_load(row, bf16, v0, n, pol, [&](int i, float t) {
+      const float x = scale_logit(t, T);
+      xs[i] = x;
+      lmax = fmaxf(lmax, x);
+    });
+  } else {
+    slice_load(row, bf16, v0, n, pol, [&](int i, float c) {
+      const float x = (c != c) ? -INFINITY : c;
+      xs[i] = x;
+      lmax = fmaxf(lmax, x);
+    });
+  }
+  lmax = block_max_f(lmax, sm);
+  const float m = cluster_max_f(cl, sm, lmax, CL);
+  if (m == -INFINITY) {
+    if (rank == 0 && tid == 0) {
+      if (is_target) {
+        ts->m = m;
+        ts->D = 1.0f;
+        ts->kd_thr = 0u;
+        ts->id_thr = 0;
+        ts->p_d = d == 0 ? 1.0f : 0.0f;
+        ts->mode = kModeOneHot;
+        ts->amax_key = 0ull;
+      } else {
+        ds->m = m;
+        ds->D = 1.0f;
+        ds->q_d = 0.0f;
+        ds->zero = 1;
+      }
+    }
+    cl.sync();
+    return;
+  }
+
+  // ---- pass 2: fixed-point mass (+ first top-p histogram) -------------------------
+  const bool topp = is_target && P.top_p[s] < 1.0f;
+  if (topp) hist_clear(sm, kRowBins);
+  __syncthreads();
+  unsigned long long F = 0ull;
+  {
+    const int lane = tid & 31;
+    for (int base = tid & ~31; base < n; base += kRowThreads) {
+      const int i = base + lane;
+      const bool valid = i < n;
+      const float x = valid ? xs[i] : -INFINITY;
+      const unsigned long long f = valid ? fixed_mass(exp_rel(x, m)) : 0ull;
+      F += f;
+      if (topp) hist_add(sm, valid, static_cast<int>(kd_of(x) >> 21), f, static_cast<uint32_t>(v0 + i));
+    }
+  }
+  F = block_sum_u64(F, sm);
+  F = cluster_sum_u64(cl, sm, F, CL);
+
+  uint32_t kd_thr = 0u;
+  int32_t id_thr = 0;
+  unsigned long long Fk = F;
+  int32_t mode = kModeKeepAll;
+  if (topp) {
+    mode = kModeThreshold;
+    const unsigned long long P32 = topp_scaled(P.top_p[s]);
+    const unsigned long long t_lo = P32 * F;
+    const unsigned long long t_hi = __umul64hi(P32, F);
+    bool resolved = false;
+    // kd stage 0: bits [31:21]
+    Found f = cluster_find(cl, sm, kRowBins, true, 0ull, t_hi, t_lo, CL, rank);
+    unsigned long long above = f.before;
+    uint32_t pre = static_cast<uint32_t>(f.bin);
+    if (f.cnt == 1u) {
+      id_thr = static_cast<int32_t>(f.id);
+      Fk = above + f.mass;
+      resolved = true;
+    }
+    if (!resolved) {  // kd stage 1: bits [20:10]
+      const uint32_t p0 = pre;
+      hist_pass(sm, xs, n, v0, m, kRowBins, [=](uint32_t kd, uint32_t) { return (kd >> 21) == p0; },
+                [](uint32_t kd, uint32_t) { return static_cast<int>((kd >> 10) & 0x7FFu); });
+      f = cluster_find(cl, sm, kRowBins, true, above, t_hi, t_lo, CL, rank);
+      above = f.before;
+      pre = (pre << 11) | static_cast<uint32_t>(f.bin);
+      if (f.cnt == 1u) {
+        id_thr = static_cast<int32_t>(f.id);
+        Fk = above + f.mass;
+        resolved = true;
+      }
+    }
+    if (!resolved) {  // kd stage 2: bits [9:0]
+      const uint32_t p1 = pre;
+      hist_pass(sm, xs, n, v0, m, 1024, [=](uint32_t kd, uint32_t) { return (kd >> 10) == p1; },
+                [](uint32_t kd, uint32_t) { return static_cast<int>(kd & 0x3FFu); });
+      f = cluster_find(cl, sm, 1024, true, above, t_hi, t_lo, CL, rank);
+      above = f.before;
+      pre = (pre << 10) | static_cast<uint32_t>(f.bin);
+      if (f.cnt == 1u) {
+        id_thr = static_cast<int32_t>(f.id);
+        Fk = above + f.mass;
+        resolved = true;
+      }
+    }
+    if (resolved) {
+      // full kd of the boundary element, read from the CTA that holds it
+      if (tid == 0) {
+        const int owner = id_thr / W;
+        const float xb = *cl.map_shared_rank(xs + (id_thr - owner * W), owner);
+        sm.bcast_i = static_cast<int>(kd_of(xb));
+      }
+      __syncthreads();
+      kd_thr = static_cast<uint32_t>(sm.bcast_i);
+    } else {
+      // exact ties at the boundary value: token id ascending, 11 + 11 bits
+      kd_thr = pre;
+      const uint32_t kt = kd_thr;
+      hist_pass(sm, xs, n, v0, m, kRowBins, [=](uint32_t kd, uint32_t) { return kd == kt; },
+                [](uint32_t, uint32_t id) { return static_cast<int>((id >> 11) & 0x7FFu); });
+      f = cluster_find(cl, sm, kRowBins, false, above, t_hi, t_lo, CL, rank);
+      above = f.before;
+      if (f.cnt == 1u) {
+        id_thr = static_cast<int32_t>(f.id);
+        Fk = above + f.mass;
+      } else {
+        const uint32_t ip = static_cast<uint32_t>(f.bin);
+        hist_pass(sm, xs, n, v0, m, kRowBins,
+                  [=](uint32_t kd, uint32_t id) { return kd == kt && (id >> 11) == ip; },
+                  [](uint32_t, uint32_t id) { return static_cast<int>(id & 0x7FFu); });
+        f = cluster_find(cl, sm, kRowBins, false, above, t_hi, t_lo, CL, rank);
+        above = f.before;
+        id_thr = static_cast<int32_t>(f.id);
+        Fk = above + f.mass;
+      }
+    }
+  }
+  const float D = __fmul_rn(__ull2float_rn(Fk), 0x1p-40f);
+
+  // ---- outputs: p or q at the drafted token (its owner), the rest (rank 0) ---------
+  if (tid == 0 && d >= v0 && d < v0 + n) {
+    const float x = xs[d - v0];
+    if (is_target) {
+      const uint32_t kd = kd_of(x);
+      const bool keep = mode == kModeKeepAll || kd > kd_thr || (kd == kd_thr && d <= id_thr);
+      ts->p_d = keep ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
+    } else {
+      ds->q_d = __fdiv_rn(exp_rel(x, m), D);
+    }
+  }
+  if (rank == 0 && tid == 0) {
+    if (is_target) {
+      ts->m = m;
+      ts->D = D;
+      ts->kd_thr = kd_thr;
+      ts->id_thr = id_thr;
+      ts->mode = mode;
+      ts->amax_key = 0ull;
+      if (!(d >= 0 && d < V)) ts->p_d = 0.0f;
+    } else {
+      ds->m = m;
+      ds->D = D;
+      ds->zero = 0;
+      if (!(d >= 0 && d < V)) ds->q_d = 0.0f;
+    }
+  }
+  cl.sync();  // no CTA leaves while another may still read its shared memory
+}
+
+}  // namespace
+
+size_t verify_rows_smem_bytes(int W) {
+  return ((sizeof(RowSmem) + 15) & ~size_t(15)) + static_cast<size_t>(W) * sizeof(float);
+}
+
+// Cluster size and slice width for vocabulary V: the smallest power-of-two
+// cluster whose slices leave room for two CTAs per SM, up to 16.
+bool verify_rows_plan(int V, int* CL, int* W) {
+  for (int cl = 1; cl <= kMaxCluster; cl *= 2) {
+    int w = (V + cl - 1) / cl;
+    w = (w + 7) & ~7;
+    if (verify_rows_smem_bytes(w) <= 100u * 1024u || cl == kMaxCluster) {
+      if (verify_rows_smem_bytes(w) > kRowSmemLimit) return false;
+      *CL = cl;
+      *W = w;
+      return true;
+    }
+  }
+  return false;
+}
+
+cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_t stream) {
+  const int rows = p.B * (p.K + 1) + p.B * p.K;
+  const size_t smem = verify_rows_smem_bytes(W);
+  cudaError_t err = cudaFuncSetAttribute(verify_rows_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  if (CL > 8) {
+    err = cudaFuncSetAttribute(verify_rows_kernel,
+                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err != cudaSuccess) return err;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(rows * CL), 1, 1);
+  cfg.blockDim = dim3(kRowThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(CL);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_rows_kernel, p, W);
+}
+
+}  // namespace dspark
