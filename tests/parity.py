@@ -5,7 +5,8 @@ the oracle's top-two noised-value gap (drafter draws, resample, bonus) or its
 accept margin |u - p/q| is below 1e-5, or where the top-p boundary mass is
 within 1e-6 of p (the pages' own exception for the kept set); such cases are
 counted. fp32 cache values agree within abs 1e-4 + rel 1e-5 with NaN matching
-NaN; a bf16 cache within abs 1e-4 + one bf16 ulp (rel 2^-8).
+NaN; a bf16 cache within abs 1e-4 + one bf16 ulp (rel 2^-7 at the bottom
+of a binade).
 """
 from __future__ import annotations
 
@@ -18,7 +19,7 @@ MARGIN_TOL = 1e-5
 SLACK_TOL = 1e-6
 CACHE_ATOL = 1e-4
 CACHE_RTOL = 1e-5
-BF16_RTOL = 2.0 ** -8
+BF16_RTOL = 2.0 ** -7
 
 
 def subset(w, idx):

@@ -13,13 +13,13 @@
 //               swizzle) into a ring of shared-memory stages, L2 evict-last
 //   warp 1      TMEM allocation; one thread issues the MMAs (4 per 64-wide K
 //               chunk) into one of two accumulator buffers and commits
-//   warps 2-17  epilogue: tcgen05.ld of the accumulator rows of their TMEM
-//               lane quarter, bias add, temperature, Gumbel noise (one
-//               Philox block per 4 columns, shared across a lane quad by a
-//               4x4 shuffle transpose), cache store, and the winner of
-//               each request over the warp's rows by two redux.sync
-//               reductions (max of the ordered value bits, then min index),
-//               kept per lane across tiles
+//   warps 2-17  epilogue: warp (q, sub) owns TMEM lane quarter q (32 rows of
+//               each tile) and a fixed set of CPW batch columns. Per chunk of
+//               4 columns: tcgen05.ld, bias add, temperature, Gumbel noise
+//               (one Philox block per lane quad, shared by a 4x4 shuffle
+//               transpose), cache store, and the running winner of each
+//               column -- per lane in registers across tiles when CPW <= 16,
+//               else reduced per tile with redux.sync.
 // The per-CTA winners are reduced by the last CTA, as in markov_step.cu.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -40,24 +40,19 @@ constexpr int kThreadsTc = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 12;
 constexpr size_t kSmemLimit = 227u * 1024u;
 
-struct ReqInfoTc {
-  float temperature;
-  int32_t valid;
-  int32_t prev;
-  int32_t pad_;
-  uint64_t seed;
-  int64_t noise_pos;
-  int64_t cache_off;
-};
-
+// Per-request data of one step, structure of arrays (Npad entries each).
 struct TcLayout {
-  size_t a, e, info, best, bars, slot, flags, total;
-  __host__ __device__ TcLayout(int B, int Npad, int NK, int ns) {
+  size_t a, e, temp, seed, npos, boff, coff, best, bars, slot, flags, total;
+  __host__ __device__ TcLayout(int Npad, int NK, int ns) {
     a = 0;
     e = a + static_cast<size_t>(ns) * kStageBytes;
-    info = e + static_cast<size_t>(NK) * Npad * 128;
-    best = info + static_cast<size_t>(B) * sizeof(ReqInfoTc);
-    bars = (best + static_cast<size_t>(Npad) * 8 + 7) & ~size_t(7);
+    temp = e + static_cast<size_t>(NK) * Npad * 128;
+    seed = temp + static_cast<size_t>(Npad) * 4;
+    npos = seed + static_cast<size_t>(Npad) * 8;
+    boff = npos + static_cast<size_t>(Npad) * 8;
+    coff = boff + static_cast<size_t>(Npad) * 8;
+    best = coff + static_cast<size_t>(Npad) * 8;
+    bars = best + static_cast<size_t>(Npad) * 8;
     slot = bars + static_cast<size_t>(2 * ns + 5) * 8;
     flags = slot + 8;
     total = flags + 8 + kMaxStages * 4 + 1024;  // + slack to align the base to 1024 B
@@ -86,17 +81,33 @@ __device__ __forceinline__ void quad_transpose(const uint32_t (&w)[4], uint32_t 
   }
 }
 
-template <int NK>  // markov_rank R = 64 * NK
+// Winner over the warp's lanes of (ord, v): largest ord, then lowest v.
+__device__ __forceinline__ unsigned long long warp_winner(uint32_t ord, uint32_t v) {
+  const uint32_t omax = __reduce_max_sync(0xFFFFFFFFu, ord);
+  const uint32_t cand = (ord == omax && ord != 0u) ? v : 0xFFFFFFFFu;
+  const uint32_t vmin = __reduce_min_sync(0xFFFFFFFFu, cand);
+  return omax == 0u ? 0ull
+                    : (static_cast<unsigned long long>(omax) << 32) | (0xFFFFFFFFu - vmin);
+}
+
+template <int CPW>  // batch columns per epilogue warp (Npad / 4)
 __global__ void __launch_bounds__(kThreadsTc, 1)
 markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepParams P, int Npad,
                       int ns, uint32_t tmem_cols) {
-  constexpr int R = 64 * NK;
+  constexpr bool kRegWinners = CPW <= 16;
+  const int R = P.R;
+  const int NK = R / 64;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  const TcLayout L(P.B, Npad, NK, ns);
+  const TcLayout L(Npad, NK, ns);
   unsigned char* a_base = smem + L.a;
   unsigned char* e_base = smem + L.e;
-  ReqInfoTc* info = reinterpret_cast<ReqInfoTc*>(smem + L.info);
+  float* s_temp = reinterpret_cast<float*>(smem + L.temp);
+  uint64_t* s_seed = reinterpret_cast<uint64_t*>(smem + L.seed);
+  int64_t* s_npos = reinterpret_cast<int64_t*>(smem + L.npos);
+  int64_t* s_boff = reinterpret_cast<int64_t*>(smem + L.boff);   // -1: inert column
+  int64_t* s_coff = reinterpret_cast<int64_t*>(smem + L.coff);   // -1: no cache store
+  int32_t* s_prev = reinterpret_cast<int32_t*>(smem + L.coff);   // prologue only (aliases coff)
   unsigned long long* best = reinterpret_cast<unsigned long long*>(smem + L.best);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ns;
@@ -112,48 +123,54 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
   const int G = gridDim.x;
   const int tiles = (V + kM - 1) / kM;
 
-  // ---- prologue ---------------------------------------------------------------
-  for (int b = tid; b < B; b += kThreadsTc) {
-    ReqInfoTc ri;
-    ri.valid = 0;
-    ri.prev = 0;
-    ri.temperature = 0.f;
-    ri.seed = 0;
-    ri.noise_pos = 0;
-    ri.cache_off = -1;
-    ri.pad_ = 0;
-    const int32_t s = P.rsi[b];
+  // ---- prologue: per-request data (thread n < Npad owns column n) ------------
+  int32_t my_prev = -1;
+  int64_t my_coff = -1;
+  if (tid < Npad) {
+    const int n = tid;
+    float temp = 0.f;
+    uint64_t seed = 0;
+    int64_t npos = 0, boff = -1, coff = -1;
+    int32_t prev = -1;
+    const int32_t s = n < B ? P.rsi[n] : -1;
     if (s >= 0) {
       if (s >= P.S) {
         report(P.status, DSPARK_ERR_BOUNDS);
       } else {
-        const int32_t prev =
-            step == 0 ? P.anchor[b] : P.out_tokens[static_cast<int64_t>(b) * K + step - 1];
-        bool ok = prev >= 0 && prev < V;
+        const int32_t pv =
+            step == 0 ? P.anchor[n] : P.out_tokens[static_cast<int64_t>(n) * K + step - 1];
+        bool ok = pv >= 0 && pv < V;
         if (!ok) report(P.status, DSPARK_ERR_BOUNDS);
-        int64_t off = -1;
         if (ok && P.cache != nullptr) {
           const int64_t row = P.row_map ? P.row_map[s] : s;
           if (row < 0 || row >= P.C) {
             report(P.status, DSPARK_ERR_BOUNDS);
             ok = false;
           } else {
-            off = (row * K + step) * static_cast<int64_t>(V);
+            coff = (row * K + step) * static_cast<int64_t>(V);
           }
         }
         if (ok) {
-          ri.valid = 1;
-          ri.prev = prev;
-          ri.temperature = P.temperature[s];
-          ri.seed = P.seeds[s];
-          ri.noise_pos = P.pos[b] + step - 1;
-          ri.cache_off = off;
+          prev = pv;
+          temp = P.temperature[s];
+          seed = P.seeds[s];
+          npos = P.pos[n] + step - 1;
+          boff = (static_cast<int64_t>(n) * K + step) * V;
+        } else {
+          coff = -1;
         }
       }
     }
-    info[b] = ri;
+    s_temp[n] = temp;
+    s_seed[n] = seed;
+    s_npos[n] = npos;
+    s_boff[n] = boff;
+    s_prev[n] = prev;
+    best[n] = 0ull;
+    my_prev = prev;
+    my_coff = coff;
   }
-  for (int n = tid; n < Npad; n += kThreadsTc) best[n] = 0ull;
+  (void)my_prev;
   if (tid == 0) {
     for (int i = 0; i < ns; ++i) {
       mbar_init(&full[i], 1);
@@ -184,13 +201,16 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
       const int n = c / per_row, rem = c % per_row;
       const int kc = rem >> 3, cc = rem & 7;
       uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (n < B && info[n].valid)
-        val = __ldg(reinterpret_cast<const uint4*>(P.w1 + static_cast<int64_t>(info[n].prev) * R +
-                                                   kc * 64) + cc);
+      const int32_t pv = s_prev[n];
+      if (pv >= 0)
+        val = __ldg(reinterpret_cast<const uint4*>(P.w1 + static_cast<int64_t>(pv) * R + kc * 64) +
+                    cc);
       *reinterpret_cast<uint4*>(e_base + static_cast<size_t>(kc) * Npad * 128 + n * 128 +
                                 ((cc ^ (n & 7)) << 4)) = val;
     }
   }
+  __syncthreads();
+  if (tid < Npad) s_coff[tid] = my_coff;  // s_prev (same storage) is no longer read
   fence_proxy_async_smem();
   tc::fence_before_thread_sync();
   __syncthreads();
@@ -273,98 +293,96 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
     }
   } else {
     // ---- epilogue -------------------------------------------------------------
-    // Warp (q, sub) owns TMEM lane quarter q (rows 32q..32q+31 of a tile) and
-    // the batch columns [sub * Npad/4, (sub + 1) * Npad/4), in chunks of 4.
-    const int q = warp & 3;
+    const int q = warp & 3;          // TMEM lane quarter: rows 32q..32q+31 of a tile
     const int sub = (warp - 2) >> 2;
-    const int cols = Npad >> 2;                 // a multiple of 4, at most 64
-    const int c_begin = sub * cols, c_end = c_begin + cols;
+    const int c_begin = sub * CPW;   // batch columns [c_begin, c_begin + CPW)
+    const int c_live = min(CPW, B - c_begin);  // columns below B (may be <= 0)
     const bool base_bf16 = P.base_bf16 != 0;
     const bool cache_bf16 = P.cache_bf16 != 0;
-    // running winner of column c_begin + 32*j + lane, j = 0, 1
-    unsigned long long run0 = 0ull, run1 = 0ull;
+    const float* base_f = static_cast<const float*>(P.base);
+    const uint16_t* base_h = static_cast<const uint16_t*>(P.base);
+    uint32_t run_ord[kRegWinners ? CPW : 1];
+    uint32_t run_v[kRegWinners ? CPW : 1];
+#pragma unroll
+    for (int j = 0; j < (kRegWinners ? CPW : 1); ++j) {
+      run_ord[j] = 0u;
+      run_v[j] = 0xFFFFFFFFu;
+    }
     for (int i = 0;; ++i) {
       const int t = blockIdx.x + i * G;
       if (t >= tiles) break;
       const int ab = i & 1;
       const uint32_t aph = (i >> 1) & 1;
+      const int v = t * kM + q * 32 + lane;
+      const bool in_range = v < V;
+      // base logits of the first chunk, issued before the accumulator wait
+      float bnext[4];
+      auto load_base = [&](int cb, float (&bv)[4]) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int64_t bo = s_boff[cb + jj];
+          bv[jj] = 0.f;
+          if (bo >= 0 && in_range)
+            bv[jj] = base_bf16 ? bf16_bits_to_float(__ldg(base_h + bo + v)) : __ldg(base_f + bo + v);
+        }
+      };
+      if (c_live > 0) load_base(c_begin, bnext);
       if (!mbar_wait(&acc_full[ab], aph, P.status)) {
         atomicExch(fail_flag, 1);
         break;
       }
       tc::fence_after_thread_sync();
-      const int v = t * kM + q * 32 + lane;
-      const bool in_range = v < V;
-      // base logits of the next chunk are loaded before the current chunk is
-      // processed
-      float bnext[4];
-      auto load_base = [&](int cb, float (&bv)[4]) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int b = cb + jj;
-          bv[jj] = 0.f;
-          if (b < B && in_range && info[b].valid)
-            bv[jj] = load_logit(P.base, base_bf16, (static_cast<int64_t>(b) * K + step) * V + v);
-        }
-      };
-      load_base(c_begin, bnext);
-      for (int cb = c_begin; cb < c_end; cb += 4) {
-        if (cb >= B) break;
+      for (int c = 0; c < CPW; c += 4) {
+        if (c >= c_live) break;
+        const int cb = c_begin + c;
         float bv[4] = {bnext[0], bnext[1], bnext[2], bnext[3]};
-        if (cb + 4 < c_end && cb + 4 < B) load_base(cb + 4, bnext);
+        if (c + 4 < c_live) load_base(cb + 4, bnext);
         uint32_t acc[4];
         tc::tmem_ld4(tmem + (static_cast<uint32_t>(q * 32) << 16) +
                          static_cast<uint32_t>(ab * Npad + cb),
                      acc);
         // Philox block of this lane quad's 4 columns, for request cb+(lane&3)
         const int bq = cb + (lane & 3);
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (bq < B) {
-          const U4 r = noise_block(info[bq].seed, info[bq].noise_pos, static_cast<uint32_t>(v),
-                                   kStreamDraft);
-          w[0] = r.x;
-          w[1] = r.y;
-          w[2] = r.z;
-          w[3] = r.w;
-        }
+        const U4 r = noise_block(s_seed[bq], s_npos[bq], static_cast<uint32_t>(v), kStreamDraft);
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
         uint32_t nw[4] = {0u, 0u, 0u, 0u};
         quad_transpose(w, nw);
+        const float4 T4 = *reinterpret_cast<const float4*>(s_temp + cb);
+        const float Ts[4] = {T4.x, T4.y, T4.z, T4.w};
         tc::tmem_wait_ld();
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
           const int b = cb + jb;
-          if (b >= B) break;
-          const ReqInfoTc& ri = info[b];
           uint32_t ord = 0u;
-          if (ri.valid && in_range) {
+          if (jb < c_live - c && s_boff[b] >= 0 && in_range) {
+            const float T = Ts[jb];
             const float z = __fadd_rn(bv[jb], __uint_as_float(acc[jb]));
             float x = z, y = z;
-            if (ri.temperature > 0.f) {
-              x = ri.temperature == 1.0f ? z : __fdiv_rn(z, ri.temperature);
+            if (T > 0.f) {
+              x = T == 1.0f ? z : __fdiv_rn(z, T);
               y = __fadd_rn(x, gumbel_of(nw[jb]));
             }
-            if (ri.cache_off >= 0) {
+            const int64_t co = s_coff[b];
+            if (co >= 0) {
               if (cache_bf16)
-                static_cast<uint16_t*>(P.cache)[ri.cache_off + v] = float_to_bf16_bits(x);
+                static_cast<uint16_t*>(P.cache)[co + v] = float_to_bf16_bits(x);
               else
-                static_cast<float*>(P.cache)[ri.cache_off + v] = x;
+                static_cast<float*>(P.cache)[co + v] = x;
             }
             ord = ordered_bits(y);  // every real value maps above 0
           }
-          // winner of this column over the warp's 32 rows: largest value,
-          // then lowest row
-          const uint32_t omax = __reduce_max_sync(0xFFFFFFFFu, ord);
-          const uint32_t cand = (ord == omax && ord != 0u) ? static_cast<uint32_t>(v) : 0xFFFFFFFFu;
-          const uint32_t vmin = __reduce_min_sync(0xFFFFFFFFu, cand);
-          if (omax != 0u) {
-            const unsigned long long key =
-                (static_cast<unsigned long long>(omax) << 32) | (0xFFFFFFFFu - vmin);
-            const int slot = b - c_begin;
-            if ((slot & 31) == lane) {
-              if (slot < 32)
-                run0 = umax64(run0, key);
-              else
-                run1 = umax64(run1, key);
+          if constexpr (kRegWinners) {
+            // rows of a lane only grow across tiles: a strict > keeps the
+            // lowest row on ties
+            if (ord > run_ord[c + jb]) {
+              run_ord[c + jb] = ord;
+              run_v[c + jb] = static_cast<uint32_t>(v);
+            }
+          } else {
+            if (jb < c_live - c) {
+              const unsigned long long key = warp_winner(ord, static_cast<uint32_t>(v));
+              if (lane == 0 && key != 0ull) atomicMax(&best[b], key);
             }
           }
         }
@@ -373,9 +391,15 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
-    if (lane < cols && c_begin + lane < B && run0) atomicMax(&best[c_begin + lane], run0);
-    if (lane + 32 < cols && c_begin + lane + 32 < B && run1)
-      atomicMax(&best[c_begin + lane + 32], run1);
+    if constexpr (kRegWinners) {
+#pragma unroll
+      for (int j = 0; j < CPW; ++j) {
+        if (j < c_live) {
+          const unsigned long long key = warp_winner(run_ord[j], run_v[j]);
+          if (lane == 0 && key != 0ull) atomicMax(&best[c_begin + j], key);
+        }
+      }
+    }
   }
 
   __syncthreads();
@@ -401,7 +425,7 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
     unsigned long long m = 0ull;
     const unsigned long long* row = P.partials + static_cast<int64_t>(b) * G;
     for (int g2 = 0; g2 < G; ++g2) m = umax64(m, __ldcg(row + g2));
-    const int32_t tok = (info[b].valid && m != 0ull) ? key_index(m) : -1;
+    const int32_t tok = (s_boff[b] >= 0 && m != 0ull) ? key_index(m) : -1;
     P.out_tokens[static_cast<int64_t>(b) * K + step] = tok;
   }
   if (tid == 0) *P.counter = 0u;
@@ -412,6 +436,18 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+template <int CPW>
+cudaError_t launch_tc_cpw(const MarkovStepParams& p, const CUtensorMap& map,
+                          const MarkovTcPlan& plan, int grid, cudaStream_t stream) {
+  cudaError_t err = cudaFuncSetAttribute(markov_step_tc_kernel<CPW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(plan.smem));
+  if (err != cudaSuccess) return err;
+  markov_step_tc_kernel<CPW><<<grid, kThreadsTc, plan.smem, stream>>>(map, p, plan.Npad,
+                                                                      plan.stages, plan.tmem_cols);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool markov_tc_plan(int B, int R, MarkovTcPlan* plan) {
@@ -420,7 +456,7 @@ bool markov_tc_plan(int B, int R, MarkovTcPlan* plan) {
   int Npad = (B + 15) & ~15;
   if (Npad < 16) Npad = 16;
   int ns = kMaxStages;
-  while (ns >= 2 && TcLayout(B, Npad, NK, ns).total > kSmemLimit) --ns;
+  while (ns >= 2 && TcLayout(Npad, NK, ns).total > kSmemLimit) --ns;
   if (ns < 2) return false;
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(2 * Npad)) cols <<= 1;
@@ -428,7 +464,7 @@ bool markov_tc_plan(int B, int R, MarkovTcPlan* plan) {
   plan->Npad = Npad;
   plan->stages = ns;
   plan->tmem_cols = cols;
-  plan->smem = TcLayout(B, Npad, NK, ns).total;
+  plan->smem = TcLayout(Npad, NK, ns).total;
   return true;
 }
 
@@ -460,32 +496,11 @@ int markov_tc_grid(int V, int num_sms) {
 cudaError_t launch_markov_step_tc(const MarkovStepParams& p, const void* tmap,
                                   const MarkovTcPlan& plan, int grid, cudaStream_t stream) {
   const CUtensorMap& map = *static_cast<const CUtensorMap*>(tmap);
-  const int nk = p.R / 64;
-  cudaError_t err = cudaSuccess;
-  switch (nk) {
-#define DSPARK_TC_CASE(N)                                                                  \
-  case N:                                                                                  \
-    err = cudaFuncSetAttribute(markov_step_tc_kernel<N>,                                   \
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,                \
-                               static_cast<int>(plan.smem));                               \
-    if (err != cudaSuccess) return err;                                                    \
-    markov_step_tc_kernel<N><<<grid, kThreadsTc, plan.smem, stream>>>(map, p, plan.Npad,   \
-                                                                      plan.stages,         \
-                                                                      plan.tmem_cols);     \
-    break;
-    DSPARK_TC_CASE(1)
-    DSPARK_TC_CASE(2)
-    DSPARK_TC_CASE(3)
-    DSPARK_TC_CASE(4)
-    DSPARK_TC_CASE(5)
-    DSPARK_TC_CASE(6)
-    DSPARK_TC_CASE(7)
-    DSPARK_TC_CASE(8)
-#undef DSPARK_TC_CASE
-    default:
-      return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  const int cpw = plan.Npad / 4;
+  if (cpw <= 4) return launch_tc_cpw<4>(p, map, plan, grid, stream);
+  if (cpw <= 8) return launch_tc_cpw<8>(p, map, plan, grid, stream);
+  if (cpw <= 16) return launch_tc_cpw<16>(p, map, plan, grid, stream);
+  return launch_tc_cpw<64>(p, map, plan, grid, stream);
 }
 
 }  // namespace dspark

@@ -54,20 +54,47 @@ struct ResSmem {
 };
 
 // p at column v of a target row from its statistics.
-__device__ __forceinline__ float p_at(const TgtStats& ts, float t, float T, int v) {
+// exp(x - m) of the row statistics (see exp_rel).
+__device__ __forceinline__ float exp_rel_fast(float x, float m) { return exp_rel(x, m); }
+
+// p at column v of a target row from its statistics (invD = 1 / D).
+__device__ __forceinline__ float p_fast(const TgtStats& ts, float t, float T, float invD, int v) {
   if (ts.mode == kModeOneHot) return v == 0 ? 1.0f : 0.0f;
   const float x = scale_logit(t, T);
   if (ts.mode == kModeThreshold) {
     const uint32_t kd = kd_of(x);
     if (!(kd > ts.kd_thr || (kd == ts.kd_thr && v <= ts.id_thr))) return 0.0f;
   }
-  return __fdiv_rn(exp_rel(x, ts.m), ts.D);
+  return exp_rel_fast(x, ts.m) * invD;
 }
 
-__device__ __forceinline__ float q_at(const DrfStats& ds, float c) {
+__device__ __forceinline__ float q_fast(const DrfStats& ds, float c, float invD) {
   if (ds.zero) return 0.0f;
   const float x = (c != c) ? -INFINITY : c;
-  return __fdiv_rn(exp_rel(x, ds.m), ds.D);
+  return exp_rel_fast(x, ds.m) * invD;
+}
+
+// Four consecutive logits [g, g+4) clipped to [.., c1), fp32 or bf16.
+__device__ __forceinline__ void load4(const void* base, bool bf16, int64_t off, int g, int c1,
+                                      bool vec, float (&out)[4]) {
+  if (vec && g + 3 < c1) {
+    if (bf16) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + off + g));
+      out[0] = __uint_as_float(raw.x << 16);
+      out[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+      out[2] = __uint_as_float(raw.y << 16);
+      out[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+    } else {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + off + g));
+      out[0] = f.x;
+      out[1] = f.y;
+      out[2] = f.z;
+      out[3] = f.w;
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) out[j] = g + j < c1 ? load_logit(base, bf16, off + g + j) : 0.0f;
 }
 
 // Winner key over columns [c0, c1) (c0 a multiple of 4) of the draw for
@@ -85,27 +112,33 @@ __device__ unsigned long long draw_chunk(const VerifyParams& P, const ResSmem& r
     ds = *(static_cast<const DrfStats*>(P.dstats) + static_cast<int64_t>(b) * K + k);
     coff = (rs.crow * K + k) * V;
   }
+  const float invD = 1.0f / ts.D;
+  const float invDq = ds.zero ? 0.0f : 1.0f / ds.D;
+  const bool tbf = P.target_bf16 != 0, cbf = P.cache_bf16 != 0;
+  // 4-element vector loads need 16-byte (fp32) or 8-byte (bf16) aligned rows
+  const bool tvec = ((reinterpret_cast<uintptr_t>(P.target) + toff * (tbf ? 2 : 4)) & (tbf ? 7u : 15u)) == 0;
+  const bool cvec = ((reinterpret_cast<uintptr_t>(P.cache) + coff * (cbf ? 2 : 4)) & (cbf ? 7u : 15u)) == 0;
   const int64_t npos = rs.P0 + k - 1;
   unsigned long long best = 0ull;
   unsigned int any = 0u;
   for (int g = c0 + 4 * threadIdx.x; g < c1; g += 4 * kResThreads) {
+    float t4[4], c4[4] = {0.f, 0.f, 0.f, 0.f};
+    load4(P.target, tbf, toff, g, c1, tvec, t4);
+    if (residual) load4(P.cache, cbf, coff, g, c1, cvec, c4);
     bool need = false;
     float w[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int v = g + j;
-      w[j] = 0.f;
-      if (v < c1) {
-        const float t = load_logit(P.target, P.target_bf16 != 0, toff + v);
-        float pv = p_at(ts, t, rs.T, v);
+      float pv = 0.0f;
+      if (g + j < c1) {
+        pv = p_fast(ts, t4[j], rs.T, invD, g + j);
         if (residual) {
-          const float c = load_logit(P.cache, P.cache_bf16 != 0, coff + v);
-          const float r = __fsub_rn(pv, q_at(ds, c));
+          const float r = __fsub_rn(pv, q_fast(ds, c4[j], invDq));
           pv = r > 0.0f ? r : 0.0f;
         }
-        w[j] = pv;
-        need |= pv > 0.0f;
       }
+      w[j] = pv;
+      need |= pv > 0.0f;
     }
     if (!need) continue;
     any = 1u;
@@ -114,7 +147,7 @@ __device__ unsigned long long draw_chunk(const VerifyParams& P, const ResSmem& r
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (w[j] > 0.0f) {
-        const float y = __fadd_rn(logf(w[j]), gumbel_of(words[j]));
+        const float y = __fadd_rn(ln_approx(w[j]), gumbel_of(words[j]));
         best = umax64(best, winner_key(y, static_cast<uint32_t>(g + j)));
       }
     }

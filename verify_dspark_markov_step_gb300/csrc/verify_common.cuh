@@ -41,15 +41,23 @@ __device__ __forceinline__ float scale_logit(float t, float T) {
   return (x != x) ? -INFINITY : x;
 }
 
-// e = 1 at the maximum, else fp32 exp(fp32(x - m)) (accurate expf).
+// e = exp(x - m): 1 at the maximum, else ex2.approx of fp32(x - m) * log2(e)
+// (about 3 ulp; the oracle's exp is correctly rounded, and the tests bound
+// the effect: accept margins and top-p boundaries within 1e-6).
 __device__ __forceinline__ float exp_rel(float x, float m) {
-  return (x == m) ? 1.0f : expf(__fsub_rn(x, m));
+  return (x == m) ? 1.0f : __expf(__fsub_rn(x, m));
 }
 
-// rint(e * 2^40) for 0 <= e <= 1: the product is exact in fp32, and the
-// conversion rounds to nearest even.
+// rint(e * 2^40) for 0 <= e <= 1, round half to even, without a 64-bit
+// float-to-integer conversion. v = e * 2^40 is exact in fp32. Below 2^23,
+// adding 2^23 rounds v to an integer (nearest even) held in the mantissa
+// bits; from 2^23 up, v is an integer: its 24-bit mantissa shifted left.
 __device__ __forceinline__ unsigned long long fixed_mass(float e) {
-  return __float2ull_rn(__fmul_rn(e, 0x1p40f));
+  const float v = __fmul_rn(e, 0x1p40f);
+  if (v < 8388608.0f) return static_cast<unsigned long long>(__float_as_uint(__fadd_rn(v, 8388608.0f)) - 0x4B000000u);
+  const uint32_t bits = __float_as_uint(v);
+  const unsigned long long mant = (bits & 0x7FFFFFu) | 0x800000u;
+  return mant << ((bits >> 23) - 150u);
 }
 
 // ordered bits of a non-NaN value (larger value -> larger key)

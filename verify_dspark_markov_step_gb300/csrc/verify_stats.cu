@@ -47,6 +47,7 @@ struct RowSmem {
   float redf[kRowWarps];
   // slots read by the other CTAs of the cluster
   float x_max;
+  int x_fail;
   int x_pos;
   unsigned long long x_key;
   unsigned long long x_sum;
@@ -61,7 +62,7 @@ struct RowSmem {
   unsigned long long found_before;
   unsigned long long bcast_u;
   float bcast_f;
-  int pad_[3];
+  int pad_[2];
 };
 
 struct Found {
@@ -118,16 +119,30 @@ __device__ unsigned long long block_max_u64(unsigned long long v, RowSmem& sm) {
 }
 
 // ---- cluster reductions of one value per CTA ---------------------------------
-__device__ float cluster_max_f(cg::cluster_group& cl, RowSmem& sm, float v, int CL) {
-  if (threadIdx.x == 0) sm.x_max = v;
+// Maximum over the cluster; *any_fail = some CTA passed fail = true.
+__device__ float cluster_max_f(cg::cluster_group& cl, RowSmem& sm, float v, bool fail, int CL,
+                               bool* any_fail) {
+  if (threadIdx.x == 0) {
+    sm.x_max = v;
+    sm.x_fail = fail ? 1 : 0;
+  }
   cl.sync();
   if (threadIdx.x < 32) {
     float m = -INFINITY;
-    if (static_cast<int>(threadIdx.x) < CL) m = *cl.map_shared_rank(&sm.x_max, threadIdx.x);
+    int f = 0;
+    if (static_cast<int>(threadIdx.x) < CL) {
+      m = *cl.map_shared_rank(&sm.x_max, threadIdx.x);
+      f = *cl.map_shared_rank(&sm.x_fail, threadIdx.x);
+    }
     m = warp_maxf(m);
-    if (threadIdx.x == 0) sm.bcast_f = m;
+    f = __reduce_or_sync(0xFFFFFFFFu, static_cast<unsigned>(f));
+    if (threadIdx.x == 0) {
+      sm.bcast_f = m;
+      sm.bcast_i = f;
+    }
   }
   __syncthreads();
+  *any_fail = sm.bcast_i != 0;
   return sm.bcast_f;
 }
 
@@ -157,84 +172,6 @@ __device__ unsigned long long cluster_max_u64(cg::cluster_group& cl, RowSmem& sm
   }
   __syncthreads();
   return sm.bcast_u;
-}
-
-// ---- slice loader: fn(local index, value) over [v0, v0 + n) of a row -----
-template <class Fn>
-__device__ __forceinline__ void slice_load(const void* row, bool bf16, int v0, int n,
-                                           uint64_t policy, Fn&& fn) {
-  const int tid = threadIdx.x;
-  if (!bf16) {
-    const float* r = static_cast<const float*>(row) + v0;
-    if ((reinterpret_cast<uintptr_t>(r) & 15u) == 0) {
-      const int n4 = n >> 2;
-      int i = tid;
-      for (; i + 3 * kRowThreads < n4; i += 4 * kRowThreads) {
-        float4 a[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] = ld_stream_f4(r + 4 * (i + u * kRowThreads), policy);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = 4 * (i + u * kRowThreads);
-          fn(j, a[u].x);
-          fn(j + 1, a[u].y);
-          fn(j + 2, a[u].z);
-          fn(j + 3, a[u].w);
-        }
-      }
-      for (; i < n4; i += kRowThreads) {
-        const float4 a = ld_stream_f4(r + 4 * i, policy);
-        fn(4 * i, a.x);
-        fn(4 * i + 1, a.y);
-        fn(4 * i + 2, a.z);
-        fn(4 * i + 3, a.w);
-      }
-      for (int j = 4 * n4 + tid; j < n; j += kRowThreads) fn(j, __ldg(r + j));
-    } else {
-      int j = tid;
-      for (; j + 3 * kRowThreads < n; j += 4 * kRowThreads) {
-        float a[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) a[u] = __ldg(r + j + u * kRowThreads);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) fn(j + u * kRowThreads, a[u]);
-      }
-      for (; j < n; j += kRowThreads) fn(j, __ldg(r + j));
-    }
-  } else {
-    const unsigned short* r = static_cast<const unsigned short*>(row) + v0;
-    if ((reinterpret_cast<uintptr_t>(r) & 15u) == 0) {
-      const int n8 = n >> 3;
-      int i = tid;
-      for (; i + kRowThreads < n8; i += 2 * kRowThreads) {
-        uint4 a[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) a[u] = __ldg(reinterpret_cast<const uint4*>(r) + i + u * kRowThreads);
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int j = 8 * (i + u * kRowThreads);
-          const uint32_t w4[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            fn(j + 2 * q, __uint_as_float(w4[q] << 16));
-            fn(j + 2 * q + 1, __uint_as_float(w4[q] & 0xFFFF0000u));
-          }
-        }
-      }
-      for (; i < n8; i += kRowThreads) {
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(r) + i);
-        const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          fn(8 * i + 2 * q, __uint_as_float(w4[q] << 16));
-          fn(8 * i + 2 * q + 1, __uint_as_float(w4[q] & 0xFFFF0000u));
-        }
-      }
-      for (int j = 8 * n8 + tid; j < n; j += kRowThreads) fn(j, bf16_bits_to_float(__ldg(r + j)));
-    } else {
-      for (int j = tid; j < n; j += kRowThreads) fn(j, bf16_bits_to_float(__ldg(r + j)));
-    }
-  }
 }
 
 // ---- histograms -------------------------------------------------------------
@@ -412,16 +349,16 @@ __device__ Found cluster_find(cg::cluster_group& cl, RowSmem& sm, int nb, bool d
 
 // One local histogram pass over the shared-memory slice: elements whose kd
 // and id pass `match` add their fixed-point mass to bin digit(kd, id).
-template <class Match, class Digit>
-__device__ void hist_pass(RowSmem& sm, const float* xs, int n, int v0, float m, int nb,
-                          Match match, Digit digit) {
+template <class Val, class Match, class Digit>
+__device__ void hist_pass(RowSmem& sm, Val xval, int n, int v0, float m, int nb, Match match,
+                          Digit digit) {
   hist_clear(sm, nb);
   __syncthreads();
   const int lane = threadIdx.x & 31;
   for (int base = threadIdx.x & ~31; base < n; base += kRowThreads) {
     const int i = base + lane;
     const bool valid = i < n;
-    const float x = valid ? xs[i] : -INFINITY;
+    const float x = valid ? xval(i) : -INFINITY;
     const uint32_t kd = kd_of(x);
     const uint32_t id = static_cast<uint32_t>(v0 + i);
     const bool act = valid && match(kd, id);
@@ -430,17 +367,47 @@ __device__ void hist_pass(RowSmem& sm, const float* xs, int n, int v0, float m, 
   }
 }
 
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParams P, int W) {
-  cg::cluster_group cl = cg::this_cluster();
-  const int CL = static_cast<int>(cl.num_blocks());
-  const int rank = static_cast<int>(cl.block_rank());
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
-  float* xs = reinterpret_cast<float*>(smem_raw + ((sizeof(RowSmem) + 15) & ~size_t(15)));
+// Loads the slice [v0, v0 + n) of a row into shared memory: one bulk copy of
+// the 16-byte-aligned body (issued by thread 0, completion on `bar`), plain
+// loads for a ragged tail or an unaligned row. fp32 rows land as fp32, bf16
+// rows as bf16 bit patterns. Returns false if the bounded wait ran out.
+__device__ bool slice_fetch(const void* row, bool bf16, int v0, int n, void* dst, uint64_t* bar,
+                            uint32_t& phase, int32_t* status) {
+  const int es = bf16 ? 2 : 4;
+  const unsigned char* src = static_cast<const unsigned char*>(row) + static_cast<size_t>(v0) * es;
+  const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+  const int body = aligned ? ((n * es) & ~15) / es : 0;  // elements moved by the bulk copy
+  if (body > 0 && threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(body * es));
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(static_cast<uint32_t>(body * es)), "r"(smem_addr(bar))
+        : "memory");
+  }
+  for (int j = body + threadIdx.x; j < n; j += kRowThreads) {
+    if (bf16)
+      static_cast<uint16_t*>(dst)[j] = __ldg(reinterpret_cast<const unsigned short*>(src) + j);
+    else
+      static_cast<float*>(dst)[j] = __ldg(reinterpret_cast<const float*>(src) + j);
+  }
+  bool ok = true;
+  if (body > 0) {
+    ok = mbar_wait(bar, phase, status);
+    phase ^= 1u;
+  }
+  __syncthreads();
+  return ok;
+}
+
+// One row: statistics written to P.tstats / P.dstats. Every CTA of the
+// cluster runs the same sequence of cluster barriers (all decisions depend on
+// the row or on cluster-reduced values only).
+__device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluster_group& cl,
+                            int CL, int rank, RowSmem& sm, float* xs, uint64_t* bar,
+                            uint32_t& phase) {
   const int tid = threadIdx.x;
   const int K = P.K, V = P.V;
-  const int row_id = blockIdx.x / CL;
   const int nT = P.B * (K + 1);
   int b, k;
   bool is_target;
@@ -454,8 +421,6 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
     k = r % K;
     is_target = false;
   }
-  // Decisions below depend only on the row, so a whole cluster returns
-  // together, before touching distributed shared memory.
   const int32_t s = P.rsi[b];
   if (s < 0 || s >= P.S) return;
   const float T = P.temperature[s];
@@ -481,18 +446,23 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
     row = bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(P.cache) + off)
                : static_cast<const void*>(static_cast<const float*>(P.cache) + off);
   }
-  const uint64_t pol = policy_evict_first();
   const int32_t d = k < K ? P.draft[static_cast<int64_t>(b) * K + k] : -1;
   TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(b) * (K + 1) + k;
   DrfStats* ds = static_cast<DrfStats*>(P.dstats) + static_cast<int64_t>(b) * K + (k < K ? k : 0);
+  const uint16_t* xh = reinterpret_cast<const uint16_t*>(xs);
+
+  // ---- the slice into shared memory (a previous row's readers are done) -------
+  fence_proxy_async_smem();
+  const bool fetched = slice_fetch(row, bf16, v0, n, xs, bar, phase, P.status);
 
   // ---- greedy target row: winner key of the raw row ----------------------------
   if (is_target && greedy) {
     unsigned long long key = 0ull;
-    slice_load(row, bf16, v0, n, pol, [&](int i, float t) {
+    for (int i = tid; i < n; i += kRowThreads) {
+      const float t = bf16 ? bf16_bits_to_float(xh[i]) : xs[i];
       key = umax64(key, winner_key(t, static_cast<uint32_t>(v0 + i)));
-    });
-    key = block_max_u64(key, sm);
+    }
+    key = block_max_u64(fetched ? key : 0ull, sm);
     key = cluster_max_u64(cl, sm, key, CL);
     if (rank == 0 && tid == 0) {
       ts->m = 0.f;
@@ -507,23 +477,35 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
     return;
   }
 
-  // ---- pass 1: HBM -> shared memory, maximum --------------------------------------
+  // ---- pass 1: scale in place (fp32) and maximum -----------------------------------
+  // bf16 slices stay as bit patterns; the passes widen them on the fly.
   float lmax = -INFINITY;
-  if (is_target) {
-    slice_load(row, bf16, v0, n, pol, [&](int i, float t) {
-      const float x = scale_logit(t, T);
-      xs[i] = x;
-      lmax = fmaxf(lmax, x);
-    });
+  if (bf16) {
+    for (int i = tid; i < n; i += kRowThreads) {
+      const float c = bf16_bits_to_float(xh[i]);
+      lmax = fmaxf(lmax, is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c));
+    }
   } else {
-    slice_load(row, bf16, v0, n, pol, [&](int i, float c) {
-      const float x = (c != c) ? -INFINITY : c;
-      xs[i] = x;
+    for (int i = tid; i < n; i += kRowThreads) {
+      const float c = xs[i];
+      const float x = is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c);
+      if (__float_as_uint(x) != __float_as_uint(c)) xs[i] = x;
       lmax = fmaxf(lmax, x);
-    });
+    }
   }
   lmax = block_max_f(lmax, sm);
-  const float m = cluster_max_f(cl, sm, lmax, CL);
+  // a timed-out copy drops the row for the whole cluster (status is set)
+  bool any_fail = false;
+  const float m = cluster_max_f(cl, sm, lmax, !fetched, CL, &any_fail);
+  if (any_fail) {
+    cl.sync();
+    return;
+  }
+  auto xval = [&](int i) -> float {
+    if (!bf16) return xs[i];
+    const float c = bf16_bits_to_float(xh[i]);
+    return is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c);
+  };
   if (m == -INFINITY) {
     if (rank == 0 && tid == 0) {
       if (is_target) {
@@ -550,16 +532,26 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
   if (topp) hist_clear(sm, kRowBins);
   __syncthreads();
   unsigned long long F = 0ull;
-  {
+  if (topp) {
     const int lane = tid & 31;
     for (int base = tid & ~31; base < n; base += kRowThreads) {
       const int i = base + lane;
       const bool valid = i < n;
-      const float x = valid ? xs[i] : -INFINITY;
+      const float x = valid ? xval(i) : -INFINITY;
       const unsigned long long f = valid ? fixed_mass(exp_rel(x, m)) : 0ull;
       F += f;
-      if (topp) hist_add(sm, valid, static_cast<int>(kd_of(x) >> 21), f, static_cast<uint32_t>(v0 + i));
+      hist_add(sm, valid, static_cast<int>(kd_of(x) >> 21), f, static_cast<uint32_t>(v0 + i));
     }
+  } else if (!bf16) {
+    const int n4 = n >> 2;
+    for (int i = tid; i < n4; i += kRowThreads) {
+      const float4 x4 = reinterpret_cast<const float4*>(xs)[i];
+      F += fixed_mass(exp_rel(x4.x, m)) + fixed_mass(exp_rel(x4.y, m)) +
+           fixed_mass(exp_rel(x4.z, m)) + fixed_mass(exp_rel(x4.w, m));
+    }
+    for (int i = 4 * n4 + tid; i < n; i += kRowThreads) F += fixed_mass(exp_rel(xs[i], m));
+  } else {
+    for (int i = tid; i < n; i += kRowThreads) F += fixed_mass(exp_rel(xval(i), m));
   }
   F = block_sum_u64(F, sm);
   F = cluster_sum_u64(cl, sm, F, CL);
@@ -585,7 +577,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
     }
     if (!resolved) {  // kd stage 1: bits [20:10]
       const uint32_t p0 = pre;
-      hist_pass(sm, xs, n, v0, m, kRowBins, [=](uint32_t kd, uint32_t) { return (kd >> 21) == p0; },
+      hist_pass(sm, xval, n, v0, m, kRowBins, [=](uint32_t kd, uint32_t) { return (kd >> 21) == p0; },
                 [](uint32_t kd, uint32_t) { return static_cast<int>((kd >> 10) & 0x7FFu); });
       f = cluster_find(cl, sm, kRowBins, true, above, t_hi, t_lo, CL, rank);
       above = f.before;
@@ -598,7 +590,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
     }
     if (!resolved) {  // kd stage 2: bits [9:0]
       const uint32_t p1 = pre;
-      hist_pass(sm, xs, n, v0, m, 1024, [=](uint32_t kd, uint32_t) { return (kd >> 10) == p1; },
+      hist_pass(sm, xval, n, v0, m, 1024, [=](uint32_t kd, uint32_t) { return (kd >> 10) == p1; },
                 [](uint32_t kd, uint32_t) { return static_cast<int>(kd & 0x3FFu); });
       f = cluster_find(cl, sm, 1024, true, above, t_hi, t_lo, CL, rank);
       above = f.before;
@@ -613,7 +605,15 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
       // full kd of the boundary element, read from the CTA that holds it
       if (tid == 0) {
         const int owner = id_thr / W;
-        const float xb = *cl.map_shared_rank(xs + (id_thr - owner * W), owner);
+        const int li = id_thr - owner * W;
+        float xb;
+        if (bf16) {
+          const float c = bf16_bits_to_float(
+              *cl.map_shared_rank(const_cast<uint16_t*>(xh) + li, owner));
+          xb = scale_logit(c, T);
+        } else {
+          xb = *cl.map_shared_rank(xs + li, owner);
+        }
         sm.bcast_i = static_cast<int>(kd_of(xb));
       }
       __syncthreads();
@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
       // exact ties at the boundary value: token id ascending, 11 + 11 bits
       kd_thr = pre;
       const uint32_t kt = kd_thr;
-      hist_pass(sm, xs, n, v0, m, kRowBins, [=](uint32_t kd, uint32_t) { return kd == kt; },
+      hist_pass(sm, xval, n, v0, m, kRowBins, [=](uint32_t kd, uint32_t) { return kd == kt; },
                 [](uint32_t, uint32_t id) { return static_cast<int>((id >> 11) & 0x7FFu); });
       f = cluster_find(cl, sm, kRowBins, false, above, t_hi, t_lo, CL, rank);
       above = f.before;
@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
         Fk = above + f.mass;
       } else {
         const uint32_t ip = static_cast<uint32_t>(f.bin);
-        hist_pass(sm, xs, n, v0, m, kRowBins,
+        hist_pass(sm, xval, n, v0, m, kRowBins,
                   [=](uint32_t kd, uint32_t id) { return kd == kt && (id >> 11) == ip; },
                   [](uint32_t, uint32_t id) { return static_cast<int>(id & 0x7FFu); });
         f = cluster_find(cl, sm, kRowBins, false, above, t_hi, t_lo, CL, rank);
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
 
   // ---- outputs: p or q at the drafted token (its owner), the rest (rank 0) ---------
   if (tid == 0 && d >= v0 && d < v0 + n) {
-    const float x = xs[d - v0];
+    const float x = xval(d - v0);
     if (is_target) {
       const uint32_t kd = kd_of(x);
       const bool keep = mode == kModeKeepAll || kd > kd_thr || (kd == kd_thr && d <= id_thr);
@@ -670,7 +670,30 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
       if (!(d >= 0 && d < V)) ds->q_d = 0.0f;
     }
   }
-  cl.sync();  // no CTA leaves while another may still read its shared memory
+  cl.sync();  // no CTA reuses its slice or slots while another may still read them
+}
+
+// ---------------------------------------------------------------------------
+// Persistent clusters: cluster c handles rows c, c + nclusters, ...
+__global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParams P, int W,
+                                                                     int nrows) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int CL = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int cid = blockIdx.x / CL;
+  const int nclusters = gridDim.x / CL;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
+  float* xs = reinterpret_cast<float*>(smem_raw + ((sizeof(RowSmem) + 15) & ~size_t(15)));
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  for (int row = cid; row < nrows; row += nclusters)
+    process_row(P, W, row, cl, CL, rank, sm, xs, &bar, phase);
 }
 
 }  // namespace
@@ -708,7 +731,6 @@ cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_
     if (err != cudaSuccess) return err;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(rows * CL), 1, 1);
   cfg.blockDim = dim3(kRowThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -719,7 +741,17 @@ cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, verify_rows_kernel, p, W);
+  // as many clusters as fit on the GPU at once, each looping over rows
+  cfg.gridDim = dim3(static_cast<unsigned>(rows * CL), 1, 1);
+  int max_clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, verify_rows_kernel, &cfg) != cudaSuccess ||
+      max_clusters < 1) {
+    (void)cudaGetLastError();
+    max_clusters = 1;
+  }
+  const int nclusters = rows < max_clusters ? rows : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
+  return cudaLaunchKernelEx(&cfg, verify_rows_kernel, p, W, rows);
 }
 
 }  // namespace dspark
