@@ -52,7 +52,7 @@ def test_odd_vocab_nan_and_temperatures():
     (3, 2, 2048, 512, {"temperature": [0.9, 1.1, 1.0]}),
     (6, 3, 5000, 64, {"base_bf16": True, "cache_bf16": True,
                       "temperature": [0.6, 1.0, 1.4, 0.0, 1.0, 0.8]}),
-    # batches of 8 and more run the bias projection on the tensor cores
+    # larger batches: more N columns per MMA, more epilogue columns per warp
     (8, 2, 129, 64, {}),
     (16, 3, 2053, 128, {"temperature": [0.0, 0.5, 1.0, 1.5] * 4}),
     (33, 2, 4100, 256, {"temperature": 0.9}),

@@ -12,8 +12,6 @@ namespace {
 
 constexpr size_t kAlign = 256;
 
-// Batches from this size on run the bias projection on the tensor cores.
-constexpr int kTensorCoreMinBatch = 8;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -35,7 +33,7 @@ struct MarkovWs {
     counter = 0;
     partials = align_up(counter + sizeof(unsigned int));
     total = align_up(partials + static_cast<size_t>(B) *
-                                    dspark::markov_simt_max_grid(V) * sizeof(unsigned long long));
+                                    dspark::markov_tc_max_grid(V) * sizeof(unsigned long long));
   }
 };
 
@@ -118,25 +116,23 @@ dspark_status dspark_markov_sample(
   p.status = status;
   if (cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), st) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  // Tensor cores once the batch makes the bias projection a real contraction.
   dspark::MarkovTcPlan plan;
   alignas(64) unsigned char tmap[128];
-  const bool use_tc = B >= kTensorCoreMinBatch && dspark::markov_tc_plan(B, R, &plan) &&
-                      dspark::markov_tc_make_tmap(tmap, markov_w2, V, R) == 0;
-  if (use_tc) {
-    const int grid = dspark::markov_tc_grid(V, sms);
-    for (int i = 0; i < K; ++i) {
-      p.step = i;
-      if (dspark::launch_markov_step_tc(p, tmap, plan, grid, st) != cudaSuccess)
-        return DSPARK_ERR_CUDA;
-    }
-    return DSPARK_OK;
-  }
-  if (dspark::markov_simt_smem_bytes(B, R) > 227u * 1024u) return DSPARK_ERR_UNSUPPORTED;
-  const int grid = dspark::markov_simt_grid(B, V, R, sms);
+  alignas(64) unsigned char bmap[128] = {};
+  const int es = base_dtype == DSPARK_BF16 ? 2 : 4;
+  // TMA can stage the base logits when their rows are 16-byte multiples
+  const bool base_tma = (static_cast<size_t>(V) * es) % 16 == 0;
+  if (!dspark::markov_tc_plan(B, R, es, base_tma, &plan)) return DSPARK_ERR_UNSUPPORTED;
+  if (dspark::markov_tc_make_tmap(tmap, markov_w2, V, R) != 0) return DSPARK_ERR_CUDA;
+  if (plan.base_stage_bytes != 0 &&
+      dspark::markov_tc_make_base_tmap(bmap, base_logits, es == 2, B, K, V) != 0 &&
+      !dspark::markov_tc_plan(B, R, es, false, &plan))
+    return DSPARK_ERR_UNSUPPORTED;
+  const int grid = dspark::markov_tc_grid(V, sms);
   for (int i = 0; i < K; ++i) {
     p.step = i;
-    if (dspark::launch_markov_step_simt(p, grid, st) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (dspark::launch_markov_step_tc(p, tmap, bmap, plan, grid, st) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
   }
   return DSPARK_OK;
 }
@@ -162,13 +158,13 @@ dspark_status dspark_rejection_sample(
   if (draft_cache && C < 1) return DSPARK_ERR_INVALID_ARG;
   if (!aligned16(target_logits) || (draft_cache && !aligned16(draft_cache)))
     return DSPARK_ERR_ALIGNMENT;
-  int cluster = 0, slice = 0;
-  if (!dspark::verify_rows_plan(V, &cluster, &slice)) return DSPARK_ERR_UNSUPPORTED;
   const VerifyWs ws(B, K, V);
   if (!workspace || workspace_bytes < ws.total || !aligned16(workspace))
     return DSPARK_ERR_WORKSPACE;
   int sms = 0;
   if (num_sms_of_current_device(&sms) != 0) return DSPARK_ERR_CUDA;
+  int cluster = 0, slice = 0;
+  if (!dspark::verify_rows_plan(V, &cluster, &slice)) return DSPARK_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   unsigned char* w = static_cast<unsigned char*>(workspace);
   dspark::VerifyParams p;

@@ -1,5 +1,5 @@
 // kernels.h -- launch interface between the C-ABI layer (api.cu) and the
-// kernels (markov_step.cu, markov_tc.cu, verify.cu). Internal to the library.
+// kernels (markov_tc.cu, verify_stats.cu, verify.cu). Internal to the library.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -8,7 +8,7 @@
 
 namespace dspark {
 
-// One Markov step: parameters shared by both Markov-step variants.
+// One Markov step.
 struct MarkovStepParams {
   const void* base;
   int base_bf16;
@@ -30,24 +30,20 @@ struct MarkovStepParams {
   int32_t* status;
 };
 
-// CUDA-core variant (markov_step.cu).
-size_t markov_simt_smem_bytes(int B, int R);
-int markov_simt_grid(int B, int V, int R, int num_sms);
-int markov_simt_max_grid(int V);
-cudaError_t launch_markov_step_simt(const MarkovStepParams& p, int grid,
-                                    cudaStream_t stream);
-
 // Tensor-core variant (markov_tc.cu).
 struct MarkovTcPlan {
   int Npad;            // batch padded to a multiple of 16 (UMMA N)
   int stages;          // shared-memory ring stages of 16 KB
   unsigned tmem_cols;  // TMEM columns allocated (two accumulator buffers)
+  unsigned base_stage_bytes;  // staged base tile bytes (0: base read directly)
   size_t smem;         // dynamic shared memory bytes
 };
-bool markov_tc_plan(int B, int R, MarkovTcPlan* plan);
+bool markov_tc_plan(int B, int R, int base_elem_bytes, bool base_tma_ok, MarkovTcPlan* plan);
 int markov_tc_make_tmap(void* tmap_out /* 128-byte CUtensorMap */, const void* w2, int V, int R);
+int markov_tc_make_base_tmap(void* tmap_out, const void* base, bool bf16, int B, int K, int V);
 int markov_tc_grid(int V, int num_sms);
-cudaError_t launch_markov_step_tc(const MarkovStepParams& p, const void* tmap,
+int markov_tc_max_grid(int V);  // upper bound of markov_tc_grid over devices
+cudaError_t launch_markov_step_tc(const MarkovStepParams& p, const void* tmap, const void* bmap,
                                   const MarkovTcPlan& plan, int grid, cudaStream_t stream);
 
 // Verification (verify.cu).

@@ -1,26 +1,37 @@
 // markov_tc.cu -- one Markov step on the 5th-generation tensor cores.
 //
-// Same operation as markov_step.cu (the "DSparkSpeculator" page's
-// _sample_markov_chain / _sample_logits; vLLM PR #65007 Part 1, per-step
-// list), for batches where the bias projection [B, R] x [R, V] is a real
-// dense contraction. markov_w2 rows are the M side of a tcgen05 MMA
+// The "DSparkSpeculator" page's _sample_markov_chain / _sample_logits and
+// vLLM PR #65007 Part 1 (per-step list): Markov embedding of the previous
+// token, the markov_w2 bias projection, bias add, temperature, Gumbel noise
+// keyed by (seed, position - 1, column), the block-argmax winner rule and the
+// draft-logits cache store, fused into one kernel per step.
+//
+// The bias projection [B, R] x [R, V] runs on the tensor cores for every
+// batch size: the step is bound by streaming markov_w2 and by the epilogue's
+// ALU work, and the MMA takes the B * R multiply-adds per column off the
+// epilogue warps (for small B the padding of N to 16 costs nothing).
+// markov_w2 rows are the M side of a tcgen05 MMA
 // (M = 128 vocabulary rows per tile, K = markov_rank), the Markov embeddings
 // of the batch are the N side (N = batch padded to a multiple of 16), and the
 // fp32 accumulator lives in tensor memory.
 //
 // Persistent, warp-specialised CTA (one per SM):
 //   warp 0      TMA producer: 128x64 bf16 boxes of markov_w2 (128-byte
-//               swizzle) into a ring of shared-memory stages, L2 evict-last
+//               swizzle) into a ring of shared-memory stages, L2 evict-last;
+//               and, per tile, the tile's base logits of every request (a
+//               128 x 1 x B box of the [B, K, V] tensor) into one of two slots
 //   warp 1      TMEM allocation; one thread issues the MMAs (4 per 64-wide K
 //               chunk) into one of two accumulator buffers and commits
 //   warps 2-17  epilogue: warp (q, sub) owns TMEM lane quarter q (32 rows of
 //               each tile) and a fixed set of CPW batch columns. Per chunk of
-//               4 columns: tcgen05.ld, bias add, temperature, Gumbel noise
-//               (one Philox block per lane quad, shared by a 4x4 shuffle
-//               transpose), cache store, and the running winner of each
+//               4 columns: tcgen05.ld, bias add, temperature (x = z * (1/T),
+//               within 1.5 ulp of z / T), Gumbel noise (one Philox block per
+//               lane quad, shared by a 4x4 butterfly transpose), cache store,
+//               and the running winner of each
 //               column -- per lane in registers across tiles when CPW <= 16,
 //               else reduced per tile with redux.sync.
-// The per-CTA winners are reduced by the last CTA, as in markov_step.cu.
+// The per-CTA winners go to the workspace; the last CTA to finish reduces
+// them per request and writes the step's tokens.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -42,42 +53,60 @@ constexpr size_t kSmemLimit = 227u * 1024u;
 
 // Per-request data of one step, structure of arrays (Npad entries each).
 struct TcLayout {
-  size_t a, e, temp, seed, npos, boff, coff, best, bars, slot, flags, total;
-  __host__ __device__ TcLayout(int Npad, int NK, int ns) {
+  size_t a, e, bases, temp, seed, npos, boff, coff, best, bars, slot, flags, total;
+  // base_stage: bytes of one staged base tile (0 = base logits read directly)
+  __host__ __device__ TcLayout(int Npad, int NK, int ns, size_t base_stage) {
     a = 0;
     e = a + static_cast<size_t>(ns) * kStageBytes;
-    temp = e + static_cast<size_t>(NK) * Npad * 128;
+    bases = e + static_cast<size_t>(NK) * Npad * 128;
+    temp = bases + 2 * ((base_stage + 1023) & ~size_t(1023));
     seed = temp + static_cast<size_t>(Npad) * 4;
     npos = seed + static_cast<size_t>(Npad) * 8;
     boff = npos + static_cast<size_t>(Npad) * 8;
     coff = boff + static_cast<size_t>(Npad) * 8;
     best = coff + static_cast<size_t>(Npad) * 8;
     bars = best + static_cast<size_t>(Npad) * 8;
-    slot = bars + static_cast<size_t>(2 * ns + 5) * 8;
+    slot = bars + static_cast<size_t>(2 * ns + 7) * 8;
     flags = slot + 8;
     total = flags + 8 + kMaxStages * 4 + 1024;  // + slack to align the base to 1024 B
   }
 };
 
-__device__ __forceinline__ uint32_t sel4(const uint32_t (&w)[4], uint32_t i) {
-  return i == 0 ? w[0] : (i == 1 ? w[1] : (i == 2 ? w[2] : w[3]));
-}
-
 // Lanes 4j..4j+3 each hold the four Philox words of request b0 + (lane & 3)
-// for the same 4-column block. Afterwards out[r] = word (lane & 3) of
-// request b0 + r, i.e. the noise of this lane's own column for request b0+r.
-__device__ __forceinline__ void quad_transpose(const uint32_t (&w)[4], uint32_t (&out)[4]) {
+// for the same 4-column block (a 4x4 matrix, one row per lane). A two-round
+// butterfly transposes it: afterwards w[r] = word (lane & 3) of request
+// b0 + r, i.e. the noise of this lane's own column for request b0 + r.
+__device__ __forceinline__ void quad_transpose(uint32_t (&w)[4]) {
   const uint32_t c = threadIdx.x & 3u;
-  const int quad = static_cast<int>(threadIdx.x & 31u) & ~3;
-#pragma unroll
-  for (uint32_t r = 0; r < 4; ++r) {
-    const uint32_t src = (c + r) & 3u;
-    const uint32_t send = (c - r) & 3u;
-    const uint32_t v = __shfl_sync(0xFFFFFFFFu, sel4(w, send), quad + static_cast<int>(src));
-    out[0] = src == 0 ? v : out[0];
-    out[1] = src == 1 ? v : out[1];
-    out[2] = src == 2 ? v : out[2];
-    out[3] = src == 3 ? v : out[3];
+  // round 1 (lanes c, c^2): the upper lane takes the lower lane's words 2,3
+  {
+    const bool up = (c & 2u) != 0u;
+    const uint32_t s0 = up ? w[0] : w[2];
+    const uint32_t s1 = up ? w[1] : w[3];
+    const uint32_t r0 = __shfl_xor_sync(0xFFFFFFFFu, s0, 2);
+    const uint32_t r1 = __shfl_xor_sync(0xFFFFFFFFu, s1, 2);
+    if (up) {
+      w[0] = r0;
+      w[1] = r1;
+    } else {
+      w[2] = r0;
+      w[3] = r1;
+    }
+  }
+  // round 2 (lanes c, c^1)
+  {
+    const bool odd = (c & 1u) != 0u;
+    const uint32_t s0 = odd ? w[0] : w[1];
+    const uint32_t s1 = odd ? w[2] : w[3];
+    const uint32_t r0 = __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+    const uint32_t r1 = __shfl_xor_sync(0xFFFFFFFFu, s1, 1);
+    if (odd) {
+      w[0] = r0;
+      w[2] = r1;
+    } else {
+      w[1] = r0;
+      w[3] = r1;
+    }
   }
 }
 
@@ -92,17 +121,21 @@ __device__ __forceinline__ unsigned long long warp_winner(uint32_t ord, uint32_t
 
 template <int CPW>  // batch columns per epilogue warp (Npad / 4)
 __global__ void __launch_bounds__(kThreadsTc, 1)
-markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepParams P, int Npad,
-                      int ns, uint32_t tmem_cols) {
+markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
+                      const __grid_constant__ CUtensorMap tmap_base, MarkovStepParams P, int Npad,
+                      int ns, uint32_t tmem_cols, uint32_t base_stage_bytes) {
   constexpr bool kRegWinners = CPW <= 16;
   const int R = P.R;
   const int NK = R / 64;
+  const bool tma_base = base_stage_bytes != 0u;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  const TcLayout L(Npad, NK, ns);
+  const TcLayout L(Npad, NK, ns, base_stage_bytes);
   unsigned char* a_base = smem + L.a;
   unsigned char* e_base = smem + L.e;
-  float* s_temp = reinterpret_cast<float*>(smem + L.temp);
+  unsigned char* base_s = smem + L.bases;  // two staged base tiles [B][128]
+  const size_t base_stride = (static_cast<size_t>(base_stage_bytes) + 1023) & ~size_t(1023);
+  float* s_temp = reinterpret_cast<float*>(smem + L.temp);      // 1/T (0: greedy)
   uint64_t* s_seed = reinterpret_cast<uint64_t*>(smem + L.seed);
   int64_t* s_npos = reinterpret_cast<int64_t*>(smem + L.npos);
   int64_t* s_boff = reinterpret_cast<int64_t*>(smem + L.boff);   // -1: inert column
@@ -114,6 +147,7 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
   uint64_t* acc_full = empty + ns;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
+  uint64_t* base_full = drain + 1;     // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.slot);
   int* fail_flag = reinterpret_cast<int*>(smem + L.flags);
   uint32_t* issued = reinterpret_cast<uint32_t*>(smem + L.flags + 8);  // last parity per stage
@@ -161,7 +195,7 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
         }
       }
     }
-    s_temp[n] = temp;
+    s_temp[n] = temp > 0.f ? __frcp_rn(temp) : 0.f;  // 1/T; 0 marks a greedy column
     s_seed[n] = seed;
     s_npos[n] = npos;
     s_boff[n] = boff;
@@ -181,10 +215,13 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
     mbar_init(&acc_empty[0], kEpiWarps);
     mbar_init(&acc_empty[1], kEpiWarps);
     mbar_init(drain, 1);
+    mbar_init(&base_full[0], 1);
+    mbar_init(&base_full[1], 1);
     for (int i = 0; i < kMaxStages; ++i) issued[i] = 0xFFFFFFFFu;
     *fail_flag = 0;
     fence_mbar_init();
     tc::prefetch_tensormap(&tmap_w2);
+    if (tma_base) tc::prefetch_tensormap(&tmap_base);
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, tmem_cols);
@@ -221,12 +258,26 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
     // ---- TMA producer -----------------------------------------------------------
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
+      const uint64_t pol_stream = policy_evict_first();
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
+      uint32_t base_par[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // parity of the last copy per slot
       for (int i = 0; ok; ++i) {
         const int t = blockIdx.x + i * G;
         if (t >= tiles) break;
+        if (tma_base) {
+          // base slot i&1 is free once the epilogue released tile i-2
+          const int bs = i & 1;
+          if (!mbar_wait(&acc_empty[bs], ((i >> 1) & 1) ^ 1u, P.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&base_full[bs], base_stage_bytes);
+          tc::tma_load_3d(base_s + bs * base_stride, &tmap_base, t * kM, step, 0, &base_full[bs],
+                          pol_stream);
+          base_par[bs] = (i >> 1) & 1;
+        }
         for (int kc = 0; kc < NK; ++kc) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, P.status)) {
             ok = false;
@@ -246,6 +297,8 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
       // every copy this CTA issued has landed before the CTA may exit
       for (int s2 = 0; s2 < ns; ++s2)
         if (issued[s2] != 0xFFFFFFFFu) (void)mbar_wait(&full[s2], issued[s2], P.status);
+      for (int bs = 0; bs < 2; ++bs)
+        if (base_par[bs] != 0xFFFFFFFFu) (void)mbar_wait(&base_full[bs], base_par[bs], P.status);
     }
   } else if (warp == 1) {
     // ---- MMA issuer -------------------------------------------------------------
@@ -301,6 +354,8 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
     const bool cache_bf16 = P.cache_bf16 != 0;
     const float* base_f = static_cast<const float*>(P.base);
     const uint16_t* base_h = static_cast<const uint16_t*>(P.base);
+    float* cache_f = static_cast<float*>(P.cache);
+    uint16_t* cache_h = static_cast<uint16_t*>(P.cache);
     uint32_t run_ord[kRegWinners ? CPW : 1];
     uint32_t run_v[kRegWinners ? CPW : 1];
 #pragma unroll
@@ -308,6 +363,26 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
       run_ord[j] = 0u;
       run_v[j] = 0xFFFFFFFFu;
     }
+    auto load_base = [&](int cb, int v, bool in_range, float (&bv)[4]) {
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int64_t bo = s_boff[cb + jj];  // warp-uniform
+        bv[jj] = 0.f;
+        if (bo >= 0 && in_range)
+          bv[jj] = base_bf16 ? bf16_bits_to_float(__ldg(base_h + bo + v)) : __ldg(base_f + bo + v);
+      }
+    };
+    // staged tile: element (b, row r) of slot ab at b * 128 + r
+    auto smem_base = [&](int ab, int cb, int r, float (&bv)[4]) {
+      const unsigned char* sb = base_s + ab * base_stride;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int b = cb + jj;
+        bv[jj] = b < B ? (base_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sb)[b * kM + r])
+                                    : reinterpret_cast<const float*>(sb)[b * kM + r])
+                       : 0.f;
+      }
+    };
     for (int i = 0;; ++i) {
       const int t = blockIdx.x + i * G;
       if (t >= tiles) break;
@@ -317,60 +392,61 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
       const bool in_range = v < V;
       // base logits of the first chunk, issued before the accumulator wait
       float bnext[4];
-      auto load_base = [&](int cb, float (&bv)[4]) {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int64_t bo = s_boff[cb + jj];
-          bv[jj] = 0.f;
-          if (bo >= 0 && in_range)
-            bv[jj] = base_bf16 ? bf16_bits_to_float(__ldg(base_h + bo + v)) : __ldg(base_f + bo + v);
-        }
-      };
-      if (c_live > 0) load_base(c_begin, bnext);
+      if (!tma_base && c_live > 0) load_base(c_begin, v, in_range, bnext);
       if (!mbar_wait(&acc_full[ab], aph, P.status)) {
         atomicExch(fail_flag, 1);
         break;
       }
+      if (tma_base && !mbar_wait(&base_full[ab], aph, P.status)) {
+        atomicExch(fail_flag, 1);
+        break;
+      }
       tc::fence_after_thread_sync();
+      if (tma_base && c_live > 0) smem_base(ab, c_begin, q * 32 + lane, bnext);
 #pragma unroll
       for (int c = 0; c < CPW; c += 4) {
         if (c >= c_live) break;
         const int cb = c_begin + c;
-        float bv[4] = {bnext[0], bnext[1], bnext[2], bnext[3]};
-        if (c + 4 < c_live) load_base(cb + 4, bnext);
+        const float bv[4] = {bnext[0], bnext[1], bnext[2], bnext[3]};
+        if (c + 4 < c_live) {
+          if (tma_base)
+            smem_base(ab, cb + 4, q * 32 + lane, bnext);
+          else
+            load_base(cb + 4, v, in_range, bnext);
+        }
         uint32_t acc[4];
         tc::tmem_ld4(tmem + (static_cast<uint32_t>(q * 32) << 16) +
                          static_cast<uint32_t>(ab * Npad + cb),
                      acc);
-        // Philox block of this lane quad's 4 columns, for request cb+(lane&3)
+        // Philox block of this lane quad's 4 columns, for request cb+(lane&3),
+        // transposed so that nw[r] is this lane's noise for request cb+r
         const int bq = cb + (lane & 3);
         const U4 r = noise_block(s_seed[bq], s_npos[bq], static_cast<uint32_t>(v), kStreamDraft);
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-        uint32_t nw[4] = {0u, 0u, 0u, 0u};
-        quad_transpose(w, nw);
-        const float4 T4 = *reinterpret_cast<const float4*>(s_temp + cb);
-        const float Ts[4] = {T4.x, T4.y, T4.z, T4.w};
+        uint32_t nw[4] = {r.x, r.y, r.z, r.w};
+        quad_transpose(nw);
+        const float4 ti4 = *reinterpret_cast<const float4*>(s_temp + cb);
+        const float tinv[4] = {ti4.x, ti4.y, ti4.z, ti4.w};
         tc::tmem_wait_ld();
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
+          if (jb >= c_live - c) break;  // warp-uniform
           const int b = cb + jb;
+          const int64_t co = s_coff[b];  // warp-uniform
           uint32_t ord = 0u;
-          if (jb < c_live - c && s_boff[b] >= 0 && in_range) {
-            const float T = Ts[jb];
+          if (s_boff[b] >= 0) {  // warp-uniform: a live request
             const float z = __fadd_rn(bv[jb], __uint_as_float(acc[jb]));
             float x = z, y = z;
-            if (T > 0.f) {
-              x = T == 1.0f ? z : __fdiv_rn(z, T);
+            if (tinv[jb] > 0.f) {  // warp-uniform: sampled (x = z * (1/T))
+              x = __fmul_rn(z, tinv[jb]);
               y = __fadd_rn(x, gumbel_of(nw[jb]));
             }
-            const int64_t co = s_coff[b];
-            if (co >= 0) {
+            if (co >= 0 && in_range) {
               if (cache_bf16)
-                static_cast<uint16_t*>(P.cache)[co + v] = float_to_bf16_bits(x);
+                cache_h[co + v] = float_to_bf16_bits(x);
               else
-                static_cast<float*>(P.cache)[co + v] = x;
+                cache_f[co + v] = x;
             }
-            ord = ordered_bits(y);  // every real value maps above 0
+            ord = in_range ? ordered_bits(y) : 0u;  // every real value maps above 0
           }
           if constexpr (kRegWinners) {
             // rows of a lane only grow across tiles: a strict > keeps the
@@ -380,10 +456,8 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2, MarkovStepPar
               run_v[c + jb] = static_cast<uint32_t>(v);
             }
           } else {
-            if (jb < c_live - c) {
-              const unsigned long long key = warp_winner(ord, static_cast<uint32_t>(v));
-              if (lane == 0 && key != 0ull) atomicMax(&best[b], key);
-            }
+            const unsigned long long key = warp_winner(ord, static_cast<uint32_t>(v));
+            if (lane == 0 && key != 0ull) atomicMax(&best[b], key);
           }
         }
       }
@@ -438,33 +512,42 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 template <int CPW>
 cudaError_t launch_tc_cpw(const MarkovStepParams& p, const CUtensorMap& map,
-                          const MarkovTcPlan& plan, int grid, cudaStream_t stream) {
+                          const CUtensorMap& bmap, const MarkovTcPlan& plan, int grid,
+                          cudaStream_t stream) {
   cudaError_t err = cudaFuncSetAttribute(markov_step_tc_kernel<CPW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(plan.smem));
   if (err != cudaSuccess) return err;
-  markov_step_tc_kernel<CPW><<<grid, kThreadsTc, plan.smem, stream>>>(map, p, plan.Npad,
-                                                                      plan.stages, plan.tmem_cols);
+  markov_step_tc_kernel<CPW><<<grid, kThreadsTc, plan.smem, stream>>>(
+      map, bmap, p, plan.Npad, plan.stages, plan.tmem_cols, plan.base_stage_bytes);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-bool markov_tc_plan(int B, int R, MarkovTcPlan* plan) {
+bool markov_tc_plan(int B, int R, int base_elem_bytes, bool base_tma_ok, MarkovTcPlan* plan) {
   if (R % 64 != 0 || R > 512 || B < 1 || B > 256) return false;
   const int NK = R / 64;
   int Npad = (B + 15) & ~15;
   if (Npad < 16) Npad = 16;
+  // stage the base logits through TMA when it leaves at least 4 w2 stages
+  size_t bstage = base_tma_ok ? static_cast<size_t>(kM) * B * base_elem_bytes : 0;
   int ns = kMaxStages;
-  while (ns >= 2 && TcLayout(Npad, NK, ns).total > kSmemLimit) --ns;
+  while (ns >= 4 && TcLayout(Npad, NK, ns, bstage).total > kSmemLimit) --ns;
+  if (TcLayout(Npad, NK, ns, bstage).total > kSmemLimit) {
+    bstage = 0;
+    ns = kMaxStages;
+    while (ns >= 2 && TcLayout(Npad, NK, ns, 0).total > kSmemLimit) --ns;
+  }
   if (ns < 2) return false;
+  plan->base_stage_bytes = static_cast<unsigned>(bstage);
   uint32_t cols = 32;
   while (cols < static_cast<uint32_t>(2 * Npad)) cols <<= 1;
   if (cols > 512) return false;
   plan->Npad = Npad;
   plan->stages = ns;
   plan->tmem_cols = cols;
-  plan->smem = TcLayout(Npad, NK, ns).total;
+  plan->smem = TcLayout(Npad, NK, ns, bstage).total;
   return true;
 }
 
@@ -488,19 +571,45 @@ int markov_tc_make_tmap(void* tmap_out, const void* w2, int V, int R) {
   return r == CUDA_SUCCESS ? 0 : -2;
 }
 
+int markov_tc_make_base_tmap(void* tmap_out, const void* base, bool bf16, int B, int K, int V) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return -1;
+  const cuuint64_t es = bf16 ? 2 : 4;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(K),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(V) * es,
+                                 static_cast<cuuint64_t>(V) * K * es};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kM), 1, static_cast<cuuint32_t>(B)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = reinterpret_cast<EncodeTiledFn>(fn)(
+      static_cast<CUtensorMap*>(tmap_out),
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -2;
+}
+
+int markov_tc_max_grid(int V) { return (V + kM - 1) / kM; }
+
 int markov_tc_grid(int V, int num_sms) {
   const int tiles = (V + kM - 1) / kM;
   return tiles < num_sms ? tiles : num_sms;
 }
 
-cudaError_t launch_markov_step_tc(const MarkovStepParams& p, const void* tmap,
+cudaError_t launch_markov_step_tc(const MarkovStepParams& p, const void* tmap, const void* bmap,
                                   const MarkovTcPlan& plan, int grid, cudaStream_t stream) {
   const CUtensorMap& map = *static_cast<const CUtensorMap*>(tmap);
+  const CUtensorMap& bm = *static_cast<const CUtensorMap*>(bmap);
   const int cpw = plan.Npad / 4;
-  if (cpw <= 4) return launch_tc_cpw<4>(p, map, plan, grid, stream);
-  if (cpw <= 8) return launch_tc_cpw<8>(p, map, plan, grid, stream);
-  if (cpw <= 16) return launch_tc_cpw<16>(p, map, plan, grid, stream);
-  return launch_tc_cpw<64>(p, map, plan, grid, stream);
+  if (cpw <= 4) return launch_tc_cpw<4>(p, map, bm, plan, grid, stream);
+  if (cpw <= 8) return launch_tc_cpw<8>(p, map, bm, plan, grid, stream);
+  if (cpw <= 16) return launch_tc_cpw<16>(p, map, bm, plan, grid, stream);
+  return launch_tc_cpw<64>(p, map, bm, plan, grid, stream);
 }
 
 }  // namespace dspark

@@ -54,10 +54,11 @@ __device__ __forceinline__ float exp_rel(float x, float m) {
 // bits; from 2^23 up, v is an integer: its 24-bit mantissa shifted left.
 __device__ __forceinline__ unsigned long long fixed_mass(float e) {
   const float v = __fmul_rn(e, 0x1p40f);
-  if (v < 8388608.0f) return static_cast<unsigned long long>(__float_as_uint(__fadd_rn(v, 8388608.0f)) - 0x4B000000u);
+  const uint32_t lo = __float_as_uint(__fadd_rn(v, 8388608.0f)) - 0x4B000000u;
   const uint32_t bits = __float_as_uint(v);
-  const unsigned long long mant = (bits & 0x7FFFFFu) | 0x800000u;
-  return mant << ((bits >> 23) - 150u);
+  const uint32_t sh = ((bits >> 23) - 150u) & 63u;
+  const unsigned long long hi = static_cast<unsigned long long>((bits & 0x7FFFFFu) | 0x800000u) << sh;
+  return v < 8388608.0f ? static_cast<unsigned long long>(lo) : hi;
 }
 
 // ordered bits of a non-NaN value (larger value -> larger key)

@@ -36,7 +36,6 @@ namespace {
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kRowBins = 2048;
-constexpr int kMaxCluster = 16;
 constexpr size_t kRowSmemLimit = 227u * 1024u;
 
 struct RowSmem {
@@ -56,6 +55,13 @@ struct RowSmem {
   unsigned long long x_mass;
   unsigned int x_cnt;
   unsigned int x_id;
+  // per-row reductions: one slot per CTA, two alternating sets (a row's slots
+  // are rewritten only after the next row's first cluster barrier)
+  unsigned int c_max[2];         // ordered bits of the CTA maximum (~0: failed)
+  unsigned long long c_sum[2];   // fixed-point mass
+  unsigned long long c_key[2];   // greedy winner key
+  unsigned int w_u32[kRowWarps];
+  unsigned long long w_u64[kRowWarps];
   // block-local scratch
   int found_pos;
   int bcast_i;
@@ -73,21 +79,6 @@ struct Found {
   unsigned int id;
 };
 
-__device__ float block_max_f(float v, RowSmem& sm) {
-  v = warp_maxf(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) sm.redf[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    float x = l < kRowWarps ? sm.redf[l] : -INFINITY;
-    x = warp_maxf(x);
-    if (l == 0) sm.redf[0] = x;
-  }
-  __syncthreads();
-  return sm.redf[0];
-}
-
 __device__ unsigned long long block_sum_u64(unsigned long long v, RowSmem& sm) {
   v = warp_sum64(v);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -103,75 +94,70 @@ __device__ unsigned long long block_sum_u64(unsigned long long v, RowSmem& sm) {
   return sm.red64[0];
 }
 
-__device__ unsigned long long block_max_u64(unsigned long long v, RowSmem& sm) {
-  v = warp_max64(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) sm.red64[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    unsigned long long x = l < kRowWarps ? sm.red64[l] : 0ull;
-    x = warp_max64(x);
-    if (l == 0) sm.red64[0] = x;
-  }
-  __syncthreads();
-  return sm.red64[0];
+// ---- cluster reductions of one value per thread --------------------------------
+// The CTA reduces its warps through shared memory and thread 0 stores the
+// result in the CTA's slot of the current set; after one cluster barrier warp
+// 0 reads the CL slots of the cluster and broadcasts the result.
+__device__ __forceinline__ float from_ordered(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// ---- cluster reductions of one value per CTA ---------------------------------
-// Maximum over the cluster; *any_fail = some CTA passed fail = true.
-__device__ float cluster_max_f(cg::cluster_group& cl, RowSmem& sm, float v, bool fail, int CL,
-                               bool* any_fail) {
-  if (threadIdx.x == 0) {
-    sm.x_max = v;
-    sm.x_fail = fail ? 1 : 0;
+template <class T, class Op>
+__device__ __forceinline__ T block_reduce(T v, T* wslots, T init, Op op) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  if ((threadIdx.x & 31) == 0) wslots[threadIdx.x >> 5] = v;
+  __syncthreads();
+  T r = init;
+  if (threadIdx.x < 32) {
+    r = threadIdx.x < kRowWarps ? wslots[threadIdx.x] : init;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = op(r, __shfl_xor_sync(0xFFFFFFFFu, r, o));
   }
+  return r;  // valid in warp 0
+}
+
+template <class T, class Op>
+__device__ __forceinline__ T cluster_reduce(cg::cluster_group& cl, RowSmem& sm, T v, T* cslot,
+                                            T* bcast, int CL, T init, Op op) {
+  v = block_reduce<T>(v, reinterpret_cast<T*>(sizeof(T) == 4 ? static_cast<void*>(sm.w_u32)
+                                                             : static_cast<void*>(sm.w_u64)),
+                      init, op);
+  if (threadIdx.x == 0) *cslot = v;
   cl.sync();
   if (threadIdx.x < 32) {
-    float m = -INFINITY;
-    int f = 0;
-    if (static_cast<int>(threadIdx.x) < CL) {
-      m = *cl.map_shared_rank(&sm.x_max, threadIdx.x);
-      f = *cl.map_shared_rank(&sm.x_fail, threadIdx.x);
-    }
-    m = warp_maxf(m);
-    f = __reduce_or_sync(0xFFFFFFFFu, static_cast<unsigned>(f));
-    if (threadIdx.x == 0) {
-      sm.bcast_f = m;
-      sm.bcast_i = f;
-    }
+    T r = static_cast<int>(threadIdx.x) < CL ? *cl.map_shared_rank(cslot, threadIdx.x) : init;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = op(r, __shfl_xor_sync(0xFFFFFFFFu, r, o));
+    if (threadIdx.x == 0) *bcast = r;
   }
   __syncthreads();
-  *any_fail = sm.bcast_i != 0;
-  return sm.bcast_f;
+  return *bcast;
+}
+
+// Maximum over the cluster; *any_fail = some CTA passed fail = true.
+__device__ float cluster_max_f(cg::cluster_group& cl, RowSmem& sm, float v, bool fail, int set,
+                               int CL, bool* any_fail) {
+  const unsigned int mine = fail ? 0xFFFFFFFFu : ordered_bits(v);
+  const unsigned int o = cluster_reduce<unsigned int>(
+      cl, sm, mine, &sm.c_max[set], reinterpret_cast<unsigned int*>(&sm.bcast_i), CL, 0u,
+      [](unsigned int a, unsigned int b) { return a > b ? a : b; });
+  *any_fail = o == 0xFFFFFFFFu;  // a real maximum is never NaN here (NaN reads as -inf)
+  return from_ordered(o);
 }
 
 __device__ unsigned long long cluster_sum_u64(cg::cluster_group& cl, RowSmem& sm,
-                                              unsigned long long v, int CL) {
-  if (threadIdx.x == 0) sm.x_sum = v;
-  cl.sync();
-  if (threadIdx.x < 32) {
-    unsigned long long s = 0ull;
-    if (static_cast<int>(threadIdx.x) < CL) s = *cl.map_shared_rank(&sm.x_sum, threadIdx.x);
-    s = warp_sum64(s);
-    if (threadIdx.x == 0) sm.bcast_u = s;
-  }
-  __syncthreads();
-  return sm.bcast_u;
+                                              unsigned long long v, int set, int CL) {
+  return cluster_reduce<unsigned long long>(
+      cl, sm, v, &sm.c_sum[set], &sm.bcast_u, CL, 0ull,
+      [](unsigned long long a, unsigned long long b) { return a + b; });
 }
 
 __device__ unsigned long long cluster_max_u64(cg::cluster_group& cl, RowSmem& sm,
-                                              unsigned long long v, int CL) {
-  if (threadIdx.x == 0) sm.x_key = v;
-  cl.sync();
-  if (threadIdx.x < 32) {
-    unsigned long long s = 0ull;
-    if (static_cast<int>(threadIdx.x) < CL) s = *cl.map_shared_rank(&sm.x_key, threadIdx.x);
-    s = warp_max64(s);
-    if (threadIdx.x == 0) sm.bcast_u = s;
-  }
-  __syncthreads();
-  return sm.bcast_u;
+                                              unsigned long long v, int set, int CL) {
+  return cluster_reduce<unsigned long long>(
+      cl, sm, v, &sm.c_key[set], &sm.bcast_u, CL, 0ull,
+      [](unsigned long long a, unsigned long long b) { return a > b ? a : b; });
 }
 
 // ---- histograms -------------------------------------------------------------
@@ -183,31 +169,14 @@ __device__ void hist_clear(RowSmem& sm, int nb) {
   }
 }
 
-// Adds (mass f, one count, id) to bin `bin`, aggregated over the lanes of the
-// warp sharing the bin. Every lane of the warp calls it; inactive lanes add
-// nothing.
+// Adds (mass f, one count, id) to bin `bin` with shared-memory atomics (one
+// per lane: the bins of a warp's 32 elements rarely collide).
 __device__ __forceinline__ void hist_add(RowSmem& sm, bool active, int bin,
                                          unsigned long long f, uint32_t id) {
-  unsigned int todo = __ballot_sync(0xFFFFFFFFu, active);
-  const int lane = threadIdx.x & 31;
-  while (todo) {
-    const int leader = __ffs(todo) - 1;
-    const int lb = __shfl_sync(0xFFFFFFFFu, bin, leader);
-    const bool mine = active && bin == lb;
-    const unsigned int peers = __ballot_sync(0xFFFFFFFFu, mine);
-    // f <= 2^40: two 20-bit halves keep the 32-bit warp sums exact
-    const unsigned int hi =
-        __reduce_add_sync(0xFFFFFFFFu, mine ? static_cast<unsigned int>(f >> 20) : 0u);
-    const unsigned int lo =
-        __reduce_add_sync(0xFFFFFFFFu, mine ? static_cast<unsigned int>(f & 0xFFFFFu) : 0u);
-    const unsigned int idm = __reduce_max_sync(0xFFFFFFFFu, mine ? id : 0u);
-    if (lane == leader) {
-      atomicAdd(&sm.hmass[lb], (static_cast<unsigned long long>(hi) << 20) + lo);
-      atomicAdd(&sm.hcnt[lb], static_cast<unsigned int>(__popc(peers)));
-      atomicMax(&sm.hid[lb], idm);
-    }
-    todo &= ~peers;
-  }
+  if (!active) return;
+  atomicAdd(&sm.hmass[bin], f);
+  atomicAdd(&sm.hcnt[bin], 1u);
+  atomicMax(&sm.hid[bin], id);
 }
 
 // Reduces the local histograms over the cluster and finds the first
@@ -217,8 +186,8 @@ __device__ Found cluster_find(cg::cluster_group& cl, RowSmem& sm, int nb, bool d
                               unsigned long long above, unsigned long long t_hi,
                               unsigned long long t_lo, int CL, int rank) {
   const int tid = threadIdx.x;
-  const int w = nb / CL;
-  const int b0 = rank * w;
+  const int b0 = rank * nb / CL;
+  const int w = (rank + 1) * nb / CL - b0;
   __syncthreads();
   cl.sync();  // every local histogram is complete
   // 1. reduce the bins this CTA owns over the cluster
@@ -396,7 +365,7 @@ __device__ bool slice_fetch(const void* row, bool bf16, int v0, int n, void* dst
     ok = mbar_wait(bar, phase, status);
     phase ^= 1u;
   }
-  __syncthreads();
+  if (body < n) __syncthreads();  // the plain-loaded tail is visible to every thread
   return ok;
 }
 
@@ -405,7 +374,7 @@ __device__ bool slice_fetch(const void* row, bool bf16, int v0, int n, void* dst
 // the row or on cluster-reduced values only).
 __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluster_group& cl,
                             int CL, int rank, RowSmem& sm, float* xs, uint64_t* bar,
-                            uint32_t& phase) {
+                            uint32_t& phase, int& jrow) {
   const int tid = threadIdx.x;
   const int K = P.K, V = P.V;
   const int nT = P.B * (K + 1);
@@ -431,6 +400,8 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
     crow = P.row_map ? P.row_map[s] : s;
     if (crow < 0 || crow >= P.C) return;
   }
+  const int set = jrow & 1;
+  ++jrow;
   const int v0 = rank * W;
   const int n = max(0, min(W, V - v0));
   const void* row;
@@ -451,7 +422,7 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
   DrfStats* ds = static_cast<DrfStats*>(P.dstats) + static_cast<int64_t>(b) * K + (k < K ? k : 0);
   const uint16_t* xh = reinterpret_cast<const uint16_t*>(xs);
 
-  // ---- the slice into shared memory (a previous row's readers are done) -------
+  // ---- the slice into shared memory --------------------------------------------
   fence_proxy_async_smem();
   const bool fetched = slice_fetch(row, bf16, v0, n, xs, bar, phase, P.status);
 
@@ -462,8 +433,7 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
       const float t = bf16 ? bf16_bits_to_float(xh[i]) : xs[i];
       key = umax64(key, winner_key(t, static_cast<uint32_t>(v0 + i)));
     }
-    key = block_max_u64(fetched ? key : 0ull, sm);
-    key = cluster_max_u64(cl, sm, key, CL);
+    key = cluster_max_u64(cl, sm, fetched ? key : 0ull, set, CL);
     if (rank == 0 && tid == 0) {
       ts->m = 0.f;
       ts->D = 1.f;
@@ -473,7 +443,6 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
       ts->mode = kModeGreedy;
       ts->amax_key = key;
     }
-    cl.sync();
     return;
   }
 
@@ -486,26 +455,37 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
       lmax = fmaxf(lmax, is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c));
     }
   } else {
-    for (int i = tid; i < n; i += kRowThreads) {
+    auto fix = [&](float c) { return is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c); };
+    const int n4 = n >> 2;
+    float4* xs4 = reinterpret_cast<float4*>(xs);
+    for (int i = tid; i < n4; i += kRowThreads) {
+      const float4 c = xs4[i];
+      const float4 x = make_float4(fix(c.x), fix(c.y), fix(c.z), fix(c.w));
+      if (__float_as_uint(x.x) != __float_as_uint(c.x) || __float_as_uint(x.y) != __float_as_uint(c.y) ||
+          __float_as_uint(x.z) != __float_as_uint(c.z) || __float_as_uint(x.w) != __float_as_uint(c.w))
+        xs4[i] = x;
+      lmax = fmaxf(lmax, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
+    }
+    for (int i = 4 * n4 + tid; i < n; i += kRowThreads) {
       const float c = xs[i];
-      const float x = is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c);
+      const float x = fix(c);
       if (__float_as_uint(x) != __float_as_uint(c)) xs[i] = x;
       lmax = fmaxf(lmax, x);
     }
   }
-  lmax = block_max_f(lmax, sm);
   // a timed-out copy drops the row for the whole cluster (status is set)
   bool any_fail = false;
-  const float m = cluster_max_f(cl, sm, lmax, !fetched, CL, &any_fail);
-  if (any_fail) {
-    cl.sync();
-    return;
-  }
+  const float m = cluster_max_f(cl, sm, lmax, !fetched, set, CL, &any_fail);
+  if (any_fail) return;
   auto xval = [&](int i) -> float {
     if (!bf16) return xs[i];
     const float c = bf16_bits_to_float(xh[i]);
     return is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c);
   };
+  // The drafted token's value, read now: after this row's last cluster
+  // barrier the CTA's threads may already be loading the next row's slice.
+  const bool own_d = tid == 0 && d >= v0 && d < v0 + n;
+  const float xd = own_d ? xval(d - v0) : 0.0f;
   if (m == -INFINITY) {
     if (rank == 0 && tid == 0) {
       if (is_target) {
@@ -523,7 +503,6 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
         ds->zero = 1;
       }
     }
-    cl.sync();
     return;
   }
 
@@ -553,8 +532,7 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
   } else {
     for (int i = tid; i < n; i += kRowThreads) F += fixed_mass(exp_rel(xval(i), m));
   }
-  F = block_sum_u64(F, sm);
-  F = cluster_sum_u64(cl, sm, F, CL);
+  F = cluster_sum_u64(cl, sm, F, set, CL);
 
   uint32_t kd_thr = 0u;
   int32_t id_thr = 0;
@@ -616,7 +594,7 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
         }
         sm.bcast_i = static_cast<int>(kd_of(xb));
       }
-      __syncthreads();
+      cl.sync();  // the owner keeps its slice until this remote read is done
       kd_thr = static_cast<uint32_t>(sm.bcast_i);
     } else {
       // exact ties at the boundary value: token id ascending, 11 + 11 bits
@@ -644,8 +622,8 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
   const float D = __fmul_rn(__ull2float_rn(Fk), 0x1p-40f);
 
   // ---- outputs: p or q at the drafted token (its owner), the rest (rank 0) ---------
-  if (tid == 0 && d >= v0 && d < v0 + n) {
-    const float x = xval(d - v0);
+  if (own_d) {
+    const float x = xd;
     if (is_target) {
       const uint32_t kd = kd_of(x);
       const bool keep = mode == kModeKeepAll || kd > kd_thr || (kd == kd_thr && d <= id_thr);
@@ -670,7 +648,9 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
       if (!(d >= 0 && d < V)) ds->q_d = 0.0f;
     }
   }
-  cl.sync();  // no CTA reuses its slice or slots while another may still read them
+  // A CTA may start its next slice copy now: its own threads are past every
+  // read of this slice (the last cluster barrier), and the other CTAs read a
+  // remote slice only inside the top-p stages, which end with a barrier.
 }
 
 // ---------------------------------------------------------------------------
@@ -690,10 +670,12 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
     mbar_init(&bar, 1);
     fence_mbar_init();
   }
-  __syncthreads();
+  cl.sync();  // barriers initialised in every CTA before any row starts
   uint32_t phase = 0;
+  int jrow = 0;
   for (int row = cid; row < nrows; row += nclusters)
-    process_row(P, W, row, cl, CL, rank, sm, xs, &bar, phase);
+    process_row(P, W, row, cl, CL, rank, sm, xs, &bar, phase, jrow);
+  cl.sync();  // no CTA exits while another may still touch its shared memory
 }
 
 }  // namespace
@@ -702,20 +684,50 @@ size_t verify_rows_smem_bytes(int W) {
   return ((sizeof(RowSmem) + 15) & ~size_t(15)) + static_cast<size_t>(W) * sizeof(float);
 }
 
-// Cluster size and slice width for vocabulary V: the smallest power-of-two
-// cluster whose slices leave room for two CTAs per SM, up to 16.
+// Cluster size and slice width for vocabulary V: slices small enough for two
+// CTAs per SM (at most 100 KB of shared memory), and among those cluster
+// sizes the one that keeps the most CTAs resident (the GPU places a cluster
+// inside one GPC, so 16-CTA clusters can leave SMs idle).
 bool verify_rows_plan(int V, int* CL, int* W) {
-  for (int cl = 1; cl <= kMaxCluster; cl *= 2) {
+  int best_cl = 0, best_w = 0, best_ctas = -1;
+  const int candidates[] = {16, 14, 12, 10, 8, 6, 4, 2, 1};
+  for (int cl : candidates) {
     int w = (V + cl - 1) / cl;
     w = (w + 7) & ~7;
-    if (verify_rows_smem_bytes(w) <= 100u * 1024u || cl == kMaxCluster) {
-      if (verify_rows_smem_bytes(w) > kRowSmemLimit) return false;
-      *CL = cl;
-      *W = w;
-      return true;
+    const size_t smem = verify_rows_smem_bytes(w);
+    if (smem > 100u * 1024u && cl < 16) break;  // smaller clusters only get larger slices
+    if (smem > kRowSmemLimit) continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.gridDim = dim3(static_cast<unsigned>(cl * 64), 1, 1);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaFuncSetAttribute(verify_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        (cl > 8 && cudaFuncSetAttribute(verify_rows_kernel,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                       cudaSuccess) ||
+        cudaOccupancyMaxActiveClusters(&clusters, verify_rows_kernel, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      clusters = 0;
+    }
+    if (clusters * cl > best_ctas) {
+      best_ctas = clusters * cl;
+      best_cl = cl;
+      best_w = w;
     }
   }
-  return false;
+  if (best_ctas <= 0) return false;
+  *CL = best_cl;
+  *W = best_w;
+  return true;
 }
 
 cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_t stream) {
