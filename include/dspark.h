@@ -21,7 +21,9 @@
  *   Memory.  Every pointer argument is DEVICE memory owned by the caller,
  *            except `status`, which may also be pinned (mapped) host memory.
  *            The library allocates nothing and keeps no state between calls;
- *            scratch space is the caller's `workspace`.
+ *            scratch space is the caller's `workspace` (one entry point,
+ *            dspark_markov_sample_static, uses a fixed array inside the
+ *            library instead: see there).
  *   Layout.  Row-major and contiguous. fp32 tensors are IEEE binary32; bf16
  *            tensors are passed as uint16 bit patterns.
  *   Streams. All work is enqueued on `stream` (a cudaStream_t; NULL = the
@@ -71,7 +73,9 @@ typedef enum {
   DSPARK_ERR_TIMEOUT = -4,     /* device: a bounded wait ran out           */
   DSPARK_ERR_BOUNDS = -5,      /* device: token, slot or row out of range  */
   DSPARK_ERR_WORKSPACE = -6,   /* workspace null or smaller than required  */
-  DSPARK_ERR_ALIGNMENT = -7    /* a pointer is not 16-byte aligned         */
+  DSPARK_ERR_ALIGNMENT = -7,   /* a pointer is not 16-byte aligned         */
+  DSPARK_ERR_SCRATCH_LIMIT = -8 /* sizes need more scratch than the fixed
+                                   array of dspark_markov_sample_static    */
 } dspark_status;
 
 /* Limits checked on the host. */
@@ -132,6 +136,45 @@ dspark_status dspark_markov_sample(
     int32_t* out_tokens, int B, int K, int V, int R, int S, int C,
     void* workspace, size_t workspace_bytes, int32_t* status,
     dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * dspark_markov_sample_static -- dspark_markov_sample without a workspace
+ * argument: the same computation, arguments and results, with the scratch
+ * kept in a fixed device array compiled into the library. The pages describe
+ * no such variant; it exists for callers that may not allocate device memory
+ * at all: a plug-in run by an inference engine that hands out every byte of
+ * device memory itself, a real-time decode loop that must not take the
+ * latency and implicit synchronisation of cudaMalloc, or a foreign-language
+ * host that can pass pointers but has no CUDA allocator of its own. This call
+ * makes no cudaMalloc or cudaFree and calls no allocating library.
+ *
+ * Limit.    The array holds DSPARK_STATIC_SCRATCH_BYTES bytes; every GPU that
+ *           loads the library holds it until the process exits. A call whose
+ *           dspark_markov_workspace_bytes(B, K, V, R) exceeds that is rejected
+ *           on the host with DSPARK_ERR_SCRATCH_LIMIT before anything runs
+ *           (8 MiB covers every batch size up to 256 for vocabularies up to
+ *           about 500k tokens).
+ * Set-up.   The first call on a device looks up the array's device address
+ *           (cudaGetSymbolAddress, with that device current) and keeps it;
+ *           a failure returns DSPARK_ERR_CUDA. Make that first call on each
+ *           device before any stream capture begins.
+ * Sharing.  Every call on a device uses the same array, which keeps what the
+ *           last call left there. The part that must start at zero (the
+ *           kernel's arrival counter) is cleared on `stream` by each call;
+ *           the rest is written before it is read. Calls whose work overlaps
+ *           on the GPU (other streams, other host threads) race on the array
+ *           and give wrong tokens: order them on one stream or with events.
+ * ------------------------------------------------------------------------ */
+#define DSPARK_STATIC_SCRATCH_BYTES (8u << 20)
+
+dspark_status dspark_markov_sample_static(
+    const void* base_logits, dspark_dtype base_dtype,
+    const uint16_t* markov_w1, const uint16_t* markov_w2,
+    const int32_t* anchor_tokens, const int32_t* req_state_idx,
+    const int64_t* positions, const float* temperature, const uint64_t* seeds,
+    void* cache, dspark_dtype cache_dtype, const int32_t* cache_row_map,
+    int32_t* out_tokens, int B, int K, int V, int R, int S, int C,
+    int32_t* status, dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * dspark_rejection_sample -- probabilistic rejection-sampling verification.

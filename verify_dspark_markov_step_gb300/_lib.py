@@ -28,12 +28,14 @@ STATUS = {
     -5: "DSPARK_ERR_BOUNDS",
     -6: "DSPARK_ERR_WORKSPACE",
     -7: "DSPARK_ERR_ALIGNMENT",
+    -8: "DSPARK_ERR_SCRATCH_LIMIT",
 }
 
 # Every symbol include/dspark.h declares.
 EXPORTS = (
     "dspark_markov_workspace_bytes",
     "dspark_markov_sample",
+    "dspark_markov_sample_static",
     "dspark_verify_workspace_bytes",
     "dspark_rejection_sample",
     "dspark_noise",
@@ -70,6 +72,9 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.dspark_markov_sample.restype = i32
         L.dspark_markov_sample.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp,
                                            i32, i32, i32, i32, i32, i32, vp, sz, vp, vp]
+        L.dspark_markov_sample_static.restype = i32
+        L.dspark_markov_sample_static.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                  vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
         L.dspark_verify_workspace_bytes.restype = sz
         L.dspark_verify_workspace_bytes.argtypes = [i32, i32, i32]
         L.dspark_rejection_sample.restype = i32
@@ -182,6 +187,53 @@ def markov_sample(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_id
         _ptr(out_tokens), B, K, V, R, S, max(C, 1), _ptr(workspace_buf),
         workspace_buf.numel() * workspace_buf.element_size(), _ptr(status), _stream(stream))
     _check(code, "dspark_markov_sample")
+
+
+# Bytes of the library's fixed scratch array (DSPARK_STATIC_SCRATCH_BYTES).
+STATIC_SCRATCH_BYTES = 8 << 20
+
+
+def markov_sample_static(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_idx,
+                         positions, temperature, seeds, out_tokens, cache=None,
+                         cache_row_map=None, status=None, stream=None):
+    """dspark_markov_sample_static on torch tensors: dspark_markov_sample with
+    the library's fixed scratch array instead of a workspace, so that nothing
+    is allocated (for callers that may not allocate device memory). Calls
+    that overlap on the GPU race on that array (see include/dspark.h)."""
+    _dev(base_logits, "base_logits", (torch.float32,) + _BF16_LIKE)
+    B, K, V = base_logits.shape
+    _dev(markov_w1, "markov_w1", _BF16_LIKE)
+    _dev(markov_w2, "markov_w2", _BF16_LIKE)
+    R = markov_w2.shape[1]
+    if markov_w2.shape != (V, R) or markov_w1.shape[1] != R or markov_w1.shape[0] < V:
+        raise ValueError("markov_w1 / markov_w2 must be [V, R]")
+    for t, n, d in ((anchor_tokens, "anchor_tokens", torch.int32),
+                    (req_state_idx, "req_state_idx", torch.int32),
+                    (positions, "positions", torch.int64),
+                    (temperature, "temperature", torch.float32),
+                    (out_tokens, "out_tokens", torch.int32)):
+        _dev(t, n, (d,))
+    _dev(seeds, "seeds")
+    S = temperature.shape[0]
+    if seeds.shape[0] != S or anchor_tokens.shape[0] != B or req_state_idx.shape[0] != B \
+            or positions.shape[0] != B or tuple(out_tokens.shape) != (B, K):
+        raise ValueError("inconsistent shapes")
+    C = 0
+    cache_dt = DSPARK_F32
+    if cache is not None:
+        _dev(cache, "cache", (torch.float32,) + _BF16_LIKE)
+        if cache.dim() != 3 or cache.shape[1] != K or cache.shape[2] != V:
+            raise ValueError("cache must be [C, K, V]")
+        C = cache.shape[0]
+        cache_dt = _logit_dtype(cache, "cache")
+    _dev(cache_row_map, "cache_row_map", (torch.int32,))
+    _dev(status, "status", (torch.int32,))
+    code = lib().dspark_markov_sample_static(
+        _ptr(base_logits), _logit_dtype(base_logits, "base_logits"), _ptr(markov_w1),
+        _ptr(markov_w2), _ptr(anchor_tokens), _ptr(req_state_idx), _ptr(positions),
+        _ptr(temperature), _ptr(seeds), _ptr(cache), cache_dt, _ptr(cache_row_map),
+        _ptr(out_tokens), B, K, V, R, S, max(C, 1), _ptr(status), _stream(stream))
+    _check(code, "dspark_markov_sample_static")
 
 
 def rejection_sample(draft_tokens, draft_cache, target_logits, req_state_idx, positions,

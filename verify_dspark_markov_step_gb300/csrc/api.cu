@@ -230,6 +230,8 @@ const char* dspark_status_string(int status) {
       return "workspace missing or too small";
     case DSPARK_ERR_ALIGNMENT:
       return "pointer not 16-byte aligned";
+    case DSPARK_ERR_SCRATCH_LIMIT:
+      return "sizes need more scratch than the library's fixed array";
     default:
       return "unknown status";
   }

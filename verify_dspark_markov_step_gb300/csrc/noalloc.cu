@@ -1,0 +1,70 @@
+// noalloc.cu -- dspark_markov_sample_static: the Markov sampling loop for
+// callers that may not allocate device memory (an engine plug-in that is
+// handed all of its memory, a latency-bound loop that cannot afford
+// cudaMalloc, a host with no CUDA allocator). Its scratch is a fixed array
+// in the library's device image instead of a caller-supplied workspace; the
+// work itself is dspark_markov_sample's, unchanged.
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "dspark.h"
+
+// The scratch: one per GPU that loads the library, alive until the process
+// exits. Host code must not hand this name to a kernel: on the host it only
+// stands for the symbol, and its device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_markov_scratch[DSPARK_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+void* g_scratch_addr[kMaxDevices] = {};  // device address per device ordinal
+
+// Device address of the scratch on the current device, looked up once per
+// device (with that device current) and remembered.
+dspark_status scratch_on_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DSPARK_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_markov_scratch) != cudaSuccess || p == nullptr)
+      return DSPARK_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return DSPARK_OK;
+}
+
+}  // namespace
+
+extern "C" dspark_status dspark_markov_sample_static(
+    const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
+    const uint16_t* markov_w2, const int32_t* anchor_tokens, const int32_t* req_state_idx,
+    const int64_t* positions, const float* temperature, const uint64_t* seeds, void* cache,
+    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens, int B, int K,
+    int V, int R, int S, int C, int32_t* status, dspark_stream_t stream) {
+  // sizes outside the documented ranges are argument errors, as for
+  // dspark_markov_sample; the scratch limit is checked next, and both before
+  // anything touches the device
+  if (B < 0 || B > DSPARK_MAX_BATCH || K < 1 || K > DSPARK_MAX_STEPS || V < 1 ||
+      V >= DSPARK_MAX_VOCAB || S < 1)
+    return DSPARK_ERR_INVALID_ARG;
+  if (dspark_markov_workspace_bytes(B, K, V, R) > DSPARK_STATIC_SCRATCH_BYTES)
+    return DSPARK_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  const dspark_status rc = scratch_on_current_device(&scratch);
+  if (rc != DSPARK_OK) return rc;
+  // dspark_markov_sample clears the arrival counter on `stream` itself and
+  // writes every other scratch word before reading it, so what an earlier
+  // call left in the array does not matter.
+  return dspark_markov_sample(base_logits, base_dtype, markov_w1, markov_w2, anchor_tokens,
+                              req_state_idx, positions, temperature, seeds, cache, cache_dtype,
+                              cache_row_map, out_tokens, B, K, V, R, S, C, scratch,
+                              DSPARK_STATIC_SCRATCH_BYTES, status, stream);
+}
