@@ -151,9 +151,9 @@ dspark_status dspark_markov_sample(
  * Limit.    The array holds DSPARK_STATIC_SCRATCH_BYTES bytes; every GPU that
  *           loads the library holds it until the process exits. A call whose
  *           dspark_markov_workspace_bytes(B, K, V, R) exceeds that is rejected
- *           on the host with DSPARK_ERR_SCRATCH_LIMIT before anything runs
- *           (8 MiB covers every batch size up to 256 for vocabularies up to
- *           about 500k tokens).
+ *           on the host with DSPARK_ERR_SCRATCH_LIMIT before anything runs.
+ *           32 KiB holds B * K <= 4095: every batch up to 256 requests with up
+ *           to 15 draft steps, or up to 255 requests with 16.
  * Set-up.   The first call on a device looks up the array's device address
  *           (cudaGetSymbolAddress, with that device current) and keeps it;
  *           a failure returns DSPARK_ERR_CUDA. Make that first call on each
@@ -165,7 +165,7 @@ dspark_status dspark_markov_sample(
  *           on the GPU (other streams, other host threads) race on the array
  *           and give wrong tokens: order them on one stream or with events.
  * ------------------------------------------------------------------------ */
-#define DSPARK_STATIC_SCRATCH_BYTES (8u << 20)
+#define DSPARK_STATIC_SCRATCH_BYTES (32u << 10)
 
 dspark_status dspark_markov_sample_static(
     const void* base_logits, dspark_dtype base_dtype,

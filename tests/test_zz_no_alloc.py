@@ -31,18 +31,17 @@ def _library():
 
 def test_sizes_beyond_the_fixed_scratch_are_rejected_on_the_host():
     """The limit is checked before anything touches the device, so this runs
-    without a GPU. 8 MiB fits a batch of 256 at a 200k vocabulary but not at
-    the largest vocabulary the library takes."""
+    without a GPU. 32 KiB fits 256 requests with 15 draft steps but not 16."""
     L = _library()
     from verify_dspark_markov_step_gb300 import _lib
-    assert _lib.markov_workspace_bytes(256, 7, 200064, 256) <= _lib.STATIC_SCRATCH_BYTES
-    assert _lib.markov_workspace_bytes(256, 7, (1 << 22) - 1, 256) > _lib.STATIC_SCRATCH_BYTES
+    assert _lib.markov_workspace_bytes(256, 15, (1 << 22) - 1, 512) <= _lib.STATIC_SCRATCH_BYTES
+    assert _lib.markov_workspace_bytes(256, 16, 200064, 256) > _lib.STATIC_SCRATCH_BYTES
     fake = ctypes.c_void_p(256)  # never dereferenced: every call below fails first
 
     def call(B, V, K=7, R=256, S=1):
         return L.dspark_markov_sample_static(fake, 0, fake, fake, fake, fake, fake, fake, fake,
                                              None, 0, None, fake, B, K, V, R, S, 1, None, None)
-    assert call(256, (1 << 22) - 1) == -8          # DSPARK_ERR_SCRATCH_LIMIT
+    assert call(256, 200064, K=16) == -8           # DSPARK_ERR_SCRATCH_LIMIT
     assert _lib.status_string(-8).startswith("sizes need more scratch")
     assert call(-1, 1000) == -1                    # still an argument error first
     assert call(4, 1 << 22) == -1

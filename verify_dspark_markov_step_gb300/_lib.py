@@ -190,7 +190,7 @@ def markov_sample(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_id
 
 
 # Bytes of the library's fixed scratch array (DSPARK_STATIC_SCRATCH_BYTES).
-STATIC_SCRATCH_BYTES = 8 << 20
+STATIC_SCRATCH_BYTES = 32 << 10
 
 
 def markov_sample_static(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_idx,

@@ -27,13 +27,15 @@ int num_sms_of_current_device(int* out) {
   return 0;
 }
 
+// The arrival counter and the [K][B] winner keys sit back to back, so that
+// one memset clears both.
 struct MarkovWs {
-  size_t counter, partials, total;
-  MarkovWs(int B, int V) {
+  size_t counter, keys, cleared, total;
+  MarkovWs(int B, int K) {
     counter = 0;
-    partials = align_up(counter + sizeof(unsigned int));
-    total = align_up(partials + static_cast<size_t>(B) *
-                                    dspark::markov_tc_max_grid(V) * sizeof(unsigned long long));
+    keys = 8;
+    cleared = keys + static_cast<size_t>(K) * B * sizeof(unsigned long long);
+    total = align_up(cleared);
   }
 };
 
@@ -60,10 +62,10 @@ bool sizes_ok(int B, int K, int V, int S) {
 extern "C" {
 
 size_t dspark_markov_workspace_bytes(int B, int K, int V, int R) {
-  (void)K;
+  (void)V;
   (void)R;
-  if (B < 0 || V < 1) return 0;
-  return MarkovWs(B, V).total;
+  if (B < 0 || K < 1) return 0;
+  return MarkovWs(B, K).total;
 }
 
 dspark_status dspark_markov_sample(
@@ -84,7 +86,7 @@ dspark_status dspark_markov_sample(
   if (!aligned16(base_logits) || !aligned16(markov_w1) || !aligned16(markov_w2) ||
       (cache && !aligned16(cache)))
     return DSPARK_ERR_ALIGNMENT;
-  const MarkovWs ws(B, V);
+  const MarkovWs ws(B, K);
   if (!workspace || workspace_bytes < ws.total || !aligned16(workspace))
     return DSPARK_ERR_WORKSPACE;
   int sms = 0;
@@ -111,11 +113,10 @@ dspark_status dspark_markov_sample(
   p.R = R;
   p.S = S;
   p.C = C;
-  p.partials = reinterpret_cast<unsigned long long*>(w + ws.partials);
+  p.keys = reinterpret_cast<unsigned long long*>(w + ws.keys);
   p.counter = reinterpret_cast<unsigned int*>(w + ws.counter);
   p.status = status;
-  if (cudaMemsetAsync(p.counter, 0, sizeof(unsigned int), st) != cudaSuccess)
-    return DSPARK_ERR_CUDA;
+  if (cudaMemsetAsync(w, 0, ws.cleared, st) != cudaSuccess) return DSPARK_ERR_CUDA;
   dspark::MarkovTcPlan plan;
   alignas(64) unsigned char tmap[128];
   alignas(64) unsigned char bmap[128] = {};
@@ -129,11 +130,8 @@ dspark_status dspark_markov_sample(
       !dspark::markov_tc_plan(B, R, es, false, &plan))
     return DSPARK_ERR_UNSUPPORTED;
   const int grid = dspark::markov_tc_grid(V, sms);
-  for (int i = 0; i < K; ++i) {
-    p.step = i;
-    if (dspark::launch_markov_step_tc(p, tmap, bmap, plan, grid, st) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-  }
+  if (dspark::launch_markov_loop_tc(p, tmap, bmap, plan, grid, st) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
 

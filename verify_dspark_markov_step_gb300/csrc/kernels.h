@@ -8,7 +8,7 @@
 
 namespace dspark {
 
-// One Markov step.
+// The K-step Markov loop.
 struct MarkovStepParams {
   const void* base;
   int base_bf16;
@@ -24,9 +24,8 @@ struct MarkovStepParams {
   const int32_t* row_map;
   int32_t* out_tokens;
   int B, K, V, R, S, C;
-  int step;
-  unsigned long long* partials;  // [B][grid] winner keys of each CTA
-  unsigned int* counter;         // CTAs finished in this step (self-resetting)
+  unsigned long long* keys;      // [K][B] winner key of each step and request (zeroed)
+  unsigned int* counter;         // grid-barrier arrivals (zeroed before the launch)
   int32_t* status;
 };
 
@@ -42,8 +41,8 @@ bool markov_tc_plan(int B, int R, int base_elem_bytes, bool base_tma_ok, MarkovT
 int markov_tc_make_tmap(void* tmap_out /* 128-byte CUtensorMap */, const void* w2, int V, int R);
 int markov_tc_make_base_tmap(void* tmap_out, const void* base, bool bf16, int B, int K, int V);
 int markov_tc_grid(int V, int num_sms);
-int markov_tc_max_grid(int V);  // upper bound of markov_tc_grid over devices
-cudaError_t launch_markov_step_tc(const MarkovStepParams& p, const void* tmap, const void* bmap,
+// All K steps in one cooperative launch of `grid` CTAs (at most one per SM).
+cudaError_t launch_markov_loop_tc(const MarkovStepParams& p, const void* tmap, const void* bmap,
                                   const MarkovTcPlan& plan, int grid, cudaStream_t stream);
 
 // Verification (verify.cu).

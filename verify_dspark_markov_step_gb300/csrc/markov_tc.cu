@@ -1,37 +1,44 @@
-// markov_tc.cu -- one Markov step on the 5th-generation tensor cores.
+// markov_tc.cu -- the K-step Markov sampling loop on the 5th-generation
+// tensor cores, all K steps in one persistent, cooperative launch.
 //
 // The "DSparkSpeculator" page's _sample_markov_chain / _sample_logits and
 // vLLM PR #65007 Part 1 (per-step list): Markov embedding of the previous
 // token, the markov_w2 bias projection, bias add, temperature, Gumbel noise
 // keyed by (seed, position - 1, column), the block-argmax winner rule and the
-// draft-logits cache store, fused into one kernel per step.
+// draft-logits cache store, fused; the steps are chained on the device.
 //
 // The bias projection [B, R] x [R, V] runs on the tensor cores for every
-// batch size: the step is bound by streaming markov_w2 and by the epilogue's
-// ALU work, and the MMA takes the B * R multiply-adds per column off the
-// epilogue warps (for small B the padding of N to 16 costs nothing).
-// markov_w2 rows are the M side of a tcgen05 MMA
-// (M = 128 vocabulary rows per tile, K = markov_rank), the Markov embeddings
-// of the batch are the N side (N = batch padded to a multiple of 16), and the
-// fp32 accumulator lives in tensor memory.
+// batch size: each step is bound by streaming markov_w2 and the logits and by
+// the epilogue's ALU work, and the MMA takes the B * R multiply-adds per
+// column off the epilogue warps (for small B the padding of N to 16 costs
+// nothing). markov_w2 rows are the M side of a tcgen05 MMA (M = 128
+// vocabulary rows per tile, K = markov_rank), the Markov embeddings of the
+// batch are the N side (N = batch padded to a multiple of 16), and the fp32
+// accumulator lives in tensor memory.
 //
-// Persistent, warp-specialised CTA (one per SM):
+// One CTA per SM, warp-specialised; the CTAs sweep the vocabulary tiles once
+// per step and the pipeline runs across step boundaries:
 //   warp 0      TMA producer: 128x64 bf16 boxes of markov_w2 (128-byte
 //               swizzle) into a ring of shared-memory stages, L2 evict-last;
-//               and, per tile, the tile's base logits of every request (a
-//               128 x 1 x B box of the [B, K, V] tensor) into one of two slots
+//               and, per tile, the tile's base logits of every request for
+//               that step (a 128 x 1 x B box of the [B, K, V] tensor) into one
+//               of two slots. It runs ahead into the next step while the
+//               current one is being finished.
 //   warp 1      TMEM allocation; one thread issues the MMAs (4 per 64-wide K
-//               chunk) into one of two accumulator buffers and commits
+//               chunk) into one of two accumulator buffers and commits; it
+//               waits for the step's Markov embeddings before its first tile.
 //   warps 2-17  epilogue: warp (q, sub) owns TMEM lane quarter q (32 rows of
 //               each tile) and a fixed set of CPW batch columns. Per chunk of
 //               4 columns: tcgen05.ld, bias add, temperature (x = z * (1/T),
 //               within 1.5 ulp of z / T), Gumbel noise (one Philox block per
 //               lane quad, shared by a 4x4 butterfly transpose), cache store,
-//               and the running winner of each
-//               column -- per lane in registers across tiles when CPW <= 16,
-//               else reduced per tile with redux.sync.
-// The per-CTA winners go to the workspace; the last CTA to finish reduces
-// them per request and writes the step's tokens.
+//               and the running winner of each column -- per lane in
+//               registers across tiles when CPW <= 16, else reduced per tile
+//               with redux.sync.
+// At the end of a step each CTA folds its winners into the step's global
+// winner keys (64-bit atomicMax), then a grid barrier (an arrival counter,
+// bounded wait) lets every CTA read the step's tokens, gather the next Markov
+// embeddings w1[token] into shared memory and release the MMA warp.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -51,22 +58,24 @@ constexpr int kThreadsTc = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 12;
 constexpr size_t kSmemLimit = 227u * 1024u;
 
-// Per-request data of one step, structure of arrays (Npad entries each).
+// Shared-memory layout (offsets from a 1024-byte aligned base).
 struct TcLayout {
-  size_t a, e, bases, temp, seed, npos, boff, coff, best, bars, slot, flags, total;
+  size_t a, e, bases, tinv, seed, p0, bbase, cbase, prev, act, best, bars, slot, flags, total;
   // base_stage: bytes of one staged base tile (0 = base logits read directly)
   __host__ __device__ TcLayout(int Npad, int NK, int ns, size_t base_stage) {
-    a = 0;
-    e = a + static_cast<size_t>(ns) * kStageBytes;
-    bases = e + static_cast<size_t>(NK) * Npad * 128;
-    temp = bases + 2 * ((base_stage + 1023) & ~size_t(1023));
-    seed = temp + static_cast<size_t>(Npad) * 4;
-    npos = seed + static_cast<size_t>(Npad) * 8;
-    boff = npos + static_cast<size_t>(Npad) * 8;
-    coff = boff + static_cast<size_t>(Npad) * 8;
-    best = coff + static_cast<size_t>(Npad) * 8;
+    a = 0;                                                   // w2 ring
+    e = a + static_cast<size_t>(ns) * kStageBytes;           // Markov embeddings
+    bases = e + static_cast<size_t>(NK) * Npad * 128;        // two staged base tiles
+    tinv = bases + 2 * ((base_stage + 1023) & ~size_t(1023));
+    seed = tinv + static_cast<size_t>(Npad) * 4;             // per-request constants
+    p0 = seed + static_cast<size_t>(Npad) * 8;
+    bbase = p0 + static_cast<size_t>(Npad) * 8;
+    cbase = bbase + static_cast<size_t>(Npad) * 8;
+    prev = cbase + static_cast<size_t>(Npad) * 8;             // per-step state
+    act = prev + static_cast<size_t>(Npad) * 4;
+    best = act + static_cast<size_t>(Npad) * 4;
     bars = best + static_cast<size_t>(Npad) * 8;
-    slot = bars + static_cast<size_t>(2 * ns + 7) * 8;
+    slot = bars + static_cast<size_t>(2 * ns + 9) * 8;
     flags = slot + 8;
     total = flags + 8 + kMaxStages * 4 + 1024;  // + slack to align the base to 1024 B
   }
@@ -119,9 +128,21 @@ __device__ __forceinline__ unsigned long long warp_winner(uint32_t ord, uint32_t
                     : (static_cast<unsigned long long>(omax) << 32) | (0xFFFFFFFFu - vmin);
 }
 
+constexpr int kEpiThreads = 32 * kEpiWarps;
+
+__device__ __forceinline__ void epi_bar() {  // the epilogue warps only
+  asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 template <int CPW>  // batch columns per epilogue warp (Npad / 4)
 __global__ void __launch_bounds__(kThreadsTc, 1)
-markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
+markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                       const __grid_constant__ CUtensorMap tmap_base, MarkovStepParams P, int Npad,
                       int ns, uint32_t tmem_cols, uint32_t base_stage_bytes) {
   constexpr bool kRegWinners = CPW <= 16;
@@ -135,44 +156,46 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   unsigned char* e_base = smem + L.e;
   unsigned char* base_s = smem + L.bases;  // two staged base tiles [B][128]
   const size_t base_stride = (static_cast<size_t>(base_stage_bytes) + 1023) & ~size_t(1023);
-  float* s_temp = reinterpret_cast<float*>(smem + L.temp);      // 1/T (0: greedy)
+  float* s_tinv = reinterpret_cast<float*>(smem + L.tinv);        // 1/T (0: greedy)
   uint64_t* s_seed = reinterpret_cast<uint64_t*>(smem + L.seed);
-  int64_t* s_npos = reinterpret_cast<int64_t*>(smem + L.npos);
-  int64_t* s_boff = reinterpret_cast<int64_t*>(smem + L.boff);   // -1: inert column
-  int64_t* s_coff = reinterpret_cast<int64_t*>(smem + L.coff);   // -1: no cache store
-  int32_t* s_prev = reinterpret_cast<int32_t*>(smem + L.coff);   // prologue only (aliases coff)
+  int64_t* s_p0 = reinterpret_cast<int64_t*>(smem + L.p0);        // position of draft 0
+  int64_t* s_bbase = reinterpret_cast<int64_t*>(smem + L.bbase);  // b*K*V
+  int64_t* s_cbase = reinterpret_cast<int64_t*>(smem + L.cbase);  // row*K*V (-1: no cache)
+  int32_t* s_prev = reinterpret_cast<int32_t*>(smem + L.prev);    // token feeding this step
+  int32_t* s_act = reinterpret_cast<int32_t*>(smem + L.act);      // request live
   unsigned long long* best = reinterpret_cast<unsigned long long*>(smem + L.best);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + ns;
   uint64_t* acc_full = empty + ns;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint64_t* base_full = drain + 1;     // [2]
+  uint64_t* base_full = drain + 1;    // [2]
+  uint64_t* e_ready = base_full + 2;  // one phase per step
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.slot);
-  int* fail_flag = reinterpret_cast<int*>(smem + L.flags);
+  volatile int* fail_flag = reinterpret_cast<volatile int*>(smem + L.flags);
+  volatile int* stop_word = fail_flag + 1;  // the epilogue's decision at a step end
   uint32_t* issued = reinterpret_cast<uint32_t*>(smem + L.flags + 8);  // last parity per stage
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int B = P.B, V = P.V, K = P.K, step = P.step;
+  const int B = P.B, V = P.V, K = P.K;
   const int G = gridDim.x;
   const int tiles = (V + kM - 1) / kM;
+  const int n_loc = (tiles - static_cast<int>(blockIdx.x) + G - 1) / G;  // tiles of this CTA
+  const int n_iter = n_loc * K;  // (step, tile) pairs, step-major
 
-  // ---- prologue: per-request data (thread n < Npad owns column n) ------------
-  int32_t my_prev = -1;
-  int64_t my_coff = -1;
+  // ---- prologue: per-request constants (thread n < Npad owns column n) --------
   if (tid < Npad) {
     const int n = tid;
-    float temp = 0.f;
+    float tinv = 0.f;
     uint64_t seed = 0;
-    int64_t npos = 0, boff = -1, coff = -1;
+    int64_t p0 = 0, bbase = 0, cbase = -1;
     int32_t prev = -1;
     const int32_t s = n < B ? P.rsi[n] : -1;
     if (s >= 0) {
       if (s >= P.S) {
         report(P.status, DSPARK_ERR_BOUNDS);
       } else {
-        const int32_t pv =
-            step == 0 ? P.anchor[n] : P.out_tokens[static_cast<int64_t>(n) * K + step - 1];
+        const int32_t pv = P.anchor[n];
         bool ok = pv >= 0 && pv < V;
         if (!ok) report(P.status, DSPARK_ERR_BOUNDS);
         if (ok && P.cache != nullptr) {
@@ -181,30 +204,30 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             report(P.status, DSPARK_ERR_BOUNDS);
             ok = false;
           } else {
-            coff = (row * K + step) * static_cast<int64_t>(V);
+            cbase = row * K * static_cast<int64_t>(V);
           }
         }
         if (ok) {
-          prev = pv;
-          temp = P.temperature[s];
+          const float T = P.temperature[s];
+          tinv = T > 0.f ? __frcp_rn(T) : 0.f;  // 0 marks a greedy column
           seed = P.seeds[s];
-          npos = P.pos[n] + step - 1;
-          boff = (static_cast<int64_t>(n) * K + step) * V;
+          p0 = P.pos[n];
+          bbase = static_cast<int64_t>(n) * K * V;
+          prev = pv;
         } else {
-          coff = -1;
+          cbase = -1;
         }
       }
     }
-    s_temp[n] = temp > 0.f ? __frcp_rn(temp) : 0.f;  // 1/T; 0 marks a greedy column
+    s_tinv[n] = tinv;
     s_seed[n] = seed;
-    s_npos[n] = npos;
-    s_boff[n] = boff;
+    s_p0[n] = p0;
+    s_bbase[n] = bbase;
+    s_cbase[n] = cbase;
     s_prev[n] = prev;
+    s_act[n] = prev >= 0;
     best[n] = 0ull;
-    my_prev = prev;
-    my_coff = coff;
   }
-  (void)my_prev;
   if (tid == 0) {
     for (int i = 0; i < ns; ++i) {
       mbar_init(&full[i], 1);
@@ -217,8 +240,10 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     mbar_init(drain, 1);
     mbar_init(&base_full[0], 1);
     mbar_init(&base_full[1], 1);
+    mbar_init(e_ready, 1);
     for (int i = 0; i < kMaxStages; ++i) issued[i] = 0xFFFFFFFFu;
     *fail_flag = 0;
+    *stop_word = 0;
     fence_mbar_init();
     tc::prefetch_tensormap(&tmap_w2);
     if (tma_base) tc::prefetch_tensormap(&tmap_base);
@@ -231,10 +256,10 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
 
   // Markov embeddings e[n] = w1[prev_n] as the N-side operand, K-major,
   // 128-byte swizzle: chunk c of row n of K-chunk kc at n*128 + (c ^ (n%8))*16.
-  {
+  auto gather_e = [&](int t0, int nt) {
     const int per_row = NK * 8;
     const int total = Npad * per_row;
-    for (int c = tid; c < total; c += kThreadsTc) {
+    for (int c = t0; c < total; c += nt) {
       const int n = c / per_row, rem = c % per_row;
       const int kc = rem >> 3, cc = rem & 7;
       uint4 val = make_uint4(0u, 0u, 0u, 0u);
@@ -245,17 +270,17 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       *reinterpret_cast<uint4*>(e_base + static_cast<size_t>(kc) * Npad * 128 + n * 128 +
                                 ((cc ^ (n & 7)) << 4)) = val;
     }
-  }
-  __syncthreads();
-  if (tid < Npad) s_coff[tid] = my_coff;  // s_prev (same storage) is no longer read
-  fence_proxy_async_smem();
+    fence_proxy_async_smem();  // generic writes -> visible to the tensor core
+  };
+  gather_e(tid, kThreadsTc);
   tc::fence_before_thread_sync();
   __syncthreads();
   tc::fence_after_thread_sync();
+  if (tid == 0) mbar_arrive(e_ready);  // step 0's embeddings are in place
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---- TMA producer -----------------------------------------------------------
+    // ---- TMA producer: markov_w2 boxes and base tiles of every step -------------
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
       const uint64_t pol_stream = policy_evict_first();
@@ -263,20 +288,21 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       uint32_t ph = 0;
       bool ok = true;
       uint32_t base_par[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // parity of the last copy per slot
-      for (int i = 0; ok; ++i) {
-        const int t = blockIdx.x + i * G;
-        if (t >= tiles) break;
+      for (int g = 0; g < n_iter && ok; ++g) {
+        if (*fail_flag) break;
+        const int step = g / n_loc;
+        const int t = blockIdx.x + (g - step * n_loc) * G;
         if (tma_base) {
-          // base slot i&1 is free once the epilogue released tile i-2
-          const int bs = i & 1;
-          if (!mbar_wait(&acc_empty[bs], ((i >> 1) & 1) ^ 1u, P.status)) {
+          // base slot g&1 is free once the epilogue released iteration g-2
+          const int bs = g & 1;
+          if (!mbar_wait(&acc_empty[bs], ((g >> 1) & 1) ^ 1u, P.status)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&base_full[bs], base_stage_bytes);
           tc::tma_load_3d(base_s + bs * base_stride, &tmap_base, t * kM, step, 0, &base_full[bs],
                           pol_stream);
-          base_par[bs] = (i >> 1) & 1;
+          base_par[bs] = (g >> 1) & 1;
         }
         for (int kc = 0; kc < NK; ++kc) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, P.status)) {
@@ -293,7 +319,7 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           }
         }
       }
-      if (!ok) atomicExch(fail_flag, 1);
+      if (!ok) *fail_flag = 1;
       // every copy this CTA issued has landed before the CTA may exit
       for (int s2 = 0; s2 < ns; ++s2)
         if (issued[s2] != 0xFFFFFFFFu) (void)mbar_wait(&full[s2], issued[s2], P.status);
@@ -307,12 +333,18 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int i = 0; ok; ++i) {
-        const int t = blockIdx.x + i * G;
-        if (t >= tiles) break;
-        const int ab = i & 1;
-        const uint32_t aph = (i >> 1) & 1;
-        if (!mbar_wait(&acc_empty[ab], aph ^ 1u, P.status)) {
+      for (int g = 0; g < n_iter && ok; ++g) {
+        if (*fail_flag) break;
+        const int step = g / n_loc;
+        if (g == step * n_loc) {  // first tile of a step: wait for its embeddings
+          if (!mbar_wait(e_ready, static_cast<uint32_t>(step) & 1u, P.status)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_thread_sync();
+        }
+        const int ab = g & 1;
+        if (!mbar_wait(&acc_empty[ab], ((g >> 1) & 1) ^ 1u, P.status)) {
           ok = false;
           break;
         }
@@ -339,13 +371,14 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         if (!ok) break;
         tc::mma_commit(&acc_full[ab]);
       }
-      if (!ok) atomicExch(fail_flag, 1);
+      if (!ok) *fail_flag = 1;
       // every MMA this thread issued has completed before TMEM is freed
       tc::mma_commit(drain);
       (void)mbar_wait(drain, 0u, P.status);
     }
   } else {
     // ---- epilogue -------------------------------------------------------------
+    const int etid = tid - 64;       // 0..511 among the epilogue threads
     const int q = warp & 3;          // TMEM lane quarter: rows 32q..32q+31 of a tile
     const int sub = (warp - 2) >> 2;
     const int c_begin = sub * CPW;   // batch columns [c_begin, c_begin + CPW)
@@ -363,13 +396,15 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       run_ord[j] = 0u;
       run_v[j] = 0xFFFFFFFFu;
     }
-    auto load_base = [&](int cb, int v, bool in_range, float (&bv)[4]) {
+    auto load_base = [&](int step, int cb, int v, bool in_range, float (&bv)[4]) {
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
-        const int64_t bo = s_boff[cb + jj];  // warp-uniform
+        const int b = cb + jj;
         bv[jj] = 0.f;
-        if (bo >= 0 && in_range)
+        if (s_act[b] && in_range) {  // warp-uniform request test
+          const int64_t bo = s_bbase[b] + static_cast<int64_t>(step) * V;
           bv[jj] = base_bf16 ? bf16_bits_to_float(__ldg(base_h + bo + v)) : __ldg(base_f + bo + v);
+        }
       }
     };
     // staged tile: element (b, row r) of slot ab at b * 128 + r
@@ -383,95 +418,157 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                        : 0.f;
       }
     };
-    for (int i = 0;; ++i) {
-      const int t = blockIdx.x + i * G;
-      if (t >= tiles) break;
-      const int ab = i & 1;
-      const uint32_t aph = (i >> 1) & 1;
+    bool skip = false;  // set after a failed wait: the warp then only walks the loop
+    for (int g = 0; g < n_iter; ++g) {
+      const int step = g / n_loc;
+      const int t = blockIdx.x + (g - step * n_loc) * G;
+      const int ab = g & 1;
+      const uint32_t aph = (g >> 1) & 1;
       const int v = t * kM + q * 32 + lane;
       const bool in_range = v < V;
       // base logits of the first chunk, issued before the accumulator wait
       float bnext[4];
-      if (!tma_base && c_live > 0) load_base(c_begin, v, in_range, bnext);
-      if (!mbar_wait(&acc_full[ab], aph, P.status)) {
-        atomicExch(fail_flag, 1);
-        break;
-      }
-      if (tma_base && !mbar_wait(&base_full[ab], aph, P.status)) {
-        atomicExch(fail_flag, 1);
-        break;
-      }
-      tc::fence_after_thread_sync();
-      if (tma_base && c_live > 0) smem_base(ab, c_begin, q * 32 + lane, bnext);
-#pragma unroll
-      for (int c = 0; c < CPW; c += 4) {
-        if (c >= c_live) break;
-        const int cb = c_begin + c;
-        const float bv[4] = {bnext[0], bnext[1], bnext[2], bnext[3]};
-        if (c + 4 < c_live) {
-          if (tma_base)
-            smem_base(ab, cb + 4, q * 32 + lane, bnext);
-          else
-            load_base(cb + 4, v, in_range, bnext);
+      if (!skip && !tma_base && c_live > 0) load_base(step, c_begin, v, in_range, bnext);
+      if (!skip) {
+        bool ok = mbar_wait(&acc_full[ab], aph, P.status);
+        if (ok && tma_base) ok = mbar_wait(&base_full[ab], aph, P.status);
+        if (!ok) {
+          *fail_flag = 1;
+          skip = true;
         }
-        uint32_t acc[4];
-        tc::tmem_ld4(tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                         static_cast<uint32_t>(ab * Npad + cb),
-                     acc);
-        // Philox block of this lane quad's 4 columns, for request cb+(lane&3),
-        // transposed so that nw[r] is this lane's noise for request cb+r
-        const int bq = cb + (lane & 3);
-        const U4 r = noise_block(s_seed[bq], s_npos[bq], static_cast<uint32_t>(v), kStreamDraft);
-        uint32_t nw[4] = {r.x, r.y, r.z, r.w};
-        quad_transpose(nw);
-        const float4 ti4 = *reinterpret_cast<const float4*>(s_temp + cb);
-        const float tinv[4] = {ti4.x, ti4.y, ti4.z, ti4.w};
-        tc::tmem_wait_ld();
+      }
+      if (!skip) {
+        tc::fence_after_thread_sync();
+        if (tma_base && c_live > 0) smem_base(ab, c_begin, q * 32 + lane, bnext);
 #pragma unroll
-        for (int jb = 0; jb < 4; ++jb) {
-          if (jb >= c_live - c) break;  // warp-uniform
-          const int b = cb + jb;
-          const int64_t co = s_coff[b];  // warp-uniform
-          uint32_t ord = 0u;
-          if (s_boff[b] >= 0) {  // warp-uniform: a live request
-            const float z = __fadd_rn(bv[jb], __uint_as_float(acc[jb]));
-            float x = z, y = z;
-            if (tinv[jb] > 0.f) {  // warp-uniform: sampled (x = z * (1/T))
-              x = __fmul_rn(z, tinv[jb]);
-              y = __fadd_rn(x, gumbel_of(nw[jb]));
-            }
-            if (co >= 0 && in_range) {
-              if (cache_bf16)
-                cache_h[co + v] = float_to_bf16_bits(x);
-              else
-                cache_f[co + v] = x;
-            }
-            ord = in_range ? ordered_bits(y) : 0u;  // every real value maps above 0
+        for (int c = 0; c < CPW; c += 4) {
+          if (c >= c_live) break;
+          const int cb = c_begin + c;
+          const float bv[4] = {bnext[0], bnext[1], bnext[2], bnext[3]};
+          if (c + 4 < c_live) {
+            if (tma_base)
+              smem_base(ab, cb + 4, q * 32 + lane, bnext);
+            else
+              load_base(step, cb + 4, v, in_range, bnext);
           }
-          if constexpr (kRegWinners) {
-            // rows of a lane only grow across tiles: a strict > keeps the
-            // lowest row on ties
-            if (ord > run_ord[c + jb]) {
-              run_ord[c + jb] = ord;
-              run_v[c + jb] = static_cast<uint32_t>(v);
+          uint32_t acc[4];
+          tc::tmem_ld4(tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                           static_cast<uint32_t>(ab * Npad + cb),
+                       acc);
+          // Philox block of this lane quad's 4 columns, for request cb+(lane&3),
+          // transposed so that nw[r] is this lane's noise for request cb+r
+          const int bq = cb + (lane & 3);
+          const U4 r = noise_block(s_seed[bq], s_p0[bq] + step - 1, static_cast<uint32_t>(v),
+                                   kStreamDraft);
+          uint32_t nw[4] = {r.x, r.y, r.z, r.w};
+          quad_transpose(nw);
+          const float4 ti4 = *reinterpret_cast<const float4*>(s_tinv + cb);
+          const float tinv[4] = {ti4.x, ti4.y, ti4.z, ti4.w};
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int jb = 0; jb < 4; ++jb) {
+            if (jb >= c_live - c) break;  // warp-uniform
+            const int b = cb + jb;
+            uint32_t ord = 0u;
+            if (s_act[b]) {  // warp-uniform: a live request
+              const float z = __fadd_rn(bv[jb], __uint_as_float(acc[jb]));
+              float x = z, y = z;
+              if (tinv[jb] > 0.f) {  // warp-uniform: sampled (x = z * (1/T))
+                x = __fmul_rn(z, tinv[jb]);
+                y = __fadd_rn(x, gumbel_of(nw[jb]));
+              }
+              const int64_t cb0 = s_cbase[b];
+              if (cb0 >= 0 && in_range) {
+                const int64_t co = cb0 + static_cast<int64_t>(step) * V + v;
+                if (cache_bf16)
+                  cache_h[co] = float_to_bf16_bits(x);
+                else
+                  cache_f[co] = x;
+              }
+              ord = in_range ? ordered_bits(y) : 0u;  // every real value maps above 0
             }
-          } else {
-            const unsigned long long key = warp_winner(ord, static_cast<uint32_t>(v));
-            if (lane == 0 && key != 0ull) atomicMax(&best[b], key);
+            if constexpr (kRegWinners) {
+              // rows of a lane only grow across a step's tiles: a strict >
+              // keeps the lowest row on ties
+              if (ord > run_ord[c + jb]) {
+                run_ord[c + jb] = ord;
+                run_v[c + jb] = static_cast<uint32_t>(v);
+              }
+            } else {
+              const unsigned long long key = warp_winner(ord, static_cast<uint32_t>(v));
+              if (lane == 0 && key != 0ull) atomicMax(&best[b], key);
+            }
           }
         }
+        tc::fence_before_thread_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[ab]);
       }
-      tc::fence_before_thread_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[ab]);
-    }
-    if constexpr (kRegWinners) {
+      if (g != (step + 1) * n_loc - 1) continue;
+
+      // ---- end of a step: fold winners, grid barrier, tokens, next embeddings ----
+      if constexpr (kRegWinners) {
 #pragma unroll
-      for (int j = 0; j < CPW; ++j) {
-        if (j < c_live) {
-          const unsigned long long key = warp_winner(run_ord[j], run_v[j]);
-          if (lane == 0 && key != 0ull) atomicMax(&best[c_begin + j], key);
+        for (int j = 0; j < CPW; ++j) {
+          if (j < c_live && !skip) {
+            const unsigned long long key = warp_winner(run_ord[j], run_v[j]);
+            if (lane == 0 && key != 0ull) atomicMax(&best[c_begin + j], key);
+          }
+          run_ord[j] = 0u;
+          run_v[j] = 0xFFFFFFFFu;
         }
+      }
+      epi_bar();
+      unsigned long long* keys = P.keys + static_cast<size_t>(step) * B;
+      for (int b = etid; b < B; b += kEpiThreads) {
+        const unsigned long long k = best[b];
+        if (k != 0ull) atomicMax(keys + b, k);
+        best[b] = 0ull;
+      }
+      __threadfence();
+      epi_bar();
+      const bool last = step + 1 == K;
+      if (etid == 0) {
+        // one decision for all epilogue warps: stop at the first failure
+        int stop = *fail_flag;
+        if (!stop) {
+          atomicAdd(P.counter, 1u);
+          // the last step's tokens are needed by CTA 0 alone
+          if (!last || blockIdx.x == 0) {
+            const unsigned int target =
+                static_cast<unsigned int>(step + 1) * static_cast<unsigned int>(G);
+            const unsigned long long t0 = globaltimer_ns();
+            while (ld_acquire_u32(P.counter) < target) {
+              if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                report(P.status, DSPARK_ERR_TIMEOUT);
+                *fail_flag = 1;
+                stop = 1;
+                break;
+              }
+            }
+            __threadfence();
+          }
+        }
+        *stop_word = stop;
+      }
+      epi_bar();
+      if (*stop_word || (last && blockIdx.x != 0)) break;  // uniform over the epilogue
+      for (int b = etid; b < B; b += kEpiThreads) {
+        int32_t tok = -1;
+        if (s_act[b]) {
+          const unsigned long long m = __ldcg(keys + b);
+          if (m != 0ull) tok = key_index(m);
+        }
+        if (blockIdx.x == 0) P.out_tokens[static_cast<int64_t>(b) * K + step] = tok;
+        s_prev[b] = tok;
+        s_act[b] = tok >= 0;
+      }
+      if (!last) {
+        epi_bar();
+        gather_e(etid, kEpiThreads);
+        tc::fence_before_thread_sync();
+        epi_bar();
+        if (etid == 0) mbar_arrive(e_ready);  // the MMA warp may start the next step
       }
     }
   }
@@ -481,28 +578,6 @@ markov_step_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     tc::fence_after_thread_sync();
     tc::tmem_dealloc(tmem, tmem_cols);
   }
-
-  // ---- publish this CTA's winners; the last CTA reduces -----------------------
-  for (int b = tid; b < B; b += kThreadsTc)
-    P.partials[static_cast<int64_t>(b) * G + blockIdx.x] = best[b];
-  __threadfence();
-  __syncthreads();
-  __shared__ unsigned int s_last;
-  if (tid == 0) {
-    const unsigned int ticket = atomicAdd(P.counter, 1u);
-    s_last = (ticket == static_cast<unsigned int>(G) - 1u);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int b = tid; b < B; b += kThreadsTc) {
-    unsigned long long m = 0ull;
-    const unsigned long long* row = P.partials + static_cast<int64_t>(b) * G;
-    for (int g2 = 0; g2 < G; ++g2) m = umax64(m, __ldcg(row + g2));
-    const int32_t tok = (s_boff[b] >= 0 && m != 0ull) ? key_index(m) : -1;
-    P.out_tokens[static_cast<int64_t>(b) * K + step] = tok;
-  }
-  if (tid == 0) *P.counter = 0u;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -514,13 +589,24 @@ template <int CPW>
 cudaError_t launch_tc_cpw(const MarkovStepParams& p, const CUtensorMap& map,
                           const CUtensorMap& bmap, const MarkovTcPlan& plan, int grid,
                           cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(markov_step_tc_kernel<CPW>,
+  cudaError_t err = cudaFuncSetAttribute(markov_loop_tc_kernel<CPW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(plan.smem));
   if (err != cudaSuccess) return err;
-  markov_step_tc_kernel<CPW><<<grid, kThreadsTc, plan.smem, stream>>>(
-      map, bmap, p, plan.Npad, plan.stages, plan.tmem_cols, plan.base_stage_bytes);
-  return cudaGetLastError();
+  // cooperative: every CTA is resident at once, which the grid barrier
+  // between steps relies on
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreadsTc, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, markov_loop_tc_kernel<CPW>, map, bmap, p, plan.Npad,
+                            plan.stages, plan.tmem_cols, plan.base_stage_bytes);
 }
 
 }  // namespace
@@ -594,14 +680,12 @@ int markov_tc_make_base_tmap(void* tmap_out, const void* base, bool bf16, int B,
   return r == CUDA_SUCCESS ? 0 : -2;
 }
 
-int markov_tc_max_grid(int V) { return (V + kM - 1) / kM; }
-
 int markov_tc_grid(int V, int num_sms) {
   const int tiles = (V + kM - 1) / kM;
   return tiles < num_sms ? tiles : num_sms;
 }
 
-cudaError_t launch_markov_step_tc(const MarkovStepParams& p, const void* tmap, const void* bmap,
+cudaError_t launch_markov_loop_tc(const MarkovStepParams& p, const void* tmap, const void* bmap,
                                   const MarkovTcPlan& plan, int grid, cudaStream_t stream) {
   const CUtensorMap& map = *static_cast<const CUtensorMap*>(tmap);
   const CUtensorMap& bm = *static_cast<const CUtensorMap*>(bmap);

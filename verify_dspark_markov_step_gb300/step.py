@@ -74,3 +74,29 @@ class DecodeStep:
 
     def status_code(self) -> int:
         return int(self.status.item())
+
+
+def main(argv=None):
+    """Run decode steps of a named synthetic workload, e.g. under a profiler:
+    python -m verify_dspark_markov_step_gb300.step --config minimax --batch 32 --steps 2"""
+    import argparse
+
+    from . import build, workloads
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--config", default="minimax")
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--steps", type=int, default=2)
+    args = ap.parse_args(argv)
+    build.build()
+    w = workloads.make(args.config, batch=args.batch)
+    st = DecodeStep(w)
+    for _ in range(args.steps):
+        st.run()
+    torch.cuda.synchronize()
+    print(f"{args.config} B={w.B}: status {st.status_code()}, mean accepted "
+          f"{st.num_accepted.float().mean().item():.3f}")
+
+
+if __name__ == "__main__":
+    main()
