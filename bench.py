@@ -52,24 +52,86 @@ def _dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """SM clock and clock-event (throttle) samples during the timed region.
 
+    NVML (the library behind nvidia-smi, loaded with ctypes) is polled every
+    2 ms from a thread, so that even a timed region of a few tens of
+    milliseconds gets samples; nvidia-smi -lms is the fallback. Read-only: no
+    setting of the GPU is touched."""
+
+    # NVML clock-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.samples = []      # (sm_mhz, max_mhz, reason bits)
+        self.lines = []        # nvidia-smi fallback
         self.proc = None
-        self.lines = []
+        self._stop = threading.Event()
         self._t = None
+        self._nvml = None
+        self._h = None
+        self.source = None
+
+    def _uuid(self):
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.dev).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return None
+
+    def _nvml_open(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        uuid = self._uuid()
+        ok = uuid is not None and lib.nvmlDeviceGetHandleByUUID(uuid.encode(),
+                                                                ctypes.byref(h)) == 0
+        if not ok:
+            return False
+        self._nvml, self._h = lib, h
+        self._reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return True
+
+    def _nvml_sample(self):
+        import ctypes
+        sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(sm)) != 0:
+            return
+        self._nvml.nvmlDeviceGetMaxClockInfo(self._h, 1, ctypes.byref(mx))
+        self._reason_fn(self._h, ctypes.byref(rs))
+        self.samples.append((float(sm.value), float(mx.value), int(rs.value)))
+
+    def _poll(self):
+        while not self._stop.is_set():
+            self._nvml_sample()
+            time.sleep(0.002)
 
     def start(self):
+        if self._nvml_open():
+            self.source = "nvml"
+            self._nvml_sample()
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+            return
         try:
+            target = self._uuid() or str(self.dev)
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nvidia-smi", "-i", target, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
         except (OSError, ValueError):
             self.proc = None
             return
@@ -81,8 +143,21 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self):
+        if self.source == "nvml":
+            self._stop.set()
+            self._t.join(timeout=2)
+            self._nvml_sample()
+            reasons = set()
+            for _, _, bits in self.samples:
+                for bit, name in self.REASONS.items():
+                    if bits & bit:
+                        reasons.add(name)
+            sm = [a for a, _, _ in self.samples]
+            return {"sm_mhz": statistics.median(sm) if sm else None,
+                    "sm_max_mhz": max(b for _, b, _ in self.samples) if self.samples else None,
+                    "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -106,7 +181,7 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi"}
 
 
 def algorithmic_bytes(w):
@@ -345,19 +420,28 @@ def run_ours(args, rank, world, local):
 
 
 def _traffic_from_profile(args):
-    """DRAM bytes per Markov-step launch from the committed ncu summary, if it
-    was taken on the current kernel; else None."""
-    p = os.path.join(ROOT, "profiles", "markov_step_traffic.json")
-    if not os.path.exists(p):
+    """DRAM bytes (read + write) per launch of the Markov loop kernel from the
+    committed ncu summary, if it was taken on this workload and on the current
+    kernel sources (its source hash matches); else None."""
+    import hashlib
+    import re
+    if args.config != "minimax" or args.batch != 32:
         return None
+    p = os.path.join(ROOT, "profiles", "markov_loop_tc_minimax_b32.md")
     try:
         with open(p) as f:
-            d = json.load(f)
-        if d.get("batch") == args.batch and d.get("config") == args.config:
-            return d.get("dram_bytes_per_launch")
-    except (OSError, ValueError):
-        pass
-    return None
+            txt = f.read()
+        t = re.search(r"^traffic_bytes_per_launch: (\d+)", txt, re.M)
+        h = re.search(r"^source_sha256: ([0-9a-f]+)", txt, re.M)
+        if not t or not h:
+            return None
+        m = hashlib.sha256()
+        for name in ("markov_tc.cu", "common.cuh", "tc_ptx.cuh"):
+            with open(os.path.join(ROOT, "verify_dspark_markov_step_gb300", "csrc", name), "rb") as f:
+                m.update(f.read())
+        return int(t.group(1)) if m.hexdigest().startswith(h.group(1)) else None
+    except OSError:
+        return None
 
 
 def main():

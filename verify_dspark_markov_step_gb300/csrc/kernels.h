@@ -32,9 +32,11 @@ struct MarkovStepParams {
 // Tensor-core variant (markov_tc.cu).
 struct MarkovTcPlan {
   int Npad;            // batch padded to a multiple of 16 (UMMA N)
-  int stages;          // shared-memory ring stages of 16 KB
-  unsigned tmem_cols;  // TMEM columns allocated (two accumulator buffers)
-  unsigned base_stage_bytes;  // staged base tile bytes (0: base read directly)
+  int stages;          // shared-memory ring stages of 16 KB (markov_w2)
+  int acc_buffers;     // TMEM accumulator buffers (2-4)
+  int base_slots;      // staged base tiles (0: base read directly)
+  unsigned tmem_cols;  // TMEM columns allocated
+  unsigned base_stage_bytes;  // bytes of one staged base tile
   size_t smem;         // dynamic shared memory bytes
 };
 bool markov_tc_plan(int B, int R, int base_elem_bytes, bool base_tma_ok, MarkovTcPlan* plan);

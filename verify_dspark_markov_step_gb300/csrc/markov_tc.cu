@@ -18,18 +18,21 @@
 //
 // One CTA per SM, warp-specialised; the CTAs sweep the vocabulary tiles once
 // per step and the pipeline runs across step boundaries:
-//   warp 0      TMA producer: 128x64 bf16 boxes of markov_w2 (128-byte
-//               swizzle) into a ring of shared-memory stages, L2 evict-last;
-//               and, per tile, the tile's base logits of every request for
-//               that step (a 128 x 1 x B box of the [B, K, V] tensor) into one
-//               of two slots. It runs ahead into the next step while the
-//               current one is being finished.
+//   warp 0      TMA producer of markov_w2: 128x64 bf16 boxes (128-byte
+//               swizzle) into a ring of up to 12 shared-memory stages, L2
+//               evict-last, as far ahead as the ring allows (into the next
+//               step while the current one is being finished).
+//   warp 18     TMA producer of the base logits: per tile, the tile's logits
+//               of every request for that step (a 128 x 1 x B box of the
+//               [B, K, V] tensor) into one of up to 8 slots, L2 evict-first;
+//               for large batches the epilogue reads them from global memory.
 //   warp 1      TMEM allocation; one thread issues the MMAs (4 per 64-wide K
-//               chunk) into one of two accumulator buffers and commits; it
+//               chunk) into one of 2-4 accumulator buffers and commits; it
 //               waits for the step's Markov embeddings before its first tile.
 //   warps 2-17  epilogue: warp (q, sub) owns TMEM lane quarter q (32 rows of
-//               each tile) and a fixed set of CPW batch columns. Per chunk of
-//               4 columns: tcgen05.ld, bias add, temperature (x = z * (1/T),
+//               each tile) and a fixed set of CPW batch columns. Per group of
+//               8 (or 4) columns: one tcgen05.ld and the Philox blocks, then
+//               per column: bias add, temperature (x = z * (1/T),
 //               within 1.5 ulp of z / T), Gumbel noise (one Philox block per
 //               lane quad, shared by a 4x4 butterfly transpose), cache store,
 //               and the running winner of each column -- per lane in
@@ -53,31 +56,47 @@ namespace {
 
 constexpr int kM = 128;                 // vocabulary rows per tile (UMMA M)
 constexpr int kStageBytes = kM * 128;   // one 64-element K chunk of a tile
-constexpr int kEpiWarps = 16;           // four per TMEM lane quarter
-constexpr int kThreadsTc = 64 + 32 * kEpiWarps;
+constexpr int kEpiWarps = 16;           // four per TMEM lane quarter (warps 2..17)
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kBaseWarp = 2 + kEpiWarps;  // TMA producer of the base logits
+constexpr int kThreadsTc = 32 * (kBaseWarp + 1);
 constexpr int kMaxStages = 12;
+constexpr int kMaxAcc = 4;              // accumulator buffers in TMEM
+constexpr int kMaxBaseSlots = 8;        // staged base tiles
 constexpr size_t kSmemLimit = 227u * 1024u;
+
+struct TcCfg {
+  int Npad;                   // batch padded to a multiple of 16 (UMMA N)
+  int ns;                     // markov_w2 ring stages of 16 KB
+  int na;                     // accumulator buffers (na * Npad TMEM columns)
+  int nb;                     // staged base tiles (0: base logits read directly)
+  uint32_t tmem_cols;
+  uint32_t base_stage_bytes;  // bytes of one staged base tile
+};
+
+__host__ __device__ inline size_t base_slot_stride(size_t base_stage) {
+  return (base_stage + 1023) & ~size_t(1023);
+}
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 struct TcLayout {
-  size_t a, e, bases, tinv, seed, p0, bbase, cbase, prev, act, best, bars, slot, flags, total;
-  // base_stage: bytes of one staged base tile (0 = base logits read directly)
-  __host__ __device__ TcLayout(int Npad, int NK, int ns, size_t base_stage) {
-    a = 0;                                                   // w2 ring
-    e = a + static_cast<size_t>(ns) * kStageBytes;           // Markov embeddings
-    bases = e + static_cast<size_t>(NK) * Npad * 128;        // two staged base tiles
-    tinv = bases + 2 * ((base_stage + 1023) & ~size_t(1023));
-    seed = tinv + static_cast<size_t>(Npad) * 4;             // per-request constants
-    p0 = seed + static_cast<size_t>(Npad) * 8;
-    bbase = p0 + static_cast<size_t>(Npad) * 8;
-    cbase = bbase + static_cast<size_t>(Npad) * 8;
-    prev = cbase + static_cast<size_t>(Npad) * 8;             // per-step state
+  size_t a, e, bases, tinv, seed, npos, bptr, cptr, prev, act, best, bars, slot, flags, total;
+  __host__ __device__ TcLayout(int Npad, int NK, int ns, int nb, size_t base_stage) {
+    a = 0;                                                       // markov_w2 ring
+    e = a + static_cast<size_t>(ns) * kStageBytes;               // Markov embeddings
+    bases = e + static_cast<size_t>(NK) * Npad * 128;            // staged base tiles
+    tinv = bases + static_cast<size_t>(nb) * base_slot_stride(base_stage);
+    seed = tinv + static_cast<size_t>(Npad) * 4;                 // per request:
+    npos = seed + static_cast<size_t>(Npad) * 8;                 //   noise position
+    bptr = npos + static_cast<size_t>(Npad) * 8;                 //   base row of the step
+    cptr = bptr + static_cast<size_t>(Npad) * 8;                 //   cache row of the step
+    prev = cptr + static_cast<size_t>(Npad) * 8;                 //   token feeding the step
     act = prev + static_cast<size_t>(Npad) * 4;
     best = act + static_cast<size_t>(Npad) * 4;
     bars = best + static_cast<size_t>(Npad) * 8;
-    slot = bars + static_cast<size_t>(2 * ns + 9) * 8;
+    slot = bars + static_cast<size_t>(2 * kMaxStages + 2 * kMaxAcc + 2 * kMaxBaseSlots + 2) * 8;
     flags = slot + 8;
-    total = flags + 8 + kMaxStages * 4 + 1024;  // + slack to align the base to 1024 B
+    total = flags + 16 + 1024;  // + slack to align the base to 1024 B
   }
 };
 
@@ -85,9 +104,8 @@ struct TcLayout {
 // for the same 4-column block (a 4x4 matrix, one row per lane). A two-round
 // butterfly transposes it: afterwards w[r] = word (lane & 3) of request
 // b0 + r, i.e. the noise of this lane's own column for request b0 + r.
-__device__ __forceinline__ void quad_transpose(uint32_t (&w)[4]) {
+__device__ __forceinline__ void quad_transpose(uint32_t* w) {
   const uint32_t c = threadIdx.x & 3u;
-  // round 1 (lanes c, c^2): the upper lane takes the lower lane's words 2,3
   {
     const bool up = (c & 2u) != 0u;
     const uint32_t s0 = up ? w[0] : w[2];
@@ -102,7 +120,6 @@ __device__ __forceinline__ void quad_transpose(uint32_t (&w)[4]) {
       w[3] = r1;
     }
   }
-  // round 2 (lanes c, c^1)
   {
     const bool odd = (c & 1u) != 0u;
     const uint32_t s0 = odd ? w[0] : w[1];
@@ -128,8 +145,6 @@ __device__ __forceinline__ unsigned long long warp_winner(uint32_t ord, uint32_t
                     : (static_cast<unsigned long long>(omax) << 32) | (0xFFFFFFFFu - vmin);
 }
 
-constexpr int kEpiThreads = 32 * kEpiWarps;
-
 __device__ __forceinline__ void epi_bar() {  // the epilogue warps only
   asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
 }
@@ -140,41 +155,52 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
   return v;
 }
 
+template <int GW>
+__device__ __forceinline__ void tmem_load_group(uint32_t taddr, uint32_t (&r)[GW]) {
+  if constexpr (GW == 8) {
+    tc::tmem_ld8(taddr, r);
+  } else {
+    tc::tmem_ld4(taddr, r);
+  }
+}
+
 template <int CPW>  // batch columns per epilogue warp (Npad / 4)
 __global__ void __launch_bounds__(kThreadsTc, 1)
 markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
-                      const __grid_constant__ CUtensorMap tmap_base, MarkovStepParams P, int Npad,
-                      int ns, uint32_t tmem_cols, uint32_t base_stage_bytes) {
+                      const __grid_constant__ CUtensorMap tmap_base, MarkovStepParams P,
+                      TcCfg cfg) {
   constexpr bool kRegWinners = CPW <= 16;
+  constexpr int GW = CPW >= 8 ? 8 : 4;  // columns per TMEM load and Philox group
+  const int Npad = cfg.Npad, ns = cfg.ns, na = cfg.na, nb = cfg.nb;
   const int R = P.R;
   const int NK = R / 64;
-  const bool tma_base = base_stage_bytes != 0u;
+  const bool tma_base = nb != 0;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  const TcLayout L(Npad, NK, ns, base_stage_bytes);
+  const TcLayout L(Npad, NK, ns, nb, cfg.base_stage_bytes);
   unsigned char* a_base = smem + L.a;
   unsigned char* e_base = smem + L.e;
-  unsigned char* base_s = smem + L.bases;  // two staged base tiles [B][128]
-  const size_t base_stride = (static_cast<size_t>(base_stage_bytes) + 1023) & ~size_t(1023);
-  float* s_tinv = reinterpret_cast<float*>(smem + L.tinv);        // 1/T (0: greedy)
+  unsigned char* base_s = smem + L.bases;  // nb staged base tiles [B][128]
+  const size_t base_stride = base_slot_stride(cfg.base_stage_bytes);
+  float* s_tinv = reinterpret_cast<float*>(smem + L.tinv);          // 1/T (0: greedy)
   uint64_t* s_seed = reinterpret_cast<uint64_t*>(smem + L.seed);
-  int64_t* s_p0 = reinterpret_cast<int64_t*>(smem + L.p0);        // position of draft 0
-  int64_t* s_bbase = reinterpret_cast<int64_t*>(smem + L.bbase);  // b*K*V
-  int64_t* s_cbase = reinterpret_cast<int64_t*>(smem + L.cbase);  // row*K*V (-1: no cache)
-  int32_t* s_prev = reinterpret_cast<int32_t*>(smem + L.prev);    // token feeding this step
-  int32_t* s_act = reinterpret_cast<int32_t*>(smem + L.act);      // request live
+  int64_t* s_npos = reinterpret_cast<int64_t*>(smem + L.npos);      // P0 + step - 1
+  const unsigned char** s_bptr = reinterpret_cast<const unsigned char**>(smem + L.bptr);
+  unsigned char** s_cptr = reinterpret_cast<unsigned char**>(smem + L.cptr);  // null: no store
+  int32_t* s_prev = reinterpret_cast<int32_t*>(smem + L.prev);
+  int32_t* s_act = reinterpret_cast<int32_t*>(smem + L.act);        // request live
   unsigned long long* best = reinterpret_cast<unsigned long long*>(smem + L.best);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + ns;
-  uint64_t* acc_full = empty + ns;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
-  uint64_t* base_full = drain + 1;    // [2]
-  uint64_t* e_ready = base_full + 2;  // one phase per step
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* acc_full = empty + kMaxStages;
+  uint64_t* acc_empty = acc_full + kMaxAcc;
+  uint64_t* bfull = acc_empty + kMaxAcc;
+  uint64_t* bempty = bfull + kMaxBaseSlots;
+  uint64_t* drain = bempty + kMaxBaseSlots;
+  uint64_t* e_ready = drain + 1;  // one phase per step
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.slot);
   volatile int* fail_flag = reinterpret_cast<volatile int*>(smem + L.flags);
   volatile int* stop_word = fail_flag + 1;  // the epilogue's decision at a step end
-  uint32_t* issued = reinterpret_cast<uint32_t*>(smem + L.flags + 8);  // last parity per stage
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = P.B, V = P.V, K = P.K;
@@ -182,13 +208,17 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   const int tiles = (V + kM - 1) / kM;
   const int n_loc = (tiles - static_cast<int>(blockIdx.x) + G - 1) / G;  // tiles of this CTA
   const int n_iter = n_loc * K;  // (step, tile) pairs, step-major
+  const int bes = P.base_bf16 ? 2 : 4;
+  const int ces = P.cache_bf16 ? 2 : 4;
 
-  // ---- prologue: per-request constants (thread n < Npad owns column n) --------
+  // ---- prologue: per-request state (thread n < Npad owns column n) -----------
   if (tid < Npad) {
     const int n = tid;
     float tinv = 0.f;
     uint64_t seed = 0;
-    int64_t p0 = 0, bbase = 0, cbase = -1;
+    int64_t npos = 0;
+    const unsigned char* bp = nullptr;
+    unsigned char* cp = nullptr;
     int32_t prev = -1;
     const int32_t s = n < B ? P.rsi[n] : -1;
     if (s >= 0) {
@@ -198,32 +228,32 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         const int32_t pv = P.anchor[n];
         bool ok = pv >= 0 && pv < V;
         if (!ok) report(P.status, DSPARK_ERR_BOUNDS);
+        int64_t row = -1;
         if (ok && P.cache != nullptr) {
-          const int64_t row = P.row_map ? P.row_map[s] : s;
+          row = P.row_map ? P.row_map[s] : s;
           if (row < 0 || row >= P.C) {
             report(P.status, DSPARK_ERR_BOUNDS);
             ok = false;
-          } else {
-            cbase = row * K * static_cast<int64_t>(V);
           }
         }
         if (ok) {
           const float T = P.temperature[s];
           tinv = T > 0.f ? __frcp_rn(T) : 0.f;  // 0 marks a greedy column
           seed = P.seeds[s];
-          p0 = P.pos[n];
-          bbase = static_cast<int64_t>(n) * K * V;
+          npos = P.pos[n] - 1;
+          bp = static_cast<const unsigned char*>(P.base) +
+               static_cast<int64_t>(n) * K * V * bes;
+          if (row >= 0)
+            cp = static_cast<unsigned char*>(P.cache) + row * K * static_cast<int64_t>(V) * ces;
           prev = pv;
-        } else {
-          cbase = -1;
         }
       }
     }
     s_tinv[n] = tinv;
     s_seed[n] = seed;
-    s_p0[n] = p0;
-    s_bbase[n] = bbase;
-    s_cbase[n] = cbase;
+    s_npos[n] = npos;
+    s_bptr[n] = bp;
+    s_cptr[n] = cp;
     s_prev[n] = prev;
     s_act[n] = prev >= 0;
     best[n] = 0ull;
@@ -233,15 +263,16 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(&acc_full[0], 1);
-    mbar_init(&acc_full[1], 1);
-    mbar_init(&acc_empty[0], kEpiWarps);
-    mbar_init(&acc_empty[1], kEpiWarps);
+    for (int i = 0; i < na; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarps);
+    }
+    for (int i = 0; i < nb; ++i) {
+      mbar_init(&bfull[i], 1);
+      mbar_init(&bempty[i], kEpiWarps);
+    }
     mbar_init(drain, 1);
-    mbar_init(&base_full[0], 1);
-    mbar_init(&base_full[1], 1);
     mbar_init(e_ready, 1);
-    for (int i = 0; i < kMaxStages; ++i) issued[i] = 0xFFFFFFFFu;
     *fail_flag = 0;
     *stop_word = 0;
     fence_mbar_init();
@@ -249,7 +280,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     if (tma_base) tc::prefetch_tensormap(&tmap_base);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, tmem_cols);
+    tc::tmem_alloc(tmem_slot, cfg.tmem_cols);
     tc::tmem_relinquish();
   }
   __syncthreads();
@@ -280,30 +311,19 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---- TMA producer: markov_w2 boxes and base tiles of every step -------------
+    // ---- TMA producer of markov_w2: as far ahead as the ring allows ------------
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
-      const uint64_t pol_stream = policy_evict_first();
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
-      uint32_t base_par[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // parity of the last copy per slot
+      uint32_t issued[kMaxStages];  // parity of the last copy per stage
+#pragma unroll
+      for (int i = 0; i < kMaxStages; ++i) issued[i] = 0xFFFFFFFFu;
       for (int g = 0; g < n_iter && ok; ++g) {
         if (*fail_flag) break;
         const int step = g / n_loc;
         const int t = blockIdx.x + (g - step * n_loc) * G;
-        if (tma_base) {
-          // base slot g&1 is free once the epilogue released iteration g-2
-          const int bs = g & 1;
-          if (!mbar_wait(&acc_empty[bs], ((g >> 1) & 1) ^ 1u, P.status)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&base_full[bs], base_stage_bytes);
-          tc::tma_load_3d(base_s + bs * base_stride, &tmap_base, t * kM, step, 0, &base_full[bs],
-                          pol_stream);
-          base_par[bs] = (g >> 1) & 1;
-        }
         for (int kc = 0; kc < NK; ++kc) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, P.status)) {
             ok = false;
@@ -323,8 +343,31 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       // every copy this CTA issued has landed before the CTA may exit
       for (int s2 = 0; s2 < ns; ++s2)
         if (issued[s2] != 0xFFFFFFFFu) (void)mbar_wait(&full[s2], issued[s2], P.status);
-      for (int bs = 0; bs < 2; ++bs)
-        if (base_par[bs] != 0xFFFFFFFFu) (void)mbar_wait(&base_full[bs], base_par[bs], P.status);
+    }
+  } else if (warp == kBaseWarp) {
+    // ---- TMA producer of the base logits: one [B] x 128 box per tile ------------
+    if (lane == 0 && tma_base) {
+      const uint64_t pol_stream = policy_evict_first();
+      uint32_t last[kMaxBaseSlots];
+#pragma unroll
+      for (int i = 0; i < kMaxBaseSlots; ++i) last[i] = 0xFFFFFFFFu;
+      for (int g = 0; g < n_iter; ++g) {
+        if (*fail_flag) break;
+        const int step = g / n_loc;
+        const int t = blockIdx.x + (g - step * n_loc) * G;
+        const int bs = g % nb;
+        const uint32_t bph = static_cast<uint32_t>(g / nb) & 1u;
+        if (!mbar_wait(&bempty[bs], bph ^ 1u, P.status)) {
+          *fail_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&bfull[bs], cfg.base_stage_bytes);
+        tc::tma_load_3d(base_s + bs * base_stride, &tmap_base, t * kM, step, 0, &bfull[bs],
+                        pol_stream);
+        last[bs] = bph;
+      }
+      for (int bs = 0; bs < nb; ++bs)
+        if (last[bs] != 0xFFFFFFFFu) (void)mbar_wait(&bfull[bs], last[bs], P.status);
     }
   } else if (warp == 1) {
     // ---- MMA issuer -------------------------------------------------------------
@@ -343,8 +386,8 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           }
           tc::fence_after_thread_sync();
         }
-        const int ab = g & 1;
-        if (!mbar_wait(&acc_empty[ab], ((g >> 1) & 1) ^ 1u, P.status)) {
+        const int ab = g % na;
+        if (!mbar_wait(&acc_empty[ab], (static_cast<uint32_t>(g / na) & 1u) ^ 1u, P.status)) {
           ok = false;
           break;
         }
@@ -377,18 +420,13 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       (void)mbar_wait(drain, 0u, P.status);
     }
   } else {
-    // ---- epilogue -------------------------------------------------------------
+    // ---- epilogue (warps 2..17) -----------------------------------------------
     const int etid = tid - 64;       // 0..511 among the epilogue threads
     const int q = warp & 3;          // TMEM lane quarter: rows 32q..32q+31 of a tile
     const int sub = (warp - 2) >> 2;
     const int c_begin = sub * CPW;   // batch columns [c_begin, c_begin + CPW)
     const int c_live = min(CPW, B - c_begin);  // columns below B (may be <= 0)
-    const bool base_bf16 = P.base_bf16 != 0;
-    const bool cache_bf16 = P.cache_bf16 != 0;
-    const float* base_f = static_cast<const float*>(P.base);
-    const uint16_t* base_h = static_cast<const uint16_t*>(P.base);
-    float* cache_f = static_cast<float*>(P.cache);
-    uint16_t* cache_h = static_cast<uint16_t*>(P.cache);
+    const int r = q * 32 + lane;     // this lane's row of a tile
     uint32_t run_ord[kRegWinners ? CPW : 1];
     uint32_t run_v[kRegWinners ? CPW : 1];
 #pragma unroll
@@ -396,42 +434,32 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       run_ord[j] = 0u;
       run_v[j] = 0xFFFFFFFFu;
     }
-    auto load_base = [&](int step, int cb, int v, bool in_range, float (&bv)[4]) {
+    // base logits straight from global memory (no staged tile)
+    auto load_direct = [&](int cb, int v, bool in_range, float (&bv)[GW]) {
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int b = cb + jj;
-        bv[jj] = 0.f;
-        if (s_act[b] && in_range) {  // warp-uniform request test
-          const int64_t bo = s_bbase[b] + static_cast<int64_t>(step) * V;
-          bv[jj] = base_bf16 ? bf16_bits_to_float(__ldg(base_h + bo + v)) : __ldg(base_f + bo + v);
-        }
-      }
-    };
-    // staged tile: element (b, row r) of slot ab at b * 128 + r
-    auto smem_base = [&](int ab, int cb, int r, float (&bv)[4]) {
-      const unsigned char* sb = base_s + ab * base_stride;
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int b = cb + jj;
-        bv[jj] = b < B ? (base_bf16 ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sb)[b * kM + r])
-                                    : reinterpret_cast<const float*>(sb)[b * kM + r])
-                       : 0.f;
+      for (int j = 0; j < GW; ++j) {
+        const unsigned char* bp = s_bptr[cb + j];  // null: not a live request
+        bv[j] = 0.f;
+        if (bp != nullptr && in_range)
+          bv[j] = bes == 2 ? bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(bp) + v))
+                           : __ldg(reinterpret_cast<const float*>(bp) + v);
       }
     };
     bool skip = false;  // set after a failed wait: the warp then only walks the loop
     for (int g = 0; g < n_iter; ++g) {
       const int step = g / n_loc;
       const int t = blockIdx.x + (g - step * n_loc) * G;
-      const int ab = g & 1;
-      const uint32_t aph = (g >> 1) & 1;
-      const int v = t * kM + q * 32 + lane;
+      const int ab = g % na;
+      const uint32_t aph = static_cast<uint32_t>(g / na) & 1u;
+      const int bs = tma_base ? g % nb : 0;
+      const uint32_t bph = tma_base ? static_cast<uint32_t>(g / nb) & 1u : 0u;
+      const int v = t * kM + r;
       const bool in_range = v < V;
-      // base logits of the first chunk, issued before the accumulator wait
-      float bnext[4];
-      if (!skip && !tma_base && c_live > 0) load_base(step, c_begin, v, in_range, bnext);
+      float bnext[GW];
+      if (!skip && !tma_base && c_live > 0) load_direct(c_begin, v, in_range, bnext);
       if (!skip) {
         bool ok = mbar_wait(&acc_full[ab], aph, P.status);
-        if (ok && tma_base) ok = mbar_wait(&base_full[ab], aph, P.status);
+        if (ok && tma_base) ok = mbar_wait(&bfull[bs], bph, P.status);
         if (!ok) {
           *fail_flag = 1;
           skip = true;
@@ -439,60 +467,79 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       }
       if (!skip) {
         tc::fence_after_thread_sync();
-        if (tma_base && c_live > 0) smem_base(ab, c_begin, q * 32 + lane, bnext);
+        const unsigned char* sb = base_s + bs * base_stride;
 #pragma unroll
-        for (int c = 0; c < CPW; c += 4) {
-          if (c >= c_live) break;
+        for (int c = 0; c < CPW; c += GW) {
+          if (c >= c_live) break;  // warp-uniform
           const int cb = c_begin + c;
-          const float bv[4] = {bnext[0], bnext[1], bnext[2], bnext[3]};
-          if (c + 4 < c_live) {
-            if (tma_base)
-              smem_base(ab, cb + 4, q * 32 + lane, bnext);
-            else
-              load_base(step, cb + 4, v, in_range, bnext);
+          uint32_t acc[GW];
+          tmem_load_group<GW>(tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                                  static_cast<uint32_t>(ab * Npad + cb),
+                              acc);
+          float bv[GW];
+          if (tma_base) {
+#pragma unroll
+            for (int j = 0; j < GW; ++j) {
+              const int b = cb + j;
+              bv[j] = b < B ? (bes == 2 ? bf16_bits_to_float(
+                                              reinterpret_cast<const uint16_t*>(sb)[b * kM + r])
+                                        : reinterpret_cast<const float*>(sb)[b * kM + r])
+                            : 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < GW; ++j) bv[j] = bnext[j];
+            if (c + GW < c_live) load_direct(cb + GW, v, in_range, bnext);
           }
-          uint32_t acc[4];
-          tc::tmem_ld4(tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                           static_cast<uint32_t>(ab * Npad + cb),
-                       acc);
-          // Philox block of this lane quad's 4 columns, for request cb+(lane&3),
-          // transposed so that nw[r] is this lane's noise for request cb+r
-          const int bq = cb + (lane & 3);
-          const U4 r = noise_block(s_seed[bq], s_p0[bq] + step - 1, static_cast<uint32_t>(v),
-                                   kStreamDraft);
-          uint32_t nw[4] = {r.x, r.y, r.z, r.w};
-          quad_transpose(nw);
-          const float4 ti4 = *reinterpret_cast<const float4*>(s_tinv + cb);
-          const float tinv[4] = {ti4.x, ti4.y, ti4.z, ti4.w};
+          // Philox blocks of this lane quad's 4 columns: block h for request
+          // cb + 4h + (lane & 3), transposed so that nw[4h + i] is this
+          // lane's noise for request cb + 4h + i
+          uint32_t nw[GW];
+#pragma unroll
+          for (int h = 0; h < GW / 4; ++h) {
+            const int bq = cb + 4 * h + (lane & 3);
+            const U4 blk = noise_block(s_seed[bq], s_npos[bq], static_cast<uint32_t>(v),
+                                       kStreamDraft);
+            nw[4 * h + 0] = blk.x;
+            nw[4 * h + 1] = blk.y;
+            nw[4 * h + 2] = blk.z;
+            nw[4 * h + 3] = blk.w;
+            quad_transpose(nw + 4 * h);
+          }
+          float tinv[GW];
+#pragma unroll
+          for (int h = 0; h < GW / 4; ++h) {
+            const float4 t4 = *reinterpret_cast<const float4*>(s_tinv + cb + 4 * h);
+            tinv[4 * h + 0] = t4.x;
+            tinv[4 * h + 1] = t4.y;
+            tinv[4 * h + 2] = t4.z;
+            tinv[4 * h + 3] = t4.w;
+          }
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int jb = 0; jb < 4; ++jb) {
-            if (jb >= c_live - c) break;  // warp-uniform
-            const int b = cb + jb;
-            uint32_t ord = 0u;
-            if (s_act[b]) {  // warp-uniform: a live request
-              const float z = __fadd_rn(bv[jb], __uint_as_float(acc[jb]));
-              float x = z, y = z;
-              if (tinv[jb] > 0.f) {  // warp-uniform: sampled (x = z * (1/T))
-                x = __fmul_rn(z, tinv[jb]);
-                y = __fadd_rn(x, gumbel_of(nw[jb]));
-              }
-              const int64_t cb0 = s_cbase[b];
-              if (cb0 >= 0 && in_range) {
-                const int64_t co = cb0 + static_cast<int64_t>(step) * V + v;
-                if (cache_bf16)
-                  cache_h[co] = float_to_bf16_bits(x);
-                else
-                  cache_f[co] = x;
-              }
-              ord = in_range ? ordered_bits(y) : 0u;  // every real value maps above 0
+          for (int j = 0; j < GW; ++j) {
+            if (j >= c_live - c) break;  // warp-uniform
+            const int b = cb + j;
+            const float z = __fadd_rn(bv[j], __uint_as_float(acc[j]));
+            float x = z, y = z;
+            if (tinv[j] > 0.f) {  // warp-uniform: sampled (x = z * (1/T))
+              x = __fmul_rn(z, tinv[j]);
+              y = __fadd_rn(x, gumbel_of(nw[j]));
             }
+            unsigned char* cp = s_cptr[b];  // warp-uniform; null: no store
+            if (cp != nullptr && in_range) {
+              if (ces == 2)
+                reinterpret_cast<uint16_t*>(cp)[v] = float_to_bf16_bits(x);
+              else
+                reinterpret_cast<float*>(cp)[v] = x;
+            }
+            const uint32_t ord = in_range ? ordered_bits(y) : 0u;  // real values map above 0
             if constexpr (kRegWinners) {
               // rows of a lane only grow across a step's tiles: a strict >
               // keeps the lowest row on ties
-              if (ord > run_ord[c + jb]) {
-                run_ord[c + jb] = ord;
-                run_v[c + jb] = static_cast<uint32_t>(v);
+              if (ord > run_ord[c + j]) {
+                run_ord[c + j] = ord;
+                run_v[c + j] = static_cast<uint32_t>(v);
               }
             } else {
               const unsigned long long key = warp_winner(ord, static_cast<uint32_t>(v));
@@ -502,7 +549,10 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         }
         tc::fence_before_thread_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[ab]);
+        if (lane == 0) {
+          mbar_arrive(&acc_empty[ab]);
+          if (tma_base) mbar_arrive(&bempty[bs]);
+        }
       }
       if (g != (step + 1) * n_loc - 1) continue;
 
@@ -553,15 +603,25 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       }
       epi_bar();
       if (*stop_word || (last && blockIdx.x != 0)) break;  // uniform over the epilogue
-      for (int b = etid; b < B; b += kEpiThreads) {
+      for (int b = etid; b < Npad; b += kEpiThreads) {
         int32_t tok = -1;
-        if (s_act[b]) {
+        if (b < B && s_act[b]) {
           const unsigned long long m = __ldcg(keys + b);
           if (m != 0ull) tok = key_index(m);
         }
-        if (blockIdx.x == 0) P.out_tokens[static_cast<int64_t>(b) * K + step] = tok;
+        if (blockIdx.x == 0 && b < B) P.out_tokens[static_cast<int64_t>(b) * K + step] = tok;
         s_prev[b] = tok;
         s_act[b] = tok >= 0;
+        if (!last) {  // advance the per-request state to the next step
+          s_npos[b] += 1;
+          if (tok >= 0) {
+            if (s_bptr[b] != nullptr) s_bptr[b] += static_cast<int64_t>(V) * bes;
+            if (s_cptr[b] != nullptr) s_cptr[b] += static_cast<int64_t>(V) * ces;
+          } else {
+            s_bptr[b] = nullptr;
+            s_cptr[b] = nullptr;
+          }
+        }
       }
       if (!last) {
         epi_bar();
@@ -576,7 +636,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_thread_sync();
-    tc::tmem_dealloc(tmem, tmem_cols);
+    tc::tmem_dealloc(tmem, cfg.tmem_cols);
   }
 }
 
@@ -593,20 +653,26 @@ cudaError_t launch_tc_cpw(const MarkovStepParams& p, const CUtensorMap& map,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(plan.smem));
   if (err != cudaSuccess) return err;
+  TcCfg cfg;
+  cfg.Npad = plan.Npad;
+  cfg.ns = plan.stages;
+  cfg.na = plan.acc_buffers;
+  cfg.nb = plan.base_slots;
+  cfg.tmem_cols = plan.tmem_cols;
+  cfg.base_stage_bytes = plan.base_stage_bytes;
   // cooperative: every CTA is resident at once, which the grid barrier
   // between steps relies on
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreadsTc, 1, 1);
-  cfg.dynamicSmemBytes = plan.smem;
-  cfg.stream = stream;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  lc.blockDim = dim3(kThreadsTc, 1, 1);
+  lc.dynamicSmemBytes = plan.smem;
+  lc.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, markov_loop_tc_kernel<CPW>, map, bmap, p, plan.Npad,
-                            plan.stages, plan.tmem_cols, plan.base_stage_bytes);
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, markov_loop_tc_kernel<CPW>, map, bmap, p, cfg);
 }
 
 }  // namespace
@@ -616,24 +682,49 @@ bool markov_tc_plan(int B, int R, int base_elem_bytes, bool base_tma_ok, MarkovT
   const int NK = R / 64;
   int Npad = (B + 15) & ~15;
   if (Npad < 16) Npad = 16;
-  // stage the base logits through TMA when it leaves at least 4 w2 stages
-  size_t bstage = base_tma_ok ? static_cast<size_t>(kM) * B * base_elem_bytes : 0;
-  int ns = kMaxStages;
-  while (ns >= 4 && TcLayout(Npad, NK, ns, bstage).total > kSmemLimit) --ns;
-  if (TcLayout(Npad, NK, ns, bstage).total > kSmemLimit) {
-    bstage = 0;
-    ns = kMaxStages;
-    while (ns >= 2 && TcLayout(Npad, NK, ns, 0).total > kSmemLimit) --ns;
-  }
-  if (ns < 2) return false;
-  plan->base_stage_bytes = static_cast<unsigned>(bstage);
+  int na = 512 / Npad;  // accumulator buffers: as many as TMEM holds, up to 4
+  if (na > kMaxAcc) na = kMaxAcc;
+  if (na < 2) return false;
   uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(2 * Npad)) cols <<= 1;
+  while (cols < static_cast<uint32_t>(na * Npad)) cols <<= 1;
   if (cols > 512) return false;
+  auto max_stages = [&](int nb, size_t bstage) {
+    int ns = kMaxStages;
+    while (ns > 0 && TcLayout(Npad, NK, ns, nb, bstage).total > kSmemLimit) --ns;
+    return ns;
+  };
+  // Stage the base logits through TMA when that leaves a deep markov_w2 ring:
+  // the most base slots that keep 8 ring stages, else that keep 4.
+  int ns = 0, nb = 0;
+  size_t bstage = 0;
+  if (base_tma_ok) {
+    const size_t bt = static_cast<size_t>(kM) * B * base_elem_bytes;
+    const int slot_choices[] = {8, 6, 4, 3, 2};
+    const int min_stages[] = {8, 4};
+    for (int min_ns : min_stages) {
+      for (int cand : slot_choices) {
+        const int s = max_stages(cand, bt);
+        if (s >= min_ns) {
+          ns = s;
+          nb = cand;
+          break;
+        }
+      }
+      if (nb != 0) break;
+    }
+    if (nb != 0) bstage = bt;
+  }
+  if (nb == 0) {
+    ns = max_stages(0, 0);
+    if (ns < 2) return false;
+  }
   plan->Npad = Npad;
   plan->stages = ns;
+  plan->acc_buffers = na;
+  plan->base_slots = nb;
+  plan->base_stage_bytes = static_cast<unsigned>(bstage);
   plan->tmem_cols = cols;
-  plan->smem = TcLayout(Npad, NK, ns, bstage).total;
+  plan->smem = TcLayout(Npad, NK, ns, nb, bstage).total;
   return true;
 }
 
