@@ -302,6 +302,39 @@ __device__ __forceinline__ float4 ld_stream_f4(const float* p, uint64_t policy) 
   return v;
 }
 
+// Loads of read-only rows with an L2 eviction priority from `policy` (no L1
+// allocation). Not volatile: the compiler may batch them for more loads in
+// flight.
+__device__ __forceinline__ float4 ld_hint_f4(const float* p, uint64_t policy) {
+  float4 v;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_hint_u2(const void* p, uint64_t policy) {
+  uint2 v;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+      : "=r"(v.x), "=r"(v.y)
+      : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ float ld_hint_f32(const float* p, uint64_t policy) {
+  float v;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ uint16_t ld_hint_u16(const uint16_t* p, uint64_t policy) {
+  unsigned short v;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(policy));
+  return v;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Streaming 16-byte store (evict-first in L1 and L2).
 __device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
   asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x),

@@ -7,18 +7,23 @@
 // whose mass reaches p, plus the row max. Draft rows (the cache) get their
 // maximum and fixed-point mass. Greedy target rows get their winner key.
 //
-// A row is split over the CL CTAs of a cluster (CL up to 16). Each CTA reads
-// its slice from HBM exactly once into shared memory and every later pass
-// (fixed-point mass, the radix stages of the top-p select) runs on the
-// shared-memory copy. Reductions across the cluster go through distributed
-// shared memory: scalars by each CTA reading the others' slots, histograms
-// by each CTA reducing its own range of bins over the cluster.
+// A row is split over the CL CTAs of a cluster (CL up to 16, slices of at
+// most 32768 values). Each CTA reads its slice from HBM once (the maximum)
+// with an L2 evict-last hint, and the later passes (fixed-point mass, the
+// radix stages of the top-p select) read it again from L2; with nothing held
+// in shared memory but histograms, four CTAs share an SM and many rows are
+// in flight. Reductions across the cluster go through distributed shared
+// memory: scalars by each CTA reading the others' slots, histograms by each
+// CTA reducing its own range of bins over the cluster.
 //
-// Top-p select: a radix select on the ordered bits kd of the scaled logits,
-// most significant first (11 + 11 + 10 bits), with histograms of fixed-point
-// mass; each stage finds the first bin (in descending kd order) at which the
-// running mass reaches P32 * F / 2^32. Exact ties at the boundary value are
-// resolved by two more stages on the token id (ascending, 11 + 11 bits).
+// Top-p select: a radix select in (logit descending, token id ascending)
+// order with histograms of fixed-point mass; each stage finds the first bin at
+// which the running mass reaches P32 * F / 2^32 and the next stage splits
+// that bin, until the bin holds one element. The first two stages bin by the
+// distance to the row maximum (2048 bins of 1/64 over [0, 32), then 2048
+// sub-bins of the chosen bin), which spreads typical rows over many bins;
+// then come the ordered bits kd of the logit (11 + 11 + 10 bits) and, for
+// exact ties, the token id (11 + 11 bits).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -33,10 +38,9 @@ namespace dspark {
 
 namespace {
 
-constexpr int kRowThreads = 512;
+constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kRowBins = 2048;
-constexpr size_t kRowSmemLimit = 227u * 1024u;
 
 struct RowSmem {
   unsigned long long hmass[kRowBins];
@@ -316,65 +320,98 @@ __device__ Found cluster_find(cg::cluster_group& cl, RowSmem& sm, int nb, bool d
   return f;
 }
 
-// One local histogram pass over the shared-memory slice: elements whose kd
-// and id pass `match` add their fixed-point mass to bin digit(kd, id).
-template <class Val, class Match, class Digit>
-__device__ void hist_pass(RowSmem& sm, Val xval, int n, int v0, float m, int nb, Match match,
-                          Digit digit) {
-  hist_clear(sm, nb);
-  __syncthreads();
-  const int lane = threadIdx.x & 31;
-  for (int base = threadIdx.x & ~31; base < n; base += kRowThreads) {
-    const int i = base + lane;
-    const bool valid = i < n;
-    const float x = valid ? xval(i) : -INFINITY;
-    const uint32_t kd = kd_of(x);
-    const uint32_t id = static_cast<uint32_t>(v0 + i);
-    const bool act = valid && match(kd, id);
-    const unsigned long long f = act ? fixed_mass(exp_rel(x, m)) : 0ull;
-    hist_add(sm, act, act ? digit(kd, id) : 0, f, id);
-  }
+// Digits of the first two top-p stages: the distance to the maximum in bins
+// of 1/64 (the last bin takes everything from 2047/64 on, -inf included),
+// then 2048 sub-bins of bin a0. Both are non-decreasing in m - x (fp32
+// rounding is monotone and the scalings are exact; for x in bin a0 the
+// subtraction of a0 is exact), so bins follow the descending order of x and
+// equal values share a bin.
+__device__ __forceinline__ int adigit0(float x, float m) {
+  return static_cast<int>(fminf(__fmul_rn(__fsub_rn(m, x), 64.0f), 2047.0f));
+}
+__device__ __forceinline__ int adigit1(float x, float m, int a0) {
+  const float t = __fsub_rn(__fmul_rn(__fsub_rn(m, x), 64.0f), static_cast<float>(a0));
+  return static_cast<int>(fminf(__fmul_rn(t, 2048.0f), 2047.0f));
 }
 
-// Loads the slice [v0, v0 + n) of a row into shared memory: one bulk copy of
-// the 16-byte-aligned body (issued by thread 0, completion on `bar`), plain
-// loads for a ragged tail or an unaligned row. fp32 rows land as fp32, bf16
-// rows as bf16 bit patterns. Returns false if the bounded wait ran out.
-__device__ bool slice_fetch(const void* row, bool bf16, int v0, int n, void* dst, uint64_t* bar,
-                            uint32_t& phase, int32_t* status) {
-  const int es = bf16 ? 2 : 4;
-  const unsigned char* src = static_cast<const unsigned char*>(row) + static_cast<size_t>(v0) * es;
-  const bool aligned = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-  const int body = aligned ? ((n * es) & ~15) / es : 0;  // elements moved by the bulk copy
-  if (body > 0 && threadIdx.x == 0) {
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(body * es));
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(static_cast<uint32_t>(body * es)), "r"(smem_addr(bar))
-        : "memory");
+// Reads of one row's slice [v0, v0 + n) straight from global memory. The
+// first pass brings the slice from HBM (L2 evict-last: every later pass of
+// the row reads it again from L2); `fix` maps a raw value to x (temperature,
+// NaN read as -inf). `vec` = the slice start is 16-byte aligned (fp32) or
+// 8-byte aligned (bf16), so it can be read 4 values at a time.
+struct RowView {
+  const float* f;
+  const uint16_t* h;
+  bool bf16;
+  bool vec;
+  int n;
+};
+
+template <class Fix, class Body>
+__device__ __forceinline__ void row_sweep(const RowView& rv, uint64_t pol, Fix fix, Body body) {
+  const int tid = threadIdx.x;
+  int done = 0;
+  if (rv.vec) {
+    const int n4 = rv.n >> 2;
+    constexpr int kU = 4;  // 16-byte loads in flight per thread
+    int i = tid;
+    for (; i + (kU - 1) * kRowThreads < n4; i += kU * kRowThreads) {
+      float v[kU][4];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = i + u * kRowThreads;
+        if (rv.bf16) {
+          const uint2 w = ld_hint_u2(rv.h + 4 * j, pol);
+          v[u][0] = bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu));
+          v[u][1] = bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16));
+          v[u][2] = bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu));
+          v[u][3] = bf16_bits_to_float(static_cast<uint16_t>(w.y >> 16));
+        } else {
+          const float4 c = ld_hint_f4(rv.f + 4 * j, pol);
+          v[u][0] = c.x;
+          v[u][1] = c.y;
+          v[u][2] = c.z;
+          v[u][3] = c.w;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = 4 * (i + u * kRowThreads);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) body(j + e, fix(v[u][e]));
+      }
+    }
+    for (; i < n4; i += kRowThreads) {
+      float v[4];
+      if (rv.bf16) {
+        const uint2 w = ld_hint_u2(rv.h + 4 * i, pol);
+        v[0] = bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu));
+        v[1] = bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16));
+        v[2] = bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu));
+        v[3] = bf16_bits_to_float(static_cast<uint16_t>(w.y >> 16));
+      } else {
+        const float4 c = ld_hint_f4(rv.f + 4 * i, pol);
+        v[0] = c.x;
+        v[1] = c.y;
+        v[2] = c.z;
+        v[3] = c.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) body(4 * i + e, fix(v[e]));
+    }
+    done = 4 * n4;
   }
-  for (int j = body + threadIdx.x; j < n; j += kRowThreads) {
-    if (bf16)
-      static_cast<uint16_t*>(dst)[j] = __ldg(reinterpret_cast<const unsigned short*>(src) + j);
-    else
-      static_cast<float*>(dst)[j] = __ldg(reinterpret_cast<const float*>(src) + j);
+  for (int i = done + tid; i < rv.n; i += kRowThreads) {
+    const float c = rv.bf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol)) : ld_hint_f32(rv.f + i, pol);
+    body(i, fix(c));
   }
-  bool ok = true;
-  if (body > 0) {
-    ok = mbar_wait(bar, phase, status);
-    phase ^= 1u;
-  }
-  if (body < n) __syncthreads();  // the plain-loaded tail is visible to every thread
-  return ok;
 }
 
 // One row: statistics written to P.tstats / P.dstats. Every CTA of the
 // cluster runs the same sequence of cluster barriers (all decisions depend on
 // the row or on cluster-reduced values only).
 __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluster_group& cl,
-                            int CL, int rank, RowSmem& sm, float* xs, uint64_t* bar,
-                            uint32_t& phase, int& jrow) {
+                            int CL, int rank, RowSmem& sm, int& jrow) {
   const int tid = threadIdx.x;
   const int K = P.K, V = P.V;
   const int nT = P.B * (K + 1);
@@ -404,36 +441,42 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
   ++jrow;
   const int v0 = rank * W;
   const int n = max(0, min(W, V - v0));
-  const void* row;
+  int64_t off;
   bool bf16;
   if (is_target) {
-    const int64_t off = (static_cast<int64_t>(b) * (K + 1) + k) * V;
+    off = (static_cast<int64_t>(b) * (K + 1) + k) * V;
     bf16 = P.target_bf16 != 0;
-    row = bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(P.target) + off)
-               : static_cast<const void*>(static_cast<const float*>(P.target) + off);
   } else {
-    const int64_t off = (crow * K + k) * V;
+    off = (crow * K + k) * V;
     bf16 = P.cache_bf16 != 0;
-    row = bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(P.cache) + off)
-               : static_cast<const void*>(static_cast<const float*>(P.cache) + off);
   }
+  const void* base = is_target ? P.target : P.cache;
+  RowView rv;
+  rv.bf16 = bf16;
+  rv.f = static_cast<const float*>(base) + off + v0;
+  rv.h = static_cast<const uint16_t*>(base) + off + v0;
+  rv.vec = bf16 ? (reinterpret_cast<uintptr_t>(rv.h) & 7u) == 0
+                : (reinterpret_cast<uintptr_t>(rv.f) & 15u) == 0;
+  rv.n = n;
   const int32_t d = k < K ? P.draft[static_cast<int64_t>(b) * K + k] : -1;
   TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(b) * (K + 1) + k;
   DrfStats* ds = static_cast<DrfStats*>(P.dstats) + static_cast<int64_t>(b) * K + (k < K ? k : 0);
-  const uint16_t* xh = reinterpret_cast<const uint16_t*>(xs);
-
-  // ---- the slice into shared memory --------------------------------------------
-  fence_proxy_async_smem();
-  const bool fetched = slice_fetch(row, bf16, v0, n, xs, bar, phase, P.status);
+  const uint64_t pol_keep = policy_evict_last();
+  const uint64_t pol_last_use = policy_evict_first();
+  // one element of the row by token id (any CTA may read any element)
+  auto raw_at = [&](int v) -> float {
+    const int64_t o = off + v;
+    return bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(base)[o])
+                : static_cast<const float*>(base)[o];
+  };
 
   // ---- greedy target row: winner key of the raw row ----------------------------
   if (is_target && greedy) {
     unsigned long long key = 0ull;
-    for (int i = tid; i < n; i += kRowThreads) {
-      const float t = bf16 ? bf16_bits_to_float(xh[i]) : xs[i];
+    row_sweep(rv, pol_last_use, [](float c) { return c; }, [&](int i, float t) {
       key = umax64(key, winner_key(t, static_cast<uint32_t>(v0 + i)));
-    }
-    key = cluster_max_u64(cl, sm, fetched ? key : 0ull, set, CL);
+    });
+    key = cluster_max_u64(cl, sm, key, set, CL);
     if (rank == 0 && tid == 0) {
       ts->m = 0.f;
       ts->D = 1.f;
@@ -446,46 +489,19 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
     return;
   }
 
-  // ---- pass 1: scale in place (fp32) and maximum -----------------------------------
-  // bf16 slices stay as bit patterns; the passes widen them on the fly.
-  float lmax = -INFINITY;
-  if (bf16) {
-    for (int i = tid; i < n; i += kRowThreads) {
-      const float c = bf16_bits_to_float(xh[i]);
-      lmax = fmaxf(lmax, is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c));
-    }
-  } else {
-    auto fix = [&](float c) { return is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c); };
-    const int n4 = n >> 2;
-    float4* xs4 = reinterpret_cast<float4*>(xs);
-    for (int i = tid; i < n4; i += kRowThreads) {
-      const float4 c = xs4[i];
-      const float4 x = make_float4(fix(c.x), fix(c.y), fix(c.z), fix(c.w));
-      if (__float_as_uint(x.x) != __float_as_uint(c.x) || __float_as_uint(x.y) != __float_as_uint(c.y) ||
-          __float_as_uint(x.z) != __float_as_uint(c.z) || __float_as_uint(x.w) != __float_as_uint(c.w))
-        xs4[i] = x;
-      lmax = fmaxf(lmax, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
-    }
-    for (int i = 4 * n4 + tid; i < n; i += kRowThreads) {
-      const float c = xs[i];
-      const float x = fix(c);
-      if (__float_as_uint(x) != __float_as_uint(c)) xs[i] = x;
-      lmax = fmaxf(lmax, x);
-    }
-  }
-  // a timed-out copy drops the row for the whole cluster (status is set)
-  bool any_fail = false;
-  const float m = cluster_max_f(cl, sm, lmax, !fetched, set, CL, &any_fail);
-  if (any_fail) return;
-  auto xval = [&](int i) -> float {
-    if (!bf16) return xs[i];
-    const float c = bf16_bits_to_float(xh[i]);
-    return is_target ? scale_logit(c, T) : ((c != c) ? -INFINITY : c);
+  // x: the target row after temperature, the draft row as stored; NaN reads as -inf
+  const bool scale = is_target && T != 1.0f;
+  auto fix = [=](float c) -> float {
+    const float x = scale ? __fdiv_rn(c, T) : c;
+    return (x != x) ? -INFINITY : x;
   };
-  // The drafted token's value, read now: after this row's last cluster
-  // barrier the CTA's threads may already be loading the next row's slice.
-  const bool own_d = tid == 0 && d >= v0 && d < v0 + n;
-  const float xd = own_d ? xval(d - v0) : 0.0f;
+  const bool topp = is_target && P.top_p[s] < 1.0f;
+
+  // ---- pass 1 (HBM): maximum --------------------------------------------------------
+  float lmax = -INFINITY;
+  row_sweep(rv, pol_keep, fix, [&](int, float x) { lmax = fmaxf(lmax, x); });
+  bool any_fail = false;
+  const float m = cluster_max_f(cl, sm, lmax, false, set, CL, &any_fail);
   if (m == -INFINITY) {
     if (rank == 0 && tid == 0) {
       if (is_target) {
@@ -506,31 +522,18 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
     return;
   }
 
-  // ---- pass 2: fixed-point mass (+ first top-p histogram) -------------------------
-  const bool topp = is_target && P.top_p[s] < 1.0f;
+  // ---- pass 2 (L2): fixed-point mass (+ first top-p histogram) -----------------
   if (topp) hist_clear(sm, kRowBins);
   __syncthreads();
   unsigned long long F = 0ull;
   if (topp) {
-    const int lane = tid & 31;
-    for (int base = tid & ~31; base < n; base += kRowThreads) {
-      const int i = base + lane;
-      const bool valid = i < n;
-      const float x = valid ? xval(i) : -INFINITY;
-      const unsigned long long f = valid ? fixed_mass(exp_rel(x, m)) : 0ull;
+    row_sweep(rv, pol_keep, fix, [&](int i, float x) {
+      const unsigned long long f = fixed_mass(exp_rel(x, m));
       F += f;
-      hist_add(sm, valid, static_cast<int>(kd_of(x) >> 21), f, static_cast<uint32_t>(v0 + i));
-    }
-  } else if (!bf16) {
-    const int n4 = n >> 2;
-    for (int i = tid; i < n4; i += kRowThreads) {
-      const float4 x4 = reinterpret_cast<const float4*>(xs)[i];
-      F += fixed_mass(exp_rel(x4.x, m)) + fixed_mass(exp_rel(x4.y, m)) +
-           fixed_mass(exp_rel(x4.z, m)) + fixed_mass(exp_rel(x4.w, m));
-    }
-    for (int i = 4 * n4 + tid; i < n; i += kRowThreads) F += fixed_mass(exp_rel(xs[i], m));
+      hist_add(sm, true, adigit0(x, m), f, static_cast<uint32_t>(v0 + i));
+    });
   } else {
-    for (int i = tid; i < n; i += kRowThreads) F += fixed_mass(exp_rel(xval(i), m));
+    row_sweep(rv, pol_last_use, fix, [&](int, float x) { F += fixed_mass(exp_rel(x, m)); });
   }
   F = cluster_sum_u64(cl, sm, F, set, CL);
 
@@ -543,119 +546,92 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
     const unsigned long long P32 = topp_scaled(P.top_p[s]);
     const unsigned long long t_lo = P32 * F;
     const unsigned long long t_hi = __umul64hi(P32, F);
-    bool resolved = false;
-    // kd stage 0: bits [31:21]
-    Found f = cluster_find(cl, sm, kRowBins, true, 0ull, t_hi, t_lo, CL, rank);
+    // stage 0 (its histogram was built in pass 2): distance bins, ascending
+    Found f = cluster_find(cl, sm, kRowBins, false, 0ull, t_hi, t_lo, CL, rank);
     unsigned long long above = f.before;
-    uint32_t pre = static_cast<uint32_t>(f.bin);
-    if (f.cnt == 1u) {
-      id_thr = static_cast<int32_t>(f.id);
-      Fk = above + f.mass;
-      resolved = true;
-    }
-    if (!resolved) {  // kd stage 1: bits [20:10]
-      const uint32_t p0 = pre;
-      hist_pass(sm, xval, n, v0, m, kRowBins, [=](uint32_t kd, uint32_t) { return (kd >> 21) == p0; },
-                [](uint32_t kd, uint32_t) { return static_cast<int>((kd >> 10) & 0x7FFu); });
-      f = cluster_find(cl, sm, kRowBins, true, above, t_hi, t_lo, CL, rank);
-      above = f.before;
-      pre = (pre << 11) | static_cast<uint32_t>(f.bin);
-      if (f.cnt == 1u) {
-        id_thr = static_cast<int32_t>(f.id);
-        Fk = above + f.mass;
-        resolved = true;
-      }
-    }
-    if (!resolved) {  // kd stage 2: bits [9:0]
-      const uint32_t p1 = pre;
-      hist_pass(sm, xval, n, v0, m, 1024, [=](uint32_t kd, uint32_t) { return (kd >> 10) == p1; },
-                [](uint32_t kd, uint32_t) { return static_cast<int>(kd & 0x3FFu); });
-      f = cluster_find(cl, sm, 1024, true, above, t_hi, t_lo, CL, rank);
-      above = f.before;
-      pre = (pre << 10) | static_cast<uint32_t>(f.bin);
-      if (f.cnt == 1u) {
-        id_thr = static_cast<int32_t>(f.id);
-        Fk = above + f.mass;
-        resolved = true;
-      }
-    }
-    if (resolved) {
-      // full kd of the boundary element, read from the CTA that holds it
-      if (tid == 0) {
-        const int owner = id_thr / W;
-        const int li = id_thr - owner * W;
-        float xb;
-        if (bf16) {
-          const float c = bf16_bits_to_float(
-              *cl.map_shared_rank(const_cast<uint16_t*>(xh) + li, owner));
-          xb = scale_logit(c, T);
-        } else {
-          xb = *cl.map_shared_rank(xs + li, owner);
+    const int a0 = f.bin;
+    int a1 = -1;
+    int kd_len = 0, id_len = 0;
+    uint32_t kd_pre = 0u, id_pre = 0u;
+    // Stages 1..6 split the boundary bin until it holds one element: the
+    // distance sub-bins, kd bits [31:21], [20:10], [9:0], id bits [21:11],
+    // [10:0]. After the last id stage the bin is a single token.
+    for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
+      const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
+      const uint32_t c_kp = kd_pre, c_ip = id_pre;
+      auto match = [=](float x, uint32_t kd, uint32_t id) {
+        if (adigit0(x, m) != a0) return false;
+        if (c_a1 >= 0 && adigit1(x, m, a0) != c_a1) return false;
+        if (c_kl > 0 && (kd >> (32 - c_kl)) != c_kp) return false;
+        if (c_il > 0 && (id >> (22 - c_il)) != c_ip) return false;
+        return true;
+      };
+      auto digit = [=](float x, uint32_t kd, uint32_t id) -> int {
+        switch (stage) {
+          case 1: return adigit1(x, m, a0);
+          case 2: return static_cast<int>(kd >> 21);
+          case 3: return static_cast<int>((kd >> 10) & 0x7FFu);
+          case 4: return static_cast<int>(kd & 0x3FFu);
+          case 5: return static_cast<int>((id >> 11) & 0x7FFu);
+          default: return static_cast<int>(id & 0x7FFu);
         }
-        sm.bcast_i = static_cast<int>(kd_of(xb));
-      }
-      cl.sync();  // the owner keeps its slice until this remote read is done
-      kd_thr = static_cast<uint32_t>(sm.bcast_i);
-    } else {
-      // exact ties at the boundary value: token id ascending, 11 + 11 bits
-      kd_thr = pre;
-      const uint32_t kt = kd_thr;
-      hist_pass(sm, xval, n, v0, m, kRowBins, [=](uint32_t kd, uint32_t) { return kd == kt; },
-                [](uint32_t, uint32_t id) { return static_cast<int>((id >> 11) & 0x7FFu); });
-      f = cluster_find(cl, sm, kRowBins, false, above, t_hi, t_lo, CL, rank);
+      };
+      const int nb = stage == 4 ? 1024 : kRowBins;
+      const bool desc = stage >= 2 && stage <= 4;  // larger kd first; distance and id ascending
+      hist_clear(sm, nb);
+      __syncthreads();
+      row_sweep(rv, pol_keep, fix, [&](int i, float x) {
+        const uint32_t kd = kd_of(x);
+        const uint32_t id = static_cast<uint32_t>(v0 + i);
+        if (match(x, kd, id))
+          hist_add(sm, true, digit(x, kd, id), fixed_mass(exp_rel(x, m)), id);
+      });
+      f = cluster_find(cl, sm, nb, desc, above, t_hi, t_lo, CL, rank);
       above = f.before;
-      if (f.cnt == 1u) {
-        id_thr = static_cast<int32_t>(f.id);
-        Fk = above + f.mass;
+      const uint32_t bin = static_cast<uint32_t>(f.bin);
+      if (stage == 1) {
+        a1 = f.bin;
+      } else if (stage <= 4) {
+        kd_pre = (kd_pre << (stage == 4 ? 10 : 11)) | bin;
+        kd_len += stage == 4 ? 10 : 11;
       } else {
-        const uint32_t ip = static_cast<uint32_t>(f.bin);
-        hist_pass(sm, xval, n, v0, m, kRowBins,
-                  [=](uint32_t kd, uint32_t id) { return kd == kt && (id >> 11) == ip; },
-                  [](uint32_t, uint32_t id) { return static_cast<int>(id & 0x7FFu); });
-        f = cluster_find(cl, sm, kRowBins, false, above, t_hi, t_lo, CL, rank);
-        above = f.before;
-        id_thr = static_cast<int32_t>(f.id);
-        Fk = above + f.mass;
+        id_pre = (id_pre << 11) | bin;
+        id_len += 11;
       }
     }
+    // f is the one-element bin at the boundary: its token, mass and logit
+    id_thr = static_cast<int32_t>(f.id);
+    Fk = above + f.mass;
+    kd_thr = kd_of(fix(raw_at(id_thr)));
   }
   const float D = __fmul_rn(__ull2float_rn(Fk), 0x1p-40f);
 
-  // ---- outputs: p or q at the drafted token (its owner), the rest (rank 0) ---------
-  if (own_d) {
-    const float x = xd;
+  // ---- outputs (rank 0): p or q at the drafted token, the row statistics --------
+  if (rank == 0 && tid == 0) {
+    const bool has_d = d >= 0 && d < V;
+    const float x = has_d ? fix(raw_at(d)) : 0.0f;
     if (is_target) {
       const uint32_t kd = kd_of(x);
       const bool keep = mode == kModeKeepAll || kd > kd_thr || (kd == kd_thr && d <= id_thr);
-      ts->p_d = keep ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
-    } else {
-      ds->q_d = __fdiv_rn(exp_rel(x, m), D);
-    }
-  }
-  if (rank == 0 && tid == 0) {
-    if (is_target) {
+      ts->p_d = has_d && keep ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
       ts->m = m;
       ts->D = D;
       ts->kd_thr = kd_thr;
       ts->id_thr = id_thr;
       ts->mode = mode;
       ts->amax_key = 0ull;
-      if (!(d >= 0 && d < V)) ts->p_d = 0.0f;
     } else {
+      ds->q_d = has_d ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
       ds->m = m;
       ds->D = D;
       ds->zero = 0;
-      if (!(d >= 0 && d < V)) ds->q_d = 0.0f;
     }
   }
-  // A CTA may start its next slice copy now: its own threads are past every
-  // read of this slice (the last cluster barrier), and the other CTAs read a
-  // remote slice only inside the top-p stages, which end with a barrier.
 }
 
 // ---------------------------------------------------------------------------
 // Persistent clusters: cluster c handles rows c, c + nclusters, ...
-__global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParams P, int W,
+__global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyParams P, int W,
                                                                      int nrows) {
   cg::cluster_group cl = cg::this_cluster();
   const int CL = static_cast<int>(cl.num_blocks());
@@ -664,70 +640,32 @@ __global__ void __launch_bounds__(kRowThreads, 2) verify_rows_kernel(VerifyParam
   const int nclusters = gridDim.x / CL;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
-  float* xs = reinterpret_cast<float*>(smem_raw + ((sizeof(RowSmem) + 15) & ~size_t(15)));
-  __shared__ __align__(8) uint64_t bar;
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-  }
-  cl.sync();  // barriers initialised in every CTA before any row starts
-  uint32_t phase = 0;
   int jrow = 0;
-  for (int row = cid; row < nrows; row += nclusters)
-    process_row(P, W, row, cl, CL, rank, sm, xs, &bar, phase, jrow);
-  cl.sync();  // no CTA exits while another may still touch its shared memory
+  for (int row = cid; row < nrows; row += nclusters) process_row(P, W, row, cl, CL, rank, sm, jrow);
+  cl.sync();  // no CTA exits while another may still read its shared memory
 }
 
 }  // namespace
 
 size_t verify_rows_smem_bytes(int W) {
-  return ((sizeof(RowSmem) + 15) & ~size_t(15)) + static_cast<size_t>(W) * sizeof(float);
+  (void)W;
+  return (sizeof(RowSmem) + 15) & ~size_t(15);
 }
 
-// Cluster size and slice width for vocabulary V: slices small enough for two
-// CTAs per SM (at most 100 KB of shared memory), and among those cluster
-// sizes the one that keeps the most CTAs resident (the GPU places a cluster
-// inside one GPC, so 16-CTA clusters can leave SMs idle).
+// Cluster size and slice width for vocabulary V: the smallest cluster whose
+// slices are at most 32768 values (128 per thread and pass).
 bool verify_rows_plan(int V, int* CL, int* W) {
-  int best_cl = 0, best_w = 0, best_ctas = -1;
-  const int candidates[] = {16, 14, 12, 10, 8, 6, 4, 2, 1};
+  const int candidates[] = {1, 2, 4, 8, 16};
   for (int cl : candidates) {
     int w = (V + cl - 1) / cl;
     w = (w + 7) & ~7;
-    const size_t smem = verify_rows_smem_bytes(w);
-    if (smem > 100u * 1024u && cl < 16) break;  // smaller clusters only get larger slices
-    if (smem > kRowSmemLimit) continue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kRowThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.gridDim = dim3(static_cast<unsigned>(cl * 64), 1, 1);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaFuncSetAttribute(verify_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
-        (cl > 8 && cudaFuncSetAttribute(verify_rows_kernel,
-                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                       cudaSuccess) ||
-        cudaOccupancyMaxActiveClusters(&clusters, verify_rows_kernel, &cfg) != cudaSuccess) {
-      (void)cudaGetLastError();
-      clusters = 0;
-    }
-    if (clusters * cl > best_ctas) {
-      best_ctas = clusters * cl;
-      best_cl = cl;
-      best_w = w;
+    if (w <= 32768 || cl == 16) {
+      *CL = cl;
+      *W = w;
+      return true;
     }
   }
-  if (best_ctas <= 0) return false;
-  *CL = best_cl;
-  *W = best_w;
-  return true;
+  return false;
 }
 
 cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_t stream) {
@@ -753,7 +691,9 @@ cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // as many clusters as fit on the GPU at once, each looping over rows
+  // As many clusters as fit on the GPU at once, each looping over rows, but
+  // no more rows in flight than about 48 MB of L2 holds: every pass after
+  // the first reads the row again from L2.
   cfg.gridDim = dim3(static_cast<unsigned>(rows * CL), 1, 1);
   int max_clusters = 0;
   if (cudaOccupancyMaxActiveClusters(&max_clusters, verify_rows_kernel, &cfg) != cudaSuccess ||
@@ -761,7 +701,11 @@ cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_
     (void)cudaGetLastError();
     max_clusters = 1;
   }
-  const int nclusters = rows < max_clusters ? rows : max_clusters;
+  const size_t row_bytes = static_cast<size_t>(p.V) * (p.target_bf16 ? 2 : 4);
+  const int l2_rows = static_cast<int>((48ull << 20) / (row_bytes > 0 ? row_bytes : 1));
+  int nclusters = rows < max_clusters ? rows : max_clusters;
+  if (l2_rows >= 1 && nclusters > l2_rows) nclusters = l2_rows;
+  if (nclusters < 1) nclusters = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
   return cudaLaunchKernelEx(&cfg, verify_rows_kernel, p, W, rows);
 }
