@@ -46,6 +46,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -80,13 +82,14 @@ __host__ __device__ inline size_t base_slot_stride(size_t base_stage) {
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 struct TcLayout {
-  size_t a, e, bases, tinv, seed, npos, bptr, cptr, prev, act, best, bars, slot, flags, total;
+  size_t a, e, bases, xs, gs, seed, npos, bptr, cptr, prev, act, best, bars, slot, flags, total;
   __host__ __device__ TcLayout(int Npad, int NK, int ns, int nb, size_t base_stage) {
     a = 0;                                                       // markov_w2 ring
     e = a + static_cast<size_t>(ns) * kStageBytes;               // Markov embeddings
     bases = e + static_cast<size_t>(NK) * Npad * 128;            // staged base tiles
-    tinv = bases + static_cast<size_t>(nb) * base_slot_stride(base_stage);
-    seed = tinv + static_cast<size_t>(Npad) * 4;                 // per request:
+    xs = bases + static_cast<size_t>(nb) * base_slot_stride(base_stage);
+    gs = xs + static_cast<size_t>(Npad) * 4;
+    seed = gs + static_cast<size_t>(Npad) * 4;                   // per request:
     npos = seed + static_cast<size_t>(Npad) * 8;                 //   noise position
     bptr = npos + static_cast<size_t>(Npad) * 8;                 //   base row of the step
     cptr = bptr + static_cast<size_t>(Npad) * 8;                 //   cache row of the step
@@ -155,6 +158,53 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
   return v;
 }
 
+// The Gumbel variate -log(-log u) without a branch: -log u is the series
+// 2 atanh(t / (2 - t)), t = 1 - u, for u > 3/4 (where a plain log2 would
+// lose the relative accuracy of a small result) and -ln2 * log2(u) below;
+// both are computed and one is selected, so a warp never diverges here.
+__device__ __forceinline__ float gumbel_sel(uint32_t w) {
+  constexpr float kLn2 = 0.693147180559945309f;
+  const float u = uniform_of(w);
+  const float t = __fsub_rn(1.0f, u);
+  const float sr = __fdividef(t, __fsub_rn(2.0f, t));
+  const float s2 = sr * sr;
+  float p = fmaf(s2, 1.0f / 9.0f, 1.0f / 7.0f);
+  p = fmaf(s2, p, 1.0f / 5.0f);
+  p = fmaf(s2, p, 1.0f / 3.0f);
+  p = fmaf(s2, p, 1.0f);
+  const float e_near = 2.0f * sr * p;
+  const float e_far = -kLn2 * lg2_approx(u);
+  const float E = u > 0.75f ? e_near : e_far;
+  return -kLn2 * lg2_approx(E);
+}
+
+// Stores without a branch: the predicate travels into the instruction.
+__device__ __forceinline__ void st_pred(float* p, float v, bool pred) {
+  asm volatile("{ .reg .pred q; setp.ne.u32 q, %2, 0; @q st.global.f32 [%0], %1; }" ::"l"(p),
+               "f"(v), "r"(static_cast<uint32_t>(pred))
+               : "memory");
+}
+__device__ __forceinline__ void st_pred(uint16_t* p, float v, bool pred) {
+  asm volatile("{ .reg .pred q; setp.ne.u32 q, %2, 0; @q st.global.u16 [%0], %1; }" ::"l"(p),
+               "h"(float_to_bf16_bits(v)), "r"(static_cast<uint32_t>(pred))
+               : "memory");
+}
+// Loads without a branch: 0 where the predicate is false.
+__device__ __forceinline__ float ld_pred(const float* p, bool pred) {
+  float v;
+  asm volatile("{ .reg .pred q; setp.ne.u32 q, %2, 0; mov.f32 %0, 0f00000000; @q ld.global.nc.f32 %0, [%1]; }"
+               : "=f"(v)
+               : "l"(p), "r"(static_cast<uint32_t>(pred)));
+  return v;
+}
+__device__ __forceinline__ float ld_pred(const uint16_t* p, bool pred) {
+  unsigned short h;
+  asm volatile("{ .reg .pred q; setp.ne.u32 q, %2, 0; mov.u16 %0, 0; @q ld.global.nc.u16 %0, [%1]; }"
+               : "=h"(h)
+               : "l"(p), "r"(static_cast<uint32_t>(pred)));
+  return bf16_bits_to_float(h);
+}
+
 template <int GW>
 __device__ __forceinline__ void tmem_load_group(uint32_t taddr, uint32_t (&r)[GW]) {
   if constexpr (GW == 8) {
@@ -164,13 +214,13 @@ __device__ __forceinline__ void tmem_load_group(uint32_t taddr, uint32_t (&r)[GW
   }
 }
 
-template <int CPW>  // batch columns per epilogue warp (Npad / 4)
+template <int CPW, bool kBaseBf16, bool kCacheBf16>  // CPW: batch columns per epilogue warp
 __global__ void __launch_bounds__(kThreadsTc, 1)
 markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                       const __grid_constant__ CUtensorMap tmap_base, MarkovStepParams P,
                       TcCfg cfg) {
   constexpr bool kRegWinners = CPW <= 16;
-  constexpr int GW = CPW >= 8 ? 8 : 4;  // columns per TMEM load and Philox group
+  constexpr int GW = CPW == 8 ? 8 : 4;  // columns per TMEM load and Philox group
   const int Npad = cfg.Npad, ns = cfg.ns, na = cfg.na, nb = cfg.nb;
   const int R = P.R;
   const int NK = R / 64;
@@ -182,7 +232,8 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   unsigned char* e_base = smem + L.e;
   unsigned char* base_s = smem + L.bases;  // nb staged base tiles [B][128]
   const size_t base_stride = base_slot_stride(cfg.base_stage_bytes);
-  float* s_tinv = reinterpret_cast<float*>(smem + L.tinv);          // 1/T (0: greedy)
+  float* s_xs = reinterpret_cast<float*>(smem + L.xs);  // x = z * xs: 1/T, or 1 (greedy)
+  float* s_gs = reinterpret_cast<float*>(smem + L.gs);  // y = x + gs * g: 1, or 0 (greedy)
   uint64_t* s_seed = reinterpret_cast<uint64_t*>(smem + L.seed);
   int64_t* s_npos = reinterpret_cast<int64_t*>(smem + L.npos);      // P0 + step - 1
   const unsigned char** s_bptr = reinterpret_cast<const unsigned char**>(smem + L.bptr);
@@ -208,13 +259,15 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   const int tiles = (V + kM - 1) / kM;
   const int n_loc = (tiles - static_cast<int>(blockIdx.x) + G - 1) / G;  // tiles of this CTA
   const int n_iter = n_loc * K;  // (step, tile) pairs, step-major
-  const int bes = P.base_bf16 ? 2 : 4;
-  const int ces = P.cache_bf16 ? 2 : 4;
+  using BaseT = typename std::conditional<kBaseBf16, uint16_t, float>::type;
+  using CacheT = typename std::conditional<kCacheBf16, uint16_t, float>::type;
+  constexpr int bes = sizeof(BaseT);
+  constexpr int ces = sizeof(CacheT);
 
   // ---- prologue: per-request state (thread n < Npad owns column n) -----------
   if (tid < Npad) {
     const int n = tid;
-    float tinv = 0.f;
+    float xscale = 1.f, gscale = 0.f;
     uint64_t seed = 0;
     int64_t npos = 0;
     const unsigned char* bp = nullptr;
@@ -238,7 +291,10 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         }
         if (ok) {
           const float T = P.temperature[s];
-          tinv = T > 0.f ? __frcp_rn(T) : 0.f;  // 0 marks a greedy column
+          if (T > 0.f) {  // sampled; a greedy column keeps x = z and no noise
+            xscale = __frcp_rn(T);
+            gscale = 1.f;
+          }
           seed = P.seeds[s];
           npos = P.pos[n] - 1;
           bp = static_cast<const unsigned char*>(P.base) +
@@ -249,7 +305,8 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         }
       }
     }
-    s_tinv[n] = tinv;
+    s_xs[n] = xscale;
+    s_gs[n] = gscale;
     s_seed[n] = seed;
     s_npos[n] = npos;
     s_bptr[n] = bp;
@@ -438,11 +495,8 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     auto load_direct = [&](int cb, int v, bool in_range, float (&bv)[GW]) {
 #pragma unroll
       for (int j = 0; j < GW; ++j) {
-        const unsigned char* bp = s_bptr[cb + j];  // null: not a live request
-        bv[j] = 0.f;
-        if (bp != nullptr && in_range)
-          bv[j] = bes == 2 ? bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(bp) + v))
-                           : __ldg(reinterpret_cast<const float*>(bp) + v);
+        const BaseT* bp = reinterpret_cast<const BaseT*>(s_bptr[cb + j]);  // null: not live
+        bv[j] = ld_pred(bp + v, bp != nullptr && in_range);
       }
     };
     bool skip = false;  // set after a failed wait: the warp then only walks the loop
@@ -478,13 +532,15 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                               acc);
           float bv[GW];
           if (tma_base) {
+            // rows of padding columns (b >= B) read row B - 1: their results are unused
 #pragma unroll
             for (int j = 0; j < GW; ++j) {
-              const int b = cb + j;
-              bv[j] = b < B ? (bes == 2 ? bf16_bits_to_float(
-                                              reinterpret_cast<const uint16_t*>(sb)[b * kM + r])
-                                        : reinterpret_cast<const float*>(sb)[b * kM + r])
-                            : 0.f;
+              const int bb = min(cb + j, B - 1);
+              const BaseT raw = reinterpret_cast<const BaseT*>(sb)[bb * kM + r];
+              if constexpr (kBaseBf16)
+                bv[j] = bf16_bits_to_float(raw);
+              else
+                bv[j] = raw;
             }
           } else {
 #pragma unroll
@@ -506,33 +562,31 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             nw[4 * h + 3] = blk.w;
             quad_transpose(nw + 4 * h);
           }
-          float tinv[GW];
+          float xsc[GW], gsc[GW];
 #pragma unroll
           for (int h = 0; h < GW / 4; ++h) {
-            const float4 t4 = *reinterpret_cast<const float4*>(s_tinv + cb + 4 * h);
-            tinv[4 * h + 0] = t4.x;
-            tinv[4 * h + 1] = t4.y;
-            tinv[4 * h + 2] = t4.z;
-            tinv[4 * h + 3] = t4.w;
+            const float4 x4 = *reinterpret_cast<const float4*>(s_xs + cb + 4 * h);
+            const float4 g4 = *reinterpret_cast<const float4*>(s_gs + cb + 4 * h);
+            xsc[4 * h + 0] = x4.x;
+            xsc[4 * h + 1] = x4.y;
+            xsc[4 * h + 2] = x4.z;
+            xsc[4 * h + 3] = x4.w;
+            gsc[4 * h + 0] = g4.x;
+            gsc[4 * h + 1] = g4.y;
+            gsc[4 * h + 2] = g4.z;
+            gsc[4 * h + 3] = g4.w;
           }
           tc::tmem_wait_ld();
+          // straight-line per column; padding columns (b >= B) compute
+          // values that are neither stored nor folded into a token
 #pragma unroll
           for (int j = 0; j < GW; ++j) {
-            if (j >= c_live - c) break;  // warp-uniform
             const int b = cb + j;
             const float z = __fadd_rn(bv[j], __uint_as_float(acc[j]));
-            float x = z, y = z;
-            if (tinv[j] > 0.f) {  // warp-uniform: sampled (x = z * (1/T))
-              x = __fmul_rn(z, tinv[j]);
-              y = __fadd_rn(x, gumbel_of(nw[j]));
-            }
-            unsigned char* cp = s_cptr[b];  // warp-uniform; null: no store
-            if (cp != nullptr && in_range) {
-              if (ces == 2)
-                reinterpret_cast<uint16_t*>(cp)[v] = float_to_bf16_bits(x);
-              else
-                reinterpret_cast<float*>(cp)[v] = x;
-            }
+            const float x = __fmul_rn(z, xsc[j]);                  // z / T (greedy: z)
+            const float y = __fmaf_rn(gumbel_sel(nw[j]), gsc[j], x);  // x + g (greedy: x)
+            CacheT* cp = reinterpret_cast<CacheT*>(s_cptr[b]);      // null: no store
+            st_pred(cp + v, x, cp != nullptr && in_range);
             const uint32_t ord = in_range ? ordered_bits(y) : 0u;  // real values map above 0
             if constexpr (kRegWinners) {
               // rows of a lane only grow across a step's tiles: a strict >
@@ -645,11 +699,11 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-template <int CPW>
+template <int CPW, bool kBaseBf16, bool kCacheBf16>
 cudaError_t launch_tc_cpw(const MarkovStepParams& p, const CUtensorMap& map,
                           const CUtensorMap& bmap, const MarkovTcPlan& plan, int grid,
                           cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(markov_loop_tc_kernel<CPW>,
+  cudaError_t err = cudaFuncSetAttribute(markov_loop_tc_kernel<CPW, kBaseBf16, kCacheBf16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(plan.smem));
   if (err != cudaSuccess) return err;
@@ -672,7 +726,20 @@ cudaError_t launch_tc_cpw(const MarkovStepParams& p, const CUtensorMap& map,
   attr[0].val.cooperative = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, markov_loop_tc_kernel<CPW>, map, bmap, p, cfg);
+  return cudaLaunchKernelEx(&lc, markov_loop_tc_kernel<CPW, kBaseBf16, kCacheBf16>, map, bmap, p,
+                            cfg);
+}
+
+template <int CPW>
+cudaError_t launch_tc_dtypes(const MarkovStepParams& p, const CUtensorMap& map,
+                             const CUtensorMap& bmap, const MarkovTcPlan& plan, int grid,
+                             cudaStream_t stream) {
+  if (p.base_bf16) {
+    return p.cache_bf16 ? launch_tc_cpw<CPW, true, true>(p, map, bmap, plan, grid, stream)
+                        : launch_tc_cpw<CPW, true, false>(p, map, bmap, plan, grid, stream);
+  }
+  return p.cache_bf16 ? launch_tc_cpw<CPW, false, true>(p, map, bmap, plan, grid, stream)
+                      : launch_tc_cpw<CPW, false, false>(p, map, bmap, plan, grid, stream);
 }
 
 }  // namespace
@@ -781,10 +848,10 @@ cudaError_t launch_markov_loop_tc(const MarkovStepParams& p, const void* tmap, c
   const CUtensorMap& map = *static_cast<const CUtensorMap*>(tmap);
   const CUtensorMap& bm = *static_cast<const CUtensorMap*>(bmap);
   const int cpw = plan.Npad / 4;
-  if (cpw <= 4) return launch_tc_cpw<4>(p, map, bm, plan, grid, stream);
-  if (cpw <= 8) return launch_tc_cpw<8>(p, map, bm, plan, grid, stream);
-  if (cpw <= 16) return launch_tc_cpw<16>(p, map, bm, plan, grid, stream);
-  return launch_tc_cpw<64>(p, map, bm, plan, grid, stream);
+  if (cpw <= 4) return launch_tc_dtypes<4>(p, map, bm, plan, grid, stream);
+  if (cpw <= 8) return launch_tc_dtypes<8>(p, map, bm, plan, grid, stream);
+  if (cpw <= 16) return launch_tc_dtypes<16>(p, map, bm, plan, grid, stream);
+  return launch_tc_dtypes<64>(p, map, bm, plan, grid, stream);
 }
 
 }  // namespace dspark
