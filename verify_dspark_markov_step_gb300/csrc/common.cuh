@@ -68,7 +68,10 @@ __device__ __forceinline__ uint32_t pick_word(const U4& r, uint32_t j) {
 
 // u = ((w >> 9) + 1/2) * 2^-23: every step is exact in fp32.
 __device__ __forceinline__ float uniform_of(uint32_t w) {
-  return __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 0x1p-23f);
+  // 1 + k 2^-23 (k = w >> 9) from its bits, then minus (1 - 2^-24): the
+  // exact result (k + 1/2) 2^-23 has at most 24 significant bits, so the one
+  // rounding is exact and no integer conversion is needed
+  return __fadd_rn(__uint_as_float(0x3F800000u | (w >> 9)), -0x1.fffffep-1f);
 }
 
 // lg2.approx.f32: log2 with an absolute error of about 2^-22.6 on the
@@ -116,6 +119,14 @@ __device__ __forceinline__ float ln_approx(float x) {
 // then lower column index. -0 and +0 map to the same value bits.
 // 0 is below every real key ("no candidate").
 // ---------------------------------------------------------------------------
+// The same order key without branches: -0 becomes +0 by adding +0, every
+// NaN maps to the largest key.
+__device__ __forceinline__ uint32_t ordered_key(float y) {
+  const uint32_t b = __float_as_uint(__fadd_rn(y, 0.0f));
+  const uint32_t k = b ^ (static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u);
+  return (y != y) ? 0xFFFFFFFFu : k;
+}
+
 __device__ __forceinline__ uint32_t ordered_bits(float y) {
   if (y != y) return 0xFFFFFFFFu;
   uint32_t b = __float_as_uint(y);
@@ -252,6 +263,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` for the phase
+// to complete instead of returning at once (no spinning on the issue slots
+// of the warps that do the work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t phase,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(phase), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with parity `phase` to complete. Returns false (and
 // records DSPARK_ERR_TIMEOUT) if it has not completed within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase,
@@ -259,8 +288,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase,
   if (mbar_try_wait(bar, phase)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, phase)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_sleep(bar, phase, 2000u)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       report(status, DSPARK_ERR_TIMEOUT);
       return false;

@@ -168,11 +168,11 @@ __device__ __forceinline__ float gumbel_sel(uint32_t w) {
   const float t = __fsub_rn(1.0f, u);
   const float sr = __fdividef(t, __fsub_rn(2.0f, t));
   const float s2 = sr * sr;
-  float p = fmaf(s2, 1.0f / 9.0f, 1.0f / 7.0f);
-  p = fmaf(s2, p, 1.0f / 5.0f);
-  p = fmaf(s2, p, 1.0f / 3.0f);
-  p = fmaf(s2, p, 1.0f);
-  const float e_near = 2.0f * sr * p;
+  float p = fmaf(s2, 2.0f / 9.0f, 2.0f / 7.0f);  // 2 (1 + s^2/3 + s^4/5 + s^6/7 + s^8/9)
+  p = fmaf(s2, p, 2.0f / 5.0f);
+  p = fmaf(s2, p, 2.0f / 3.0f);
+  p = fmaf(s2, p, 2.0f);
+  const float e_near = sr * p;
   const float e_far = -kLn2 * lg2_approx(u);
   const float E = u > 0.75f ? e_near : e_far;
   return -kLn2 * lg2_approx(E);
@@ -587,7 +587,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             const float y = __fmaf_rn(gumbel_sel(nw[j]), gsc[j], x);  // x + g (greedy: x)
             CacheT* cp = reinterpret_cast<CacheT*>(s_cptr[b]);      // null: no store
             st_pred(cp + v, x, cp != nullptr && in_range);
-            const uint32_t ord = in_range ? ordered_bits(y) : 0u;  // real values map above 0
+            const uint32_t ord = in_range ? ordered_key(y) : 0u;  // real values map above 0
             if constexpr (kRegWinners) {
               // rows of a lane only grow across a step's tiles: a strict >
               // keeps the lowest row on ties
@@ -643,6 +643,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                 static_cast<unsigned int>(step + 1) * static_cast<unsigned int>(G);
             const unsigned long long t0 = globaltimer_ns();
             while (ld_acquire_u32(P.counter) < target) {
+              __nanosleep(64);
               if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 report(P.status, DSPARK_ERR_TIMEOUT);
                 *fail_flag = 1;
