@@ -334,6 +334,30 @@ __device__ __forceinline__ int adigit1(float x, float m, int a0) {
   return static_cast<int>(fminf(__fmul_rn(t, 2048.0f), 2047.0f));
 }
 
+// Fixed-point mass rint(e * 2^40) of e in [0, 1], summed as two 32-bit
+// partials: vh = rint(e * 2^20) and vl = e * 2^40 - vh * 2^20 (exact, |vl| <=
+// 2^19), so rint(e * 2^40) = vh * 2^20 + rint(vl). Both roundings are the
+// add-1.5*2^23 trick (the sum lands in [2^23, 2^24), where the spacing is 1).
+// A thread adds at most 2^7 values per row, so neither partial overflows.
+struct MassAcc {
+  uint32_t hi = 0u;  // sum of vh
+  int32_t lo = 0;    // sum of rint(vl)
+  __device__ __forceinline__ void add(float e) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    constexpr uint32_t kMagicBits = 0x4B400000u;
+    const float s = __fadd_rn(__fmul_rn(e, 0x1p20f), kMagic);
+    const float vh = __fsub_rn(s, kMagic);
+    const float vl = __fmaf_rn(vh, -0x1p20f, __fmul_rn(e, 0x1p40f));
+    const float r = __fadd_rn(vl, kMagic);
+    hi += __float_as_uint(s) - kMagicBits;
+    lo += static_cast<int32_t>(__float_as_uint(r) - kMagicBits);
+  }
+  __device__ __forceinline__ unsigned long long total() const {
+    return (static_cast<unsigned long long>(hi) << 20) +
+           static_cast<unsigned long long>(static_cast<long long>(lo));
+  }
+};
+
 // Reads of one row's slice [v0, v0 + n) straight from global memory. The
 // first pass brings the slice from HBM (L2 evict-last: every later pass of
 // the row reads it again from L2); `fix` maps a raw value to x (temperature,
@@ -402,7 +426,8 @@ __device__ __forceinline__ void row_sweep(const RowView& rv, uint64_t pol, Fix f
     done = 4 * n4;
   }
   for (int i = done + tid; i < rv.n; i += kRowThreads) {
-    const float c = rv.bf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol)) : ld_hint_f32(rv.f + i, pol);
+    const float c =
+        rv.bf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol)) : ld_hint_f32(rv.f + i, pol);
     body(i, fix(c));
   }
 }
@@ -489,144 +514,153 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
     return;
   }
 
-  // x: the target row after temperature, the draft row as stored; NaN reads as -inf
-  const bool scale = is_target && T != 1.0f;
-  auto fix = [=](float c) -> float {
-    const float x = scale ? __fdiv_rn(c, T) : c;
-    return (x != x) ? -INFINITY : x;
-  };
+  // x: the target row after temperature, the draft row as stored; NaN reads
+  // as -inf. The passes are instantiated for scaled and unscaled rows, so an
+  // unscaled row never evaluates a division.
   const bool topp = is_target && P.top_p[s] < 1.0f;
+  auto passes = [&](auto prescale) {
+    auto fix = [=](float c) -> float {
+      const float x = prescale(c);
+      return (x != x) ? -INFINITY : x;
+    };
 
-  // ---- pass 1 (HBM): maximum --------------------------------------------------------
-  float lmax = -INFINITY;
-  row_sweep(rv, pol_keep, fix, [&](int, float x) { lmax = fmaxf(lmax, x); });
-  bool any_fail = false;
-  const float m = cluster_max_f(cl, sm, lmax, false, set, CL, &any_fail);
-  if (m == -INFINITY) {
+    // ---- pass 1 (HBM): maximum (fmaxf skips NaN, as if it were -inf) ---------------
+    float lmax = -INFINITY;
+    row_sweep(rv, pol_keep, prescale, [&](int, float x) { lmax = fmaxf(lmax, x); });
+    bool any_fail = false;
+    const float m = cluster_max_f(cl, sm, lmax, false, set, CL, &any_fail);
+    if (m == -INFINITY) {
+      if (rank == 0 && tid == 0) {
+        if (is_target) {
+          ts->m = m;
+          ts->D = 1.0f;
+          ts->kd_thr = 0u;
+          ts->id_thr = 0;
+          ts->p_d = d == 0 ? 1.0f : 0.0f;
+          ts->mode = kModeOneHot;
+          ts->amax_key = 0ull;
+        } else {
+          ds->m = m;
+          ds->D = 1.0f;
+          ds->q_d = 0.0f;
+          ds->zero = 1;
+        }
+      }
+      return;
+    }
+
+    // ---- pass 2 (L2): fixed-point mass (+ first top-p histogram) -----------------
+    if (topp) hist_clear(sm, kRowBins);
+    __syncthreads();
+    unsigned long long F = 0ull;
+    if (topp) {
+      row_sweep(rv, pol_keep, fix, [&](int i, float x) {
+        const unsigned long long f = fixed_mass(exp_rel(x, m));
+        F += f;
+        hist_add(sm, true, adigit0(x, m), f, static_cast<uint32_t>(v0 + i));
+      });
+    } else {
+      MassAcc acc;
+      row_sweep(rv, pol_last_use, fix, [&](int, float x) { acc.add(exp_rel(x, m)); });
+      F = acc.total();
+    }
+    F = cluster_sum_u64(cl, sm, F, set, CL);
+
+    uint32_t kd_thr = 0u;
+    int32_t id_thr = 0;
+    unsigned long long Fk = F;
+    int32_t mode = kModeKeepAll;
+    if (topp) {
+      mode = kModeThreshold;
+      const unsigned long long P32 = topp_scaled(P.top_p[s]);
+      const unsigned long long t_lo = P32 * F;
+      const unsigned long long t_hi = __umul64hi(P32, F);
+      // stage 0 (its histogram was built in pass 2): distance bins, ascending
+      Found f = cluster_find(cl, sm, kRowBins, false, 0ull, t_hi, t_lo, CL, rank);
+      unsigned long long above = f.before;
+      const int a0 = f.bin;
+      int a1 = -1;
+      int kd_len = 0, id_len = 0;
+      uint32_t kd_pre = 0u, id_pre = 0u;
+      // Stages 1..6 split the boundary bin until it holds one element: the
+      // distance sub-bins, kd bits [31:21], [20:10], [9:0], id bits [21:11],
+      // [10:0]. After the last id stage the bin is a single token.
+      for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
+        const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
+        const uint32_t c_kp = kd_pre, c_ip = id_pre;
+        auto match = [=](float x, uint32_t kd, uint32_t id) {
+          if (adigit0(x, m) != a0) return false;
+          if (c_a1 >= 0 && adigit1(x, m, a0) != c_a1) return false;
+          if (c_kl > 0 && (kd >> (32 - c_kl)) != c_kp) return false;
+          if (c_il > 0 && (id >> (22 - c_il)) != c_ip) return false;
+          return true;
+        };
+        auto digit = [=](float x, uint32_t kd, uint32_t id) -> int {
+          switch (stage) {
+            case 1: return adigit1(x, m, a0);
+            case 2: return static_cast<int>(kd >> 21);
+            case 3: return static_cast<int>((kd >> 10) & 0x7FFu);
+            case 4: return static_cast<int>(kd & 0x3FFu);
+            case 5: return static_cast<int>((id >> 11) & 0x7FFu);
+            default: return static_cast<int>(id & 0x7FFu);
+          }
+        };
+        const int nb = stage == 4 ? 1024 : kRowBins;
+        const bool desc = stage >= 2 && stage <= 4;  // larger kd first; distance and id ascending
+        hist_clear(sm, nb);
+        __syncthreads();
+        row_sweep(rv, pol_keep, fix, [&](int i, float x) {
+          const uint32_t kd = kd_of(x);
+          const uint32_t id = static_cast<uint32_t>(v0 + i);
+          if (match(x, kd, id))
+            hist_add(sm, true, digit(x, kd, id), fixed_mass(exp_rel(x, m)), id);
+        });
+        f = cluster_find(cl, sm, nb, desc, above, t_hi, t_lo, CL, rank);
+        above = f.before;
+        const uint32_t bin = static_cast<uint32_t>(f.bin);
+        if (stage == 1) {
+          a1 = f.bin;
+        } else if (stage <= 4) {
+          kd_pre = (kd_pre << (stage == 4 ? 10 : 11)) | bin;
+          kd_len += stage == 4 ? 10 : 11;
+        } else {
+          id_pre = (id_pre << 11) | bin;
+          id_len += 11;
+        }
+      }
+      // f is the one-element bin at the boundary: its token, mass and logit
+      id_thr = static_cast<int32_t>(f.id);
+      Fk = above + f.mass;
+      kd_thr = kd_of(fix(raw_at(id_thr)));
+    }
+    const float D = __fmul_rn(__ull2float_rn(Fk), 0x1p-40f);
+
+    // ---- outputs (rank 0): p or q at the drafted token, the row statistics --------
     if (rank == 0 && tid == 0) {
+      const bool has_d = d >= 0 && d < V;
+      const float x = has_d ? fix(raw_at(d)) : 0.0f;
       if (is_target) {
+        const uint32_t kd = kd_of(x);
+        const bool keep = mode == kModeKeepAll || kd > kd_thr || (kd == kd_thr && d <= id_thr);
+        ts->p_d = has_d && keep ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
         ts->m = m;
-        ts->D = 1.0f;
-        ts->kd_thr = 0u;
-        ts->id_thr = 0;
-        ts->p_d = d == 0 ? 1.0f : 0.0f;
-        ts->mode = kModeOneHot;
+        ts->D = D;
+        ts->kd_thr = kd_thr;
+        ts->id_thr = id_thr;
+        ts->mode = mode;
         ts->amax_key = 0ull;
       } else {
+        ds->q_d = has_d ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
         ds->m = m;
-        ds->D = 1.0f;
-        ds->q_d = 0.0f;
-        ds->zero = 1;
+        ds->D = D;
+        ds->zero = 0;
       }
     }
-    return;
-  }
-
-  // ---- pass 2 (L2): fixed-point mass (+ first top-p histogram) -----------------
-  if (topp) hist_clear(sm, kRowBins);
-  __syncthreads();
-  unsigned long long F = 0ull;
-  if (topp) {
-    row_sweep(rv, pol_keep, fix, [&](int i, float x) {
-      const unsigned long long f = fixed_mass(exp_rel(x, m));
-      F += f;
-      hist_add(sm, true, adigit0(x, m), f, static_cast<uint32_t>(v0 + i));
-    });
-  } else {
-    row_sweep(rv, pol_last_use, fix, [&](int, float x) { F += fixed_mass(exp_rel(x, m)); });
-  }
-  F = cluster_sum_u64(cl, sm, F, set, CL);
-
-  uint32_t kd_thr = 0u;
-  int32_t id_thr = 0;
-  unsigned long long Fk = F;
-  int32_t mode = kModeKeepAll;
-  if (topp) {
-    mode = kModeThreshold;
-    const unsigned long long P32 = topp_scaled(P.top_p[s]);
-    const unsigned long long t_lo = P32 * F;
-    const unsigned long long t_hi = __umul64hi(P32, F);
-    // stage 0 (its histogram was built in pass 2): distance bins, ascending
-    Found f = cluster_find(cl, sm, kRowBins, false, 0ull, t_hi, t_lo, CL, rank);
-    unsigned long long above = f.before;
-    const int a0 = f.bin;
-    int a1 = -1;
-    int kd_len = 0, id_len = 0;
-    uint32_t kd_pre = 0u, id_pre = 0u;
-    // Stages 1..6 split the boundary bin until it holds one element: the
-    // distance sub-bins, kd bits [31:21], [20:10], [9:0], id bits [21:11],
-    // [10:0]. After the last id stage the bin is a single token.
-    for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
-      const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
-      const uint32_t c_kp = kd_pre, c_ip = id_pre;
-      auto match = [=](float x, uint32_t kd, uint32_t id) {
-        if (adigit0(x, m) != a0) return false;
-        if (c_a1 >= 0 && adigit1(x, m, a0) != c_a1) return false;
-        if (c_kl > 0 && (kd >> (32 - c_kl)) != c_kp) return false;
-        if (c_il > 0 && (id >> (22 - c_il)) != c_ip) return false;
-        return true;
-      };
-      auto digit = [=](float x, uint32_t kd, uint32_t id) -> int {
-        switch (stage) {
-          case 1: return adigit1(x, m, a0);
-          case 2: return static_cast<int>(kd >> 21);
-          case 3: return static_cast<int>((kd >> 10) & 0x7FFu);
-          case 4: return static_cast<int>(kd & 0x3FFu);
-          case 5: return static_cast<int>((id >> 11) & 0x7FFu);
-          default: return static_cast<int>(id & 0x7FFu);
-        }
-      };
-      const int nb = stage == 4 ? 1024 : kRowBins;
-      const bool desc = stage >= 2 && stage <= 4;  // larger kd first; distance and id ascending
-      hist_clear(sm, nb);
-      __syncthreads();
-      row_sweep(rv, pol_keep, fix, [&](int i, float x) {
-        const uint32_t kd = kd_of(x);
-        const uint32_t id = static_cast<uint32_t>(v0 + i);
-        if (match(x, kd, id))
-          hist_add(sm, true, digit(x, kd, id), fixed_mass(exp_rel(x, m)), id);
-      });
-      f = cluster_find(cl, sm, nb, desc, above, t_hi, t_lo, CL, rank);
-      above = f.before;
-      const uint32_t bin = static_cast<uint32_t>(f.bin);
-      if (stage == 1) {
-        a1 = f.bin;
-      } else if (stage <= 4) {
-        kd_pre = (kd_pre << (stage == 4 ? 10 : 11)) | bin;
-        kd_len += stage == 4 ? 10 : 11;
-      } else {
-        id_pre = (id_pre << 11) | bin;
-        id_len += 11;
-      }
-    }
-    // f is the one-element bin at the boundary: its token, mass and logit
-    id_thr = static_cast<int32_t>(f.id);
-    Fk = above + f.mass;
-    kd_thr = kd_of(fix(raw_at(id_thr)));
-  }
-  const float D = __fmul_rn(__ull2float_rn(Fk), 0x1p-40f);
-
-  // ---- outputs (rank 0): p or q at the drafted token, the row statistics --------
-  if (rank == 0 && tid == 0) {
-    const bool has_d = d >= 0 && d < V;
-    const float x = has_d ? fix(raw_at(d)) : 0.0f;
-    if (is_target) {
-      const uint32_t kd = kd_of(x);
-      const bool keep = mode == kModeKeepAll || kd > kd_thr || (kd == kd_thr && d <= id_thr);
-      ts->p_d = has_d && keep ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
-      ts->m = m;
-      ts->D = D;
-      ts->kd_thr = kd_thr;
-      ts->id_thr = id_thr;
-      ts->mode = mode;
-      ts->amax_key = 0ull;
-    } else {
-      ds->q_d = has_d ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
-      ds->m = m;
-      ds->D = D;
-      ds->zero = 0;
-    }
-  }
+  };
+  if (is_target && T != 1.0f)
+    passes([T](float c) { return __fdiv_rn(c, T); });
+  else
+    passes([](float c) { return c; });
 }
 
 // ---------------------------------------------------------------------------
