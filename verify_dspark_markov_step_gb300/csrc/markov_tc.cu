@@ -205,6 +205,37 @@ __device__ __forceinline__ float ld_pred(const uint16_t* p, bool pred) {
   return bf16_bits_to_float(h);
 }
 
+// Position of loop iteration g = step * n_loc + il of a CTA (tile t of its
+// share), and the slot/parity of a ring of n buffers, advanced without
+// integer division.
+struct TileIter {
+  int step, il, t, n_loc, G;
+  __device__ TileIter(int n_loc_, int G_)
+      : step(0), il(0), t(static_cast<int>(blockIdx.x)), n_loc(n_loc_), G(G_) {}
+  __device__ __forceinline__ bool first() const { return il == 0; }
+  __device__ __forceinline__ bool last() const { return il == n_loc - 1; }
+  __device__ __forceinline__ void next() {
+    if (++il == n_loc) {
+      il = 0;
+      ++step;
+      t = static_cast<int>(blockIdx.x);
+    } else {
+      t += G;
+    }
+  }
+};
+struct RingPos {
+  int slot, n;
+  uint32_t phase;
+  __device__ explicit RingPos(int n_) : slot(0), n(n_), phase(0u) {}
+  __device__ __forceinline__ void next() {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 template <int GW>
 __device__ __forceinline__ void tmem_load_group(uint32_t taddr, uint32_t (&r)[GW]) {
   if constexpr (GW == 8) {
@@ -377,10 +408,10 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       uint32_t issued[kMaxStages];  // parity of the last copy per stage
 #pragma unroll
       for (int i = 0; i < kMaxStages; ++i) issued[i] = 0xFFFFFFFFu;
-      for (int g = 0; g < n_iter && ok; ++g) {
+      TileIter it(n_loc, G);
+      for (int g = 0; g < n_iter && ok; ++g, it.next()) {
         if (*fail_flag) break;
-        const int step = g / n_loc;
-        const int t = blockIdx.x + (g - step * n_loc) * G;
+        const int t = it.t;
         for (int kc = 0; kc < NK; ++kc) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, P.status)) {
             ok = false;
@@ -408,12 +439,14 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       uint32_t last[kMaxBaseSlots];
 #pragma unroll
       for (int i = 0; i < kMaxBaseSlots; ++i) last[i] = 0xFFFFFFFFu;
-      for (int g = 0; g < n_iter; ++g) {
+      TileIter it(n_loc, G);
+      RingPos br(nb);
+      for (int g = 0; g < n_iter; ++g, it.next(), br.next()) {
         if (*fail_flag) break;
-        const int step = g / n_loc;
-        const int t = blockIdx.x + (g - step * n_loc) * G;
-        const int bs = g % nb;
-        const uint32_t bph = static_cast<uint32_t>(g / nb) & 1u;
+        const int step = it.step;
+        const int t = it.t;
+        const int bs = br.slot;
+        const uint32_t bph = br.phase;
         if (!mbar_wait(&bempty[bs], bph ^ 1u, P.status)) {
           *fail_flag = 1;
           break;
@@ -433,18 +466,19 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int g = 0; g < n_iter && ok; ++g) {
+      TileIter it(n_loc, G);
+      RingPos ar(na);
+      for (int g = 0; g < n_iter && ok; ++g, it.next(), ar.next()) {
         if (*fail_flag) break;
-        const int step = g / n_loc;
-        if (g == step * n_loc) {  // first tile of a step: wait for its embeddings
-          if (!mbar_wait(e_ready, static_cast<uint32_t>(step) & 1u, P.status)) {
+        if (it.first()) {  // first tile of a step: wait for its embeddings
+          if (!mbar_wait(e_ready, static_cast<uint32_t>(it.step) & 1u, P.status)) {
             ok = false;
             break;
           }
           tc::fence_after_thread_sync();
         }
-        const int ab = g % na;
-        if (!mbar_wait(&acc_empty[ab], (static_cast<uint32_t>(g / na) & 1u) ^ 1u, P.status)) {
+        const int ab = ar.slot;
+        if (!mbar_wait(&acc_empty[ab], ar.phase ^ 1u, P.status)) {
           ok = false;
           break;
         }
@@ -500,13 +534,15 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       }
     };
     bool skip = false;  // set after a failed wait: the warp then only walks the loop
-    for (int g = 0; g < n_iter; ++g) {
-      const int step = g / n_loc;
-      const int t = blockIdx.x + (g - step * n_loc) * G;
-      const int ab = g % na;
-      const uint32_t aph = static_cast<uint32_t>(g / na) & 1u;
-      const int bs = tma_base ? g % nb : 0;
-      const uint32_t bph = tma_base ? static_cast<uint32_t>(g / nb) & 1u : 0u;
+    TileIter it(n_loc, G);
+    RingPos ar(na), br(tma_base ? nb : 1);
+    for (int g = 0; g < n_iter; ++g, it.next(), ar.next(), br.next()) {
+      const int step = it.step;
+      const int t = it.t;
+      const int ab = ar.slot;
+      const uint32_t aph = ar.phase;
+      const int bs = br.slot;
+      const uint32_t bph = br.phase;
       const int v = t * kM + r;
       const bool in_range = v < V;
       float bnext[GW];
@@ -608,7 +644,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           if (tma_base) mbar_arrive(&bempty[bs]);
         }
       }
-      if (g != (step + 1) * n_loc - 1) continue;
+      if (!it.last()) continue;
 
       // ---- end of a step: fold winners, grid barrier, tokens, next embeddings ----
       if constexpr (kRegWinners) {
