@@ -726,7 +726,7 @@ cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // As many clusters as fit on the GPU at once, each looping over rows, but
-  // no more rows in flight than about 48 MB of L2 holds: every pass after
+  // no more rows in flight than about 80 MB of L2 holds: every pass after
   // the first reads the row again from L2.
   cfg.gridDim = dim3(static_cast<unsigned>(rows * CL), 1, 1);
   int max_clusters = 0;
@@ -736,7 +736,7 @@ cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_
     max_clusters = 1;
   }
   const size_t row_bytes = static_cast<size_t>(p.V) * (p.target_bf16 ? 2 : 4);
-  const int l2_rows = static_cast<int>((48ull << 20) / (row_bytes > 0 ? row_bytes : 1));
+  const int l2_rows = static_cast<int>((80ull << 20) / (row_bytes > 0 ? row_bytes : 1));
   int nclusters = rows < max_clusters ? rows : max_clusters;
   if (l2_rows >= 1 && nclusters > l2_rows) nclusters = l2_rows;
   if (nclusters < 1) nclusters = 1;
