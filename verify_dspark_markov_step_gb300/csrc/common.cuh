@@ -90,21 +90,22 @@ __device__ __forceinline__ float lg2_approx(float x) {
 // g = -ln 2 * lg2(E). The absolute error on g stays below about 1.3e-6 over
 // the whole grid (checked against an fp64 evaluation in the tests).
 __device__ __forceinline__ float gumbel_of(uint32_t w) {
+  // -log u is 2 atanh(t / (2 - t)), t = 1 - u, for u > 3/4 (where log2 of u
+  // near 1 would lose the relative accuracy of a small result) and
+  // -ln2 * log2(u) below; both are computed and one is selected, so a warp
+  // never diverges here
   constexpr float kLn2 = 0.693147180559945309f;
   const float u = uniform_of(w);
-  float E;
-  if (u > 0.75f) {
-    const float t = __fsub_rn(1.0f, u);
-    const float s = __fdividef(t, __fsub_rn(2.0f, t));
-    const float s2 = s * s;
-    float p = fmaf(s2, 1.0f / 9.0f, 1.0f / 7.0f);
-    p = fmaf(s2, p, 1.0f / 5.0f);
-    p = fmaf(s2, p, 1.0f / 3.0f);
-    p = fmaf(s2, p, 1.0f);
-    E = 2.0f * s * p;
-  } else {
-    E = -kLn2 * lg2_approx(u);
-  }
+  const float t = __fsub_rn(1.0f, u);
+  const float sr = __fdividef(t, __fsub_rn(2.0f, t));
+  const float s2 = sr * sr;
+  float p = fmaf(s2, 2.0f / 9.0f, 2.0f / 7.0f);  // 2 (1 + s^2/3 + s^4/5 + s^6/7 + s^8/9)
+  p = fmaf(s2, p, 2.0f / 5.0f);
+  p = fmaf(s2, p, 2.0f / 3.0f);
+  p = fmaf(s2, p, 2.0f);
+  const float e_near = sr * p;
+  const float e_far = -kLn2 * lg2_approx(u);
+  const float E = u > 0.75f ? e_near : e_far;
   return -kLn2 * lg2_approx(E);
 }
 

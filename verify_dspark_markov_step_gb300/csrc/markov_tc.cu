@@ -158,26 +158,6 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
   return v;
 }
 
-// The Gumbel variate -log(-log u) without a branch: -log u is the series
-// 2 atanh(t / (2 - t)), t = 1 - u, for u > 3/4 (where a plain log2 would
-// lose the relative accuracy of a small result) and -ln2 * log2(u) below;
-// both are computed and one is selected, so a warp never diverges here.
-__device__ __forceinline__ float gumbel_sel(uint32_t w) {
-  constexpr float kLn2 = 0.693147180559945309f;
-  const float u = uniform_of(w);
-  const float t = __fsub_rn(1.0f, u);
-  const float sr = __fdividef(t, __fsub_rn(2.0f, t));
-  const float s2 = sr * sr;
-  float p = fmaf(s2, 2.0f / 9.0f, 2.0f / 7.0f);  // 2 (1 + s^2/3 + s^4/5 + s^6/7 + s^8/9)
-  p = fmaf(s2, p, 2.0f / 5.0f);
-  p = fmaf(s2, p, 2.0f / 3.0f);
-  p = fmaf(s2, p, 2.0f);
-  const float e_near = sr * p;
-  const float e_far = -kLn2 * lg2_approx(u);
-  const float E = u > 0.75f ? e_near : e_far;
-  return -kLn2 * lg2_approx(E);
-}
-
 // Stores without a branch: the predicate travels into the instruction.
 __device__ __forceinline__ void st_pred(float* p, float v, bool pred) {
   asm volatile("{ .reg .pred q; setp.ne.u32 q, %2, 0; @q st.global.f32 [%0], %1; }" ::"l"(p),
@@ -620,7 +600,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             const int b = cb + j;
             const float z = __fadd_rn(bv[j], __uint_as_float(acc[j]));
             const float x = __fmul_rn(z, xsc[j]);                  // z / T (greedy: z)
-            const float y = __fmaf_rn(gumbel_sel(nw[j]), gsc[j], x);  // x + g (greedy: x)
+            const float y = __fmaf_rn(gumbel_of(nw[j]), gsc[j], x);  // x + g (greedy: x)
             CacheT* cp = reinterpret_cast<CacheT*>(s_cptr[b]);      // null: no store
             st_pred(cp + v, x, cp != nullptr && in_range);
             const uint32_t ord = in_range ? ordered_key(y) : 0u;  // real values map above 0

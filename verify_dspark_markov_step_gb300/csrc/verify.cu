@@ -97,6 +97,61 @@ __device__ __forceinline__ void load4(const void* base, bool bf16, int64_t off, 
   for (int j = 0; j < 4; ++j) out[j] = g + j < c1 ? load_logit(base, bf16, off + g + j) : 0.0f;
 }
 
+// The common draw, specialised at compile time: a sampled row kept whole or
+// cut at a top-p threshold, temperature 1 or not, from p or from the
+// residual max(0, p - q) with a nonzero draft row. Straight-line per column;
+// the noise of a 4-column block is drawn only if one of its weights is
+// positive, as in the generic path.
+template <bool kResidual, bool kScale, bool kThreshold>
+__device__ unsigned long long draw_fast(const VerifyParams& P, const TgtStats& ts,
+                                        const DrfStats& ds, float T, uint64_t seed,
+                                        int64_t npos, int64_t toff, int64_t coff, int c0,
+                                        int c1, bool tvec, bool cvec, unsigned int* anypos) {
+  const bool tbf = P.target_bf16 != 0, cbf = P.cache_bf16 != 0;
+  const float invD = 1.0f / ts.D;
+  const float invDq = kResidual ? 1.0f / ds.D : 0.0f;
+  unsigned long long best = 0ull;
+  unsigned int any = 0u;
+  for (int g = c0 + 4 * threadIdx.x; g < c1; g += 4 * kResThreads) {
+    float t4[4], c4[4];
+    load4(P.target, tbf, toff, g, c1, tvec, t4);
+    if (kResidual) load4(P.cache, cbf, coff, g, c1, cvec, c4);
+    float w[4];
+    bool need = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float x = kScale ? __fdiv_rn(t4[j], T) : t4[j];
+      x = (x != x) ? -INFINITY : x;
+      float pv = __fmul_rn(exp_rel(x, ts.m), invD);
+      if (kThreshold) {
+        const uint32_t kd = kd_of(x);
+        const bool keep = kd > ts.kd_thr || (kd == ts.kd_thr && g + j <= ts.id_thr);
+        pv = keep ? pv : 0.0f;
+      }
+      if (kResidual) {
+        const float c = (c4[j] != c4[j]) ? -INFINITY : c4[j];
+        pv = fmaxf(__fsub_rn(pv, __fmul_rn(exp_rel(c, ds.m), invDq)), 0.0f);
+      }
+      w[j] = g + j < c1 ? pv : 0.0f;
+      need |= w[j] > 0.0f;
+    }
+    if (!need) continue;
+    any = 1u;
+    const U4 r = noise_block(seed, npos, static_cast<uint32_t>(g), kStreamTarget);
+    const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float y = __fadd_rn(ln_approx(w[j]), gumbel_of(words[j]));
+      const unsigned long long key =
+          (static_cast<unsigned long long>(ordered_key(y)) << 32) |
+          static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(g + j));
+      best = w[j] > 0.0f ? umax64(best, key) : best;
+    }
+  }
+  *anypos = any;
+  return best;
+}
+
 // Winner key over columns [c0, c1) (c0 a multiple of 4) of the draw for
 // this request; *anypos = some residual entry was positive.
 __device__ unsigned long long draw_chunk(const VerifyParams& P, const ResSmem& rs,
@@ -119,6 +174,29 @@ __device__ unsigned long long draw_chunk(const VerifyParams& P, const ResSmem& r
   const bool tvec = ((reinterpret_cast<uintptr_t>(P.target) + toff * (tbf ? 2 : 4)) & (tbf ? 7u : 15u)) == 0;
   const bool cvec = ((reinterpret_cast<uintptr_t>(P.cache) + coff * (cbf ? 2 : 4)) & (cbf ? 7u : 15u)) == 0;
   const int64_t npos = rs.P0 + k - 1;
+  if (ts.mode != kModeOneHot && !(residual && ds.zero)) {
+    const bool scale = rs.T != 1.0f;
+    const bool thr = ts.mode == kModeThreshold;
+#define DSPARK_DRAW(R, S, H)                                                                   \
+  return draw_fast<R, S, H>(P, ts, ds, rs.T, rs.seed, npos, toff, coff, c0, c1, tvec, cvec, \
+                            anypos)
+    if (residual) {
+      if (scale) {
+        if (thr) DSPARK_DRAW(true, true, true);
+        DSPARK_DRAW(true, true, false);
+      }
+      if (thr) DSPARK_DRAW(true, false, true);
+      DSPARK_DRAW(true, false, false);
+    }
+    if (scale) {
+      if (thr) DSPARK_DRAW(false, true, true);
+      DSPARK_DRAW(false, true, false);
+    }
+    if (thr) DSPARK_DRAW(false, false, true);
+    DSPARK_DRAW(false, false, false);
+#undef DSPARK_DRAW
+  }
+  // generic path: one-hot target rows and all-zero draft rows
   unsigned long long best = 0ull;
   unsigned int any = 0u;
   for (int g = c0 + 4 * threadIdx.x; g < c1; g += 4 * kResThreads) {
