@@ -78,6 +78,14 @@ typedef enum {
                                    array of dspark_markov_sample_static    */
 } dspark_status;
 
+/* Statistics of one draft-logits cache row (one request, one draft step):
+ * m = the maximum of the row's stored values (NaN read as -inf; for a bf16
+ * cache the stored bf16 value). Exact, whatever order it is taken in. */
+typedef struct {
+  float m;
+  uint32_t scratch; /* used by dspark_markov_sample while it runs */
+} dspark_row_stats;
+
 /* Limits checked on the host. */
 #define DSPARK_MAX_VOCAB (1 << 22)  /* token ids fit 22 bits; V * 2^40 < 2^63 */
 #define DSPARK_MAX_BATCH 256
@@ -117,6 +125,12 @@ typedef enum {
  *   cache         [C, K, V] cache_dtype, or NULL for no cache write
  *   cache_row_map [S] int32 in [0, C), or NULL for row = slot
  *   out_tokens    [B, K] int32   (written)
+ *   draft_stats   [B, K] dspark_row_stats, or NULL: if given (and cache is
+ *                 not NULL), the maximum of every cache row the call writes,
+ *                 so that dspark_rejection_sample can skip its own pass for
+ *                 it (padding requests: zero; B > 64: NaN, "not recorded").
+ *                 No counterpart in the pages: the loop has every value of
+ *                 the row at hand.
  *   B in [0, 256], K in [1, 16], V in [1, 2^22), R a multiple of 64 up to
  *   512, S >= 1, C >= 1 if cache != NULL.
  *   workspace     device scratch of at least dspark_markov_workspace_bytes()
@@ -133,9 +147,9 @@ dspark_status dspark_markov_sample(
     const int32_t* anchor_tokens, const int32_t* req_state_idx,
     const int64_t* positions, const float* temperature, const uint64_t* seeds,
     void* cache, dspark_dtype cache_dtype, const int32_t* cache_row_map,
-    int32_t* out_tokens, int B, int K, int V, int R, int S, int C,
-    void* workspace, size_t workspace_bytes, int32_t* status,
-    dspark_stream_t stream);
+    int32_t* out_tokens, dspark_row_stats* draft_stats, int B, int K, int V,
+    int R, int S, int C, void* workspace, size_t workspace_bytes,
+    int32_t* status, dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * dspark_markov_sample_static -- dspark_markov_sample without a workspace
@@ -173,8 +187,8 @@ dspark_status dspark_markov_sample_static(
     const int32_t* anchor_tokens, const int32_t* req_state_idx,
     const int64_t* positions, const float* temperature, const uint64_t* seeds,
     void* cache, dspark_dtype cache_dtype, const int32_t* cache_row_map,
-    int32_t* out_tokens, int B, int K, int V, int R, int S, int C,
-    int32_t* status, dspark_stream_t stream);
+    int32_t* out_tokens, dspark_row_stats* draft_stats, int B, int K, int V,
+    int R, int S, int C, int32_t* status, dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * dspark_rejection_sample -- probabilistic rejection-sampling verification.
@@ -211,6 +225,11 @@ dspark_status dspark_markov_sample_static(
  *   draft_tokens  [B, K] int32 in [0, V) or -1
  *   draft_cache   [C, K, V] cache_dtype (may be NULL if every slot is greedy)
  *   cache_row_map [S] int32 or NULL (row = slot)
+ *   draft_stats   [B, K] dspark_row_stats or NULL: the maxima that
+ *                 dspark_markov_sample wrote for these cache rows; each draft
+ *                 row with a recorded (non-NaN) maximum is then read once
+ *                 (for its mass) instead of twice. They must describe the
+ *                 cache passed here.
  *   target_logits [B, K+1, V] target_dtype
  *   req_state_idx [B], positions [B], temperature [S], top_p [S] fp32,
  *   seeds [S] as for dspark_markov_sample
@@ -223,7 +242,8 @@ size_t dspark_verify_workspace_bytes(int B, int K, int V);
 dspark_status dspark_rejection_sample(
     const int32_t* draft_tokens, const void* draft_cache,
     dspark_dtype cache_dtype, const int32_t* cache_row_map,
-    const void* target_logits, dspark_dtype target_dtype,
+    const dspark_row_stats* draft_stats, const void* target_logits,
+    dspark_dtype target_dtype,
     const int32_t* req_state_idx, const int64_t* positions,
     const float* temperature, const float* top_p, const uint64_t* seeds,
     int32_t* out_tokens, int32_t* num_accepted, int B, int K, int V, int S,

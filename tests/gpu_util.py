@@ -27,7 +27,7 @@ def run_verify(w, draft, cache):
     """Verify given host drafts and cache (numpy) on the GPU."""
     import torch
     from verify_dspark_markov_step_gb300.step import DecodeStep, to_device
-    st = DecodeStep(w)
+    st = DecodeStep(w, draft_stats=False)  # the cache is the caller's: rows are read
     st.draft.copy_(torch.from_numpy(np.ascontiguousarray(draft, np.int32)))
     st.cache = to_device(np.ascontiguousarray(cache))
     st.verify()

@@ -63,7 +63,7 @@ def test_argument_checks_return_before_any_launch(L):
     null = None
     def markov(B=1, K=1, V=10, R=64, S=1, C=1, base=fake, bdt=0, cdt=0, ws=fake, wsb=1 << 20):
         return L.dspark_markov_sample(base, bdt, fake, fake, fake, fake, fake, fake, fake,
-                                      null, cdt, null, fake, B, K, V, R, S, C, ws, wsb,
+                                      null, cdt, null, fake, null, B, K, V, R, S, C, ws, wsb,
                                       null, null)
     assert markov(B=-1) == -1
     assert markov(B=257) == -1
@@ -81,8 +81,8 @@ def test_argument_checks_return_before_any_launch(L):
     assert markov(wsb=8) == -6
     assert markov(base=vp(258)) == -7     # misaligned logits
     def verify(B=1, K=1, V=10, S=1, target=fake, tdt=0, ws=fake, wsb=1 << 20):
-        return L.dspark_rejection_sample(fake, null, 0, null, target, tdt, fake, fake, fake,
-                                         fake, fake, fake, fake, B, K, V, S, 1, ws, wsb,
+        return L.dspark_rejection_sample(fake, null, 0, null, null, target, tdt, fake, fake,
+                                         fake, fake, fake, fake, fake, B, K, V, S, 1, ws, wsb,
                                          null, null)
     assert verify(B=300) == -1
     assert verify(tdt=3) == -1

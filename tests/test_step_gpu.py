@@ -48,3 +48,56 @@ def test_decode_step_graph_replay_is_bitwise_stable():
         for a, b in zip(ref, (st.draft, st.cache, st.out, st.num_accepted)):
             assert torch.equal(a, b)
     assert st.status_code() == 0
+
+
+def _row_max_reference(cache, rsi, row_map, K, bf16):
+    """Maximum of every cache row a request wrote, from the stored values
+    (NaN read as -inf)."""
+    from verify_dspark_markov_step_gb300.workloads import bf16_bits_to_f32
+    x = bf16_bits_to_f32(cache) if bf16 else cache.astype(np.float32)
+    out = {}
+    for b, s in enumerate(rsi):
+        if s < 0:
+            continue
+        row = s if row_map is None else row_map[s]
+        for k in range(K):
+            out[(b, k)] = np.float32(np.where(np.isnan(x[row, k]), -np.inf, x[row, k]).max())
+    return out
+
+
+@pytest.mark.parametrize("name", ["odd", "bf16_rowmap", "wide"])
+def test_draft_row_maxima_from_the_loop(name):
+    """The loop's cache-row maxima equal the stored rows' maxima, and the
+    verifier gives identical outputs whether it takes them or finds them."""
+    torch = require_gpu()
+    from verify_dspark_markov_step_gb300.step import DecodeStep, to_numpy
+    if name == "odd":
+        w = wl.make("odd")
+    elif name == "wide":  # more than 64 requests: maxima reported as not recorded
+        w = wl.custom(70, 2, 4099, 64, seed=8, temperature=0.9, top_p=0.95)
+    else:
+        w = wl.custom(12, 3, 30011, 192, seed=5, base_bf16=True, cache_bf16=True, S=16,
+                      rsi=[15, 2, -1, 7, 0, 11, 3, 9, -1, 4, 13, 1],
+                      row_map=[3, 0, 5, 1, 2, 4, 15, 14, 13, 12, 11, 10, 9, 8, 7, 6],
+                      temperature=[1.0, 0.7, 0.0, 1.3] * 4, top_p=[1.0, 0.9] * 8)
+    st = DecodeStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    assert st.status_code() == 0
+    raw = np.ascontiguousarray(st.dstats.cpu().numpy().reshape(w.B, w.K))
+    m_all = raw.view(np.uint32).reshape(w.B, w.K, 2)[..., 0].view(np.float32)  # {m, scratch}
+    ref = _row_max_reference(to_numpy(st.cache), w.req_state_idx, w.row_map, w.K, w.cache_bf16)
+    for (b, k), m in ref.items():
+        if w.B > 64:
+            assert np.isnan(m_all[b, k]), (b, k, m_all[b, k])
+        else:
+            assert m_all[b, k] == m, (b, k, m_all[b, k], m)
+    # the verifier with the maxima equals the verifier finding them itself
+    with_stats = (st.out.clone(), st.num_accepted.clone())
+    st2 = DecodeStep(w, draft_stats=False)
+    st2.draft.copy_(st.draft)
+    st2.cache.copy_(st.cache)
+    st2.verify()
+    torch.cuda.synchronize()
+    assert st2.status_code() == 0
+    assert torch.equal(with_stats[0], st2.out) and torch.equal(with_stats[1], st2.num_accepted)

@@ -40,7 +40,8 @@ def test_sizes_beyond_the_fixed_scratch_are_rejected_on_the_host():
 
     def call(B, V, K=7, R=256, S=1):
         return L.dspark_markov_sample_static(fake, 0, fake, fake, fake, fake, fake, fake, fake,
-                                             None, 0, None, fake, B, K, V, R, S, 1, None, None)
+                                             None, 0, None, fake, None, B, K, V, R, S, 1, None,
+                                             None)
     assert call(256, 200064, K=16) == -8           # DSPARK_ERR_SCRATCH_LIMIT
     assert _lib.status_string(-8).startswith("sizes need more scratch")
     assert call(-1, 1000) == -1                    # still an argument error first

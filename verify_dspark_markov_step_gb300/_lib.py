@@ -71,15 +71,16 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.dspark_markov_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.dspark_markov_sample.restype = i32
         L.dspark_markov_sample.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp,
-                                           i32, i32, i32, i32, i32, i32, vp, sz, vp, vp]
+                                           vp, i32, i32, i32, i32, i32, i32, vp, sz, vp, vp]
         L.dspark_markov_sample_static.restype = i32
         L.dspark_markov_sample_static.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32,
-                                                  vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+                                                  vp, vp, vp, i32, i32, i32, i32, i32, i32, vp,
+                                                  vp]
         L.dspark_verify_workspace_bytes.restype = sz
         L.dspark_verify_workspace_bytes.argtypes = [i32, i32, i32]
         L.dspark_rejection_sample.restype = i32
-        L.dspark_rejection_sample.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp,
-                                              vp, i32, i32, i32, i32, i32, vp, sz, vp, vp]
+        L.dspark_rejection_sample.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp,
+                                              vp, vp, i32, i32, i32, i32, i32, vp, sz, vp, vp]
         L.dspark_noise.restype = i32
         L.dspark_noise.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp]
         L.dspark_status_string.restype = ctypes.c_char_p
@@ -141,6 +142,21 @@ def verify_workspace_bytes(B, K, V) -> int:
     return int(lib().dspark_verify_workspace_bytes(B, K, V))
 
 
+def row_stats(B: int, K: int, device=None) -> torch.Tensor:
+    """A device buffer for [B, K] dspark_row_stats (8 bytes each: the row
+    maximum as fp32 in the low half)."""
+    return torch.zeros((B, K), dtype=torch.int64, device=device or "cuda")
+
+
+def _stats(t, B, K, name="draft_stats"):
+    if t is None:
+        return None
+    _dev(t, name)
+    if t.numel() * t.element_size() != B * K * 8:
+        raise ValueError(f"{name} must hold [B, K] 8-byte records")
+    return t
+
+
 def workspace(nbytes: int, device=None) -> torch.Tensor:
     """A device byte buffer usable as a workspace."""
     return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device or "cuda")
@@ -148,7 +164,8 @@ def workspace(nbytes: int, device=None) -> torch.Tensor:
 
 def markov_sample(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_idx,
                   positions, temperature, seeds, out_tokens, cache=None,
-                  cache_row_map=None, workspace_buf=None, status=None, stream=None):
+                  cache_row_map=None, workspace_buf=None, status=None, stream=None,
+                  draft_stats=None):
     """dspark_markov_sample on torch tensors (see include/dspark.h)."""
     _dev(base_logits, "base_logits", (torch.float32,) + _BF16_LIKE)
     B, K, V = base_logits.shape
@@ -180,11 +197,12 @@ def markov_sample(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_id
     if workspace_buf is None:
         workspace_buf = workspace(need, base_logits.device)
     _dev(status, "status", (torch.int32,))
+    _stats(draft_stats, B, K)
     code = lib().dspark_markov_sample(
         _ptr(base_logits), _logit_dtype(base_logits, "base_logits"), _ptr(markov_w1),
         _ptr(markov_w2), _ptr(anchor_tokens), _ptr(req_state_idx), _ptr(positions),
         _ptr(temperature), _ptr(seeds), _ptr(cache), cache_dt, _ptr(cache_row_map),
-        _ptr(out_tokens), B, K, V, R, S, max(C, 1), _ptr(workspace_buf),
+        _ptr(out_tokens), _ptr(draft_stats), B, K, V, R, S, max(C, 1), _ptr(workspace_buf),
         workspace_buf.numel() * workspace_buf.element_size(), _ptr(status), _stream(stream))
     _check(code, "dspark_markov_sample")
 
@@ -195,7 +213,7 @@ STATIC_SCRATCH_BYTES = 32 << 10
 
 def markov_sample_static(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_idx,
                          positions, temperature, seeds, out_tokens, cache=None,
-                         cache_row_map=None, status=None, stream=None):
+                         cache_row_map=None, status=None, stream=None, draft_stats=None):
     """dspark_markov_sample_static on torch tensors: dspark_markov_sample with
     the library's fixed scratch array instead of a workspace, so that nothing
     is allocated (for callers that may not allocate device memory). Calls
@@ -228,17 +246,20 @@ def markov_sample_static(base_logits, markov_w1, markov_w2, anchor_tokens, req_s
         cache_dt = _logit_dtype(cache, "cache")
     _dev(cache_row_map, "cache_row_map", (torch.int32,))
     _dev(status, "status", (torch.int32,))
+    _stats(draft_stats, B, K)
     code = lib().dspark_markov_sample_static(
         _ptr(base_logits), _logit_dtype(base_logits, "base_logits"), _ptr(markov_w1),
         _ptr(markov_w2), _ptr(anchor_tokens), _ptr(req_state_idx), _ptr(positions),
         _ptr(temperature), _ptr(seeds), _ptr(cache), cache_dt, _ptr(cache_row_map),
-        _ptr(out_tokens), B, K, V, R, S, max(C, 1), _ptr(status), _stream(stream))
+        _ptr(out_tokens), _ptr(draft_stats), B, K, V, R, S, max(C, 1), _ptr(status),
+        _stream(stream))
     _check(code, "dspark_markov_sample_static")
 
 
 def rejection_sample(draft_tokens, draft_cache, target_logits, req_state_idx, positions,
                      temperature, top_p, seeds, out_tokens, num_accepted,
-                     cache_row_map=None, workspace_buf=None, status=None, stream=None):
+                     cache_row_map=None, workspace_buf=None, status=None, stream=None,
+                     draft_stats=None):
     """dspark_rejection_sample on torch tensors (see include/dspark.h)."""
     _dev(draft_tokens, "draft_tokens", (torch.int32,))
     B, K = draft_tokens.shape
@@ -271,8 +292,9 @@ def rejection_sample(draft_tokens, draft_cache, target_logits, req_state_idx, po
     if workspace_buf is None:
         workspace_buf = workspace(need, target_logits.device)
     _dev(status, "status", (torch.int32,))
+    _stats(draft_stats, B, K)
     code = lib().dspark_rejection_sample(
-        _ptr(draft_tokens), _ptr(draft_cache), cache_dt, _ptr(cache_row_map),
+        _ptr(draft_tokens), _ptr(draft_cache), cache_dt, _ptr(cache_row_map), _ptr(draft_stats),
         _ptr(target_logits), _logit_dtype(target_logits, "target_logits"),
         _ptr(req_state_idx), _ptr(positions), _ptr(temperature), _ptr(top_p), _ptr(seeds),
         _ptr(out_tokens), _ptr(num_accepted), B, K, V, S, max(C, 1), _ptr(workspace_buf),

@@ -72,9 +72,9 @@ dspark_status dspark_markov_sample(
     const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
     const uint16_t* markov_w2, const int32_t* anchor_tokens, const int32_t* req_state_idx,
     const int64_t* positions, const float* temperature, const uint64_t* seeds, void* cache,
-    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens, int B, int K,
-    int V, int R, int S, int C, void* workspace, size_t workspace_bytes, int32_t* status,
-    dspark_stream_t stream) {
+    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens,
+    dspark_row_stats* draft_stats, int B, int K, int V, int R, int S, int C, void* workspace,
+    size_t workspace_bytes, int32_t* status, dspark_stream_t stream) {
   if (!sizes_ok(B, K, V, S) || R < 1) return DSPARK_ERR_INVALID_ARG;
   if (!valid_dtype(base_dtype) || !valid_dtype(cache_dtype)) return DSPARK_ERR_INVALID_ARG;
   if (R % 64 != 0 || R > 512) return DSPARK_ERR_UNSUPPORTED;
@@ -116,7 +116,13 @@ dspark_status dspark_markov_sample(
   p.keys = reinterpret_cast<unsigned long long*>(w + ws.keys);
   p.counter = reinterpret_cast<unsigned int*>(w + ws.counter);
   p.status = status;
+  p.draft_stats = cache != nullptr ? draft_stats : nullptr;
   if (cudaMemsetAsync(w, 0, ws.cleared, st) != cudaSuccess) return DSPARK_ERR_CUDA;
+  // the statistics' mass and order-key fields accumulate from zero
+  if (p.draft_stats != nullptr &&
+      cudaMemsetAsync(p.draft_stats, 0, static_cast<size_t>(B) * K * sizeof(dspark_row_stats),
+                      st) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   dspark::MarkovTcPlan plan;
   alignas(64) unsigned char tmap[128];
   alignas(64) unsigned char bmap[128] = {};
@@ -142,7 +148,8 @@ size_t dspark_verify_workspace_bytes(int B, int K, int V) {
 
 dspark_status dspark_rejection_sample(
     const int32_t* draft_tokens, const void* draft_cache, dspark_dtype cache_dtype,
-    const int32_t* cache_row_map, const void* target_logits, dspark_dtype target_dtype,
+    const int32_t* cache_row_map, const dspark_row_stats* draft_stats, const void* target_logits,
+    dspark_dtype target_dtype,
     const int32_t* req_state_idx, const int64_t* positions, const float* temperature,
     const float* top_p, const uint64_t* seeds, int32_t* out_tokens, int32_t* num_accepted,
     int B, int K, int V, int S, int C, void* workspace, size_t workspace_bytes,
@@ -170,6 +177,7 @@ dspark_status dspark_rejection_sample(
   p.cache = draft_cache;
   p.cache_bf16 = cache_dtype == DSPARK_BF16;
   p.row_map = cache_row_map;
+  p.draft_stats = draft_stats;
   p.target = target_logits;
   p.target_bf16 = target_dtype == DSPARK_BF16;
   p.rsi = req_state_idx;

@@ -120,6 +120,36 @@ __device__ __forceinline__ float ln_approx(float x) {
 // then lower column index. -0 and +0 map to the same value bits.
 // 0 is below every real key ("no candidate").
 // ---------------------------------------------------------------------------
+// e = exp(x - m): ex2.approx of fp32(x - m) * log2(e), which is exactly 1 at
+// the maximum (ex2 of +-0 is 1) and within about 3 ulp elsewhere (the
+// oracle's exp is correctly rounded, and the tests bound the effect: accept
+// margins and top-p boundaries within 1e-6). -inf gives 0.
+__device__ __forceinline__ float exp_rel(float x, float m) { return __expf(__fsub_rn(x, m)); }
+
+// Fixed-point mass rint(e * 2^40) of e in [0, 1], summed as two 32-bit
+// partials: vh = rint(e * 2^20) and vl = e * 2^40 - vh * 2^20 (exact, |vl| <=
+// 2^19), so rint(e * 2^40) = vh * 2^20 + rint(vl). Both roundings are the
+// add-1.5*2^23 trick (the sum lands in [2^23, 2^24), where the spacing is 1).
+// Neither partial overflows while a thread adds fewer than 2^11 values.
+struct MassAcc {
+  uint32_t hi = 0u;  // sum of vh
+  int32_t lo = 0;    // sum of rint(vl)
+  __device__ __forceinline__ void add(float e) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    constexpr uint32_t kMagicBits = 0x4B400000u;
+    const float s = __fadd_rn(__fmul_rn(e, 0x1p20f), kMagic);
+    const float vh = __fsub_rn(s, kMagic);
+    const float vl = __fmaf_rn(vh, -0x1p20f, __fmul_rn(e, 0x1p40f));
+    const float r = __fadd_rn(vl, kMagic);
+    hi += __float_as_uint(s) - kMagicBits;
+    lo += static_cast<int32_t>(__float_as_uint(r) - kMagicBits);
+  }
+  __device__ __forceinline__ unsigned long long total() const {
+    return (static_cast<unsigned long long>(hi) << 20) +
+           static_cast<unsigned long long>(static_cast<long long>(lo));
+  }
+};
+
 // The same order key without branches: -0 becomes +0 by adding +0, every
 // NaN maps to the largest key.
 __device__ __forceinline__ uint32_t ordered_key(float y) {

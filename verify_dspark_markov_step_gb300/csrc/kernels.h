@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "dspark.h"
+
 namespace dspark {
 
 // The K-step Markov loop.
@@ -25,6 +27,7 @@ struct MarkovStepParams {
   int32_t* out_tokens;
   int B, K, V, R, S, C;
   unsigned long long* keys;      // [K][B] winner key of each step and request (zeroed)
+  dspark_row_stats* draft_stats; // [B][K] statistics of the cache rows written, or null (zeroed)
   unsigned int* counter;         // grid-barrier arrivals (zeroed before the launch)
   int32_t* status;
 };
@@ -53,6 +56,7 @@ struct VerifyParams {
   const void* cache;
   int cache_bf16;
   const int32_t* row_map;
+  const dspark_row_stats* draft_stats;  // [B][K] from the Markov loop, or null
   const void* target;
   int target_bf16;
   const int32_t* rsi;

@@ -82,7 +82,8 @@ __host__ __device__ inline size_t base_slot_stride(size_t base_stage) {
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 struct TcLayout {
-  size_t a, e, bases, xs, gs, seed, npos, bptr, cptr, prev, act, best, bars, slot, flags, total;
+  size_t a, e, bases, xs, gs, seed, npos, bptr, cptr, cb0, prev, act, best, xbest, bars, slot,
+      flags, total;
   __host__ __device__ TcLayout(int Npad, int NK, int ns, int nb, size_t base_stage) {
     a = 0;                                                       // markov_w2 ring
     e = a + static_cast<size_t>(ns) * kStageBytes;               // Markov embeddings
@@ -93,10 +94,12 @@ struct TcLayout {
     npos = seed + static_cast<size_t>(Npad) * 8;                 //   noise position
     bptr = npos + static_cast<size_t>(Npad) * 8;                 //   base row of the step
     cptr = bptr + static_cast<size_t>(Npad) * 8;                 //   cache row of the step
-    prev = cptr + static_cast<size_t>(Npad) * 8;                 //   token feeding the step
+    cb0 = cptr + static_cast<size_t>(Npad) * 8;                  //   cache row of step 0
+    prev = cb0 + static_cast<size_t>(Npad) * 8;                  //   token feeding the step
     act = prev + static_cast<size_t>(Npad) * 4;
     best = act + static_cast<size_t>(Npad) * 4;
-    bars = best + static_cast<size_t>(Npad) * 8;
+    xbest = best + static_cast<size_t>(Npad) * 8;                //   cache-row maximum key
+    bars = xbest + static_cast<size_t>(Npad) * 8;
     slot = bars + static_cast<size_t>(2 * kMaxStages + 2 * kMaxAcc + 2 * kMaxBaseSlots + 2) * 8;
     flags = slot + 8;
     total = flags + 16 + 1024;  // + slack to align the base to 1024 B
@@ -169,6 +172,17 @@ __device__ __forceinline__ void st_pred(uint16_t* p, float v, bool pred) {
                "h"(float_to_bf16_bits(v)), "r"(static_cast<uint32_t>(pred))
                : "memory");
 }
+__device__ __forceinline__ void st_pred_bits(uint16_t* p, uint16_t h, bool pred) {
+  asm volatile("{ .reg .pred q; setp.ne.u32 q, %2, 0; @q st.global.u16 [%0], %1; }" ::"l"(p),
+               "h"(h), "r"(static_cast<uint32_t>(pred))
+               : "memory");
+}
+// The value of an order key (0, the empty key, reads as -inf).
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  if (k == 0u) return -INFINITY;
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Loads without a branch: 0 where the predicate is false.
 __device__ __forceinline__ float ld_pred(const float* p, bool pred) {
   float v;
@@ -249,6 +263,11 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   int64_t* s_npos = reinterpret_cast<int64_t*>(smem + L.npos);      // P0 + step - 1
   const unsigned char** s_bptr = reinterpret_cast<const unsigned char**>(smem + L.bptr);
   unsigned char** s_cptr = reinterpret_cast<unsigned char**>(smem + L.cptr);  // null: no store
+  unsigned char** s_cb0 = reinterpret_cast<unsigned char**>(smem + L.cb0);
+  uint32_t* xbest = reinterpret_cast<uint32_t*>(smem + L.xbest);
+  // cache-row maxima are recorded by the register-winner epilogue (up to 64
+  // requests); wider batches report them unknown (NaN)
+  const bool want_stats = kRegWinners && P.draft_stats != nullptr;
   int32_t* s_prev = reinterpret_cast<int32_t*>(smem + L.prev);
   int32_t* s_act = reinterpret_cast<int32_t*>(smem + L.act);        // request live
   unsigned long long* best = reinterpret_cast<unsigned long long*>(smem + L.best);
@@ -322,6 +341,8 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     s_npos[n] = npos;
     s_bptr[n] = bp;
     s_cptr[n] = cp;
+    s_cb0[n] = cp;
+    xbest[n] = 0u;
     s_prev[n] = prev;
     s_act[n] = prev >= 0;
     best[n] = 0ull;
@@ -498,12 +519,14 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     const int c_begin = sub * CPW;   // batch columns [c_begin, c_begin + CPW)
     const int c_live = min(CPW, B - c_begin);  // columns below B (may be <= 0)
     const int r = q * 32 + lane;     // this lane's row of a tile
+    float run_xm[kRegWinners ? CPW : 1];  // running maximum of the stored values
     uint32_t run_ord[kRegWinners ? CPW : 1];
     uint32_t run_v[kRegWinners ? CPW : 1];
 #pragma unroll
     for (int j = 0; j < (kRegWinners ? CPW : 1); ++j) {
       run_ord[j] = 0u;
       run_v[j] = 0xFFFFFFFFu;
+      run_xm[j] = -INFINITY;
     }
     // base logits straight from global memory (no staged tile)
     auto load_direct = [&](int cb, int v, bool in_range, float (&bv)[GW]) {
@@ -602,7 +625,17 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             const float x = __fmul_rn(z, xsc[j]);                  // z / T (greedy: z)
             const float y = __fmaf_rn(gumbel_of(nw[j]), gsc[j], x);  // x + g (greedy: x)
             CacheT* cp = reinterpret_cast<CacheT*>(s_cptr[b]);      // null: no store
-            st_pred(cp + v, x, cp != nullptr && in_range);
+            float xr;  // the value as stored (a bf16 cache rounds it)
+            if constexpr (kCacheBf16) {
+              const uint16_t h = float_to_bf16_bits(x);
+              st_pred_bits(cp + v, h, cp != nullptr && in_range);
+              xr = bf16_bits_to_float(h);
+            } else {
+              st_pred(cp + v, x, cp != nullptr && in_range);
+              xr = x;
+            }
+            xr = in_range ? xr : -INFINITY;  // fmaxf below skips NaN, read as -inf
+            if constexpr (kRegWinners) run_xm[c + j] = fmaxf(run_xm[c + j], xr);
             const uint32_t ord = in_range ? ordered_key(y) : 0u;  // real values map above 0
             if constexpr (kRegWinners) {
               // rows of a lane only grow across a step's tiles: a strict >
@@ -633,9 +666,14 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           if (j < c_live && !skip) {
             const unsigned long long key = warp_winner(run_ord[j], run_v[j]);
             if (lane == 0 && key != 0ull) atomicMax(&best[c_begin + j], key);
+            if (want_stats) {
+              const uint32_t xk = __reduce_max_sync(0xFFFFFFFFu, ordered_key(run_xm[j]));
+              if (lane == 0) atomicMax(&xbest[c_begin + j], xk);
+            }
           }
           run_ord[j] = 0u;
           run_v[j] = 0xFFFFFFFFu;
+          run_xm[j] = -INFINITY;
         }
       }
       epi_bar();
@@ -644,6 +682,10 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         const unsigned long long k = best[b];
         if (k != 0ull) atomicMax(keys + b, k);
         best[b] = 0ull;
+        // the cache row's maximum, as an order key in the scratch word
+        if (want_stats && s_cb0[b] != nullptr)
+          atomicMax(&P.draft_stats[static_cast<int64_t>(b) * K + step].scratch, xbest[b]);
+        xbest[b] = 0u;
       }
       __threadfence();
       epi_bar();
@@ -680,7 +722,13 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           const unsigned long long m = __ldcg(keys + b);
           if (m != 0ull) tok = key_index(m);
         }
-        if (blockIdx.x == 0 && b < B) P.out_tokens[static_cast<int64_t>(b) * K + step] = tok;
+        if (blockIdx.x == 0 && b < B) {
+          P.out_tokens[static_cast<int64_t>(b) * K + step] = tok;
+          if (P.draft_stats != nullptr && s_cb0[b] != nullptr) {  // the row's maximum
+            dspark_row_stats* st = &P.draft_stats[static_cast<int64_t>(b) * K + step];
+            st->m = want_stats ? key_to_float(__ldcg(&st->scratch)) : __int_as_float(0x7FC00000);
+          }
+        }
         s_prev[b] = tok;
         s_act[b] = tok >= 0;
         if (!last) {  // advance the per-request state to the next step

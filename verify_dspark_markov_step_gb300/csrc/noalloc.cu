@@ -47,8 +47,9 @@ extern "C" dspark_status dspark_markov_sample_static(
     const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
     const uint16_t* markov_w2, const int32_t* anchor_tokens, const int32_t* req_state_idx,
     const int64_t* positions, const float* temperature, const uint64_t* seeds, void* cache,
-    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens, int B, int K,
-    int V, int R, int S, int C, int32_t* status, dspark_stream_t stream) {
+    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens,
+    dspark_row_stats* draft_stats, int B, int K, int V, int R, int S, int C, int32_t* status,
+    dspark_stream_t stream) {
   // sizes outside the documented ranges are argument errors, as for
   // dspark_markov_sample; the scratch limit is checked next, and both before
   // anything touches the device
@@ -65,6 +66,6 @@ extern "C" dspark_status dspark_markov_sample_static(
   // call left in the array does not matter.
   return dspark_markov_sample(base_logits, base_dtype, markov_w1, markov_w2, anchor_tokens,
                               req_state_idx, positions, temperature, seeds, cache, cache_dtype,
-                              cache_row_map, out_tokens, B, K, V, R, S, C, scratch,
+                              cache_row_map, out_tokens, draft_stats, B, K, V, R, S, C, scratch,
                               DSPARK_STATIC_SCRATCH_BYTES, status, stream);
 }

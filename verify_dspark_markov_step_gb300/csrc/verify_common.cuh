@@ -41,11 +41,6 @@ __device__ __forceinline__ float scale_logit(float t, float T) {
   return (x != x) ? -INFINITY : x;
 }
 
-// e = exp(x - m): ex2.approx of fp32(x - m) * log2(e), which is exactly 1 at
-// the maximum (ex2 of +-0 is 1) and within about 3 ulp elsewhere (the
-// oracle's exp is correctly rounded, and the tests bound the effect: accept
-// margins and top-p boundaries within 1e-6). -inf gives 0.
-__device__ __forceinline__ float exp_rel(float x, float m) { return __expf(__fsub_rn(x, m)); }
 
 // rint(e * 2^40) for 0 <= e <= 1, round half to even, without a 64-bit
 // float-to-integer conversion. v = e * 2^40 is exact in fp32. Below 2^23,

@@ -334,30 +334,6 @@ __device__ __forceinline__ int adigit1(float x, float m, int a0) {
   return static_cast<int>(fminf(__fmul_rn(t, 2048.0f), 2047.0f));
 }
 
-// Fixed-point mass rint(e * 2^40) of e in [0, 1], summed as two 32-bit
-// partials: vh = rint(e * 2^20) and vl = e * 2^40 - vh * 2^20 (exact, |vl| <=
-// 2^19), so rint(e * 2^40) = vh * 2^20 + rint(vl). Both roundings are the
-// add-1.5*2^23 trick (the sum lands in [2^23, 2^24), where the spacing is 1).
-// A thread adds at most 2^7 values per row, so neither partial overflows.
-struct MassAcc {
-  uint32_t hi = 0u;  // sum of vh
-  int32_t lo = 0;    // sum of rint(vl)
-  __device__ __forceinline__ void add(float e) {
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    constexpr uint32_t kMagicBits = 0x4B400000u;
-    const float s = __fadd_rn(__fmul_rn(e, 0x1p20f), kMagic);
-    const float vh = __fsub_rn(s, kMagic);
-    const float vl = __fmaf_rn(vh, -0x1p20f, __fmul_rn(e, 0x1p40f));
-    const float r = __fadd_rn(vl, kMagic);
-    hi += __float_as_uint(s) - kMagicBits;
-    lo += static_cast<int32_t>(__float_as_uint(r) - kMagicBits);
-  }
-  __device__ __forceinline__ unsigned long long total() const {
-    return (static_cast<unsigned long long>(hi) << 20) +
-           static_cast<unsigned long long>(static_cast<long long>(lo));
-  }
-};
-
 // Reads of one row's slice [v0, v0 + n) straight from global memory. The
 // first pass brings the slice from HBM (L2 evict-last: every later pass of
 // the row reads it again from L2); `fix` maps a raw value to x (temperature,
@@ -525,10 +501,20 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
     };
 
     // ---- pass 1 (HBM): maximum (fmaxf skips NaN, as if it were -inf) ---------------
-    float lmax = -INFINITY;
-    row_sweep(rv, pol_keep, prescale, [&](int, float x) { lmax = fmaxf(lmax, x); });
-    bool any_fail = false;
-    const float m = cluster_max_f(cl, sm, lmax, false, set, CL, &any_fail);
+    // A draft row whose maximum the Markov loop recorded skips this pass and
+    // is read once, by pass 2 (every CTA of the cluster decides alike).
+    const float m_rec = (!is_target && P.draft_stats != nullptr)
+                            ? P.draft_stats[static_cast<int64_t>(b) * K + k].m
+                            : __int_as_float(0x7FC00000);
+    float m;
+    if (m_rec == m_rec) {  // recorded (NaN: not recorded)
+      m = m_rec;
+    } else {
+      float lmax = -INFINITY;
+      row_sweep(rv, pol_keep, prescale, [&](int, float x) { lmax = fmaxf(lmax, x); });
+      bool any_fail = false;
+      m = cluster_max_f(cl, sm, lmax, false, set, CL, &any_fail);
+    }
     if (m == -INFINITY) {
       if (rank == 0 && tid == 0) {
         if (is_target) {

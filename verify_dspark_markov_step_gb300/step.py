@@ -32,7 +32,8 @@ def to_numpy(t: torch.Tensor) -> np.ndarray:
 class DecodeStep:
     """Device buffers of one workload and the two library calls."""
 
-    def __init__(self, w: Workload, device="cuda", with_target: bool = True):
+    def __init__(self, w: Workload, device="cuda", with_target: bool = True,
+                 draft_stats: bool = True):
         self.w = w
         self.device = device
         self.base = to_device(w.base, device)
@@ -54,19 +55,22 @@ class DecodeStep:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.ws_markov = _lib.workspace(_lib.markov_workspace_bytes(w.B, w.K, w.V, w.R), device)
         self.ws_verify = _lib.workspace(_lib.verify_workspace_bytes(w.B, w.K, w.V), device)
+        # statistics of the cache rows, written by the Markov loop and read by
+        # the verifier instead of the rows themselves
+        self.dstats = _lib.row_stats(w.B, w.K, device) if draft_stats else None
 
     def markov(self, stream=None):
         _lib.markov_sample(self.base, self.w1, self.w2, self.anchor, self.rsi, self.pos,
                            self.temperature, self.seeds, self.draft, cache=self.cache,
                            cache_row_map=self.row_map, workspace_buf=self.ws_markov,
-                           status=self.status, stream=stream)
+                           status=self.status, stream=stream, draft_stats=self.dstats)
 
     def verify(self, stream=None):
         _lib.rejection_sample(self.draft, self.cache, self.target, self.rsi, self.pos,
                               self.temperature, self.top_p, self.seeds, self.out,
                               self.num_accepted, cache_row_map=self.row_map,
                               workspace_buf=self.ws_verify, status=self.status,
-                              stream=stream)
+                              stream=stream, draft_stats=self.dstats)
 
     def run(self, stream=None):
         self.markov(stream)
