@@ -347,13 +347,12 @@ struct RowView {
   int n;
 };
 
-template <class Fix, class Body>
+template <int kU = 8, class Fix, class Body>  // kU: 16-byte loads in flight per thread
 __device__ __forceinline__ void row_sweep(const RowView& rv, uint64_t pol, Fix fix, Body body) {
   const int tid = threadIdx.x;
   int done = 0;
   if (rv.vec) {
     const int n4 = rv.n >> 2;
-    constexpr int kU = 4;  // 16-byte loads in flight per thread
     int i = tid;
     for (; i + (kU - 1) * kRowThreads < n4; i += kU * kRowThreads) {
       float v[kU][4];
@@ -540,7 +539,7 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
     __syncthreads();
     unsigned long long F = 0ull;
     if (topp) {
-      row_sweep(rv, pol_keep, fix, [&](int i, float x) {
+      row_sweep<4>(rv, pol_keep, fix, [&](int i, float x) {
         const unsigned long long f = fixed_mass(exp_rel(x, m));
         F += f;
         hist_add(sm, true, adigit0(x, m), f, static_cast<uint32_t>(v0 + i));
@@ -595,7 +594,7 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
         const bool desc = stage >= 2 && stage <= 4;  // larger kd first; distance and id ascending
         hist_clear(sm, nb);
         __syncthreads();
-        row_sweep(rv, pol_keep, fix, [&](int i, float x) {
+        row_sweep<4>(rv, pol_keep, fix, [&](int i, float x) {
           const uint32_t kd = kd_of(x);
           const uint32_t id = static_cast<uint32_t>(v0 + i);
           if (match(x, kd, id))
