@@ -347,15 +347,23 @@ def run_ours(args, rank, world, local):
         sum(t.numel() * t.element_size() for t in small_h)
     d2h = out_h.numel() * 4 + nacc_h.numel() * 4
 
+    # The target logits are needed only by the verifier: their copy runs on a
+    # second stream, beside the base-logit copy and the Markov loop.
+    tstream = torch.cuda.Stream()
+
     def e2e_step(ev):
         with torch.cuda.stream(stream):
             flush.fill_(1)
             ev[0].record(stream)
-            st.base.copy_(base_h, non_blocking=True)
-            st.target.copy_(tgt_h, non_blocking=True)
+            tstream.wait_event(ev[0])
+            with torch.cuda.stream(tstream):
+                st.target.copy_(tgt_h, non_blocking=True)
             for h, d in zip(small_h, small_d):
                 d.copy_(h, non_blocking=True)
-            st.run(stream=stream)
+            st.base.copy_(base_h, non_blocking=True)
+            st.markov(stream=stream)
+            stream.wait_stream(tstream)
+            st.verify(stream=stream)
             out_h.copy_(st.out, non_blocking=True)
             nacc_h.copy_(st.num_accepted, non_blocking=True)
             ev[1].record(stream)
