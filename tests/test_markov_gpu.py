@@ -59,6 +59,8 @@ def test_odd_vocab_nan_and_temperatures():
     (20, 2, 3001, 192, {"S": 24, "rsi": list(range(23, 3, -1)), "temperature": 1.1}),
     (12, 2, 1500, 512, {"base_bf16": True, "cache_bf16": True}),
     (64, 1, 777, 256, {}),
+    # the most draft steps the library takes
+    (3, 16, 3001, 128, {"temperature": [1.0, 0.0, 0.6]}),
 ])
 def test_edge_shapes(B, K, V, R, kw):
     w = wl.custom(B, K, V, R, seed=B * 7 + V, **kw)

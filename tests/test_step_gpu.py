@@ -101,3 +101,21 @@ def test_draft_row_maxima_from_the_loop(name):
     torch.cuda.synchronize()
     assert st2.status_code() == 0
     assert torch.equal(with_stats[0], st2.out) and torch.equal(with_stats[1], st2.num_accepted)
+
+
+def test_largest_vocabulary_decode_step():
+    """V = 2^22 - 1, the largest vocabulary the library takes: every 32-bit
+    token index and the 64-bit row offsets at their extremes, a ragged last
+    tile, and a top-p row over the whole vocabulary."""
+    torch = require_gpu()
+    from verify_dspark_markov_step_gb300.step import DecodeStep, to_numpy
+    w = wl.custom(2, 2, (1 << 22) - 1, 64, seed=31, temperature=[1.0, 0.8], top_p=[1.0, 0.9])
+    st = DecodeStep(w)
+    st.run()
+    torch.cuda.synchronize()
+    assert st.status_code() == 0
+    draft = st.draft.cpu().numpy()
+    cache = to_numpy(st.cache)
+    assert markov_parity(w, draft, cache) <= 1
+    verify_parity(w, draft, cache, st.out.cpu().numpy(), st.num_accepted.cpu().numpy(),
+                  max_exception_frac=0.5)
