@@ -245,7 +245,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                       const __grid_constant__ CUtensorMap tmap_base, MarkovStepParams P,
                       TcCfg cfg) {
   constexpr bool kRegWinners = CPW <= 16;
-  constexpr int GW = CPW == 8 ? 8 : 4;  // columns per TMEM load and Philox group
+  constexpr int GW = 4;  // columns per TMEM load and Philox group
   const int Npad = cfg.Npad, ns = cfg.ns, na = cfg.na, nb = cfg.nb;
   const int R = P.R;
   const int NK = R / 64;
