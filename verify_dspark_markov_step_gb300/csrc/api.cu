@@ -169,7 +169,11 @@ dspark_status dspark_rejection_sample(
   int sms = 0;
   if (num_sms_of_current_device(&sms) != 0) return DSPARK_ERR_CUDA;
   int cluster = 0, slice = 0;
-  if (!dspark::verify_rows_plan(V, &cluster, &slice)) return DSPARK_ERR_UNSUPPORTED;
+  // fp32 unless both the target and the (present) cache are bf16
+  const bool all_bf16 =
+      target_dtype == DSPARK_BF16 && (!draft_cache || cache_dtype == DSPARK_BF16);
+  const int es = all_bf16 ? 2 : 4;
+  if (!dspark::verify_rows_plan(V, es, &cluster, &slice)) return DSPARK_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   unsigned char* w = static_cast<unsigned char*>(workspace);
   dspark::VerifyParams p;

@@ -81,7 +81,7 @@ size_t verify_dstats_bytes(int B, int K);
 int verify_max_chunks(int V);
 int verify_chunks(int B, int V, int num_sms);
 size_t verify_rows_smem_bytes(int W);
-bool verify_rows_plan(int V, int* CL, int* W);
+bool verify_rows_plan(int V, int es, int* CL, int* W);
 cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_t stream);
 cudaError_t launch_verify(const VerifyParams& p, int CL, int W, cudaStream_t stream);
 

@@ -110,7 +110,9 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const TgtStats& t
   const bool tbf = P.target_bf16 != 0, cbf = P.cache_bf16 != 0;
   const float invD = 1.0f / ts.D;
   const float invDq = kResidual ? 1.0f / ds.D : 0.0f;
-  unsigned long long best = 0ull;
+  // running winner of this thread: its columns only grow, so a strict >
+  // keeps the lowest column on ties
+  uint32_t run_o = 0u, run_c = 0u;
   unsigned int any = 0u;
   for (int g = c0 + 4 * threadIdx.x; g < c1; g += 4 * kResThreads) {
     float t4[4], c4[4];
@@ -120,8 +122,7 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const TgtStats& t
     bool need = false;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float x = kScale ? __fdiv_rn(t4[j], T) : t4[j];
-      x = (x != x) ? -INFINITY : x;
+      const float x = fmaxf(kScale ? __fdiv_rn(t4[j], T) : t4[j], -INFINITY);  // NaN -> -inf
       float pv = __fmul_rn(exp_rel(x, ts.m), invD);
       if (kThreshold) {
         const uint32_t kd = kd_of(x);
@@ -129,7 +130,7 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const TgtStats& t
         pv = keep ? pv : 0.0f;
       }
       if (kResidual) {
-        const float c = (c4[j] != c4[j]) ? -INFINITY : c4[j];
+        const float c = fmaxf(c4[j], -INFINITY);
         pv = fmaxf(__fsub_rn(pv, __fmul_rn(exp_rel(c, ds.m), invDq)), 0.0f);
       }
       w[j] = g + j < c1 ? pv : 0.0f;
@@ -142,14 +143,17 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const TgtStats& t
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float y = __fadd_rn(ln_approx(w[j]), gumbel_of(words[j]));
-      const unsigned long long key =
-          (static_cast<unsigned long long>(ordered_key(y)) << 32) |
-          static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(g + j));
-      best = w[j] > 0.0f ? umax64(best, key) : best;
+      const uint32_t o = w[j] > 0.0f ? ordered_key(y) : 0u;
+      if (o > run_o) {
+        run_o = o;
+        run_c = static_cast<uint32_t>(g + j);
+      }
     }
   }
   *anypos = any;
-  return best;
+  return run_o == 0u ? 0ull
+                     : (static_cast<unsigned long long>(run_o) << 32) |
+                           static_cast<unsigned long long>(0xFFFFFFFFu - run_c);
 }
 
 // Winner key over columns [c0, c1) (c0 a multiple of 4) of the draw for

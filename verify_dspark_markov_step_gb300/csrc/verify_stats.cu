@@ -495,8 +495,7 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
   const bool topp = is_target && P.top_p[s] < 1.0f;
   auto passes = [&](auto prescale) {
     auto fix = [=](float c) -> float {
-      const float x = prescale(c);
-      return (x != x) ? -INFINITY : x;
+      return fmaxf(prescale(c), -INFINITY);  // fmaxf returns the other operand for NaN
     };
 
     // ---- pass 1 (HBM): maximum (fmaxf skips NaN, as if it were -inf) ---------------
@@ -671,14 +670,16 @@ size_t verify_rows_smem_bytes(int W) {
   return (sizeof(RowSmem) + 15) & ~size_t(15);
 }
 
-// Cluster size and slice width for vocabulary V: the smallest cluster whose
-// slices are at most 32768 values (128 per thread and pass).
-bool verify_rows_plan(int V, int* CL, int* W) {
+// Cluster size and slice width for vocabulary V and element size es (the
+// larger of the target and cache dtypes): the smallest cluster whose slices
+// are at most 128 KB (32768 fp32 or 65536 bf16 values per CTA).
+bool verify_rows_plan(int V, int es, int* CL, int* W) {
   const int candidates[] = {1, 2, 4, 8, 16};
+  const int max_w = (128 * 1024) / (es > 0 ? es : 4);
   for (int cl : candidates) {
     int w = (V + cl - 1) / cl;
     w = (w + 7) & ~7;
-    if (w <= 32768 || cl == 16) {
+    if (w <= max_w || cl == 16) {
       *CL = cl;
       *W = w;
       return true;
