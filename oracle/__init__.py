@@ -67,6 +67,8 @@ def lib():
             L.orc_markov_sample.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp,
                                             vp, i32, vp, vp, vp, vp,
                                             i32, i32, i32, i32, i32, i32]
+            L.orc_markov_sample_topk.restype = i32
+            L.orc_markov_sample_topk.argtypes = L.orc_markov_sample.argtypes + [i32]
             L.orc_markov_step.restype = i32
             L.orc_markov_step.argtypes = [vp, i32, vp, vp, ctypes.c_int32, f32,
                                           u64, i64, i32, i32, vp, vp, vp]
@@ -159,9 +161,10 @@ def block_argmax(y):
 # --------------------------------------------------------------------------
 def markov_sample(base, w1, w2, anchor, req_state_idx, positions, temperature,
                   seeds, cache_rows=None, cache_bf16=False, row_map=None,
-                  forced=None, write_cache=True):
+                  forced=None, write_cache=True, topk=0):
     """Run the K-step Markov loop. Returns (tokens [B,K] int32, cache or None,
-    gaps [B,K] float64). ``cache_rows`` is C (default S)."""
+    gaps [B,K] float64). ``cache_rows`` is C (default S). ``topk`` > 0 runs the
+    top-k variant (the bias only on the top-k base logits of each step)."""
     base, base_bf16 = _logit_array(base)
     B, K, V = base.shape
     w1 = _c(w1, np.uint16)
@@ -181,10 +184,13 @@ def markov_sample(base, w1, w2, anchor, req_state_idx, positions, temperature,
         cache = np.zeros((C, K, V), np.uint16 if cache_bf16 else np.float32)
     tokens = np.empty((B, K), np.int32)
     gaps = np.empty((B, K), np.float64)
-    rc = lib().orc_markov_sample(
-        _ptr(base), base_bf16, _ptr(w1), _ptr(w2), _ptr(anchor), _ptr(rsi),
-        _ptr(pos), _ptr(temp), _ptr(seeds), _ptr(cache), int(bool(cache_bf16)),
-        _ptr(row_map), _ptr(forced), _ptr(tokens), _ptr(gaps), B, K, V, R, S, C)
+    args = (_ptr(base), base_bf16, _ptr(w1), _ptr(w2), _ptr(anchor), _ptr(rsi),
+            _ptr(pos), _ptr(temp), _ptr(seeds), _ptr(cache), int(bool(cache_bf16)),
+            _ptr(row_map), _ptr(forced), _ptr(tokens), _ptr(gaps), B, K, V, R, S, C)
+    if topk:
+        rc = lib().orc_markov_sample_topk(*args, int(topk))
+    else:
+        rc = lib().orc_markov_sample(*args)
     _check(rc, "markov_sample")
     return tokens, cache, gaps
 

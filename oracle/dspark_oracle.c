@@ -239,19 +239,25 @@ static orc_winner block_argmax(const float* y, int64_t n) {
 static int markov_step_one(const void* base_row, int base_bf16,
                            const uint16_t* w1, const uint16_t* w2, int32_t prev,
                            float temperature, uint64_t seed, int64_t noise_pos,
-                           int V, int R, float* x_out, float* y_scratch,
-                           double* e_scratch, int32_t* tok_out,
+                           int V, int R, const unsigned char* cand, float* x_out,
+                           float* y_scratch, double* e_scratch, int32_t* tok_out,
                            double* gap_out) {
   if (prev < 0 || prev >= V) return ORC_EBOUNDS;
   for (int r = 0; r < R; r++)
     e_scratch[r] = (double)bf16_to_f32(w1[(int64_t)prev * R + r]);
   const int sampled = temperature > 0.0f;
   for (int64_t v = 0; v < V; v++) {
-    double acc = 0.0;
-    const uint16_t* wrow = w2 + v * (int64_t)R;
-    for (int r = 0; r < R; r++) acc += (double)bf16_to_f32(wrow[r]) * e_scratch[r];
-    float bias = (float)acc;
-    float z = load_elem(base_row, base_bf16, v) + bias;
+    float z;
+    if (cand && !cand[v]) {
+      /* top-k variant: a column outside the candidates is -inf */
+      z = -INFINITY;
+    } else {
+      double acc = 0.0;
+      const uint16_t* wrow = w2 + v * (int64_t)R;
+      for (int r = 0; r < R; r++) acc += (double)bf16_to_f32(wrow[r]) * e_scratch[r];
+      float bias = (float)acc;
+      z = load_elem(base_row, base_bf16, v) + bias;
+    }
     float x, y;
     if (sampled) {
       x = z / temperature;
@@ -268,6 +274,47 @@ static int markov_step_one(const void* base_row, int base_bf16,
   orc_winner w = block_argmax(y_scratch, V);
   *tok_out = (int32_t)w.idx;
   if (gap_out) *gap_out = w.gap;
+  return ORC_OK;
+}
+
+/* Top-k candidates of one base-logit row ([DSP] _sample_sequential_topk:
+ * "Apply the sequential Markov head only to top-k base-logit candidates",
+ * chosen once per draft position from the base logits). READING: the k
+ * largest by value, ties broken by the lower token id, -0 equal to +0, NaN
+ * above every number (the ranking of a descending torch sort); k >= V keeps
+ * every column. mask[v] = 1 for the candidates. */
+typedef struct {
+  uint32_t key;
+  int64_t idx;
+} orc_rank;
+
+static uint32_t rank_key(float x) {
+  if (x != x) return 0xFFFFFFFFu;
+  if (x == 0.0f) x = 0.0f; /* -0 -> +0 */
+  uint32_t b;
+  memcpy(&b, &x, 4);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+static int rank_cmp(const void* a, const void* b) {
+  const orc_rank* p = (const orc_rank*)a;
+  const orc_rank* q = (const orc_rank*)b;
+  if (p->key != q->key) return p->key > q->key ? -1 : 1; /* value descending */
+  return p->idx < q->idx ? -1 : (p->idx > q->idx ? 1 : 0); /* id ascending */
+}
+
+static int topk_mask(const void* base_row, int base_bf16, int64_t V, int64_t k,
+                     unsigned char* mask) {
+  orc_rank* r = (orc_rank*)malloc(sizeof(orc_rank) * (size_t)V);
+  if (!r) return ORC_ENOMEM;
+  for (int64_t v = 0; v < V; v++) {
+    r[v].key = rank_key(load_elem(base_row, base_bf16, v));
+    r[v].idx = v;
+  }
+  qsort(r, (size_t)V, sizeof(orc_rank), rank_cmp);
+  memset(mask, 0, (size_t)V);
+  for (int64_t j = 0; j < V && j < k; j++) mask[r[j].idx] = 1;
+  free(r);
   return ORC_OK;
 }
 
@@ -291,24 +338,26 @@ static int markov_step_one(const void* base_row, int base_bf16,
  * tokens    [B,K] out
  * gaps      [B,K] out or NULL: top-two gap of the noised values per step
  */
-int orc_markov_sample(const void* base, int base_bf16, const uint16_t* w1,
-                      const uint16_t* w2, const int32_t* anchor,
-                      const int32_t* rsi, const int64_t* pos,
-                      const float* temperature, const uint64_t* seeds,
-                      void* cache, int cache_bf16, const int32_t* row_map,
-                      const int32_t* forced, int32_t* tokens, double* gaps,
-                      int B, int K, int V, int R, int S, int C) {
-  if (B < 0 || K <= 0 || V <= 0 || R <= 0 || S <= 0) return ORC_EINVAL;
+static int markov_sample_impl(const void* base, int base_bf16, const uint16_t* w1,
+                              const uint16_t* w2, const int32_t* anchor,
+                              const int32_t* rsi, const int64_t* pos,
+                              const float* temperature, const uint64_t* seeds,
+                              void* cache, int cache_bf16, const int32_t* row_map,
+                              const int32_t* forced, int32_t* tokens, double* gaps,
+                              int B, int K, int V, int R, int S, int C, int topk) {
+  if (B < 0 || K <= 0 || V <= 0 || R <= 0 || S <= 0 || topk < 0) return ORC_EINVAL;
   if (!base || !w1 || !w2 || !anchor || !rsi || !pos || !temperature || !seeds ||
       !tokens)
     return ORC_EINVAL;
   float* x = (float*)malloc(sizeof(float) * (size_t)V);
   float* y = (float*)malloc(sizeof(float) * (size_t)V);
   double* e = (double*)malloc(sizeof(double) * (size_t)R);
-  if (!x || !y || !e) {
+  unsigned char* cand = topk > 0 ? (unsigned char*)malloc((size_t)V) : NULL;
+  if (!x || !y || !e || (topk > 0 && !cand)) {
     free(x);
     free(y);
     free(e);
+    free(cand);
     return ORC_ENOMEM;
   }
   int rc = ORC_OK;
@@ -338,8 +387,12 @@ int orc_markov_sample(const void* base, int base_bf16, const uint16_t* w1,
                     : (const void*)((const float*)base + base_off);
       int32_t tok;
       double gap;
+      if (cand) {
+        rc = topk_mask(base_row, base_bf16, V, topk, cand);
+        if (rc != ORC_OK) break;
+      }
       rc = markov_step_one(base_row, base_bf16, w1, w2, prev, temperature[s],
-                           seeds[s], pos[b] + i - 1, V, R, x, y, e, &tok, &gap);
+                           seeds[s], pos[b] + i - 1, V, R, cand, x, y, e, &tok, &gap);
       if (rc != ORC_OK) break;
       tokens[(int64_t)b * K + i] = tok;
       if (gaps) gaps[(int64_t)b * K + i] = gap;
@@ -358,7 +411,37 @@ int orc_markov_sample(const void* base, int base_bf16, const uint16_t* w1,
   free(x);
   free(y);
   free(e);
+  free(cand);
   return rc;
+}
+
+int orc_markov_sample(const void* base, int base_bf16, const uint16_t* w1,
+                      const uint16_t* w2, const int32_t* anchor,
+                      const int32_t* rsi, const int64_t* pos,
+                      const float* temperature, const uint64_t* seeds,
+                      void* cache, int cache_bf16, const int32_t* row_map,
+                      const int32_t* forced, int32_t* tokens, double* gaps,
+                      int B, int K, int V, int R, int S, int C) {
+  return markov_sample_impl(base, base_bf16, w1, w2, anchor, rsi, pos, temperature,
+                            seeds, cache, cache_bf16, row_map, forced, tokens, gaps,
+                            B, K, V, R, S, C, 0);
+}
+
+/* The top-k variant of the loop ([DSP] _sample_sequential_topk): per request
+ * and draft step, the Markov bias is applied to the top-k base-logit
+ * candidates of that step and every other column is -inf; sampling, the
+ * winner rule and the cache store are then the dense ones. topk >= 1. */
+int orc_markov_sample_topk(const void* base, int base_bf16, const uint16_t* w1,
+                           const uint16_t* w2, const int32_t* anchor,
+                           const int32_t* rsi, const int64_t* pos,
+                           const float* temperature, const uint64_t* seeds,
+                           void* cache, int cache_bf16, const int32_t* row_map,
+                           const int32_t* forced, int32_t* tokens, double* gaps,
+                           int B, int K, int V, int R, int S, int C, int topk) {
+  if (topk < 1) return ORC_EINVAL;
+  return markov_sample_impl(base, base_bf16, w1, w2, anchor, rsi, pos, temperature,
+                            seeds, cache, cache_bf16, row_map, forced, tokens, gaps,
+                            B, K, V, R, S, C, topk);
 }
 
 /* One step of one request with an explicit `prev` (for sampled checks at full
@@ -377,7 +460,7 @@ int orc_markov_step(const void* base_row, int base_bf16, const uint16_t* w1,
     return ORC_ENOMEM;
   }
   int rc = markov_step_one(base_row, base_bf16, w1, w2, prev, temperature, seed,
-                           noise_pos, V, R, x_out, y, e, tok_out, gap_out);
+                           noise_pos, V, R, NULL, x_out, y, e, tok_out, gap_out);
   free(y);
   free(e);
   return rc;

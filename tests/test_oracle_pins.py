@@ -618,3 +618,70 @@ def test_rejection_padding_and_bounds(orc):
     with pytest.raises(RuntimeError):
         orc.rejection_sample(bad, np.zeros((2, 2, 100), np.float32), w.target,
                              w.req_state_idx, w.positions, w.temperature, w.top_p, w.seeds)
+
+
+# ---- the top-k variant of the Markov loop ([DSP] _sample_sequential_topk) ----
+
+def _topk_set(row, k):
+    """Brute-force top-k: value descending (NaN above every number, -0 == +0),
+    token id ascending; the first k of that order."""
+    vals = np.asarray(row, np.float64)
+    nan = np.isnan(vals)
+    key = np.where(nan, np.inf, vals)
+    order = sorted(range(len(vals)), key=lambda v: (-int(nan[v]), -key[v], v))
+    return set(order[:k])
+
+
+def test_topk_covering_the_vocabulary_is_the_dense_loop(orc):
+    w = wl.custom(3, 3, 500, 64, seed=4, temperature=[1.0, 0.0, 0.7])
+    args = (w.base, w.w1, w.w2, w.anchor, w.req_state_idx, w.positions, w.temperature, w.seeds)
+    t0, c0, _ = orc.markov_sample(*args)
+    for k in (500, 501, 10 ** 6):
+        t1, c1, _ = orc.markov_sample(*args, topk=k)
+        assert np.array_equal(t0, t1) and np.array_equal(c0, c1, equal_nan=True)
+
+
+def test_topk_candidates_against_brute_force(orc):
+    """Every cached row is finite exactly on the brute-force top-k of its base
+    row and -inf elsewhere; ties, -0/+0 and NaN columns included."""
+    rng = np.random.default_rng(7)
+    w = wl.custom(4, 3, 300, 64, seed=9, temperature=[1.0, 0.5, 0.0, 1.3])
+    base = w.base.copy()
+    base[0, 0, ::7] = 1.25                      # a run of ties
+    base[1, 1, 3] = -0.0
+    base[1, 1, 4] = 0.0
+    base[2, 2, rng.integers(0, 300, 6)] = np.nan  # more NaNs than k in one row
+    base[3, 0, [5, 17]] = np.nan
+    w.base = base
+    k = 5
+    _, cache, _ = orc.markov_sample(w.base, w.w1, w.w2, w.anchor, w.req_state_idx,
+                                    w.positions, w.temperature, w.seeds, topk=k)
+    for b in range(4):
+        for i in range(3):
+            want = _topk_set(base[b, i], k)
+            got = set(np.flatnonzero(~np.isneginf(cache[b, i])).tolist())
+            assert got == want, (b, i, sorted(got), sorted(want))
+
+
+def test_topk_draws_follow_the_truncated_softmax(orc):
+    """One step over many slots with their own seeds: the tokens follow the
+    softmax of the biased logits restricted to the top-k candidates."""
+    V, R, k, N = 12, 64, 4, 20000
+    w = wl.custom(1, 1, V, R, seed=3, base_std=1.0)
+    base = np.repeat(w.base, N, axis=0)
+    anchor = np.repeat(w.anchor, N)
+    seeds = (np.arange(N, dtype=np.uint64) * np.uint64(0x9E3779B97F4A7C15)) ^ np.uint64(17)
+    temp = np.ones(N, np.float32)
+    tok, _, _ = orc.markov_sample(base, w.w1, w.w2, anchor, np.arange(N, dtype=np.int32),
+                                  np.full(N, 100, np.int64), temp, seeds, write_cache=False,
+                                  topk=k)
+    # z = fp32(base + fp32(bias)), bias an fp64 dot of the bf16 weights
+    w1 = wl.bf16_bits_to_f32(w.w1).astype(np.float64)
+    w2 = wl.bf16_bits_to_f32(w.w2).astype(np.float64)
+    bias = (w2 @ w1[int(w.anchor[0])]).astype(np.float32)
+    z = (w.base[0, 0] + bias).astype(np.float32).astype(np.float64)
+    cand = sorted(_topk_set(w.base[0, 0], k))
+    assert set(np.unique(tok).tolist()) <= set(cand)
+    p = np.exp(z[cand] - z[cand].max())
+    counts = [(tok[:, 0] == c).sum() for c in cand]
+    assert _chi2_pvalue(counts, p) > 1e-4
