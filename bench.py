@@ -263,9 +263,10 @@ def run_reference(args, rank, world):
 
 
 def _config(w, args):
+    topk = f", top-{args.draft_topk} Markov candidates" if args.draft_topk else ""
     return {"workload": f"{w.name}-like drafter: batch {w.B}, K={w.K}, vocab {w.V}, "
                         f"markov_rank {w.R}, {'bf16' if w.base_bf16 else 'fp32'} logits, "
-                        f"{'bf16' if w.cache_bf16 else 'fp32'} draft cache",
+                        f"{'bf16' if w.cache_bf16 else 'fp32'} draft cache{topk}",
             "batch": w.B, "K": w.K, "vocab": w.V, "markov_rank": w.R,
             "l2": "flushed (512 MiB write) before every timed step",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
@@ -280,7 +281,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     build.build()
     w = build_workload(args)
-    st = DecodeStep(w)
+    st = DecodeStep(w, draft_topk=args.draft_topk)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -385,10 +386,20 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = _peaks()
     per_step, ver_bytes = algorithmic_bytes(w)
     per_launch = per_step * w.K  # one launch runs all K Markov steps
+    loop_kernel = "markov_loop_tc (one launch = all K Markov steps)"
+    if args.draft_topk:
+        # top-k variant: the base logits read once and the cache rows written
+        # once (candidate selection and -inf fill), the candidates' w2 rows
+        # gathered, the embeddings; two launches
+        s_base = 2 if w.base_bf16 else 4
+        s_cache = 2 if w.cache_bf16 else 4
+        k = min(args.draft_topk, w.V)
+        per_launch = w.B * w.K * (w.V * (s_base + s_cache) + k * (2 * w.R + 8) + 2 * w.R)
+        loop_kernel = "topk_rows + markov_topk_loop (candidate selection, then the K steps)"
     loop_us = statistics.mean(loop_ms) * 1e3
     ver_us = statistics.mean(ver_ms) * 1e3
     achieved = per_launch / (loop_us * 1e-6) / 1e9
-    traffic = _traffic_from_profile(args)
+    traffic = None if args.draft_topk else _traffic_from_profile(args)
     line = {
         "metric": METRIC, "value": round(ms * 1e3, 2), "unit": "us", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -404,7 +415,7 @@ def run_ours(args, rank, world, local):
         "hbm_frac_8tbs": {
             "loop": round(per_launch / (loop_us * 1e-6) / 1e9 / PAGES_ROOFLINE_GBS, 3),
             "verify": round(ver_bytes / (ver_us * 1e-6) / 1e9 / PAGES_ROOFLINE_GBS, 3)},
-        "roofline": {"bound": "hbm", "kernel": "markov_loop_tc (one launch = all K Markov steps)",
+        "roofline": {"bound": "hbm", "kernel": loop_kernel,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "peak_kind": peak_kind,
                      "traffic": traffic,
@@ -413,7 +424,8 @@ def run_ours(args, rank, world, local):
                      "verify_frac": round(ver_bytes / (ver_us * 1e-6) / 1e9 / peak, 3)},
         "e2e": {"value": round(e2e_ms * 1e3, 1), "unit": "us", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps * 3,  # Markov loop, verify rows, verify resample
+        # the Markov loop (top-k: selection + loop), verify rows, verify resample
+        "gpu_launches": args.steps * (4 if args.draft_topk else 3),
         "clocks": clk, "status": status, "wall_s_timed_region": round(wall, 4),
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -462,6 +474,8 @@ def main():
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--cpu-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--draft-topk", type=int, default=0,
+                    help="time the top-k variant of the Markov loop (0: the dense loop)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

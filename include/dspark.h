@@ -152,6 +152,39 @@ dspark_status dspark_markov_sample(
     int32_t* status, dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * dspark_markov_sample_topk -- the top-k variant of the Markov loop.
+ * ("DSparkSpeculator" page, _sample_sequential_topk.)
+ *
+ * As dspark_markov_sample, except that for each request and draft step i the
+ * Markov bias is applied only to the `topk` candidates of that step -- the
+ * topk largest base_logits[b, i, :] by value, ties to the lower token id,
+ * NaN above every number, -0 equal to +0 (topk >= V: every column) -- and
+ * every other column of z is -inf:
+ *   z_v = base_logits[b, i, v] + bias_v   for the candidates, -inf otherwise;
+ * temperature, Gumbel noise, the winner rule and the cache store are then the
+ * dense ones (so cache[row, i, :] is -inf outside the candidates, and
+ * dspark_rejection_sample consumes the truncated distribution unchanged).
+ * Only the candidates' markov_w2 rows are read.
+ *
+ * Arguments as for dspark_markov_sample, plus
+ *   topk          candidates per request and step, in [1, 65536]
+ *   workspace     at least dspark_markov_topk_workspace_bytes() bytes,
+ *                 256-byte aligned (the candidate lists); no initialisation.
+ * Alignment: base_logits, markov_w2 and cache must be 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+size_t dspark_markov_topk_workspace_bytes(int B, int K, int V, int R, int topk);
+
+dspark_status dspark_markov_sample_topk(
+    const void* base_logits, dspark_dtype base_dtype,
+    const uint16_t* markov_w1, const uint16_t* markov_w2,
+    const int32_t* anchor_tokens, const int32_t* req_state_idx,
+    const int64_t* positions, const float* temperature, const uint64_t* seeds,
+    void* cache, dspark_dtype cache_dtype, const int32_t* cache_row_map,
+    int32_t* out_tokens, int topk, int B, int K, int V, int R, int S, int C,
+    void* workspace, size_t workspace_bytes, int32_t* status,
+    dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * dspark_markov_sample_static -- dspark_markov_sample without a workspace
  * argument: the same computation, arguments and results, with the scratch
  * kept in a fixed device array compiled into the library. The pages describe

@@ -39,6 +39,11 @@ def subset(w, idx):
 
 def check_cache(gpu, ora, bf16, mask_rows=None):
     """Compare cache tensors ([C,K,V]); returns the max abs deviation."""
+    with np.errstate(invalid="ignore"):  # inf - inf in the deviation of equal infinities
+        return _check_cache(gpu, ora, bf16)
+
+
+def _check_cache(gpu, ora, bf16):
     if bf16:
         gf = (gpu.astype(np.uint32) << 16).view(np.float32)
         of = (ora.astype(np.uint32) << 16).view(np.float32)
@@ -61,13 +66,14 @@ def check_cache(gpu, ora, bf16, mask_rows=None):
     return float(d.max()) if d.size else 0.0
 
 
-def markov_parity(w, gpu_tokens, gpu_cache=None, check_cache_values=True):
+def markov_parity(w, gpu_tokens, gpu_cache=None, check_cache_values=True, topk=0):
     """Teacher-forced comparison of the drafter: the oracle replays every step
-    from the same previous token the GPU used. Returns the exception count."""
+    from the same previous token the GPU used. Returns the exception count.
+    topk > 0 compares the top-k variant of the loop."""
     tok_o, cache_o, gaps = oracle.markov_sample(
         w.base, w.w1, w.w2, w.anchor, w.req_state_idx, w.positions, w.temperature,
         w.seeds, cache_rows=w.C, cache_bf16=w.cache_bf16, row_map=w.row_map,
-        forced=gpu_tokens, write_cache=gpu_cache is not None)
+        forced=gpu_tokens, write_cache=gpu_cache is not None, topk=topk)
     diff = tok_o != gpu_tokens
     exc = int(diff.sum())
     if exc:

@@ -36,6 +36,8 @@ EXPORTS = (
     "dspark_markov_workspace_bytes",
     "dspark_markov_sample",
     "dspark_markov_sample_static",
+    "dspark_markov_topk_workspace_bytes",
+    "dspark_markov_sample_topk",
     "dspark_verify_workspace_bytes",
     "dspark_rejection_sample",
     "dspark_noise",
@@ -76,6 +78,12 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.dspark_markov_sample_static.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                                   vp, vp, vp, i32, i32, i32, i32, i32, i32, vp,
                                                   vp]
+        L.dspark_markov_topk_workspace_bytes.restype = sz
+        L.dspark_markov_topk_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        L.dspark_markov_sample_topk.restype = i32
+        L.dspark_markov_sample_topk.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp,
+                                                vp, i32, i32, i32, i32, i32, i32, i32, vp, sz,
+                                                vp, vp]
         L.dspark_verify_workspace_bytes.restype = sz
         L.dspark_verify_workspace_bytes.argtypes = [i32, i32, i32]
         L.dspark_rejection_sample.restype = i32
@@ -254,6 +262,51 @@ def markov_sample_static(base_logits, markov_w1, markov_w2, anchor_tokens, req_s
         _ptr(out_tokens), _ptr(draft_stats), B, K, V, R, S, max(C, 1), _ptr(status),
         _stream(stream))
     _check(code, "dspark_markov_sample_static")
+
+
+def markov_sample_topk(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_idx,
+                       positions, temperature, seeds, out_tokens, topk, cache=None,
+                       cache_row_map=None, workspace_buf=None, status=None, stream=None):
+    """dspark_markov_sample_topk on torch tensors: the Markov bias only on the
+    top-k base logits of each request and step (see include/dspark.h)."""
+    _dev(base_logits, "base_logits", (torch.float32,) + _BF16_LIKE)
+    B, K, V = base_logits.shape
+    _dev(markov_w1, "markov_w1", _BF16_LIKE)
+    _dev(markov_w2, "markov_w2", _BF16_LIKE)
+    R = markov_w2.shape[1]
+    if markov_w2.shape != (V, R) or markov_w1.shape[1] != R or markov_w1.shape[0] < V:
+        raise ValueError("markov_w1 / markov_w2 must be [V, R]")
+    for t, n, d in ((anchor_tokens, "anchor_tokens", torch.int32),
+                    (req_state_idx, "req_state_idx", torch.int32),
+                    (positions, "positions", torch.int64),
+                    (temperature, "temperature", torch.float32),
+                    (out_tokens, "out_tokens", torch.int32)):
+        _dev(t, n, (d,))
+    _dev(seeds, "seeds")
+    S = temperature.shape[0]
+    if seeds.shape[0] != S or anchor_tokens.shape[0] != B or req_state_idx.shape[0] != B \
+            or positions.shape[0] != B or tuple(out_tokens.shape) != (B, K):
+        raise ValueError("inconsistent shapes")
+    C = 0
+    cache_dt = DSPARK_F32
+    if cache is not None:
+        _dev(cache, "cache", (torch.float32,) + _BF16_LIKE)
+        if cache.dim() != 3 or cache.shape[1] != K or cache.shape[2] != V:
+            raise ValueError("cache must be [C, K, V]")
+        C = cache.shape[0]
+        cache_dt = _logit_dtype(cache, "cache")
+    _dev(cache_row_map, "cache_row_map", (torch.int32,))
+    need = int(lib().dspark_markov_topk_workspace_bytes(B, K, V, R, int(topk)))
+    if workspace_buf is None:
+        workspace_buf = workspace(need, base_logits.device)
+    _dev(status, "status", (torch.int32,))
+    code = lib().dspark_markov_sample_topk(
+        _ptr(base_logits), _logit_dtype(base_logits, "base_logits"), _ptr(markov_w1),
+        _ptr(markov_w2), _ptr(anchor_tokens), _ptr(req_state_idx), _ptr(positions),
+        _ptr(temperature), _ptr(seeds), _ptr(cache), cache_dt, _ptr(cache_row_map),
+        _ptr(out_tokens), int(topk), B, K, V, R, S, max(C, 1), _ptr(workspace_buf),
+        workspace_buf.numel() * workspace_buf.element_size(), _ptr(status), _stream(stream))
+    _check(code, "dspark_markov_sample_topk")
 
 
 def rejection_sample(draft_tokens, draft_cache, target_logits, req_state_idx, positions,

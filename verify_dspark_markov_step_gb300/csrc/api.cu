@@ -141,6 +141,69 @@ dspark_status dspark_markov_sample(
   return DSPARK_OK;
 }
 
+size_t dspark_markov_topk_workspace_bytes(int B, int K, int V, int R, int topk) {
+  (void)V;
+  (void)R;
+  if (B < 0 || K < 1 || topk < 1) return 0;
+  const size_t list = align_up(static_cast<size_t>(B) * K * topk * sizeof(int32_t));
+  return 2 * list;
+}
+
+dspark_status dspark_markov_sample_topk(
+    const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
+    const uint16_t* markov_w2, const int32_t* anchor_tokens, const int32_t* req_state_idx,
+    const int64_t* positions, const float* temperature, const uint64_t* seeds, void* cache,
+    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens, int topk, int B,
+    int K, int V, int R, int S, int C, void* workspace, size_t workspace_bytes, int32_t* status,
+    dspark_stream_t stream) {
+  if (!sizes_ok(B, K, V, S) || R < 1 || topk < 1) return DSPARK_ERR_INVALID_ARG;
+  if (!valid_dtype(base_dtype) || !valid_dtype(cache_dtype)) return DSPARK_ERR_INVALID_ARG;
+  if (R % 64 != 0 || R > 512 || topk > 65536) return DSPARK_ERR_UNSUPPORTED;
+  if (B == 0) return DSPARK_OK;
+  if (!base_logits || !markov_w1 || !markov_w2 || !anchor_tokens || !req_state_idx ||
+      !positions || !temperature || !seeds || !out_tokens)
+    return DSPARK_ERR_INVALID_ARG;
+  if (cache && C < 1) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(base_logits) || !aligned16(markov_w1) || !aligned16(markov_w2) ||
+      (cache && !aligned16(cache)))
+    return DSPARK_ERR_ALIGNMENT;
+  const size_t need = dspark_markov_topk_workspace_bytes(B, K, V, R, topk);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return DSPARK_ERR_WORKSPACE;
+  int cluster = 0, slice = 0;
+  if (!dspark::verify_rows_plan(V, base_dtype == DSPARK_BF16 ? 2 : 4, &cluster, &slice))
+    return DSPARK_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  dspark::TopkParams p;
+  p.base = base_logits;
+  p.base_bf16 = base_dtype == DSPARK_BF16;
+  p.w1 = markov_w1;
+  p.w2 = markov_w2;
+  p.anchor = anchor_tokens;
+  p.rsi = req_state_idx;
+  p.pos = positions;
+  p.temperature = temperature;
+  p.seeds = seeds;
+  p.cache = cache;
+  p.cache_bf16 = cache_dtype == DSPARK_BF16;
+  p.row_map = cache_row_map;
+  p.out_tokens = out_tokens;
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.R = R;
+  p.S = S;
+  p.C = C;
+  p.k = topk;
+  p.cand_idx = reinterpret_cast<int32_t*>(w);
+  p.cand_val = reinterpret_cast<float*>(w + need / 2);
+  p.status = status;
+  if (dspark::launch_topk_rows(p, cluster, slice, st) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (dspark::launch_markov_topk_loop(p, st) != cudaSuccess) return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
 size_t dspark_verify_workspace_bytes(int B, int K, int V) {
   if (B < 0 || K < 1 || V < 1) return 0;
   return VerifyWs(B, K, V).total;

@@ -50,6 +50,30 @@ int markov_tc_grid(int V, int num_sms);
 cudaError_t launch_markov_loop_tc(const MarkovStepParams& p, const void* tmap, const void* bmap,
                                   const MarkovTcPlan& plan, int grid, cudaStream_t stream);
 
+// Top-k variant of the Markov loop: candidate selection (verify_stats.cu)
+// and the loop over the candidates (markov_topk.cu).
+struct TopkParams {
+  const void* base;
+  int base_bf16;
+  const uint16_t* w1;
+  const uint16_t* w2;
+  const int32_t* anchor;
+  const int32_t* rsi;
+  const int64_t* pos;
+  const float* temperature;
+  const uint64_t* seeds;
+  void* cache;
+  int cache_bf16;
+  const int32_t* row_map;
+  int32_t* out_tokens;
+  int B, K, V, R, S, C, k;
+  int32_t* cand_idx;  // [B*K][k] candidate token ids
+  float* cand_val;    // [B*K][k] their base logits
+  int32_t* status;
+};
+cudaError_t launch_topk_rows(const TopkParams& p, int CL, int W, cudaStream_t stream);
+cudaError_t launch_markov_topk_loop(const TopkParams& p, cudaStream_t stream);
+
 // Verification (verify.cu).
 struct VerifyParams {
   const int32_t* draft;

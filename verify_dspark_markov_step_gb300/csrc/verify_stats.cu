@@ -59,6 +59,7 @@ struct RowSmem {
   unsigned long long x_mass;
   unsigned int x_cnt;
   unsigned int x_id;
+  unsigned int x_pref;  // a per-CTA count for a cluster prefix
   // per-row reductions: one slot per CTA, two alternating sets (a row's slots
   // are rewritten only after the next row's first cluster barrier)
   unsigned int c_max[2];         // ordered bits of the CTA maximum (~0: failed)
@@ -663,6 +664,247 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyParam
   cl.sync();  // no CTA exits while another may still read its shared memory
 }
 
+// ---------------------------------------------------------------------------
+// Top-k candidates of the base-logit rows for the top-k Markov loop (the
+// "DSparkSpeculator" page, _sample_sequential_topk): per (request, draft
+// step) the k largest base logits by (value descending, token id
+// ascending), NaN above every number, -0 equal to +0. The same radix select
+// as the top-p keep set, with a unit mass per element: the boundary is the
+// k-th element of that order. The cluster also fills the step's cache row
+// with -inf (the loop writes the candidates' values).
+
+// Exclusive prefix over the cluster's ranks of one per-CTA count, and the
+// total (one cluster barrier; every CTA must call it).
+__device__ void cluster_prefix(cg::cluster_group& cl, RowSmem& sm, unsigned int v, int CL,
+                               int rank, unsigned int* before, unsigned int* total) {
+  if (threadIdx.x == 0) sm.x_pref = v;
+  cl.sync();
+  if (threadIdx.x < 32) {
+    const int r = threadIdx.x;
+    unsigned int x = r < CL ? *cl.map_shared_rank(&sm.x_pref, r) : 0u;
+    unsigned int lower = r < rank ? x : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+      lower += __shfl_xor_sync(0xFFFFFFFFu, lower, o);
+    }
+    if (threadIdx.x == 0) {
+      sm.w_u32[0] = lower;
+      sm.w_u32[1] = x;
+    }
+  }
+  __syncthreads();
+  *before = sm.w_u32[0];
+  *total = sm.w_u32[1];
+  cl.sync();  // the slots may be rewritten by the next call
+}
+
+// Exclusive prefix of a per-thread count over the block, and the block total.
+__device__ unsigned int block_prefix(RowSmem& sm, unsigned int v, unsigned int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  unsigned int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  __syncthreads();
+  if (lane == 31) sm.w_u32[w] = incl;
+  __syncthreads();
+  unsigned int before_w = 0u, tot = 0u;
+  for (int i = 0; i < kRowWarps; ++i) {
+    const unsigned int x = sm.w_u32[i];
+    if (i < w) before_w += x;
+    tot += x;
+  }
+  *total = tot;
+  __syncthreads();  // w_u32 may be reused right after
+  return before_w + incl - v;
+}
+
+__device__ void topk_row(const TopkParams& P, int W, int row_id, cg::cluster_group& cl, int CL,
+                         int rank, RowSmem& sm, int& jrow) {
+  const int tid = threadIdx.x;
+  const int K = P.K, V = P.V;
+  const int b = row_id / K, i = row_id % K;
+  const int32_t s = P.rsi[b];
+  if (s < 0) return;
+  if (s >= P.S) {
+    if (rank == 0 && tid == 0) report(P.status, DSPARK_ERR_BOUNDS);
+    return;
+  }
+  const int set = jrow & 1;
+  ++jrow;
+  const int v0 = rank * W;
+  const int n = max(0, min(W, V - v0));
+  const int64_t off = (static_cast<int64_t>(b) * K + i) * V;
+  RowView rv;
+  rv.bf16 = P.base_bf16 != 0;
+  rv.f = static_cast<const float*>(P.base) + off + v0;
+  rv.h = static_cast<const uint16_t*>(P.base) + off + v0;
+  rv.vec = rv.bf16 ? (reinterpret_cast<uintptr_t>(rv.h) & 7u) == 0
+                   : (reinterpret_cast<uintptr_t>(rv.f) & 15u) == 0;
+  rv.n = n;
+  const uint64_t pol = policy_evict_last();
+  int32_t* cidx = P.cand_idx + static_cast<int64_t>(row_id) * P.k;
+  float* cval = P.cand_val + static_cast<int64_t>(row_id) * P.k;
+  auto ident = [](float c) { return c; };
+
+  // the cache row starts as -inf: the loop stores only the candidates
+  if (P.cache != nullptr) {
+    const int64_t row = P.row_map ? P.row_map[s] : s;
+    if (row >= 0 && row < P.C) {
+      const int64_t co = (row * K + i) * V + v0;
+      if (P.cache_bf16) {
+        uint16_t* c = static_cast<uint16_t*>(P.cache) + co;
+        for (int j = tid; j < n; j += kRowThreads) c[j] = 0xFF80u;  // bf16 -inf
+      } else {
+        float* c = static_cast<float*>(P.cache) + co;
+        for (int j = tid; j < n; j += kRowThreads) c[j] = -INFINITY;
+      }
+    }
+  }
+  const int k_eff = P.k < V ? P.k : V;
+  if (k_eff == V) {  // every column is a candidate
+    row_sweep(rv, pol, ident, [&](int j, float x) {
+      cidx[v0 + j] = v0 + j;
+      cval[v0 + j] = x;
+    });
+    return;
+  }
+
+  // ---- pass 1: maximum over the numbers and the NaN count ---------------------
+  float lmax = -INFINITY;
+  unsigned long long nan_loc = 0ull;
+  row_sweep(rv, pol, ident, [&](int, float x) {
+    lmax = fmaxf(lmax, x);
+    nan_loc += (x != x) ? 1ull : 0ull;
+  });
+  bool any_fail = false;
+  const float m = cluster_max_f(cl, sm, lmax, false, set, CL, &any_fail);
+  const unsigned long long nan_tot = cluster_sum_u64(cl, sm, nan_loc, set, CL);
+
+  if (nan_tot >= static_cast<unsigned long long>(k_eff)) {
+    // the candidates are the first k NaN columns: warp 0 walks the slice in
+    // order and takes this CTA's share of them
+    unsigned int before, total;
+    const unsigned int mine = static_cast<unsigned int>(block_sum_u64(nan_loc, sm));
+    cluster_prefix(cl, sm, mine, CL, rank, &before, &total);
+    if (tid < 32 && before < static_cast<unsigned int>(k_eff)) {
+      unsigned int pos = before;
+      for (int c0 = 0; c0 < n && pos < static_cast<unsigned int>(k_eff); c0 += 32) {
+        const int j = c0 + tid;
+        float x = 0.0f;
+        if (j < n) x = rv.bf16 ? bf16_bits_to_float(rv.h[j]) : rv.f[j];
+        const bool isn = j < n && x != x;
+        const unsigned int bal = __ballot_sync(0xFFFFFFFFu, isn);
+        const unsigned int at = pos + __popc(bal & ((1u << tid) - 1u));
+        if (isn && at < static_cast<unsigned int>(k_eff)) {
+          cidx[at] = v0 + j;
+          cval[at] = x;
+        }
+        pos += __popc(bal);
+      }
+    }
+    return;
+  }
+
+  // ---- the top (k - NaNs) numbers: radix select with unit masses -------------
+  const unsigned long long need = static_cast<unsigned long long>(k_eff) - nan_tot;
+  // reach: count * 2^32 >= need * 2^32, as the 128-bit target (t_hi:t_lo)
+  const unsigned long long t_hi = 0ull, t_lo = need << 32;
+  hist_clear(sm, kRowBins);
+  __syncthreads();
+  row_sweep<4>(rv, pol, ident, [&](int j, float x) {
+    if (x == x) hist_add(sm, true, adigit0(x, m), 1ull, static_cast<uint32_t>(v0 + j));
+  });
+  Found f = cluster_find(cl, sm, kRowBins, false, 0ull, t_hi, t_lo, CL, rank);
+  unsigned long long above = f.before;
+  const int a0 = f.bin;
+  int a1 = -1;
+  int kd_len = 0, id_len = 0;
+  uint32_t kd_pre = 0u, id_pre = 0u;
+  for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
+    const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
+    const uint32_t c_kp = kd_pre, c_ip = id_pre;
+    auto match = [=](float x, uint32_t kd, uint32_t id) {
+      if (x != x || adigit0(x, m) != a0) return false;
+      if (c_a1 >= 0 && adigit1(x, m, a0) != c_a1) return false;
+      if (c_kl > 0 && (kd >> (32 - c_kl)) != c_kp) return false;
+      if (c_il > 0 && (id >> (22 - c_il)) != c_ip) return false;
+      return true;
+    };
+    auto digit = [=](float x, uint32_t kd, uint32_t id) -> int {
+      switch (stage) {
+        case 1: return adigit1(x, m, a0);
+        case 2: return static_cast<int>(kd >> 21);
+        case 3: return static_cast<int>((kd >> 10) & 0x7FFu);
+        case 4: return static_cast<int>(kd & 0x3FFu);
+        case 5: return static_cast<int>((id >> 11) & 0x7FFu);
+        default: return static_cast<int>(id & 0x7FFu);
+      }
+    };
+    const int nb = stage == 4 ? 1024 : kRowBins;
+    const bool desc = stage >= 2 && stage <= 4;
+    hist_clear(sm, nb);
+    __syncthreads();
+    row_sweep<4>(rv, pol, ident, [&](int j, float x) {
+      const uint32_t kd = kd_of(x);
+      const uint32_t id = static_cast<uint32_t>(v0 + j);
+      if (match(x, kd, id)) hist_add(sm, true, digit(x, kd, id), 1ull, id);
+    });
+    f = cluster_find(cl, sm, nb, desc, above, t_hi, t_lo, CL, rank);
+    above = f.before;
+    const uint32_t bin = static_cast<uint32_t>(f.bin);
+    if (stage == 1) {
+      a1 = f.bin;
+    } else if (stage <= 4) {
+      kd_pre = (kd_pre << (stage == 4 ? 10 : 11)) | bin;
+      kd_len += stage == 4 ? 10 : 11;
+    } else {
+      id_pre = (id_pre << 11) | bin;
+      id_len += 11;
+    }
+  }
+  const int32_t id_thr = static_cast<int32_t>(f.id);
+  const float xb = rv.bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(P.base)[off + id_thr])
+                           : static_cast<const float*>(P.base)[off + id_thr];
+  const uint32_t kd_thr = kd_of(xb);
+  auto is_cand = [=](float x, int id) {
+    if (x != x) return true;
+    const uint32_t kd = kd_of(x);
+    return kd > kd_thr || (kd == kd_thr && id <= id_thr);
+  };
+  // ---- compaction: this CTA's candidates after the lower ranks' -------------
+  unsigned int cnt = 0u;
+  row_sweep<4>(rv, pol, ident, [&](int j, float x) { cnt += is_cand(x, v0 + j) ? 1u : 0u; });
+  unsigned int blk_total;
+  const unsigned int tpos = block_prefix(sm, cnt, &blk_total);
+  unsigned int before, total;
+  cluster_prefix(cl, sm, blk_total, CL, rank, &before, &total);
+  unsigned int at = before + tpos;
+  row_sweep<4>(rv, pol, ident, [&](int j, float x) {
+    if (is_cand(x, v0 + j) && at < static_cast<unsigned int>(k_eff)) {
+      cidx[at] = v0 + j;
+      cval[at] = x;
+      ++at;
+    }
+  });
+}
+
+__global__ void __launch_bounds__(kRowThreads, 4) topk_rows_kernel(TopkParams P, int W, int nrows) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int CL = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  const int cid = blockIdx.x / CL;
+  const int nclusters = gridDim.x / CL;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
+  int jrow = 0;
+  for (int row = cid; row < nrows; row += nclusters) topk_row(P, W, row, cl, CL, rank, sm, jrow);
+  cl.sync();  // no CTA exits while another may still read its shared memory
+}
+
 }  // namespace
 
 size_t verify_rows_smem_bytes(int W) {
@@ -728,6 +970,46 @@ cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_
   if (nclusters < 1) nclusters = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
   return cudaLaunchKernelEx(&cfg, verify_rows_kernel, p, W, rows);
+}
+
+cudaError_t launch_topk_rows(const TopkParams& p, int CL, int W, cudaStream_t stream) {
+  const int rows = p.B * p.K;
+  if (rows == 0) return cudaSuccess;
+  const size_t smem = verify_rows_smem_bytes(W);
+  cudaError_t err = cudaFuncSetAttribute(topk_rows_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  if (CL > 8) {
+    err = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                               1);
+    if (err != cudaSuccess) return err;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kRowThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(CL);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(rows * CL), 1, 1);
+  int max_clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, topk_rows_kernel, &cfg) != cudaSuccess ||
+      max_clusters < 1) {
+    (void)cudaGetLastError();
+    max_clusters = 1;
+  }
+  const size_t row_bytes = static_cast<size_t>(p.V) * (p.base_bf16 ? 2 : 4);
+  const int l2_rows = static_cast<int>((80ull << 20) / (row_bytes > 0 ? row_bytes : 1));
+  int nclusters = rows < max_clusters ? rows : max_clusters;
+  if (l2_rows >= 1 && nclusters > l2_rows) nclusters = l2_rows;
+  if (nclusters < 1) nclusters = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
+  return cudaLaunchKernelEx(&cfg, topk_rows_kernel, p, W, rows);
 }
 
 }  // namespace dspark

@@ -33,7 +33,7 @@ class DecodeStep:
     """Device buffers of one workload and the two library calls."""
 
     def __init__(self, w: Workload, device="cuda", with_target: bool = True,
-                 draft_stats: bool = True):
+                 draft_stats: bool = True, draft_topk: int = 0):
         self.w = w
         self.device = device
         self.base = to_device(w.base, device)
@@ -58,8 +58,21 @@ class DecodeStep:
         # statistics of the cache rows, written by the Markov loop and read by
         # the verifier instead of the rows themselves
         self.dstats = _lib.row_stats(w.B, w.K, device) if draft_stats else None
+        # top-k variant of the loop (0: dense); it reports no row maxima
+        self.draft_topk = int(draft_topk)
+        if self.draft_topk:
+            self.dstats = None
+            self.ws_topk = _lib.workspace(_lib.lib().dspark_markov_topk_workspace_bytes(
+                w.B, w.K, w.V, w.R, self.draft_topk), device)
 
     def markov(self, stream=None):
+        if self.draft_topk:
+            _lib.markov_sample_topk(self.base, self.w1, self.w2, self.anchor, self.rsi, self.pos,
+                                    self.temperature, self.seeds, self.draft, self.draft_topk,
+                                    cache=self.cache, cache_row_map=self.row_map,
+                                    workspace_buf=self.ws_topk, status=self.status,
+                                    stream=stream)
+            return
         _lib.markov_sample(self.base, self.w1, self.w2, self.anchor, self.rsi, self.pos,
                            self.temperature, self.seeds, self.draft, cache=self.cache,
                            cache_row_map=self.row_map, workspace_buf=self.ws_markov,
