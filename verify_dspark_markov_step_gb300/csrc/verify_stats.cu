@@ -813,18 +813,22 @@ __device__ void topk_row(const TopkParams& P, int W, int row_id, cg::cluster_gro
   const unsigned long long need = static_cast<unsigned long long>(k_eff) - nan_tot;
   // reach: count * 2^32 >= need * 2^32, as the 128-bit target (t_hi:t_lo)
   const unsigned long long t_hi = 0ull, t_lo = need << 32;
+  // stage 0 counts only (one shared atomic per element); the mass of a bin
+  // is its count, and the bin's token id is found by stage 1
   hist_clear(sm, kRowBins);
   __syncthreads();
-  row_sweep<4>(rv, pol, ident, [&](int j, float x) {
-    if (x == x) hist_add(sm, true, adigit0(x, m), 1ull, static_cast<uint32_t>(v0 + j));
+  row_sweep<4>(rv, pol, ident, [&](int, float x) {
+    if (x == x) atomicAdd(&sm.hcnt[adigit0(x, m)], 1u);
   });
+  __syncthreads();
+  for (int q = tid; q < kRowBins; q += kRowThreads) sm.hmass[q] = sm.hcnt[q];
   Found f = cluster_find(cl, sm, kRowBins, false, 0ull, t_hi, t_lo, CL, rank);
   unsigned long long above = f.before;
   const int a0 = f.bin;
   int a1 = -1;
   int kd_len = 0, id_len = 0;
   uint32_t kd_pre = 0u, id_pre = 0u;
-  for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
+  for (int stage = 1; (stage == 1 || f.cnt != 1u) && stage <= 6; ++stage) {
     const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
     const uint32_t c_kp = kd_pre, c_ip = id_pre;
     auto match = [=](float x, uint32_t kd, uint32_t id) {
@@ -876,6 +880,31 @@ __device__ void topk_row(const TopkParams& P, int W, int row_id, cg::cluster_gro
     return kd > kd_thr || (kd == kd_thr && id <= id_thr);
   };
   // ---- compaction: this CTA's candidates after the lower ranks' -------------
+  if (k_eff <= kRowBins) {
+    // one sweep: append to a shared list (the order inside a CTA does not
+    // matter to the loop), then copy it after the lower ranks' lists
+    int2* list = reinterpret_cast<int2*>(sm.hmass);  // kRowBins (id, value bits) pairs
+    if (tid == 0) sm.x_pref = 0u;
+    __syncthreads();
+    row_sweep<4>(rv, pol, ident, [&](int j, float x) {
+      if (is_cand(x, v0 + j)) {
+        const unsigned int at = atomicAdd(&sm.x_pref, 1u);
+        if (at < static_cast<unsigned int>(kRowBins)) list[at] = make_int2(v0 + j, __float_as_int(x));
+      }
+    });
+    __syncthreads();
+    const unsigned int mine = sm.x_pref;
+    unsigned int before, total;
+    cluster_prefix(cl, sm, mine, CL, rank, &before, &total);
+    for (unsigned int q = tid; q < mine; q += kRowThreads) {
+      const unsigned int at = before + q;
+      if (at < static_cast<unsigned int>(k_eff)) {
+        cidx[at] = list[q].x;
+        cval[at] = __int_as_float(list[q].y);
+      }
+    }
+    return;
+  }
   unsigned int cnt = 0u;
   row_sweep<4>(rv, pol, ident, [&](int j, float x) { cnt += is_cand(x, v0 + j) ? 1u : 0u; });
   unsigned int blk_total;
