@@ -191,12 +191,6 @@ __device__ __forceinline__ unsigned long long warp_sum64(unsigned long long v) {
   return v;
 }
 
-__device__ __forceinline__ float warp_maxf(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  return v;
-}
-
 // ---------------------------------------------------------------------------
 // Element access.
 // ---------------------------------------------------------------------------
@@ -212,25 +206,6 @@ __device__ __forceinline__ float load_logit(const void* p, bool bf16, int64_t i)
 // fp32 -> bf16, round to nearest even (NaN stays NaN).
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
-
-// rint(e * 2^40) as uint64 for a finite e >= 0, round half to even, in
-// integer arithmetic (GB300's fp64 rate is far too low for a per-element
-// conversion). e = mant * 2^(E - 23), so e * 2^40 = mant * 2^(E + 17).
-__device__ __forceinline__ unsigned long long to_fixed(float e) {
-  const uint32_t bits = __float_as_uint(e);
-  const int ex = static_cast<int>((bits >> 23) & 0xFFu);
-  if (ex == 0) return 0ull;  // zero or subnormal (< 2^-126): far below 2^-41
-  const uint32_t mant = (bits & 0x7FFFFFu) | 0x800000u;
-  const int sh = ex - 127 + 17;
-  if (sh >= 0) return static_cast<unsigned long long>(mant) << sh;
-  const int rs = -sh;
-  if (rs > 24) return 0ull;  // mant * 2^-rs < 1/2
-  const uint32_t q = mant >> rs;
-  const uint32_t rem = mant & ((1u << rs) - 1u);
-  const uint32_t half = 1u << (rs - 1);
-  const uint32_t up = (rem > half) || (rem == half && (q & 1u));
-  return static_cast<unsigned long long>(q + up);
 }
 
 // ---------------------------------------------------------------------------
@@ -328,17 +303,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase,
   }
 }
 
-// 1-D bulk copy global -> shared, completion counted on `bar` (bytes and
-// both addresses multiples of 16).
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -349,17 +313,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
-}
-
-// Streaming 16-byte load: no L1 allocation, L2 eviction priority from
-// `policy` (data read exactly once).
-__device__ __forceinline__ float4 ld_stream_f4(const float* p, uint64_t policy) {
-  float4 v;
-  asm volatile(
-      "ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0,%1,%2,%3}, [%4], %5;"
-      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-      : "l"(p), "l"(policy));
-  return v;
 }
 
 // Loads of read-only rows with an L2 eviction priority from `policy` (no L1
@@ -389,17 +342,4 @@ __device__ __forceinline__ uint16_t ld_hint_u16(const uint16_t* p, uint64_t poli
   asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(policy));
   return v;
 }
-__device__ __forceinline__ uint64_t policy_evict_normal() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-// Streaming 16-byte store (evict-first in L1 and L2).
-__device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
-  asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x),
-               "f"(v.y), "f"(v.z), "f"(v.w)
-               : "memory");
-}
-
 }  // namespace dspark

@@ -167,11 +167,6 @@ __device__ __forceinline__ void st_pred(float* p, float v, bool pred) {
                "f"(v), "r"(static_cast<uint32_t>(pred))
                : "memory");
 }
-__device__ __forceinline__ void st_pred(uint16_t* p, float v, bool pred) {
-  asm volatile("{ .reg .pred q; setp.ne.u32 q, %2, 0; @q st.global.u16 [%0], %1; }" ::"l"(p),
-               "h"(float_to_bf16_bits(v)), "r"(static_cast<uint32_t>(pred))
-               : "memory");
-}
 __device__ __forceinline__ void st_pred_bits(uint16_t* p, uint16_t h, bool pred) {
   asm volatile("{ .reg .pred q; setp.ne.u32 q, %2, 0; @q st.global.u16 [%0], %1; }" ::"l"(p),
                "h"(h), "r"(static_cast<uint32_t>(pred))
