@@ -127,20 +127,22 @@ __device__ __forceinline__ float ln_approx(float x) {
 __device__ __forceinline__ float exp_rel(float x, float m) { return __expf(__fsub_rn(x, m)); }
 
 // Fixed-point mass rint(e * 2^40) of e in [0, 1], summed as two 32-bit
-// partials: vh = rint(e * 2^20) and vl = e * 2^40 - vh * 2^20 (exact, |vl| <=
-// 2^19), so rint(e * 2^40) = vh * 2^20 + rint(vl). Both roundings are the
-// add-1.5*2^23 trick (the sum lands in [2^23, 2^24), where the spacing is 1).
-// Neither partial overflows while a thread adds fewer than 2^11 values.
+// partials: vh = rint(e * 2^20) and f = e * 2^20 - vh (exact: the fraction
+// bits of e * 2^20, |f| <= 1/2), so rint(e * 2^40) = vh * 2^20 +
+// rint(f * 2^20). Both roundings are the add-1.5*2^23 trick inside one FMA
+// (the sum lands in [2^23, 2^24), where the spacing is 1, and the product is
+// exact), read back from the sum's mantissa bits. Neither partial overflows
+// while a thread adds fewer than 2^11 values.
 struct MassAcc {
   uint32_t hi = 0u;  // sum of vh
-  int32_t lo = 0;    // sum of rint(vl)
+  int32_t lo = 0;    // sum of rint(f * 2^20)
   __device__ __forceinline__ void add(float e) {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
     constexpr uint32_t kMagicBits = 0x4B400000u;
-    const float s = __fadd_rn(__fmul_rn(e, 0x1p20f), kMagic);
+    const float s = __fmaf_rn(e, 0x1p20f, kMagic);
     const float vh = __fsub_rn(s, kMagic);
-    const float vl = __fmaf_rn(vh, -0x1p20f, __fmul_rn(e, 0x1p40f));
-    const float r = __fadd_rn(vl, kMagic);
+    const float f = __fmaf_rn(e, 0x1p20f, -vh);
+    const float r = __fmaf_rn(f, 0x1p20f, kMagic);
     hi += __float_as_uint(s) - kMagicBits;
     lo += static_cast<int32_t>(__float_as_uint(r) - kMagicBits);
   }

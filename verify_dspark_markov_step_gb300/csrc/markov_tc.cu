@@ -17,7 +17,9 @@
 // accumulator lives in tensor memory.
 //
 // One CTA per SM, warp-specialised; the CTAs sweep the vocabulary tiles once
-// per step and the pipeline runs across step boundaries:
+// per step, forward on even steps and backward on odd ones (the tiles a step
+// ends on, still in L2, start the next), and the pipeline runs across step
+// boundaries:
 //   warp 0      TMA producer of markov_w2: 128x64 bf16 boxes (128-byte
 //               swizzle) into a ring of up to 12 shared-memory stages, L2
 //               evict-last, as far ahead as the ring allows (into the next
@@ -39,8 +41,9 @@
 //               registers across tiles when CPW <= 16, else reduced per tile
 //               with redux.sync.
 // At the end of a step each CTA folds its winners into the step's global
-// winner keys (64-bit atomicMax), then a grid barrier (an arrival counter,
-// bounded wait) lets every CTA read the step's tokens, gather the next Markov
+// winner keys (64-bit atomicMax) and starts L2 prefetches of the embedding
+// rows of its own winners; then a grid barrier (an arrival counter, bounded
+// wait) lets every CTA read the step's tokens, gather the next Markov
 // embeddings w1[token] into shared memory and release the MMA warp.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -82,8 +85,8 @@ __host__ __device__ inline size_t base_slot_stride(size_t base_stage) {
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 struct TcLayout {
-  size_t a, e, bases, xs, gs, seed, npos, bptr, cptr, cb0, prev, act, best, xbest, bars, slot,
-      flags, total;
+  size_t a, e, bases, xs, gs, seed, npos, bptr, cptr, cb0, prev, act, best, xbest, wkey, wx, bars,
+      slot, flags, total;
   __host__ __device__ TcLayout(int Npad, int NK, int ns, int nb, size_t base_stage) {
     a = 0;                                                       // markov_w2 ring
     e = a + static_cast<size_t>(ns) * kStageBytes;               // Markov embeddings
@@ -99,7 +102,9 @@ struct TcLayout {
     act = prev + static_cast<size_t>(Npad) * 4;
     best = act + static_cast<size_t>(Npad) * 4;
     xbest = best + static_cast<size_t>(Npad) * 8;                //   cache-row maximum key
-    bars = xbest + static_cast<size_t>(Npad) * 8;
+    wkey = xbest + static_cast<size_t>(Npad) * 8;                // per lane quarter: winner key,
+    wx = wkey + static_cast<size_t>(4 * Npad) * 8;               //   cache-row maximum key
+    bars = wx + static_cast<size_t>(4 * Npad) * 4;
     slot = bars + static_cast<size_t>(2 * kMaxStages + 2 * kMaxAcc + 2 * kMaxBaseSlots + 2) * 8;
     flags = slot + 8;
     total = flags + 16 + 1024;  // + slack to align the base to 1024 B
@@ -172,6 +177,11 @@ __device__ __forceinline__ void st_pred_bits(uint16_t* p, uint16_t h, bool pred)
                "h"(h), "r"(static_cast<uint32_t>(pred))
                : "memory");
 }
+// Starts bringing `bytes` (a multiple of 16) at the 16-byte aligned `p` into L2.
+__device__ __forceinline__ void l2_prefetch_row(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // The value of an order key (0, the empty key, reads as -inf).
 __device__ __forceinline__ float key_to_float(uint32_t k) {
   if (k == 0u) return -INFINITY;
@@ -195,8 +205,9 @@ __device__ __forceinline__ float ld_pred(const uint16_t* p, bool pred) {
 }
 
 // Position of loop iteration g = step * n_loc + il of a CTA (tile t of its
-// share), and the slot/parity of a ring of n buffers, advanced without
-// integer division.
+// share: blockIdx.x + j * G, j rising on even steps and falling on odd ones,
+// so a step starts on the tile the previous one ended on), and the
+// slot/parity of a ring of n buffers, advanced without integer division.
 struct TileIter {
   int step, il, t, n_loc, G;
   __device__ TileIter(int n_loc_, int G_)
@@ -207,9 +218,8 @@ struct TileIter {
     if (++il == n_loc) {
       il = 0;
       ++step;
-      t = static_cast<int>(blockIdx.x);
     } else {
-      t += G;
+      t += (step & 1) ? -G : G;
     }
   }
 };
@@ -266,6 +276,9 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   int32_t* s_prev = reinterpret_cast<int32_t*>(smem + L.prev);
   int32_t* s_act = reinterpret_cast<int32_t*>(smem + L.act);        // request live
   unsigned long long* best = reinterpret_cast<unsigned long long*>(smem + L.best);
+  // register-winner epilogue: one winner per (TMEM lane quarter, request)
+  unsigned long long* s_wkey = reinterpret_cast<unsigned long long*>(smem + L.wkey);
+  uint32_t* s_wx = reinterpret_cast<uint32_t*>(smem + L.wx);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kMaxStages;
   uint64_t* acc_full = empty + kMaxStages;
@@ -459,6 +472,8 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     // ---- MMA issuer -------------------------------------------------------------
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16_f32(kM, Npad);
+      const uint64_t a_desc0 = tc::sw128_kmajor_desc(smem_addr(a_base));
+      const uint64_t b_desc0 = tc::sw128_kmajor_desc(smem_addr(e_base));
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -486,12 +501,13 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             break;
           }
           tc::fence_after_thread_sync();
-          const uint32_t a0 = smem_addr(a_base + static_cast<size_t>(stage) * kStageBytes);
-          const uint32_t b0 = smem_addr(e_base + static_cast<size_t>(kc) * Npad * 128);
+          // the descriptor's address field is (address >> 4): a 32-byte K
+          // step adds 2, a stage or a K chunk its byte offset >> 4
+          const uint64_t ad = a_desc0 + static_cast<uint32_t>((stage * kStageBytes) >> 4);
+          const uint64_t bd = b_desc0 + static_cast<uint32_t>((kc * Npad * 128) >> 4);
+          tc::mma_bf16(d, ad, bd, idesc, kc != 0 ? 1u : 0u);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tc::mma_bf16(d, tc::sw128_kmajor_desc(a0 + j * 32), tc::sw128_kmajor_desc(b0 + j * 32),
-                         idesc, (kc | j) != 0 ? 1u : 0u);
+          for (int j = 1; j < 4; ++j) tc::mma_bf16(d, ad + 2 * j, bd + 2 * j, idesc, 1u);
           tc::mma_commit(&empty[stage]);
           if (++stage == ns) {
             stage = 0;
@@ -531,6 +547,22 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         bv[j] = ld_pred(bp + v, bp != nullptr && in_range);
       }
     };
+    // Philox blocks of this lane quad's 4 columns for the requests of group
+    // [cb, cb + GW): block h for request cb + 4h + (lane & 3), transposed so
+    // that nw[4h + i] is this lane's noise for request cb + 4h + i
+    auto noise_group = [&](int cb, int v, uint32_t (&nw)[GW]) {
+#pragma unroll
+      for (int h = 0; h < GW / 4; ++h) {
+        const int bq = cb + 4 * h + (lane & 3);
+        const U4 blk = noise_block(s_seed[bq], s_npos[bq], static_cast<uint32_t>(v),
+                                   kStreamDraft);
+        nw[4 * h + 0] = blk.x;
+        nw[4 * h + 1] = blk.y;
+        nw[4 * h + 2] = blk.z;
+        nw[4 * h + 3] = blk.w;
+        quad_transpose(nw + 4 * h);
+      }
+    };
     bool skip = false;  // set after a failed wait: the warp then only walks the loop
     TileIter it(n_loc, G);
     RingPos ar(na), br(tma_base ? nb : 1);
@@ -553,8 +585,11 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           skip = true;
         }
       }
-      if (!skip) {
-        tc::fence_after_thread_sync();
+      // One tile; kRev = the step walks its tiles backward (ties then go to
+      // the later, lower row).
+      auto tile = [&](auto rev_tag) {
+        constexpr bool kRev = decltype(rev_tag)::value;
+        static_cast<void>(kRev);  // only the register winners depend on the order
         const unsigned char* sb = base_s + bs * base_stride;
 #pragma unroll
         for (int c = 0; c < CPW; c += GW) {
@@ -581,21 +616,8 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             for (int j = 0; j < GW; ++j) bv[j] = bnext[j];
             if (c + GW < c_live) load_direct(cb + GW, v, in_range, bnext);
           }
-          // Philox blocks of this lane quad's 4 columns: block h for request
-          // cb + 4h + (lane & 3), transposed so that nw[4h + i] is this
-          // lane's noise for request cb + 4h + i
           uint32_t nw[GW];
-#pragma unroll
-          for (int h = 0; h < GW / 4; ++h) {
-            const int bq = cb + 4 * h + (lane & 3);
-            const U4 blk = noise_block(s_seed[bq], s_npos[bq], static_cast<uint32_t>(v),
-                                       kStreamDraft);
-            nw[4 * h + 0] = blk.x;
-            nw[4 * h + 1] = blk.y;
-            nw[4 * h + 2] = blk.z;
-            nw[4 * h + 3] = blk.w;
-            quad_transpose(nw + 4 * h);
-          }
+          noise_group(cb, v, nw);
           float xsc[GW], gsc[GW];
 #pragma unroll
           for (int h = 0; h < GW / 4; ++h) {
@@ -633,9 +655,9 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             if constexpr (kRegWinners) run_xm[c + j] = fmaxf(run_xm[c + j], xr);
             const uint32_t ord = in_range ? ordered_key(y) : 0u;  // real values map above 0
             if constexpr (kRegWinners) {
-              // rows of a lane only grow across a step's tiles: a strict >
-              // keeps the lowest row on ties
-              if (ord > run_ord[c + j]) {
+              // a lane's rows grow (shrink) across a forward (backward)
+              // step: > (>=) keeps the lowest row on ties
+              if (kRev ? ord >= run_ord[c + j] : ord > run_ord[c + j]) {
                 run_ord[c + j] = ord;
                 run_v[c + j] = static_cast<uint32_t>(v);
               }
@@ -644,6 +666,17 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
               if (lane == 0 && key != 0ull) atomicMax(&best[b], key);
             }
           }
+        }
+      };
+      if (!skip) {
+        tc::fence_after_thread_sync();
+        if constexpr (kRegWinners) {
+          if (step & 1)
+            tile(std::true_type{});
+          else
+            tile(std::false_type{});
+        } else {
+          tile(std::false_type{});
         }
         tc::fence_before_thread_sync();
         __syncwarp();
@@ -656,56 +689,86 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
 
       // ---- end of a step: fold winners, grid barrier, tokens, next embeddings ----
       if constexpr (kRegWinners) {
+        // the warp's winner per request column into this lane quarter's slot
+        // (plain stores, independent reductions)
+        uint32_t om[CPW], vm[CPW], xm[CPW];
 #pragma unroll
-        for (int j = 0; j < CPW; ++j) {
-          if (j < c_live && !skip) {
-            const unsigned long long key = warp_winner(run_ord[j], run_v[j]);
-            if (lane == 0 && key != 0ull) atomicMax(&best[c_begin + j], key);
-            if (want_stats) {
-              const uint32_t xk = __reduce_max_sync(0xFFFFFFFFu, ordered_key(run_xm[j]));
-              if (lane == 0) atomicMax(&xbest[c_begin + j], xk);
+        for (int j = 0; j < CPW; ++j) om[j] = __reduce_max_sync(0xFFFFFFFFu, run_ord[j]);
+#pragma unroll
+        for (int j = 0; j < CPW; ++j)
+          vm[j] = __reduce_min_sync(0xFFFFFFFFu, (run_ord[j] == om[j] && om[j] != 0u)
+                                                     ? run_v[j]
+                                                     : 0xFFFFFFFFu);
+#pragma unroll
+        for (int j = 0; j < CPW; ++j)
+          xm[j] = want_stats ? __reduce_max_sync(0xFFFFFFFFu, ordered_key(run_xm[j])) : 0u;
+        if (lane == 0 && !skip) {
+#pragma unroll
+          for (int j = 0; j < CPW; ++j) {
+            if (j < c_live) {
+              s_wkey[q * Npad + c_begin + j] =
+                  om[j] == 0u ? 0ull
+                              : (static_cast<unsigned long long>(om[j]) << 32) |
+                                    (0xFFFFFFFFu - vm[j]);
+              s_wx[q * Npad + c_begin + j] = xm[j];
             }
           }
+        }
+#pragma unroll
+        for (int j = 0; j < CPW; ++j) {
           run_ord[j] = 0u;
           run_v[j] = 0xFFFFFFFFu;
           run_xm[j] = -INFINITY;
         }
       }
       epi_bar();
+      const bool last = step + 1 == K;
       unsigned long long* keys = P.keys + static_cast<size_t>(step) * B;
       for (int b = etid; b < B; b += kEpiThreads) {
-        const unsigned long long k = best[b];
-        if (k != 0ull) atomicMax(keys + b, k);
-        best[b] = 0ull;
+        unsigned long long k;
+        uint32_t xk;
+        if constexpr (kRegWinners) {
+          k = umax64(umax64(s_wkey[b], s_wkey[Npad + b]),
+                     umax64(s_wkey[2 * Npad + b], s_wkey[3 * Npad + b]));
+          xk = max(max(s_wx[b], s_wx[Npad + b]), max(s_wx[2 * Npad + b], s_wx[3 * Npad + b]));
+        } else {
+          k = best[b];
+          best[b] = 0ull;
+          xk = 0u;
+        }
+        if (k != 0ull) {
+          atomicMax(keys + b, k);
+          // this block's winner is the likeliest next token: start bringing
+          // its embedding row into L2 while the grid meets
+          if (!last) l2_prefetch_row(P.w1 + static_cast<int64_t>(key_index(k)) * R, R * 2);
+        }
         // the cache row's maximum, as an order key in the scratch word
         if (want_stats && s_cb0[b] != nullptr)
-          atomicMax(&P.draft_stats[static_cast<int64_t>(b) * K + step].scratch, xbest[b]);
-        xbest[b] = 0u;
+          atomicMax(&P.draft_stats[static_cast<int64_t>(b) * K + step].scratch, xk);
       }
-      __threadfence();
       epi_bar();
-      const bool last = step + 1 == K;
       if (etid == 0) {
         // one decision for all epilogue warps: stop at the first failure
         int stop = *fail_flag;
         if (!stop) {
+          __threadfence();  // the block's key updates before its arrival
           atomicAdd(P.counter, 1u);
-          // the last step's tokens are needed by CTA 0 alone
-          if (!last || blockIdx.x == 0) {
-            const unsigned int target =
-                static_cast<unsigned int>(step + 1) * static_cast<unsigned int>(G);
-            const unsigned long long t0 = globaltimer_ns();
-            while (ld_acquire_u32(P.counter) < target) {
-              __nanosleep(64);
-              if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                report(P.status, DSPARK_ERR_TIMEOUT);
-                *fail_flag = 1;
-                stop = 1;
-                break;
-              }
+        }
+        // the last step's tokens are needed by CTA 0 alone
+        if (!stop && (!last || blockIdx.x == 0)) {
+          const unsigned int target =
+              static_cast<unsigned int>(step + 1) * static_cast<unsigned int>(G);
+          const unsigned long long t0 = globaltimer_ns();
+          while (ld_acquire_u32(P.counter) < target) {
+            __nanosleep(32);
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              report(P.status, DSPARK_ERR_TIMEOUT);
+              *fail_flag = 1;
+              stop = 1;
+              break;
             }
-            __threadfence();
           }
+          __threadfence();
         }
         *stop_word = stop;
       }
@@ -915,3 +978,4 @@ cudaError_t launch_markov_loop_tc(const MarkovStepParams& p, const void* tmap, c
 }
 
 }  // namespace dspark
+

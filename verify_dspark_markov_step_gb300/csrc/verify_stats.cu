@@ -660,7 +660,17 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyParam
   extern __shared__ __align__(16) unsigned char smem_raw[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
   int jrow = 0;
+#ifdef DSPARK_EXP_STAGGER
+  // odd clusters walk their rows backward: about half the clusters stream a
+  // draft row (one pass) while the others are on a target row (two passes)
+  const int nmine = nrows > cid ? (nrows - cid + nclusters - 1) / nclusters : 0;
+  for (int i = 0; i < nmine; ++i) {
+    const int k = (cid & 1) ? nmine - 1 - i : i;
+    process_row(P, W, cid + k * nclusters, cl, CL, rank, sm, jrow);
+  }
+#else
   for (int row = cid; row < nrows; row += nclusters) process_row(P, W, row, cl, CL, rank, sm, jrow);
+#endif
   cl.sync();  // no CTA exits while another may still read its shared memory
 }
 
