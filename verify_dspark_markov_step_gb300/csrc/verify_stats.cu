@@ -59,6 +59,8 @@ struct RowSmem {
   unsigned long long x_mass;
   unsigned int x_cnt;
   unsigned int x_id;
+  unsigned int x_cmin;  // value-key range of the stage's candidates in this CTA
+  unsigned int x_cmax;
   unsigned int x_pref;  // a per-CTA count for a cluster prefix
   // per-row reductions: one slot per CTA, two alternating sets (a row's slots
   // are rewritten only after the next row's first cluster barrier)
@@ -82,6 +84,7 @@ struct Found {
   unsigned int cnt;
   unsigned long long mass;
   unsigned int id;
+  unsigned int kmin, kmax;    // value-key range of all the stage's candidates
 };
 
 __device__ unsigned long long block_sum_u64(unsigned long long v, RowSmem& sm) {
@@ -186,45 +189,44 @@ __device__ __forceinline__ void hist_add(RowSmem& sm, bool active, int bin,
 
 // Reduces the local histograms over the cluster and finds the first
 // non-empty bin, in scan order (descending bin index if desc), at which the
-// running mass (starting from `above`) reaches the target (t_hi:t_lo).
+// running mass (starting from `above`) reaches the target (t_hi:t_lo). Each
+// thread passes the value-key range [kmin, kmax] of the candidates it saw
+// (~0, 0: none); Found carries the range over the cluster.
 __device__ Found cluster_find(cg::cluster_group& cl, RowSmem& sm, int nb, bool desc,
                               unsigned long long above, unsigned long long t_hi,
-                              unsigned long long t_lo, int CL, int rank) {
+                              unsigned long long t_lo, int CL, int rank,
+                              uint32_t kmin = 0xFFFFFFFFu, uint32_t kmax = 0u) {
   const int tid = threadIdx.x;
   const int b0 = rank * nb / CL;
   const int w = (rank + 1) * nb / CL - b0;
   __syncthreads();
-  cl.sync();  // every local histogram is complete
-  // 1. reduce the bins this CTA owns over the cluster
-  constexpr int kPer = kRowBins / kRowThreads;  // at most 4 owned bins per thread
-  unsigned long long rm[kPer];
-  unsigned int rc[kPer], ri[kPer];
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    rm[j] = 0ull;
-    rc[j] = 0u;
-    ri[j] = 0u;
-    const int bi = tid + j * kRowThreads;
-    if (bi < w) {
-      for (int r = 0; r < CL; ++r) {
-        RowSmem* o = cl.map_shared_rank(&sm, r);
-        rm[j] += o->hmass[b0 + bi];
-        rc[j] += o->hcnt[b0 + bi];
-        ri[j] = max(ri[j], o->hid[b0 + bi]);
-      }
-    }
+  {
+    const uint32_t lo = block_reduce<uint32_t>(kmin, sm.w_u32, 0xFFFFFFFFu,
+                                               [](uint32_t a, uint32_t b) { return min(a, b); });
+    if (tid == 0) sm.x_cmin = lo;
+    __syncthreads();  // the warp slots are reused below
+    const uint32_t hi = block_reduce<uint32_t>(kmax, sm.w_u32, 0u,
+                                               [](uint32_t a, uint32_t b) { return max(a, b); });
+    if (tid == 0) sm.x_cmax = hi;
+    __syncthreads();
   }
-  cl.sync();  // every remote read is done; owned bins may be overwritten
+  cl.sync();  // every local histogram and candidate range is complete
+  // 1. reduce the bins this CTA owns over the cluster, in place: only this
+  //    CTA reads any CTA's entries of its own range
   unsigned long long mine = 0ull;
-#pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int bi = tid + j * kRowThreads;
-    if (bi < w) {
-      sm.hmass[b0 + bi] = rm[j];
-      sm.hcnt[b0 + bi] = rc[j];
-      sm.hid[b0 + bi] = ri[j];
-      mine += rm[j];
+  for (int bi = tid; bi < w; bi += kRowThreads) {
+    unsigned long long bm = 0ull;
+    unsigned int bc = 0u, bid = 0u;
+    for (int r = 0; r < CL; ++r) {
+      const RowSmem* o = cl.map_shared_rank(&sm, r);
+      bm += o->hmass[b0 + bi];
+      bc += o->hcnt[b0 + bi];
+      bid = max(bid, o->hid[b0 + bi]);
     }
+    sm.hmass[b0 + bi] = bm;
+    sm.hcnt[b0 + bi] = bc;
+    sm.hid[b0 + bi] = bid;
+    mine += bm;
   }
   const unsigned long long range_mass = block_sum_u64(mine, sm);
   if (tid == 0) sm.x_range = range_mass;
@@ -290,14 +292,20 @@ __device__ Found cluster_find(cg::cluster_group& cl, RowSmem& sm, int nb, bool d
   // 4. the first qualifying bin over the cluster
   if (tid == 0) {
     int best_r = -1, best_pos = 0x7FFFFFFF;
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
     for (int r = 0; r < CL; ++r) {
-      const int p = cl.map_shared_rank(&sm, r)->x_pos;
+      const RowSmem* o = cl.map_shared_rank(&sm, r);
+      const int p = o->x_pos;
       if (p < best_pos) {
         best_pos = p;
         best_r = r;
       }
+      lo = min(lo, o->x_cmin);
+      hi = max(hi, o->x_cmax);
     }
     sm.bcast_i = best_r;
+    sm.w_u32[0] = lo;
+    sm.w_u32[1] = hi;
   }
   __syncthreads();
   Found f;
@@ -317,6 +325,8 @@ __device__ Found cluster_find(cg::cluster_group& cl, RowSmem& sm, int nb, bool d
     f.mass = o->x_mass;
     f.id = o->x_id;
   }
+  f.kmin = sm.w_u32[0];
+  f.kmax = sm.w_u32[1];
   cl.sync();  // slots may be rewritten by the next stage
   return f;
 }
@@ -348,8 +358,21 @@ struct RowView {
   int n;
 };
 
+template <int kU, bool kBf16, class Fix, class Body>
+__device__ __forceinline__ void row_sweep_t(RowView rv, uint64_t pol, Fix fix, Body body);
+
+// The dtype is decided once per sweep: each instantiation reads one format.
 template <int kU = 8, class Fix, class Body>  // kU: 16-byte loads in flight per thread
 __device__ __forceinline__ void row_sweep(const RowView& rv, uint64_t pol, Fix fix, Body body) {
+  if (rv.bf16)
+    row_sweep_t<kU, true>(rv, pol, fix, body);
+  else
+    row_sweep_t<kU, false>(rv, pol, fix, body);
+}
+
+template <int kU, bool kBf16, class Fix, class Body>
+__device__ __forceinline__ void row_sweep_t(RowView rv, uint64_t pol, Fix fix, Body body) {
+  rv.bf16 = kBf16;  // a compile-time constant from here on
   const int tid = threadIdx.x;
   int done = 0;
   if (rv.vec) {
@@ -569,7 +592,8 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
       uint32_t kd_pre = 0u, id_pre = 0u;
       // Stages 1..6 split the boundary bin until it holds one element: the
       // distance sub-bins, kd bits [31:21], [20:10], [9:0], id bits [21:11],
-      // [10:0]. After the last id stage the bin is a single token.
+      // [10:0]. After the last id stage the bin is a single token. Once the
+      // bin holds a single value, the value stages left are skipped.
       for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
         const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
         const uint32_t c_kp = kd_pre, c_ip = id_pre;
@@ -594,13 +618,17 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
         const bool desc = stage >= 2 && stage <= 4;  // larger kd first; distance and id ascending
         hist_clear(sm, nb);
         __syncthreads();
+        uint32_t cmin = 0xFFFFFFFFu, cmax = 0u;  // value-key range of the candidates
         row_sweep<4>(rv, pol_keep, fix, [&](int i, float x) {
           const uint32_t kd = kd_of(x);
           const uint32_t id = static_cast<uint32_t>(v0 + i);
-          if (match(x, kd, id))
+          if (match(x, kd, id)) {
             hist_add(sm, true, digit(x, kd, id), fixed_mass(exp_rel(x, m)), id);
+            cmin = min(cmin, kd);
+            cmax = max(cmax, kd);
+          }
         });
-        f = cluster_find(cl, sm, nb, desc, above, t_hi, t_lo, CL, rank);
+        f = cluster_find(cl, sm, nb, desc, above, t_hi, t_lo, CL, rank, cmin, cmax);
         above = f.before;
         const uint32_t bin = static_cast<uint32_t>(f.bin);
         if (stage == 1) {
@@ -611,6 +639,14 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
         } else {
           id_pre = (id_pre << 11) | bin;
           id_len += 11;
+        }
+        // every candidate of this stage had one value (ties, e.g. in a bf16
+        // row), so the boundary bin does too: the value stages cannot split
+        // it, go on with the token-id stages
+        if (stage < 5 && f.cnt > 1u && f.kmin == f.kmax) {
+          kd_pre = f.kmin;
+          kd_len = 32;
+          stage = 4;
         }
       }
       // f is the one-element bin at the boundary: its token, mass and logit
@@ -660,17 +696,13 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyParam
   extern __shared__ __align__(16) unsigned char smem_raw[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
   int jrow = 0;
-#ifdef DSPARK_EXP_STAGGER
   // odd clusters walk their rows backward: about half the clusters stream a
   // draft row (one pass) while the others are on a target row (two passes)
   const int nmine = nrows > cid ? (nrows - cid + nclusters - 1) / nclusters : 0;
-  for (int i = 0; i < nmine; ++i) {
-    const int k = (cid & 1) ? nmine - 1 - i : i;
-    process_row(P, W, cid + k * nclusters, cl, CL, rank, sm, jrow);
-  }
-#else
-  for (int row = cid; row < nrows; row += nclusters) process_row(P, W, row, cl, CL, rank, sm, jrow);
-#endif
+  const int first = (cid & 1) ? cid + (nmine - 1) * nclusters : cid;
+  const int stride = (cid & 1) ? -nclusters : nclusters;
+  for (int row = first; row >= cid && row < nrows; row += stride)
+    process_row(P, W, row, cl, CL, rank, sm, jrow);
   cl.sync();  // no CTA exits while another may still read its shared memory
 }
 
