@@ -40,7 +40,7 @@ struct MarkovWs {
 };
 
 struct VerifyWs {
-  size_t counters, tstats, dstats, keys, anypos, total;
+  size_t counters, tstats, dstats, keys, anypos, cand, total;
   VerifyWs(int B, int K, int V) {
     const int mc = dspark::verify_max_chunks(V);
     counters = 0;
@@ -48,7 +48,9 @@ struct VerifyWs {
     dstats = align_up(tstats + dspark::verify_tstats_bytes(B, K));
     keys = align_up(dstats + dspark::verify_dstats_bytes(B, K));
     anypos = align_up(keys + static_cast<size_t>(B) * mc * sizeof(unsigned long long));
-    total = align_up(anypos + static_cast<size_t>(B) * mc * sizeof(unsigned int));
+    cand = align_up(anypos + static_cast<size_t>(B) * mc * sizeof(unsigned int));
+    total = align_up(cand + static_cast<size_t>(dspark::kVerifyMaxCtas) *
+                                dspark::kVerifyListCap * sizeof(uint2));
   }
 };
 
@@ -264,6 +266,7 @@ dspark_status dspark_rejection_sample(
   p.dstats = w + ws.dstats;
   p.keys = reinterpret_cast<unsigned long long*>(w + ws.keys);
   p.anypos = reinterpret_cast<unsigned int*>(w + ws.anypos);
+  p.cand = reinterpret_cast<uint2*>(w + ws.cand);
   p.nchunk = dspark::verify_chunks(B, V, sms);
   p.status = status;
   if (cudaMemsetAsync(p.counters, 0, static_cast<size_t>(B) * sizeof(unsigned int), st) !=

@@ -96,9 +96,15 @@ struct VerifyParams {
   unsigned long long* keys;      // [B][nchunk] chunk winner keys
   unsigned int* anypos;          // [B][nchunk] residual had a positive entry
   unsigned int* counters;        // [B] finished chunks (self-resetting)
+  uint2* cand;                   // [kVerifyMaxCtas][kVerifyListCap] top-p candidates (id, x bits)
   int nchunk;
   int32_t* status;
 };
+
+// Row-statistics CTAs that keep a top-p candidate list in the workspace, and
+// the list's capacity per CTA (a longer candidate set is swept instead).
+constexpr int kVerifyMaxCtas = 1024;
+constexpr int kVerifyListCap = 512;
 
 size_t verify_tstats_bytes(int B, int K);
 size_t verify_dstats_bytes(int B, int K);

@@ -62,6 +62,7 @@ struct RowSmem {
   unsigned int x_cmin;  // value-key range of the stage's candidates in this CTA
   unsigned int x_cmax;
   unsigned int x_pref;  // a per-CTA count for a cluster prefix
+  unsigned int list_n;  // top-p candidates this CTA appended to its list
   // per-row reductions: one slot per CTA, two alternating sets (a row's slots
   // are rewritten only after the next row's first cluster barrier)
   unsigned int c_max[2];         // ordered bits of the CTA maximum (~0: failed)
@@ -177,6 +178,12 @@ __device__ void hist_clear(RowSmem& sm, int nb) {
   }
 }
 
+// Adds mass f alone to bin `bin` (the first top-p stage, over every element
+// of the row: its counts are not needed).
+__device__ __forceinline__ void hist_add_mass(RowSmem& sm, int bin, unsigned long long f) {
+  atomicAdd(&sm.hmass[bin], f);
+}
+
 // Adds (mass f, one count, id) to bin `bin` with shared-memory atomics (one
 // per lane: the bins of a warp's 32 elements rarely collide).
 __device__ __forceinline__ void hist_add(RowSmem& sm, bool active, int bin,
@@ -191,11 +198,14 @@ __device__ __forceinline__ void hist_add(RowSmem& sm, bool active, int bin,
 // non-empty bin, in scan order (descending bin index if desc), at which the
 // running mass (starting from `above`) reaches the target (t_hi:t_lo). Each
 // thread passes the value-key range [kmin, kmax] of the candidates it saw
-// (~0, 0: none); Found carries the range over the cluster.
+// (~0, 0: none); Found carries the range over the cluster. With counted =
+// false the histogram holds masses only: a bin qualifies by its mass, and
+// the count and id of the result are unknown (cnt reads 0).
 __device__ Found cluster_find(cg::cluster_group& cl, RowSmem& sm, int nb, bool desc,
                               unsigned long long above, unsigned long long t_hi,
                               unsigned long long t_lo, int CL, int rank,
-                              uint32_t kmin = 0xFFFFFFFFu, uint32_t kmax = 0u) {
+                              uint32_t kmin = 0xFFFFFFFFu, uint32_t kmax = 0u,
+                              bool counted = true) {
   const int tid = threadIdx.x;
   const int b0 = rank * nb / CL;
   const int w = (rank + 1) * nb / CL - b0;
@@ -270,7 +280,7 @@ __device__ Found cluster_find(cg::cluster_group& cl, RowSmem& sm, int nb, bool d
     if (pos >= w) break;
     const int bin = desc ? b0 + w - 1 - pos : b0 + pos;
     const unsigned long long mb = sm.hmass[bin];
-    if (sm.hcnt[bin] > 0u && reaches(run + mb, t_hi, t_lo)) {
+    if ((counted ? sm.hcnt[bin] > 0u : mb > 0ull) && reaches(run + mb, t_hi, t_lo)) {
       found = pos;
       fbefore = run;
       break;
@@ -562,10 +572,10 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
     __syncthreads();
     unsigned long long F = 0ull;
     if (topp) {
-      row_sweep<4>(rv, pol_keep, fix, [&](int i, float x) {
+      row_sweep<4>(rv, pol_keep, fix, [&](int, float x) {
         const unsigned long long f = fixed_mass(exp_rel(x, m));
         F += f;
-        hist_add(sm, true, adigit0(x, m), f, static_cast<uint32_t>(v0 + i));
+        hist_add_mass(sm, adigit0(x, m), f);
       });
     } else {
       MassAcc acc;
@@ -584,7 +594,10 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
       const unsigned long long t_lo = P32 * F;
       const unsigned long long t_hi = __umul64hi(P32, F);
       // stage 0 (its histogram was built in pass 2): distance bins, ascending
-      Found f = cluster_find(cl, sm, kRowBins, false, 0ull, t_hi, t_lo, CL, rank);
+      // (a mass-only histogram: the bin's count is unknown, so stage 1 always runs)
+      Found f = cluster_find(cl, sm, kRowBins, false, 0ull, t_hi, t_lo, CL, rank, 0xFFFFFFFFu,
+                             0u, false);
+      f.cnt = 0u;
       unsigned long long above = f.before;
       const int a0 = f.bin;
       int a1 = -1;
@@ -594,6 +607,11 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
       // distance sub-bins, kd bits [31:21], [20:10], [9:0], id bits [21:11],
       // [10:0]. After the last id stage the bin is a single token. Once the
       // bin holds a single value, the value stages left are skipped.
+      // Stage 1 also copies its candidates (the elements of bin a0) to this
+      // CTA's list; the later stages read the list instead of the slice
+      // unless it overflowed.
+      uint2* list = P.cand + static_cast<size_t>(blockIdx.x) * kVerifyListCap;
+      unsigned int list_len = 0xFFFFFFFFu;  // not built yet
       for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
         const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
         const uint32_t c_kp = kd_pre, c_ip = id_pre;
@@ -617,18 +635,35 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
         const int nb = stage == 4 ? 1024 : kRowBins;
         const bool desc = stage >= 2 && stage <= 4;  // larger kd first; distance and id ascending
         hist_clear(sm, nb);
+        if (stage == 1 && tid == 0) sm.list_n = 0u;
         __syncthreads();
         uint32_t cmin = 0xFFFFFFFFu, cmax = 0u;  // value-key range of the candidates
-        row_sweep<4>(rv, pol_keep, fix, [&](int i, float x) {
+        auto visit = [&](uint32_t id, float x, bool append) {
           const uint32_t kd = kd_of(x);
-          const uint32_t id = static_cast<uint32_t>(v0 + i);
           if (match(x, kd, id)) {
             hist_add(sm, true, digit(x, kd, id), fixed_mass(exp_rel(x, m)), id);
             cmin = min(cmin, kd);
             cmax = max(cmax, kd);
+            if (append) {
+              const unsigned int at = atomicAdd(&sm.list_n, 1u);
+              if (at < static_cast<unsigned int>(kVerifyListCap))
+                list[at] = make_uint2(id, __float_as_uint(x));
+            }
           }
-        });
+        };
+        if (list_len <= static_cast<unsigned int>(kVerifyListCap)) {
+          for (unsigned int j = tid; j < list_len; j += kRowThreads) {
+            const uint2 e = __ldcg(list + j);
+            visit(e.x, __uint_as_float(e.y), false);
+          }
+        } else {
+          const bool append = stage == 1;
+          row_sweep<4>(rv, pol_keep, fix, [&](int i, float x) {
+            visit(static_cast<uint32_t>(v0 + i), x, append);
+          });
+        }
         f = cluster_find(cl, sm, nb, desc, above, t_hi, t_lo, CL, rank, cmin, cmax);
+        if (stage == 1) list_len = sm.list_n;  // complete: cluster_find synchronised the CTA
         above = f.before;
         const uint32_t bin = static_cast<uint32_t>(f.bin);
         if (stage == 1) {
@@ -1038,6 +1073,7 @@ cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_
   const int l2_rows = static_cast<int>((80ull << 20) / (row_bytes > 0 ? row_bytes : 1));
   int nclusters = rows < max_clusters ? rows : max_clusters;
   if (l2_rows >= 1 && nclusters > l2_rows) nclusters = l2_rows;
+  if (nclusters * CL > kVerifyMaxCtas) nclusters = kVerifyMaxCtas / CL;  // one list per CTA
   if (nclusters < 1) nclusters = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
   return cudaLaunchKernelEx(&cfg, verify_rows_kernel, p, W, rows);
