@@ -124,7 +124,46 @@ __device__ __forceinline__ float ln_approx(float x) {
 // the maximum (ex2 of +-0 is 1) and within about 3 ulp elsewhere (the
 // oracle's exp is correctly rounded, and the tests bound the effect: accept
 // margins and top-p boundaries within 1e-6). -inf gives 0.
-__device__ __forceinline__ float exp_rel(float x, float m) { return __expf(__fsub_rn(x, m)); }
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2_approx(float t) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
+  return y;
+}
+
+// exp(y) = 2^(y log2 e), with y = fp32(x - m) and the product rounded once.
+__device__ __forceinline__ float exp_rel(float x, float m) {
+  return ex2_approx(__fmul_rn(__fsub_rn(x, m), kLog2e));
+}
+
+// ---- packed fp32 pairs (Blackwell f32x2 arithmetic, round to nearest) -------
+// Each lane of a pair is one IEEE fp32 operation, so a pair gives the same
+// bits as two scalar operations in one instruction.
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // Fixed-point mass rint(e * 2^40) of e in [0, 1], summed as two 32-bit
 // partials: vh = rint(e * 2^20) and f = e * 2^20 - vh (exact: the fraction
@@ -134,21 +173,40 @@ __device__ __forceinline__ float exp_rel(float x, float m) { return __expf(__fsu
 // exact), read back from the sum's mantissa bits. Neither partial overflows
 // while a thread adds fewer than 2^11 values.
 struct MassAcc {
-  uint32_t hi = 0u;  // sum of vh
-  int32_t lo = 0;    // sum of rint(f * 2^20)
+  uint32_t hi = 0u;  // sum of the bits of s = vh + magic
+  uint32_t lo = 0u;  // sum of the bits of r = rint(f * 2^20) + magic
+  uint32_t n = 0u;   // values added (each carried one magic)
+  static constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  static constexpr uint32_t kMagicBits = 0x4B400000u;
   __device__ __forceinline__ void add(float e) {
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    constexpr uint32_t kMagicBits = 0x4B400000u;
     const float s = __fmaf_rn(e, 0x1p20f, kMagic);
     const float vh = __fsub_rn(s, kMagic);
     const float f = __fmaf_rn(e, 0x1p20f, -vh);
     const float r = __fmaf_rn(f, 0x1p20f, kMagic);
-    hi += __float_as_uint(s) - kMagicBits;
-    lo += static_cast<int32_t>(__float_as_uint(r) - kMagicBits);
+    hi += __float_as_uint(s);
+    lo += __float_as_uint(r);
+    n += 1u;
   }
+  // Two values in packed pairs: the same operations lane by lane (-vh is
+  // formed as magic - s, exact like s - magic).
+  __device__ __forceinline__ void add2(unsigned long long e) {
+    const unsigned long long p20 = f2_pack(0x1p20f, 0x1p20f);
+    const unsigned long long mg = f2_pack(kMagic, kMagic);
+    const unsigned long long s = f2_fma(e, p20, mg);
+    const unsigned long long nvh = f2_sub(mg, s);
+    const unsigned long long f = f2_fma(e, p20, nvh);
+    const unsigned long long r = f2_fma(f, p20, mg);
+    hi += static_cast<uint32_t>(s) + static_cast<uint32_t>(s >> 32);
+    lo += static_cast<uint32_t>(r) + static_cast<uint32_t>(r >> 32);
+    n += 2u;
+  }
+  // Modulo 2^32 the magics come off exactly; the true partials fit while a
+  // thread adds fewer than 2^11 values.
   __device__ __forceinline__ unsigned long long total() const {
-    return (static_cast<unsigned long long>(hi) << 20) +
-           static_cast<unsigned long long>(static_cast<long long>(lo));
+    const uint32_t h = hi - n * kMagicBits;
+    const int32_t l = static_cast<int32_t>(lo - n * kMagicBits);
+    return (static_cast<unsigned long long>(h) << 20) +
+           static_cast<unsigned long long>(static_cast<long long>(l));
   }
 };
 

@@ -441,6 +441,81 @@ __device__ __forceinline__ void row_sweep_t(RowView rv, uint64_t pol, Fix fix, B
   }
 }
 
+// As row_sweep, with the values of each aligned group of four handed to
+// quad(x[4]) together (for packed pair arithmetic) and the rest to single(x).
+template <int kU, bool kBf16, class Fix, class Quad, class Single>
+__device__ __forceinline__ void row_sweep_quads_t(RowView rv, uint64_t pol, Fix fix, Quad quad,
+                                                  Single single) {
+  const int tid = threadIdx.x;
+  auto load4 = [&](int j, float (&v)[4]) {
+    if constexpr (kBf16) {
+      const uint2 w = ld_hint_u2(rv.h + 4 * j, pol);
+      v[0] = bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu));
+      v[1] = bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16));
+      v[2] = bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu));
+      v[3] = bf16_bits_to_float(static_cast<uint16_t>(w.y >> 16));
+    } else {
+      const float4 c = ld_hint_f4(rv.f + 4 * j, pol);
+      v[0] = c.x;
+      v[1] = c.y;
+      v[2] = c.z;
+      v[3] = c.w;
+    }
+  };
+  int done = 0;
+  if (rv.vec) {
+    const int n4 = rv.n >> 2;
+    int i = tid;
+    for (; i + (kU - 1) * kRowThreads < n4; i += kU * kRowThreads) {
+      float v[kU][4];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) load4(i + u * kRowThreads, v[u]);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[u][e] = fix(v[u][e]);
+        quad(v[u]);
+      }
+    }
+    for (; i < n4; i += kRowThreads) {
+      float v[4];
+      load4(i, v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = fix(v[e]);
+      quad(v);
+    }
+    done = 4 * n4;
+  }
+  for (int i = done + tid; i < rv.n; i += kRowThreads) {
+    const float c = kBf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol))
+                          : ld_hint_f32(rv.f + i, pol);
+    single(fix(c));
+  }
+}
+
+// Fixed-point mass of the slice relative to m: exp(x - m) per value, four at
+// a time in packed pairs.
+template <class Fix>
+__device__ __forceinline__ unsigned long long slice_mass(const RowView& rv, uint64_t pol, Fix fix,
+                                                         float m) {
+  MassAcc acc;
+  const unsigned long long mm = f2_pack(m, m);
+  const unsigned long long l2e = f2_pack(kLog2e, kLog2e);
+  auto quad = [&](const float (&x)[4]) {
+    float a, b, c, d;
+    f2_unpack(f2_mul(f2_sub(f2_pack(x[0], x[1]), mm), l2e), a, b);
+    f2_unpack(f2_mul(f2_sub(f2_pack(x[2], x[3]), mm), l2e), c, d);
+    acc.add2(f2_pack(ex2_approx(a), ex2_approx(b)));
+    acc.add2(f2_pack(ex2_approx(c), ex2_approx(d)));
+  };
+  auto single = [&](float x) { acc.add(exp_rel(x, m)); };
+  if (rv.bf16)
+    row_sweep_quads_t<8, true>(rv, pol, fix, quad, single);
+  else
+    row_sweep_quads_t<8, false>(rv, pol, fix, quad, single);
+  return acc.total();
+}
+
 // One row: statistics written to P.tstats / P.dstats. Every CTA of the
 // cluster runs the same sequence of cluster barriers (all decisions depend on
 // the row or on cluster-reduced values only).
@@ -578,9 +653,7 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
         hist_add_mass(sm, adigit0(x, m), f);
       });
     } else {
-      MassAcc acc;
-      row_sweep(rv, pol_last_use, fix, [&](int, float x) { acc.add(exp_rel(x, m)); });
-      F = acc.total();
+      F = slice_mass(rv, pol_last_use, fix, m);
     }
     F = cluster_sum_u64(cl, sm, F, set, CL);
 
