@@ -74,6 +74,39 @@ __device__ __forceinline__ float uniform_of(uint32_t w) {
   return __fadd_rn(__uint_as_float(0x3F800000u | (w >> 9)), -0x1.fffffep-1f);
 }
 
+// ---- packed fp32 pairs (Blackwell f32x2 arithmetic, round to nearest) -------
+// Each lane of a pair is one IEEE fp32 operation, so a pair gives the same
+// bits as two scalar operations in one instruction.
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // lg2.approx.f32: log2 with an absolute error of about 2^-22.6 on the
 // mantissa part (plus the rounding of the fp32 result).
 __device__ __forceinline__ float lg2_approx(float x) {
@@ -82,10 +115,18 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+// rcp.approx.ftz.f32: 1/x to about 1 ulp (x normal).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Standard Gumbel variate g = -ln(-ln u) of the uniform of word w.
 // E = -ln u is computed with small relative error on both sides of the
 // range: for u > 3/4 from t = 1 - u (exact on the 2^-23 grid) by the series
-// -ln(1 - t) = 2 atanh(s), s = t / (2 - t) <= 1/7, to s^9; for u <= 3/4 as
+// -ln(1 - t) = 2 atanh(s), s = t / (2 - t) <= 1/7 (t times an approximate
+// reciprocal), to s^9; for u <= 3/4 as
 // -ln 2 * lg2(u), where E >= 0.28 keeps the relative error near 4e-7. Then
 // g = -ln 2 * lg2(E). The absolute error on g stays below about 1.3e-6 over
 // the whole grid (checked against an fp64 evaluation in the tests).
@@ -97,16 +138,43 @@ __device__ __forceinline__ float gumbel_of(uint32_t w) {
   constexpr float kLn2 = 0.693147180559945309f;
   const float u = uniform_of(w);
   const float t = __fsub_rn(1.0f, u);
-  const float sr = __fdividef(t, __fsub_rn(2.0f, t));
-  const float s2 = sr * sr;
-  float p = fmaf(s2, 2.0f / 9.0f, 2.0f / 7.0f);  // 2 (1 + s^2/3 + s^4/5 + s^6/7 + s^8/9)
-  p = fmaf(s2, p, 2.0f / 5.0f);
-  p = fmaf(s2, p, 2.0f / 3.0f);
-  p = fmaf(s2, p, 2.0f);
-  const float e_near = sr * p;
-  const float e_far = -kLn2 * lg2_approx(u);
+  const float sr = __fmul_rn(t, rcp_approx(__fsub_rn(2.0f, t)));
+  const float s2 = __fmul_rn(sr, sr);
+  float p = __fmaf_rn(s2, 2.0f / 9.0f, 2.0f / 7.0f);  // 2 (1 + s^2/3 + s^4/5 + s^6/7 + s^8/9)
+  p = __fmaf_rn(s2, p, 2.0f / 5.0f);
+  p = __fmaf_rn(s2, p, 2.0f / 3.0f);
+  p = __fmaf_rn(s2, p, 2.0f);
+  const float e_near = __fmul_rn(sr, p);
+  const float e_far = __fmul_rn(-kLn2, lg2_approx(u));
   const float E = u > 0.75f ? e_near : e_far;
-  return -kLn2 * lg2_approx(E);
+  return __fmul_rn(-kLn2, lg2_approx(E));
+}
+
+// gumbel_of of two words at once: the same operations lane by lane, the
+// arithmetic in packed pairs (lg2, rcp and the selection per value).
+__device__ __forceinline__ void gumbel_of2(uint32_t w0, uint32_t w1, float& g0, float& g1) {
+  constexpr float kLn2 = 0.693147180559945309f;
+  const unsigned long long one = f2_pack(1.0f, 1.0f), two = f2_pack(2.0f, 2.0f);
+  const unsigned long long u = f2_add(f2_pack(__uint_as_float(0x3F800000u | (w0 >> 9)),
+                                              __uint_as_float(0x3F800000u | (w1 >> 9))),
+                                      f2_pack(-0x1.fffffep-1f, -0x1.fffffep-1f));
+  const unsigned long long t = f2_sub(one, u);
+  float d0, d1;
+  f2_unpack(f2_sub(two, t), d0, d1);
+  const unsigned long long sr = f2_mul(t, f2_pack(rcp_approx(d0), rcp_approx(d1)));
+  const unsigned long long s2 = f2_mul(sr, sr);
+  unsigned long long p = f2_fma(s2, f2_pack(2.0f / 9.0f, 2.0f / 9.0f), f2_pack(2.0f / 7.0f, 2.0f / 7.0f));
+  p = f2_fma(s2, p, f2_pack(2.0f / 5.0f, 2.0f / 5.0f));
+  p = f2_fma(s2, p, f2_pack(2.0f / 3.0f, 2.0f / 3.0f));
+  p = f2_fma(s2, p, two);
+  const unsigned long long nl2 = f2_pack(-kLn2, -kLn2);
+  float u0, u1, n0, n1, f0, f1;
+  f2_unpack(u, u0, u1);
+  f2_unpack(f2_mul(sr, p), n0, n1);
+  f2_unpack(f2_mul(f2_pack(lg2_approx(u0), lg2_approx(u1)), nl2), f0, f1);
+  const float E0 = u0 > 0.75f ? n0 : f0;
+  const float E1 = u1 > 0.75f ? n1 : f1;
+  f2_unpack(f2_mul(f2_pack(lg2_approx(E0), lg2_approx(E1)), nl2), g0, g1);
 }
 
 // Natural log of a positive, normal x with an absolute error of about 1e-7
@@ -137,33 +205,6 @@ __device__ __forceinline__ float exp_rel(float x, float m) {
   return ex2_approx(__fmul_rn(__fsub_rn(x, m), kLog2e));
 }
 
-// ---- packed fp32 pairs (Blackwell f32x2 arithmetic, round to nearest) -------
-// Each lane of a pair is one IEEE fp32 operation, so a pair gives the same
-// bits as two scalar operations in one instruction.
-__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(unsigned long long r, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
-}
-__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
-                                                     unsigned long long c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
-  unsigned long long d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
-  unsigned long long d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 
 // Fixed-point mass rint(e * 2^40) of e in [0, 1], summed as two 32-bit
 // partials: vh = rint(e * 2^20) and f = e * 2^20 - vh (exact: the fraction

@@ -632,15 +632,31 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             gsc[4 * h + 2] = g4.z;
             gsc[4 * h + 3] = g4.w;
           }
+          // z = base + bias, x = z / T (greedy: z), y = x + g (greedy: x),
+          // two columns at a time in packed fp32 pairs (fewer instructions and
+          // registers); padding columns (b >= B) compute values that are
+          // neither stored nor folded into a token
+          float gv[GW];
+#pragma unroll
+          for (int j = 0; j < GW; j += 2) gumbel_of2(nw[j], nw[j + 1], gv[j], gv[j + 1]);
           tc::tmem_wait_ld();
-          // straight-line per column; padding columns (b >= B) compute
-          // values that are neither stored nor folded into a token
+          float xv[GW], yv[GW];
+#pragma unroll
+          for (int j = 0; j < GW; j += 2) {
+            const unsigned long long z = f2_add(f2_pack(bv[j], bv[j + 1]),
+                                                f2_pack(__uint_as_float(acc[j]),
+                                                        __uint_as_float(acc[j + 1])));
+            const unsigned long long x = f2_mul(z, f2_pack(xsc[j], xsc[j + 1]));
+            const unsigned long long y =
+                f2_fma(f2_pack(gv[j], gv[j + 1]), f2_pack(gsc[j], gsc[j + 1]), x);
+            f2_unpack(x, xv[j], xv[j + 1]);
+            f2_unpack(y, yv[j], yv[j + 1]);
+          }
 #pragma unroll
           for (int j = 0; j < GW; ++j) {
             const int b = cb + j;
-            const float z = __fadd_rn(bv[j], __uint_as_float(acc[j]));
-            const float x = __fmul_rn(z, xsc[j]);                  // z / T (greedy: z)
-            const float y = __fmaf_rn(gumbel_of(nw[j]), gsc[j], x);  // x + g (greedy: x)
+            const float x = xv[j];
+            const float y = yv[j];
             CacheT* cp = reinterpret_cast<CacheT*>(s_cptr[b]);      // null: no store
             float xr;  // the value as stored (a bf16 cache rounds it)
             if constexpr (kCacheBf16) {

@@ -139,10 +139,12 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const TgtStats& t
     if (!need) continue;
     any = 1u;
     const U4 r = noise_block(seed, npos, static_cast<uint32_t>(g), kStreamTarget);
-    const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+    float gn[4];
+    gumbel_of2(r.x, r.y, gn[0], gn[1]);
+    gumbel_of2(r.z, r.w, gn[2], gn[3]);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float y = __fadd_rn(ln_approx(w[j]), gumbel_of(words[j]));
+      const float y = __fadd_rn(ln_approx(w[j]), gn[j]);
       const uint32_t o = w[j] > 0.0f ? ordered_key(y) : 0u;
       if (o > run_o) {
         run_o = o;
