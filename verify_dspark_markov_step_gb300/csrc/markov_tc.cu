@@ -990,6 +990,7 @@ cudaError_t launch_markov_loop_tc(const MarkovStepParams& p, const void* tmap, c
   if (cpw <= 4) return launch_tc_dtypes<4>(p, map, bm, plan, grid, stream);
   if (cpw <= 8) return launch_tc_dtypes<8>(p, map, bm, plan, grid, stream);
   if (cpw <= 16) return launch_tc_dtypes<16>(p, map, bm, plan, grid, stream);
+  if (cpw <= 32) return launch_tc_dtypes<32>(p, map, bm, plan, grid, stream);
   return launch_tc_dtypes<64>(p, map, bm, plan, grid, stream);
 }
 
