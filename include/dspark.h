@@ -267,7 +267,9 @@ dspark_status dspark_markov_sample_static(
  *   req_state_idx [B], positions [B], temperature [S], top_p [S] fp32,
  *   seeds [S] as for dspark_markov_sample
  *   out_tokens    [B, K+1] int32, num_accepted [B] int32 (written)
- *   workspace     at least dspark_verify_workspace_bytes() bytes
+ *   workspace     at least dspark_verify_workspace_bytes() bytes (a few
+ *                 MB: per-request statistics plus a fixed 4 MB area of
+ *                 top-p candidate lists); no initial contents required
  * Alignment: draft_cache and target_logits must be 16-byte aligned.
  * ------------------------------------------------------------------------ */
 size_t dspark_verify_workspace_bytes(int B, int K, int V);
