@@ -180,6 +180,20 @@ __device__ unsigned long long draw_chunk(const VerifyParams& P, const ResSmem& r
   const bool tvec = ((reinterpret_cast<uintptr_t>(P.target) + toff * (tbf ? 2 : 4)) & (tbf ? 7u : 15u)) == 0;
   const bool cvec = ((reinterpret_cast<uintptr_t>(P.cache) + coff * (cbf ? 2 : 4)) & (cbf ? 7u : 15u)) == 0;
   const int64_t npos = rs.P0 + k - 1;
+  // the chunk's rows come from HBM: start them as bulk L2 prefetches
+  if (threadIdx.x == 0) {
+    auto pf = [](const void* base, int64_t off, int es, int n) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(static_cast<const unsigned char*>(base) + off * es);
+      const uintptr_t a16 = (a + 15) & ~static_cast<uintptr_t>(15);
+      const uint32_t bytes = static_cast<uint32_t>(n) * es;
+      const uint32_t skip = static_cast<uint32_t>(a16 - a);
+      if (bytes > skip + 16)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a16),
+                     "r"((bytes - skip) & ~15u) : "memory");
+    };
+    pf(P.target, toff + c0, tbf ? 2 : 4, c1 - c0);
+    if (residual) pf(P.cache, coff + c0, cbf ? 2 : 4, c1 - c0);
+  }
   if (ts.mode != kModeOneHot && !(residual && ds.zero)) {
     const bool scale = rs.T != 1.0f;
     const bool thr = ts.mode == kModeThreshold;

@@ -567,6 +567,19 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
   rv.vec = bf16 ? (reinterpret_cast<uintptr_t>(rv.h) & 7u) == 0
                 : (reinterpret_cast<uintptr_t>(rv.f) & 15u) == 0;
   rv.n = n;
+  // the slice's first read comes from HBM: start it as one bulk L2 prefetch,
+  // so that the whole slice is in flight at once
+  if (tid == 0) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(bf16 ? static_cast<const void*>(rv.h)
+                                                         : static_cast<const void*>(rv.f));
+    const uintptr_t a16 = (a + 15) & ~static_cast<uintptr_t>(15);
+    const uint32_t bytes = static_cast<uint32_t>(n) * (bf16 ? 2u : 4u);
+    const uint32_t skip = static_cast<uint32_t>(a16 - a);
+    if (bytes > skip + 16) {
+      const uint32_t len = (bytes - skip) & ~15u;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a16), "r"(len) : "memory");
+    }
+  }
   const int32_t d = k < K ? P.draft[static_cast<int64_t>(b) * K + k] : -1;
   TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(b) * (K + 1) + k;
   DrfStats* ds = static_cast<DrfStats*>(P.dstats) + static_cast<int64_t>(b) * K + (k < K ? k : 0);
