@@ -576,7 +576,22 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       const int v = t * kM + r;
       const bool in_range = v < V;
       float bnext[GW];
-      if (!skip && !tma_base && c_live > 0) load_direct(c_begin, v, in_range, bnext);
+      if (!skip && !tma_base && c_live > 0) {
+        load_direct(c_begin, v, in_range, bnext);
+        // the next tile's base rows of this warp's columns into L2 (one
+        // 32-row line per column), so that its direct loads hit L2
+        if (!it.last()) {
+          const int vn = (t + ((step & 1) ? -G : G)) * kM + q * 32;
+          if (vn < V) {
+            for (int l = lane; l < c_live; l += 32) {
+              const unsigned char* bp = s_bptr[c_begin + l];
+              if (bp != nullptr)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                    bp + static_cast<size_t>(vn) * sizeof(BaseT)));
+            }
+          }
+        }
+      }
       if (!skip) {
         bool ok = mbar_wait(&acc_full[ab], aph, P.status);
         if (ok && tma_base) ok = mbar_wait(&bfull[bs], bph, P.status);
