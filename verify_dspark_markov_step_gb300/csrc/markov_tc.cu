@@ -41,9 +41,8 @@
 //               registers across tiles when CPW <= 16, else reduced per tile
 //               with redux.sync.
 // At the end of a step each CTA folds its winners into the step's global
-// winner keys (64-bit atomicMax) and starts L2 prefetches of the embedding
-// rows of its own winners; then a grid barrier (an arrival counter, bounded
-// wait) lets every CTA read the step's tokens, gather the next Markov
+// winner keys (64-bit atomicMax), then a grid barrier (an arrival counter,
+// bounded wait) lets every CTA read the step's tokens, gather the next Markov
 // embeddings w1[token] into shared memory and release the MMA warp.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -177,11 +176,6 @@ __device__ __forceinline__ void st_pred_bits(uint16_t* p, uint16_t h, bool pred)
                "h"(h), "r"(static_cast<uint32_t>(pred))
                : "memory");
 }
-// Starts bringing `bytes` (a multiple of 16) at the 16-byte aligned `p` into L2.
-__device__ __forceinline__ void l2_prefetch_row(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // The value of an order key (0, the empty key, reads as -inf).
 __device__ __forceinline__ float key_to_float(uint32_t k) {
   if (k == 0u) return -INFINITY;
@@ -767,12 +761,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           best[b] = 0ull;
           xk = 0u;
         }
-        if (k != 0ull) {
-          atomicMax(keys + b, k);
-          // this block's winner is the likeliest next token: start bringing
-          // its embedding row into L2 while the grid meets
-          if (!last) l2_prefetch_row(P.w1 + static_cast<int64_t>(key_index(k)) * R, R * 2);
-        }
+        if (k != 0ull) atomicMax(keys + b, k);
         // the cache row's maximum, as an order key in the scratch word
         if (want_stats && s_cb0[b] != nullptr)
           atomicMax(&P.draft_stats[static_cast<int64_t>(b) * K + step].scratch, xk);
