@@ -61,6 +61,10 @@ def test_odd_vocab_nan_and_temperatures():
     (64, 1, 777, 256, {}),
     # the most draft steps the library takes
     (3, 16, 3001, 128, {"temperature": [1.0, 0.0, 0.6]}),
+    # 200 tiles on a 152-SM grid: the 48 remainder tiles (the ragged last one
+    # among them) are each shared by two CTAs, half the request columns each
+    (20, 3, 25500, 128, {"temperature": [1.0, 0.0, 0.7, 1.3] * 5}),
+    (40, 2, 25500, 64, {"base_bf16": True, "cache_bf16": True, "temperature": 0.9}),
 ])
 def test_edge_shapes(B, K, V, R, kw):
     w = wl.custom(B, K, V, R, seed=B * 7 + V, **kw)

@@ -198,23 +198,54 @@ __device__ __forceinline__ float ld_pred(const uint16_t* p, bool pred) {
   return bf16_bits_to_float(h);
 }
 
-// Position of loop iteration g = step * n_loc + il of a CTA (tile t of its
-// share: blockIdx.x + j * G, j rising on even steps and falling on odd ones,
-// so a step starts on the tile the previous one ended on), and the
-// slot/parity of a ring of n buffers, advanced without integer division.
+// A CTA's share of the vocabulary tiles: n_full whole tiles blockIdx.x + j * G
+// and, when the tile count is not a multiple of the grid, possibly one
+// remainder tile tx of which it takes half the request columns (half_id 0:
+// the first two epilogue column groups, 1: the last two); two CTAs share
+// each remainder tile, so no CTA has a whole tile more than another.
+struct TileShare {
+  int n_loc, n_full, tx, half_id;
+  __device__ TileShare(int tiles, int G, bool split) {
+    const int bx = static_cast<int>(blockIdx.x);
+    const int nb = tiles / G, rem = tiles - nb * G;
+    if (split && rem > 0 && 2 * rem <= G) {
+      n_full = nb;
+      const bool has = bx < 2 * rem;
+      n_loc = nb + (has ? 1 : 0);
+      tx = has ? nb * G + (bx < rem ? bx : bx - rem) : -1;
+      half_id = bx < rem ? 0 : 1;
+    } else {
+      n_full = n_loc = nb + (bx < rem ? 1 : 0);
+      tx = -1;
+      half_id = 0;
+    }
+  }
+};
+
+// Position of loop iteration g = step * n_loc + il of a CTA: its j-th tile
+// with j rising on even steps and falling on odd ones (so a step starts on
+// the tile the previous one ended on, still in L2), and the slot/parity of a
+// ring of n buffers, advanced without integer division.
 struct TileIter {
-  int step, il, t, n_loc, G;
-  __device__ TileIter(int n_loc_, int G_)
-      : step(0), il(0), t(static_cast<int>(blockIdx.x)), n_loc(n_loc_), G(G_) {}
+  int step, il, t, n_loc, n_full, tx, G;
+  bool half;  // the remainder tile: this CTA takes half its columns
+  __device__ TileIter(const TileShare& sh, int G_)
+      : step(0), il(0), n_loc(sh.n_loc), n_full(sh.n_full), tx(sh.tx), G(G_) {
+    locate();
+  }
+  __device__ __forceinline__ void locate() {
+    const int j = (step & 1) ? n_loc - 1 - il : il;
+    half = j >= n_full;
+    t = half ? tx : static_cast<int>(blockIdx.x) + j * G;
+  }
   __device__ __forceinline__ bool first() const { return il == 0; }
   __device__ __forceinline__ bool last() const { return il == n_loc - 1; }
   __device__ __forceinline__ void next() {
     if (++il == n_loc) {
       il = 0;
       ++step;
-    } else {
-      t += (step & 1) ? -G : G;
     }
+    locate();
   }
 };
 struct RingPos {
@@ -289,8 +320,11 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   const int B = P.B, V = P.V, K = P.K;
   const int G = gridDim.x;
   const int tiles = (V + kM - 1) / kM;
-  const int n_loc = (tiles - static_cast<int>(blockIdx.x) + G - 1) / G;  // tiles of this CTA
-  const int n_iter = n_loc * K;  // (step, tile) pairs, step-major
+  // remainder tiles are split by request columns when the last two column
+  // groups hold live requests
+  const TileShare share(tiles, G, B > 2 * CPW);
+  const int n_loc = share.n_loc;  // tiles of this CTA
+  const int n_iter = n_loc * K;   // (step, tile) pairs, step-major
   using BaseT = typename std::conditional<kBaseBf16, uint16_t, float>::type;
   using CacheT = typename std::conditional<kCacheBf16, uint16_t, float>::type;
   constexpr int bes = sizeof(BaseT);
@@ -411,7 +445,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       uint32_t issued[kMaxStages];  // parity of the last copy per stage
 #pragma unroll
       for (int i = 0; i < kMaxStages; ++i) issued[i] = 0xFFFFFFFFu;
-      TileIter it(n_loc, G);
+      TileIter it(share, G);
       for (int g = 0; g < n_iter && ok; ++g, it.next()) {
         if (*fail_flag) break;
         const int t = it.t;
@@ -442,7 +476,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       uint32_t last[kMaxBaseSlots];
 #pragma unroll
       for (int i = 0; i < kMaxBaseSlots; ++i) last[i] = 0xFFFFFFFFu;
-      TileIter it(n_loc, G);
+      TileIter it(share, G);
       RingPos br(nb);
       for (int g = 0; g < n_iter; ++g, it.next(), br.next()) {
         if (*fail_flag) break;
@@ -471,7 +505,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
-      TileIter it(n_loc, G);
+      TileIter it(share, G);
       RingPos ar(na);
       for (int g = 0; g < n_iter && ok; ++g, it.next(), ar.next()) {
         if (*fail_flag) break;
@@ -558,7 +592,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       }
     };
     bool skip = false;  // set after a failed wait: the warp then only walks the loop
-    TileIter it(n_loc, G);
+    TileIter it(share, G);
     RingPos ar(na), br(tma_base ? nb : 1);
     for (int g = 0; g < n_iter; ++g, it.next(), ar.next(), br.next()) {
       const int step = it.step;
@@ -569,13 +603,18 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       const uint32_t bph = br.phase;
       const int v = t * kM + r;
       const bool in_range = v < V;
+      // live columns of this warp in this tile: none in the other half of a
+      // shared remainder tile
+      const int c_tile = (it.half && (sub >> 1) != share.half_id) ? 0 : c_live;
       float bnext[GW];
-      if (!skip && !tma_base && c_live > 0) {
+      if (!skip && !tma_base && c_tile > 0) {
         load_direct(c_begin, v, in_range, bnext);
         // the next tile's base rows of this warp's columns into L2 (one
         // 32-row line per column), so that its direct loads hit L2
         if (!it.last()) {
-          const int vn = (t + ((step & 1) ? -G : G)) * kM + q * 32;
+          TileIter nx = it;
+          nx.next();
+          const int vn = nx.t * kM + q * 32;
           if (vn < V) {
             for (int l = lane; l < c_live; l += 32) {
               const unsigned char* bp = s_bptr[c_begin + l];
@@ -602,7 +641,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         const unsigned char* sb = base_s + bs * base_stride;
 #pragma unroll
         for (int c = 0; c < CPW; c += GW) {
-          if (c >= c_live) break;  // warp-uniform
+          if (c >= c_tile) break;  // warp-uniform
           const int cb = c_begin + c;
           uint32_t acc[GW];
           tmem_load_group<GW>(tmem + (static_cast<uint32_t>(q * 32) << 16) +
@@ -623,7 +662,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           } else {
 #pragma unroll
             for (int j = 0; j < GW; ++j) bv[j] = bnext[j];
-            if (c + GW < c_live) load_direct(cb + GW, v, in_range, bnext);
+            if (c + GW < c_tile) load_direct(cb + GW, v, in_range, bnext);
           }
           uint32_t nw[GW];
           noise_group(cb, v, nw);
