@@ -110,6 +110,9 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const TgtStats& t
   const bool tbf = P.target_bf16 != 0, cbf = P.cache_bf16 != 0;
   const float invD = 1.0f / ts.D;
   const float invDq = kResidual ? 1.0f / ds.D : 0.0f;
+  const unsigned long long mm = f2_pack(ts.m, ts.m), mq = f2_pack(ds.m, ds.m);
+  const unsigned long long l2e = f2_pack(kLog2e, kLog2e);
+  const unsigned long long invD2 = f2_pack(invD, invD), invDq2 = f2_pack(invDq, invDq);
   // running winner of this thread: its columns only grow, so a strict >
   // keeps the lowest column on ties
   uint32_t run_o = 0u, run_c = 0u;
@@ -118,21 +121,36 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const TgtStats& t
     float t4[4], c4[4];
     load4(P.target, tbf, toff, g, c1, tvec, t4);
     if (kResidual) load4(P.cache, cbf, coff, g, c1, cvec, c4);
+    // p = exp(x - m) / D (and q likewise) two columns at a time in packed
+    // pairs: the same fp32 operations as exp_rel and the scalar products
+    float x4[4], p4[4], q4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      x4[j] = fmaxf(kScale ? __fdiv_rn(t4[j], T) : t4[j], -INFINITY);  // NaN -> -inf
+#pragma unroll
+    for (int j = 0; j < 4; j += 2) {
+      float a, b;
+      f2_unpack(f2_mul(f2_sub(f2_pack(x4[j], x4[j + 1]), mm), l2e), a, b);
+      f2_unpack(f2_mul(f2_pack(ex2_approx(a), ex2_approx(b)), invD2), p4[j], p4[j + 1]);
+      if (kResidual) {
+        f2_unpack(f2_mul(f2_sub(f2_pack(fmaxf(c4[j], -INFINITY), fmaxf(c4[j + 1], -INFINITY)),
+                                mq),
+                         l2e),
+                  a, b);
+        f2_unpack(f2_mul(f2_pack(ex2_approx(a), ex2_approx(b)), invDq2), q4[j], q4[j + 1]);
+      }
+    }
     float w[4];
     bool need = false;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float x = fmaxf(kScale ? __fdiv_rn(t4[j], T) : t4[j], -INFINITY);  // NaN -> -inf
-      float pv = __fmul_rn(exp_rel(x, ts.m), invD);
+      float pv = p4[j];
       if (kThreshold) {
-        const uint32_t kd = kd_of(x);
+        const uint32_t kd = kd_of(x4[j]);
         const bool keep = kd > ts.kd_thr || (kd == ts.kd_thr && g + j <= ts.id_thr);
         pv = keep ? pv : 0.0f;
       }
-      if (kResidual) {
-        const float c = fmaxf(c4[j], -INFINITY);
-        pv = fmaxf(__fsub_rn(pv, __fmul_rn(exp_rel(c, ds.m), invDq)), 0.0f);
-      }
+      if (kResidual) pv = fmaxf(__fsub_rn(pv, q4[j]), 0.0f);
       w[j] = g + j < c1 ? pv : 0.0f;
       need |= w[j] > 0.0f;
     }
