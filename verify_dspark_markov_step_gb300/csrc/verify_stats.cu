@@ -831,10 +831,12 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyParam
 // Top-k candidates of the base-logit rows for the top-k Markov loop (the
 // "DSparkSpeculator" page, _sample_sequential_topk): per (request, draft
 // step) the k largest base logits by (value descending, token id
-// ascending), NaN above every number, -0 equal to +0. The same radix select
-// as the top-p keep set, with a unit mass per element: the boundary is the
-// k-th element of that order. The cluster also fills the step's cache row
-// with -inf (the loop writes the candidates' values).
+// ascending), NaN above every number, -0 equal to +0. A radix select with a
+// unit mass per element over the order key (11 + 11 + 10 bits, its first
+// stage counted during the pass that reads the row from HBM) and then the
+// token id: the boundary is the k-th element of that order. The cluster also
+// fills the step's cache row with -inf (the loop writes the candidates'
+// values).
 
 // Exclusive prefix over the cluster's ranks of one per-CTA count, and the
 // total (one cluster barrier; every CTA must call it).
@@ -936,15 +938,18 @@ __device__ void topk_row(const TopkParams& P, int W, int row_id, cg::cluster_gro
     return;
   }
 
-  // ---- pass 1: maximum over the numbers and the NaN count ---------------------
-  float lmax = -INFINITY;
+  // ---- pass 1 (HBM): the NaN count and a count histogram of the numbers by
+  // the top 11 bits of their order key (sign, exponent, two mantissa bits),
+  // one shared atomic per element: the first radix stage needs no maximum
+  hist_clear(sm, kRowBins);
+  __syncthreads();
   unsigned long long nan_loc = 0ull;
   row_sweep(rv, pol, ident, [&](int, float x) {
-    lmax = fmaxf(lmax, x);
-    nan_loc += (x != x) ? 1ull : 0ull;
+    if (x != x)
+      nan_loc += 1ull;
+    else
+      atomicAdd(&sm.hcnt[kd_of(x) >> 21], 1u);
   });
-  bool any_fail = false;
-  const float m = cluster_max_f(cl, sm, lmax, false, set, CL, &any_fail);
   const unsigned long long nan_tot = cluster_sum_u64(cl, sm, nan_loc, set, CL);
 
   if (nan_tot >= static_cast<unsigned long long>(k_eff)) {
@@ -976,35 +981,26 @@ __device__ void topk_row(const TopkParams& P, int W, int row_id, cg::cluster_gro
   const unsigned long long need = static_cast<unsigned long long>(k_eff) - nan_tot;
   // reach: count * 2^32 >= need * 2^32, as the 128-bit target (t_hi:t_lo)
   const unsigned long long t_hi = 0ull, t_lo = need << 32;
-  // stage 0 counts only (one shared atomic per element); the mass of a bin
-  // is its count, and the bin's token id is found by stage 1
-  hist_clear(sm, kRowBins);
-  __syncthreads();
-  row_sweep<4>(rv, pol, ident, [&](int, float x) {
-    if (x == x) atomicAdd(&sm.hcnt[adigit0(x, m)], 1u);
-  });
+  // the first stage's histogram is pass 1's (counts only: the mass of a bin
+  // is its count, and the bin's token id is found by a later stage)
   __syncthreads();
   for (int q = tid; q < kRowBins; q += kRowThreads) sm.hmass[q] = sm.hcnt[q];
-  Found f = cluster_find(cl, sm, kRowBins, false, 0ull, t_hi, t_lo, CL, rank);
+  Found f = cluster_find(cl, sm, kRowBins, true, 0ull, t_hi, t_lo, CL, rank);
   unsigned long long above = f.before;
-  const int a0 = f.bin;
-  int a1 = -1;
-  int kd_len = 0, id_len = 0;
-  uint32_t kd_pre = 0u, id_pre = 0u;
-  for (int stage = 1; (stage == 1 || f.cnt != 1u) && stage <= 6; ++stage) {
-    const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
+  int kd_len = 11, id_len = 0;
+  uint32_t kd_pre = static_cast<uint32_t>(f.bin), id_pre = 0u;
+  // then kd bits [20:10] and [9:0], token id bits [21:11] and [10:0], while
+  // the boundary bin holds more than one element (at least once, for its id)
+  for (int stage = 3; (stage == 3 || f.cnt != 1u) && stage <= 6; ++stage) {
+    const int c_kl = kd_len, c_il = id_len;
     const uint32_t c_kp = kd_pre, c_ip = id_pre;
     auto match = [=](float x, uint32_t kd, uint32_t id) {
-      if (x != x || adigit0(x, m) != a0) return false;
-      if (c_a1 >= 0 && adigit1(x, m, a0) != c_a1) return false;
-      if (c_kl > 0 && (kd >> (32 - c_kl)) != c_kp) return false;
+      if (x != x || (kd >> (32 - c_kl)) != c_kp) return false;
       if (c_il > 0 && (id >> (22 - c_il)) != c_ip) return false;
       return true;
     };
-    auto digit = [=](float x, uint32_t kd, uint32_t id) -> int {
+    auto digit = [=](uint32_t kd, uint32_t id) -> int {
       switch (stage) {
-        case 1: return adigit1(x, m, a0);
-        case 2: return static_cast<int>(kd >> 21);
         case 3: return static_cast<int>((kd >> 10) & 0x7FFu);
         case 4: return static_cast<int>(kd & 0x3FFu);
         case 5: return static_cast<int>((id >> 11) & 0x7FFu);
@@ -1012,20 +1008,18 @@ __device__ void topk_row(const TopkParams& P, int W, int row_id, cg::cluster_gro
       }
     };
     const int nb = stage == 4 ? 1024 : kRowBins;
-    const bool desc = stage >= 2 && stage <= 4;
+    const bool desc = stage <= 4;  // larger kd first; token ids ascending
     hist_clear(sm, nb);
     __syncthreads();
     row_sweep<4>(rv, pol, ident, [&](int j, float x) {
       const uint32_t kd = kd_of(x);
       const uint32_t id = static_cast<uint32_t>(v0 + j);
-      if (match(x, kd, id)) hist_add(sm, true, digit(x, kd, id), 1ull, id);
+      if (match(x, kd, id)) hist_add(sm, true, digit(kd, id), 1ull, id);
     });
     f = cluster_find(cl, sm, nb, desc, above, t_hi, t_lo, CL, rank);
     above = f.before;
     const uint32_t bin = static_cast<uint32_t>(f.bin);
-    if (stage == 1) {
-      a1 = f.bin;
-    } else if (stage <= 4) {
+    if (stage <= 4) {
       kd_pre = (kd_pre << (stage == 4 ? 10 : 11)) | bin;
       kd_len += stage == 4 ? 10 : 11;
     } else {
