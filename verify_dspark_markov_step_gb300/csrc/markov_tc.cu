@@ -84,8 +84,8 @@ __host__ __device__ inline size_t base_slot_stride(size_t base_stage) {
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 struct TcLayout {
-  size_t a, e, bases, xs, gs, seed, npos, bptr, cptr, cb0, prev, act, best, xbest, wkey, wx, bars,
-      slot, flags, total;
+  size_t a, e, bases, xs, gs, seed, npos, bptr, cptr, cb0, prev, act, best, wkey, wx, bars, slot,
+      flags, total;
   __host__ __device__ TcLayout(int Npad, int NK, int ns, int nb, size_t base_stage) {
     a = 0;                                                       // markov_w2 ring
     e = a + static_cast<size_t>(ns) * kStageBytes;               // Markov embeddings
@@ -100,8 +100,7 @@ struct TcLayout {
     prev = cb0 + static_cast<size_t>(Npad) * 8;                  //   token feeding the step
     act = prev + static_cast<size_t>(Npad) * 4;
     best = act + static_cast<size_t>(Npad) * 4;
-    xbest = best + static_cast<size_t>(Npad) * 8;                //   cache-row maximum key
-    wkey = xbest + static_cast<size_t>(Npad) * 8;                // per lane quarter: winner key,
+    wkey = best + static_cast<size_t>(Npad) * 8;                 // per lane quarter: winner key,
     wx = wkey + static_cast<size_t>(4 * Npad) * 8;               //   cache-row maximum key
     bars = wx + static_cast<size_t>(4 * Npad) * 4;
     slot = bars + static_cast<size_t>(2 * kMaxStages + 2 * kMaxAcc + 2 * kMaxBaseSlots + 2) * 8;
@@ -294,7 +293,6 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   const unsigned char** s_bptr = reinterpret_cast<const unsigned char**>(smem + L.bptr);
   unsigned char** s_cptr = reinterpret_cast<unsigned char**>(smem + L.cptr);  // null: no store
   unsigned char** s_cb0 = reinterpret_cast<unsigned char**>(smem + L.cb0);
-  uint32_t* xbest = reinterpret_cast<uint32_t*>(smem + L.xbest);
   // cache-row maxima are recorded by the register-winner epilogue (up to 64
   // requests); wider batches report them unknown (NaN)
   const bool want_stats = kRegWinners && P.draft_stats != nullptr;
@@ -378,7 +376,6 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     s_bptr[n] = bp;
     s_cptr[n] = cp;
     s_cb0[n] = cp;
-    xbest[n] = 0u;
     s_prev[n] = prev;
     s_act[n] = prev >= 0;
     best[n] = 0ull;
