@@ -8,21 +8,25 @@
 // maximum and fixed-point mass. Greedy target rows get their winner key.
 //
 // A row is split over the CL CTAs of a cluster (CL up to 16, slices of at
-// most 32768 values). Each CTA reads its slice from HBM once (the maximum)
-// with an L2 evict-last hint, and the later passes (fixed-point mass, the
-// radix stages of the top-p select) read it again from L2; with nothing held
-// in shared memory but histograms, four CTAs share an SM and many rows are
-// in flight. Reductions across the cluster go through distributed shared
-// memory: scalars by each CTA reading the others' slots, histograms by each
-// CTA reducing its own range of bins over the cluster.
+// most 32768 values). Each CTA starts its slice as one bulk L2 prefetch,
+// reads it once for the maximum with an L2 evict-last hint, and the later
+// passes (fixed-point mass, the radix stages of the top-p select) read it
+// again from L2; with nothing held in shared memory but histograms, four CTAs
+// share an SM and many rows are in flight (odd clusters take their rows in
+// reverse order, so one-pass draft rows and two-pass target rows overlap).
+// Reductions across the cluster go through distributed shared memory:
+// scalars by each CTA reading the others' slots, histograms by each CTA
+// reducing its own range of bins over the cluster, in place.
 //
 // Top-p select: a radix select in (logit descending, token id ascending)
 // order with histograms of fixed-point mass; each stage finds the first bin at
 // which the running mass reaches P32 * F / 2^32 and the next stage splits
 // that bin, until the bin holds one element. The first two stages bin by the
-// distance to the row maximum (2048 bins of 1/64 over [0, 32), then 2048
-// sub-bins of the chosen bin), which spreads typical rows over many bins;
-// then come the ordered bits kd of the logit (11 + 11 + 10 bits) and, for
+// distance to the row maximum (2048 bins of 1/64 over [0, 32), counted during
+// the mass pass, then 2048 sub-bins of the chosen bin, whose elements are
+// also copied to a per-CTA candidate list that the later stages read instead
+// of the slice); then come the ordered bits kd of the logit (11 + 11 + 10
+// bits, skipped once a stage's candidates all share one value) and, for
 // exact ties, the token id (11 + 11 bits).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
