@@ -269,9 +269,8 @@ dspark_status dspark_rejection_sample(
   p.cand = reinterpret_cast<uint2*>(w + ws.cand);
   p.nchunk = dspark::verify_chunks(B, V, sms);
   p.status = status;
-  if (cudaMemsetAsync(p.counters, 0, static_cast<size_t>(B) * sizeof(unsigned int), st) !=
-      cudaSuccess)
-    return DSPARK_ERR_CUDA;
+  // (the draw kernel's per-request counters are zeroed by the row kernel,
+  // which runs before it on the stream)
   if (dspark::launch_verify(p, cluster, slice, st) != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }

@@ -820,6 +820,9 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyParam
   const int nclusters = gridDim.x / CL;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
+  // the draw kernel that follows counts its finished chunks per request here
+  if (blockIdx.x == 0)
+    for (int b = threadIdx.x; b < P.B; b += kRowThreads) P.counters[b] = 0u;
   int jrow = 0;
   // odd clusters walk their rows backward: about half the clusters stream a
   // draft row (one pass) while the others are on a target row (two passes)
