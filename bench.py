@@ -232,6 +232,19 @@ def build_workload(args):
     return wl.make(args.config, batch=args.batch)
 
 
+def max_over_ranks(value: float, world: int, device: str) -> float:
+    """The largest of every rank's value (the slowest replica sets a step's
+    time); the value itself on one process. `device` holds the one-element
+    tensor the process group reduces ("cuda" for NCCL, "cpu" for gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle on the host cores."""
     if rank != 0:
@@ -327,11 +340,7 @@ def run_ours(args, rank, world, local):
     loop_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ver_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_ms = [a + b for a, b in zip(loop_ms, ver_ms)]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), world, "cuda")
     status = st.status_code()
     nacc = st.num_accepted.float().mean().item()
     tokens = (st.num_accepted + 1).sum().item()
@@ -384,11 +393,8 @@ def run_ours(args, rank, world, local):
     for i in range(e2e_steps):
         e2e_step(eev[i])
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in eev)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in eev), world,
+                            "cuda")
 
     peak, peak_kind = _peaks()
     per_step, ver_bytes = algorithmic_bytes(w)
