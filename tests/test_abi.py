@@ -92,3 +92,10 @@ def test_argument_checks_return_before_any_launch(L):
     assert verify(B=0) == 0
     assert L.dspark_noise(fake, fake, fake, fake, null, null, null, -1, null) == -1
     assert L.dspark_noise(null, null, null, null, null, null, null, 0, null) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No CPU fallback: loading a library that is not there raises."""
+    from verify_dspark_markov_step_gb300 import _lib
+    with pytest.raises(RuntimeError, match="CUDA library not built"):
+        _lib.lib(str(tmp_path / "libdspark.so"))
