@@ -60,12 +60,25 @@ def decode_fixture(name):
                 num_accepted=res["num_accepted"].tolist())
 
 
+def topk_fixture(name, k):
+    w = wl.make(name, with_target=False)
+    tok, cache, gaps = oracle.markov_sample(
+        w.base, w.w1, w.w2, w.anchor, w.req_state_idx, w.positions, w.temperature,
+        w.seeds, cache_rows=w.C, cache_bf16=w.cache_bf16, row_map=w.row_map, topk=k)
+    c32 = wl.bf16_bits_to_f32(cache) if w.cache_bf16 else np.asarray(cache, np.float32)
+    return dict(workload=name, topk=k, draft_tokens=tok.tolist(),
+                min_draft_gap=float(np.min(gaps)),
+                finite_per_row=np.isfinite(c32).sum(axis=-1).reshape(-1).tolist())
+
+
 def main():
     with open(os.path.join(HERE, "oracle_noise.json"), "w") as f:
         json.dump(noise_fixture(), f, indent=1)
     for name in ("tiny", "odd"):
         with open(os.path.join(HERE, f"oracle_decode_{name}.json"), "w") as f:
             json.dump(decode_fixture(name), f, indent=1)
+    with open(os.path.join(HERE, "oracle_topk_odd_k64.json"), "w") as f:
+        json.dump(topk_fixture("odd", 64), f, indent=1)
 
 
 if __name__ == "__main__":

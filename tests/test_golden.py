@@ -42,6 +42,14 @@ def test_oracle_decode_matches_stored(name):
     assert got["num_accepted"] == want["num_accepted"]
 
 
+def test_oracle_topk_matches_stored():
+    import make_golden
+    want = _load("oracle_topk_odd_k64.json")
+    got = make_golden.topk_fixture(want["workload"], want["topk"])
+    assert got["draft_tokens"] == want["draft_tokens"]
+    assert got["finite_per_row"] == want["finite_per_row"]
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", ["tiny", "odd"])
 def test_gpu_tokens_match_stored(name):
