@@ -33,13 +33,13 @@
 //               waits for the step's Markov embeddings before its first tile.
 //   warps 2-17  epilogue: warp (q, sub) owns TMEM lane quarter q (32 rows of
 //               each tile) and a fixed set of CPW batch columns. Per group of
-//               8 (or 4) columns: one tcgen05.ld and the Philox blocks, then
-//               per column: bias add, temperature (x = z * (1/T),
-//               within 1.5 ulp of z / T), Gumbel noise (one Philox block per
-//               lane quad, shared by a 4x4 butterfly transpose), cache store,
-//               and the running winner of each column -- per lane in
-//               registers across tiles when CPW <= 16, else reduced per tile
-//               with redux.sync.
+//               4 columns: one tcgen05.ld and one Philox block (a lane quad
+//               shares its 4 blocks by a 4x4 butterfly transpose); per pair of
+//               columns, in packed fp32 pairs: Gumbel noise, bias add,
+//               temperature (x = z * (1/T), within 1.5 ulp of z / T) and noise
+//               add; per column: cache store and the running winner -- per
+//               lane in registers across tiles when CPW <= 16, else reduced
+//               per tile with redux.sync.
 // At the end of a step each CTA folds its winners into the step's global
 // winner keys (64-bit atomicMax), then a grid barrier (an arrival counter,
 // bounded wait) lets every CTA read the step's tokens, gather the next Markov
