@@ -7,6 +7,8 @@ its Python binding) never imports, links or runs anything here, and this
 package shares no code with it: the arithmetic lives in ``dspark_oracle.c``
 (plain C11, fp64 for transcendentals and dot products, compiled with
 ``-ffp-contract=off``), and this module only marshals numpy arrays into it.
+The same file is also built with ``-fopenmp``, which runs the independent
+requests of a batch call on several host threads and changes nothing else.
 
 What each function computes, and which passage of the pages it follows, is
 documented beside the C function it calls.
@@ -23,8 +25,12 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "dspark_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+# The same source built with -fopenmp: the batch entry points then run their
+# requests on several host threads (the CPU baseline's parallel leg).
+_OMP_PATH = os.path.join(_HERE, "_build", "liboracle_omp.so")
 _lock = threading.Lock()
 _lib = None
+_omp_lib = None
 
 ORC_OK = 0
 ORC_EINVAL = 1
@@ -36,17 +42,25 @@ STREAM_TARGET = 0
 STREAM_ACCEPT = 1 << 29
 
 
-def build(force: bool = False) -> str:
-    """Compile ``dspark_oracle.c`` into ``_build/liboracle.so`` with gcc."""
-    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
-    stale = (not os.path.exists(_LIB_PATH)) or (
-        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+def _compile(path, extra, force):
+    stale = (not os.path.exists(path)) or (os.path.getmtime(path) < os.path.getmtime(_SRC))
     if force or stale:
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        tmp = path + f".tmp{os.getpid()}"
         cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-               "-fPIC", "-shared", "-Wall", "-o", tmp, _SRC, "-lm"]
+               "-fPIC", "-shared", "-Wall", *extra, "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
-        os.replace(tmp, _LIB_PATH)
+        os.replace(tmp, path)
+
+
+def build(force: bool = False) -> str:
+    """Compile ``dspark_oracle.c`` into ``_build/liboracle.so`` with gcc, and
+    the OpenMP build ``_build/liboracle_omp.so`` where gcc supports it."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    _compile(_LIB_PATH, [], force)
+    try:
+        _compile(_OMP_PATH, ["-fopenmp"], force)
+    except (subprocess.CalledProcessError, OSError):
+        pass  # no OpenMP: only the single-threaded oracle exists
     return _LIB_PATH
 
 
@@ -54,43 +68,64 @@ def _P(t):
     return ctypes.POINTER(t)
 
 
-def lib():
-    global _lib
+def _load(path):
+    L = ctypes.CDLL(path)
+    vp, i32, i64, f32, u64 = (ctypes.c_void_p, ctypes.c_int,
+                              ctypes.c_int64, ctypes.c_float,
+                              ctypes.c_uint64)
+    L.orc_markov_sample.restype = i32
+    L.orc_markov_sample.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp,
+                                    vp, i32, vp, vp, vp, vp,
+                                    i32, i32, i32, i32, i32, i32]
+    L.orc_markov_sample_topk.restype = i32
+    L.orc_markov_sample_topk.argtypes = L.orc_markov_sample.argtypes + [i32]
+    L.orc_markov_step.restype = i32
+    L.orc_markov_step.argtypes = [vp, i32, vp, vp, ctypes.c_int32, f32,
+                                  u64, i64, i32, i32, vp, vp, vp]
+    L.orc_rejection_sample.restype = i32
+    L.orc_rejection_sample.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp,
+                                       vp, vp, vp, vp, vp, vp, vp, vp,
+                                       i32, i32, i32, i32, i32]
+    L.orc_philox_batch.restype = i32
+    L.orc_philox_batch.argtypes = [i64, vp, vp, vp]
+    L.orc_noise_batch.restype = i32
+    L.orc_noise_batch.argtypes = [i64, vp, vp, vp, vp, vp, vp, vp]
+    L.orc_block_argmax.restype = i32
+    L.orc_block_argmax.argtypes = [vp, i64, vp, vp]
+    L.orc_target_probs.restype = i32
+    L.orc_target_probs.argtypes = [vp, i32, i32, f32, f32, vp, vp, vp,
+                                   vp, vp]
+    L.orc_draft_probs.restype = i32
+    L.orc_draft_probs.argtypes = [vp, i32, i32, vp]
+    L.orc_categorical.restype = i32
+    L.orc_categorical.argtypes = [vp, i32, u64, i64, vp, vp]
+    L.orc_threads.restype = i32
+    L.orc_threads.argtypes = [i32]
+    return L
+
+
+def lib(threads: int = 1):
+    """The single-threaded oracle library; with threads > 1 the OpenMP build
+    set to that many host threads (RuntimeError if it could not be built)."""
+    global _lib, _omp_lib
     with _lock:
-        if _lib is None:
+        if threads <= 1:
+            if _lib is None:
+                build()
+                _lib = _load(_LIB_PATH)
+            return _lib
+        if _omp_lib is None:
             build()
-            L = ctypes.CDLL(_LIB_PATH)
-            vp, i32, i64, f32, u64 = (ctypes.c_void_p, ctypes.c_int,
-                                      ctypes.c_int64, ctypes.c_float,
-                                      ctypes.c_uint64)
-            L.orc_markov_sample.restype = i32
-            L.orc_markov_sample.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp,
-                                            vp, i32, vp, vp, vp, vp,
-                                            i32, i32, i32, i32, i32, i32]
-            L.orc_markov_sample_topk.restype = i32
-            L.orc_markov_sample_topk.argtypes = L.orc_markov_sample.argtypes + [i32]
-            L.orc_markov_step.restype = i32
-            L.orc_markov_step.argtypes = [vp, i32, vp, vp, ctypes.c_int32, f32,
-                                          u64, i64, i32, i32, vp, vp, vp]
-            L.orc_rejection_sample.restype = i32
-            L.orc_rejection_sample.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp,
-                                               vp, vp, vp, vp, vp, vp, vp, vp,
-                                               i32, i32, i32, i32, i32]
-            L.orc_philox_batch.restype = i32
-            L.orc_philox_batch.argtypes = [i64, vp, vp, vp]
-            L.orc_noise_batch.restype = i32
-            L.orc_noise_batch.argtypes = [i64, vp, vp, vp, vp, vp, vp, vp]
-            L.orc_block_argmax.restype = i32
-            L.orc_block_argmax.argtypes = [vp, i64, vp, vp]
-            L.orc_target_probs.restype = i32
-            L.orc_target_probs.argtypes = [vp, i32, i32, f32, f32, vp, vp, vp,
-                                           vp, vp]
-            L.orc_draft_probs.restype = i32
-            L.orc_draft_probs.argtypes = [vp, i32, i32, vp]
-            L.orc_categorical.restype = i32
-            L.orc_categorical.argtypes = [vp, i32, u64, i64, vp, vp]
-            _lib = L
-    return _lib
+            if not os.path.exists(_OMP_PATH):
+                raise RuntimeError("the OpenMP oracle could not be built (gcc -fopenmp)")
+            _omp_lib = _load(_OMP_PATH)
+        _omp_lib.orc_threads(int(threads))
+        return _omp_lib
+
+
+def threads_in_use(threads: int) -> int:
+    """Host threads the oracle runs its requests on for a `threads` request."""
+    return 1 if threads <= 1 else int(lib(threads).orc_threads(0))
 
 
 def _ptr(a):
@@ -161,10 +196,11 @@ def block_argmax(y):
 # --------------------------------------------------------------------------
 def markov_sample(base, w1, w2, anchor, req_state_idx, positions, temperature,
                   seeds, cache_rows=None, cache_bf16=False, row_map=None,
-                  forced=None, write_cache=True, topk=0):
+                  forced=None, write_cache=True, topk=0, threads=1):
     """Run the K-step Markov loop. Returns (tokens [B,K] int32, cache or None,
     gaps [B,K] float64). ``cache_rows`` is C (default S). ``topk`` > 0 runs the
-    top-k variant (the bias only on the top-k base logits of each step)."""
+    top-k variant (the bias only on the top-k base logits of each step).
+    ``threads`` > 1 runs the requests on that many host threads (OpenMP)."""
     base, base_bf16 = _logit_array(base)
     B, K, V = base.shape
     w1 = _c(w1, np.uint16)
@@ -187,10 +223,11 @@ def markov_sample(base, w1, w2, anchor, req_state_idx, positions, temperature,
     args = (_ptr(base), base_bf16, _ptr(w1), _ptr(w2), _ptr(anchor), _ptr(rsi),
             _ptr(pos), _ptr(temp), _ptr(seeds), _ptr(cache), int(bool(cache_bf16)),
             _ptr(row_map), _ptr(forced), _ptr(tokens), _ptr(gaps), B, K, V, R, S, C)
+    L = lib(threads)
     if topk:
-        rc = lib().orc_markov_sample_topk(*args, int(topk))
+        rc = L.orc_markov_sample_topk(*args, int(topk))
     else:
-        rc = lib().orc_markov_sample(*args)
+        rc = L.orc_markov_sample(*args)
     _check(rc, "markov_sample")
     return tokens, cache, gaps
 
@@ -216,9 +253,10 @@ def markov_step(base_row, w1, w2, prev, temperature, seed, noise_pos):
 # Verifier
 # --------------------------------------------------------------------------
 def rejection_sample(draft_tokens, cache, target, req_state_idx, positions,
-                     temperature, top_p, seeds, row_map=None):
+                     temperature, top_p, seeds, row_map=None, threads=1):
     """Run the verifier. Returns a dict with out_tokens [B,K+1],
-    num_accepted [B], margins [B,K], gaps [B], slack [B,K+1]."""
+    num_accepted [B], margins [B,K], gaps [B], slack [B,K+1]. ``threads`` > 1
+    runs the requests on that many host threads (OpenMP)."""
     draft = _c(draft_tokens, np.int32)
     B, K = draft.shape
     target, t_bf16 = _logit_array(target)
@@ -241,7 +279,7 @@ def rejection_sample(draft_tokens, cache, target, req_state_idx, positions,
     margins = np.empty((B, K), np.float64)
     gaps = np.empty(B, np.float64)
     slack = np.empty((B, K + 1), np.float64)
-    rc = lib().orc_rejection_sample(
+    rc = lib(threads).orc_rejection_sample(
         _ptr(draft), _ptr(cache_arr), c_bf16, _ptr(row_map), _ptr(target), t_bf16,
         _ptr(rsi), _ptr(pos), _ptr(temp), _ptr(tp), _ptr(seeds), _ptr(out),
         _ptr(nacc), _ptr(margins), _ptr(gaps), _ptr(slack), B, K, V, S, C)

@@ -36,6 +36,18 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* Requests are independent, so the batch entry points can run them on
+ * several host threads: built with -fopenmp the two batch loops below are
+ * OpenMP loops over requests (one request per thread at a time, each thread
+ * with its own scratch); built without it they are plain loops. Nothing
+ * inside a request changes. */
+#ifdef _OPENMP
+#include <omp.h>
+#define ORC_OMP(x) _Pragma(#x)
+#else
+#define ORC_OMP(x)
+#endif
+
 /* ------------------------------------------------------------------------ */
 /* Error codes of this oracle (its own; unrelated to the library's).         */
 /* ------------------------------------------------------------------------ */
@@ -312,7 +324,7 @@ static int topk_mask(const void* base_row, int base_bf16, int64_t V, int64_t k,
     r[v].idx = v;
   }
   qsort(r, (size_t)V, sizeof(orc_rank), rank_cmp);
-  memset(mask, 0, (size_t)V);
+  for (int64_t v = 0; v < V; v++) mask[v] = 0;
   for (int64_t j = 0; j < V && j < k; j++) mask[r[j].idx] = 1;
   free(r);
   return ORC_OK;
@@ -338,6 +350,58 @@ static int topk_mask(const void* base_row, int base_bf16, int64_t V, int64_t k,
  * tokens    [B,K] out
  * gaps      [B,K] out or NULL: top-two gap of the noised values per step
  */
+/* One request of the batch loop (scratch: x[V], y[V], e[R], cand[V] or
+ * NULL). */
+static int markov_request(int b, const void* base, int base_bf16, const uint16_t* w1,
+                          const uint16_t* w2, const int32_t* anchor, const int32_t* rsi,
+                          const int64_t* pos, const float* temperature,
+                          const uint64_t* seeds, void* cache, int cache_bf16,
+                          const int32_t* row_map, const int32_t* forced, int32_t* tokens,
+                          double* gaps, int K, int V, int R, int S, int C, int topk,
+                          float* x, float* y, double* e, unsigned char* cand) {
+  int32_t s = rsi[b];
+  if (s < 0) {
+    for (int i = 0; i < K; i++) {
+      tokens[(int64_t)b * K + i] = -1;
+      if (gaps) gaps[(int64_t)b * K + i] = INFINITY;
+    }
+    return ORC_OK;
+  }
+  if (s >= S) return ORC_EBOUNDS;
+  int64_t row = row_map ? (int64_t)row_map[s] : (int64_t)s;
+  if (cache && (row < 0 || row >= C)) return ORC_EBOUNDS;
+  int32_t prev = anchor[b];
+  for (int i = 0; i < K; i++) {
+    const int64_t base_off = ((int64_t)b * K + i) * V;
+    const void* base_row =
+        base_bf16 ? (const void*)((const uint16_t*)base + base_off)
+                  : (const void*)((const float*)base + base_off);
+    int32_t tok;
+    double gap;
+    int rc;
+    if (topk > 0) {
+      rc = topk_mask(base_row, base_bf16, V, topk, cand);
+      if (rc != ORC_OK) return rc;
+    }
+    rc = markov_step_one(base_row, base_bf16, w1, w2, prev, temperature[s], seeds[s],
+                         pos[b] + i - 1, V, R, topk > 0 ? cand : NULL, x, y, e, &tok, &gap);
+    if (rc != ORC_OK) return rc;
+    tokens[(int64_t)b * K + i] = tok;
+    if (gaps) gaps[(int64_t)b * K + i] = gap;
+    if (cache) {
+      const int64_t off = (row * K + i) * (int64_t)V;
+      for (int64_t v = 0; v < V; v++) {
+        if (cache_bf16)
+          ((uint16_t*)cache)[off + v] = f32_to_bf16(x[v]);
+        else
+          ((float*)cache)[off + v] = x[v];
+      }
+    }
+    prev = forced ? forced[(int64_t)b * K + i] : tok;
+  }
+  return ORC_OK;
+}
+
 static int markov_sample_impl(const void* base, int base_bf16, const uint16_t* w1,
                               const uint16_t* w2, const int32_t* anchor,
                               const int32_t* rsi, const int64_t* pos,
@@ -349,69 +413,31 @@ static int markov_sample_impl(const void* base, int base_bf16, const uint16_t* w
   if (!base || !w1 || !w2 || !anchor || !rsi || !pos || !temperature || !seeds ||
       !tokens)
     return ORC_EINVAL;
-  float* x = (float*)malloc(sizeof(float) * (size_t)V);
-  float* y = (float*)malloc(sizeof(float) * (size_t)V);
-  double* e = (double*)malloc(sizeof(double) * (size_t)R);
-  unsigned char* cand = topk > 0 ? (unsigned char*)malloc((size_t)V) : NULL;
-  if (!x || !y || !e || (topk > 0 && !cand)) {
+  int rc = ORC_OK;
+  ORC_OMP(omp parallel)
+  {
+    float* x = (float*)malloc(sizeof(float) * (size_t)V);
+    float* y = (float*)malloc(sizeof(float) * (size_t)V);
+    double* e = (double*)malloc(sizeof(double) * (size_t)R);
+    unsigned char* cand = topk > 0 ? (unsigned char*)malloc((size_t)V) : NULL;
+    const int have = x && y && e && (topk == 0 || cand);
+    ORC_OMP(omp for schedule(dynamic, 1))
+    for (int b = 0; b < B; b++) {
+      const int r = have ? markov_request(b, base, base_bf16, w1, w2, anchor, rsi, pos,
+                                          temperature, seeds, cache, cache_bf16, row_map,
+                                          forced, tokens, gaps, K, V, R, S, C, topk, x, y, e,
+                                          cand)
+                         : ORC_ENOMEM;
+      if (r != ORC_OK) {
+        ORC_OMP(omp critical(orc_rc))
+        if (rc == ORC_OK) rc = r;
+      }
+    }
     free(x);
     free(y);
     free(e);
     free(cand);
-    return ORC_ENOMEM;
   }
-  int rc = ORC_OK;
-  for (int b = 0; b < B && rc == ORC_OK; b++) {
-    int32_t s = rsi[b];
-    if (s < 0) {
-      for (int i = 0; i < K; i++) {
-        tokens[(int64_t)b * K + i] = -1;
-        if (gaps) gaps[(int64_t)b * K + i] = INFINITY;
-      }
-      continue;
-    }
-    if (s >= S) {
-      rc = ORC_EBOUNDS;
-      break;
-    }
-    int64_t row = row_map ? (int64_t)row_map[s] : (int64_t)s;
-    if (cache && (row < 0 || row >= C)) {
-      rc = ORC_EBOUNDS;
-      break;
-    }
-    int32_t prev = anchor[b];
-    for (int i = 0; i < K; i++) {
-      const int64_t base_off = ((int64_t)b * K + i) * V;
-      const void* base_row =
-          base_bf16 ? (const void*)((const uint16_t*)base + base_off)
-                    : (const void*)((const float*)base + base_off);
-      int32_t tok;
-      double gap;
-      if (cand) {
-        rc = topk_mask(base_row, base_bf16, V, topk, cand);
-        if (rc != ORC_OK) break;
-      }
-      rc = markov_step_one(base_row, base_bf16, w1, w2, prev, temperature[s],
-                           seeds[s], pos[b] + i - 1, V, R, cand, x, y, e, &tok, &gap);
-      if (rc != ORC_OK) break;
-      tokens[(int64_t)b * K + i] = tok;
-      if (gaps) gaps[(int64_t)b * K + i] = gap;
-      if (cache) {
-        const int64_t off = (row * K + i) * (int64_t)V;
-        for (int64_t v = 0; v < V; v++) {
-          if (cache_bf16)
-            ((uint16_t*)cache)[off + v] = f32_to_bf16(x[v]);
-          else
-            ((float*)cache)[off + v] = x[v];
-        }
-      }
-      prev = forced ? forced[(int64_t)b * K + i] : tok;
-    }
-  }
-  free(x);
-  free(y);
-  free(e);
-  free(cand);
   return rc;
 }
 
@@ -661,6 +687,120 @@ static orc_winner categorical_draw(const float* w, int V, uint64_t seed,
  *    cache is never read ([BSH] notes: "verification compares against the
  *    target argmax and never reads cached draft logits").
  *  padding (s < 0): all -1, num_acc 0, nothing read. */
+/* One request of the verifier (scratch: p, q, r, e [V], keep [V], kv [V]). */
+static int verify_request(int b, const int32_t* draft, const void* cache, int cache_bf16,
+                          const int32_t* row_map, const void* target, int target_bf16,
+                          const int32_t* rsi, const int64_t* pos, const float* temperature,
+                          const float* top_p, const uint64_t* seeds, int32_t* out,
+                          int32_t* num_acc, double* margins, double* gaps, double* slack,
+                          int K, int V, int S, int C, float* p, float* q, float* r, float* e,
+                          uint8_t* keep, orc_kv* kv) {
+  const int64_t K1 = (int64_t)K + 1;
+  for (int64_t k = 0; k < K1; k++) out[b * K1 + k] = -1;
+  num_acc[b] = 0;
+  if (margins)
+    for (int k = 0; k < K; k++) margins[(int64_t)b * K + k] = NAN;
+  if (gaps) gaps[b] = INFINITY;
+  if (slack)
+    for (int64_t k = 0; k < K1; k++) slack[b * K1 + k] = NAN;
+  const int32_t s = rsi[b];
+  if (s < 0) return ORC_OK;
+  if (s >= S) return ORC_EBOUNDS;
+  const float T = temperature[s];
+  const int greedy = !(T > 0.0f);
+  const uint64_t seed = seeds[s];
+  const int64_t P0 = pos[b];
+  int64_t crow = 0;
+  if (!greedy) {
+    if (!cache) return ORC_EINVAL;
+    crow = row_map ? (int64_t)row_map[s] : (int64_t)s;
+    if (crow < 0 || crow >= C) return ORC_EBOUNDS;
+  }
+  int done = 0;
+  int32_t n_acc = 0;
+  for (int64_t k = 0; k < K && !done; k++) {
+    const int32_t d = draft[(int64_t)b * K + k];
+    if (d < -1 || d >= V) return ORC_EBOUNDS;
+    const int64_t toff = ((int64_t)b * K1 + k) * V;
+    const void* trow = target_bf16
+                           ? (const void*)((const uint16_t*)target + toff)
+                           : (const void*)((const float*)target + toff);
+    if (greedy) {
+      for (int64_t v = 0; v < V; v++) r[v] = load_elem(trow, target_bf16, v);
+      orc_winner w = block_argmax(r, V);
+      if (margins) margins[(int64_t)b * K + k] = INFINITY;
+      if (d >= 0 && d == (int32_t)w.idx) {
+        out[(int64_t)b * K1 + k] = d;
+        n_acc++;
+      } else {
+        out[(int64_t)b * K1 + k] = (int32_t)w.idx;
+        if (gaps) gaps[b] = w.gap;
+        done = 1;
+      }
+      continue;
+    }
+    double sl;
+    target_probs_impl(trow, target_bf16, V, T, top_p[s], p, keep, NULL, NULL,
+                      &sl, e, kv);
+    if (slack) slack[b * K1 + k] = sl;
+    if (d == -1) {
+      orc_winner w = categorical_draw(p, V, seed, P0 + k - 1, r);
+      out[(int64_t)b * K1 + k] = (int32_t)w.idx;
+      if (gaps) gaps[b] = w.gap;
+      done = 1;
+      break;
+    }
+    const int64_t coff = (crow * K + k) * (int64_t)V;
+    const void* qrow = cache_bf16 ? (const void*)((const uint16_t*)cache + coff)
+                                  : (const void*)((const float*)cache + coff);
+    draft_probs_impl(qrow, cache_bf16, V, q);
+    const float u = uniform_from_word(
+        noise_word(seed, P0 + k - 1, 0u, ORC_STREAM_ACCEPT));
+    const float pd = p[d], qd = q[d];
+    const float uq = u * qd;
+    if (margins) {
+      margins[(int64_t)b * K + k] =
+          qd > 0.0f ? fabs((double)u - (double)pd / (double)qd) : INFINITY;
+    }
+    if (uq < pd) {
+      out[(int64_t)b * K1 + k] = d;
+      n_acc++;
+      continue;
+    }
+    int any_pos = 0;
+    for (int64_t v = 0; v < V; v++) {
+      float diff = p[v] - q[v];
+      r[v] = diff > 0.0f ? diff : 0.0f;
+      if (r[v] > 0.0f) any_pos = 1;
+    }
+    orc_winner w = categorical_draw(any_pos ? r : p, V, seed, P0 + k - 1, e);
+    out[(int64_t)b * K1 + k] = (int32_t)w.idx;
+    if (gaps) gaps[b] = w.gap;
+    done = 1;
+  }
+  if (!done) {
+    const int64_t toff = ((int64_t)b * K1 + K) * V;
+    const void* trow = target_bf16
+                           ? (const void*)((const uint16_t*)target + toff)
+                           : (const void*)((const float*)target + toff);
+    orc_winner w;
+    if (greedy) {
+      for (int64_t v = 0; v < V; v++) r[v] = load_elem(trow, target_bf16, v);
+      w = block_argmax(r, V);
+    } else {
+      double sl;
+      target_probs_impl(trow, target_bf16, V, T, top_p[s], p, keep, NULL,
+                        NULL, &sl, e, kv);
+      if (slack) slack[b * K1 + K] = sl;
+      w = categorical_draw(p, V, seed, P0 + K - 1, r);
+    }
+    out[(int64_t)b * K1 + K] = (int32_t)w.idx;
+    if (gaps) gaps[b] = w.gap;
+  }
+  num_acc[b] = n_acc;
+  return ORC_OK;
+}
+
 int orc_rejection_sample(const int32_t* draft, const void* cache,
                          int cache_bf16, const int32_t* row_map,
                          const void* target, int target_bf16,
@@ -673,147 +813,48 @@ int orc_rejection_sample(const int32_t* draft, const void* cache,
   if (!draft || !target || !rsi || !pos || !temperature || !top_p || !seeds ||
       !out || !num_acc)
     return ORC_EINVAL;
-  float* p = (float*)malloc(sizeof(float) * (size_t)V);
-  float* q = (float*)malloc(sizeof(float) * (size_t)V);
-  float* r = (float*)malloc(sizeof(float) * (size_t)V);
-  float* e = (float*)malloc(sizeof(float) * (size_t)V);
-  uint8_t* keep = (uint8_t*)malloc((size_t)V);
-  orc_kv* kv = (orc_kv*)malloc(sizeof(orc_kv) * (size_t)V);
-  if (!p || !q || !r || !e || !keep || !kv) {
+  int rc = ORC_OK;
+  ORC_OMP(omp parallel)
+  {
+    float* p = (float*)malloc(sizeof(float) * (size_t)V);
+    float* q = (float*)malloc(sizeof(float) * (size_t)V);
+    float* r = (float*)malloc(sizeof(float) * (size_t)V);
+    float* e = (float*)malloc(sizeof(float) * (size_t)V);
+    uint8_t* keep = (uint8_t*)malloc((size_t)V);
+    orc_kv* kv = (orc_kv*)malloc(sizeof(orc_kv) * (size_t)V);
+    const int have = p && q && r && e && keep && kv;
+    ORC_OMP(omp for schedule(dynamic, 1))
+    for (int b = 0; b < B; b++) {
+      const int rr = have ? verify_request(b, draft, cache, cache_bf16, row_map, target,
+                                           target_bf16, rsi, pos, temperature, top_p, seeds,
+                                           out, num_acc, margins, gaps, slack, K, V, S, C, p,
+                                           q, r, e, keep, kv)
+                          : ORC_ENOMEM;
+      if (rr != ORC_OK) {
+        ORC_OMP(omp critical(orc_rc))
+        if (rc == ORC_OK) rc = rr;
+      }
+    }
     free(p);
     free(q);
     free(r);
     free(e);
     free(keep);
     free(kv);
-    return ORC_ENOMEM;
   }
-  int rc = ORC_OK;
-  const int64_t K1 = (int64_t)K + 1;
-  for (int b = 0; b < B && rc == ORC_OK; b++) {
-    for (int64_t k = 0; k < K1; k++) out[b * K1 + k] = -1;
-    num_acc[b] = 0;
-    if (margins)
-      for (int k = 0; k < K; k++) margins[(int64_t)b * K + k] = NAN;
-    if (gaps) gaps[b] = INFINITY;
-    if (slack)
-      for (int64_t k = 0; k < K1; k++) slack[b * K1 + k] = NAN;
-    const int32_t s = rsi[b];
-    if (s < 0) continue;
-    if (s >= S) {
-      rc = ORC_EBOUNDS;
-      break;
-    }
-    const float T = temperature[s];
-    const int greedy = !(T > 0.0f);
-    const uint64_t seed = seeds[s];
-    const int64_t P0 = pos[b];
-    int64_t crow = 0;
-    if (!greedy) {
-      if (!cache) {
-        rc = ORC_EINVAL;
-        break;
-      }
-      crow = row_map ? (int64_t)row_map[s] : (int64_t)s;
-      if (crow < 0 || crow >= C) {
-        rc = ORC_EBOUNDS;
-        break;
-      }
-    }
-    int done = 0;
-    int32_t n_acc = 0;
-    for (int64_t k = 0; k < K && !done; k++) {
-      const int32_t d = draft[(int64_t)b * K + k];
-      if (d < -1 || d >= V) {
-        rc = ORC_EBOUNDS;
-        break;
-      }
-      const int64_t toff = ((int64_t)b * K1 + k) * V;
-      const void* trow = target_bf16
-                             ? (const void*)((const uint16_t*)target + toff)
-                             : (const void*)((const float*)target + toff);
-      if (greedy) {
-        for (int64_t v = 0; v < V; v++) r[v] = load_elem(trow, target_bf16, v);
-        orc_winner w = block_argmax(r, V);
-        if (margins) margins[(int64_t)b * K + k] = INFINITY;
-        if (d >= 0 && d == (int32_t)w.idx) {
-          out[(int64_t)b * K1 + k] = d;
-          n_acc++;
-        } else {
-          out[(int64_t)b * K1 + k] = (int32_t)w.idx;
-          if (gaps) gaps[b] = w.gap;
-          done = 1;
-        }
-        continue;
-      }
-      double sl;
-      target_probs_impl(trow, target_bf16, V, T, top_p[s], p, keep, NULL, NULL,
-                        &sl, e, kv);
-      if (slack) slack[b * K1 + k] = sl;
-      if (d == -1) {
-        orc_winner w = categorical_draw(p, V, seed, P0 + k - 1, r);
-        out[(int64_t)b * K1 + k] = (int32_t)w.idx;
-        if (gaps) gaps[b] = w.gap;
-        done = 1;
-        break;
-      }
-      const int64_t coff = (crow * K + k) * (int64_t)V;
-      const void* qrow = cache_bf16 ? (const void*)((const uint16_t*)cache + coff)
-                                    : (const void*)((const float*)cache + coff);
-      draft_probs_impl(qrow, cache_bf16, V, q);
-      const float u = uniform_from_word(
-          noise_word(seed, P0 + k - 1, 0u, ORC_STREAM_ACCEPT));
-      const float pd = p[d], qd = q[d];
-      const float uq = u * qd;
-      if (margins) {
-        margins[(int64_t)b * K + k] =
-            qd > 0.0f ? fabs((double)u - (double)pd / (double)qd) : INFINITY;
-      }
-      if (uq < pd) {
-        out[(int64_t)b * K1 + k] = d;
-        n_acc++;
-        continue;
-      }
-      int any_pos = 0;
-      for (int64_t v = 0; v < V; v++) {
-        float diff = p[v] - q[v];
-        r[v] = diff > 0.0f ? diff : 0.0f;
-        if (r[v] > 0.0f) any_pos = 1;
-      }
-      orc_winner w = categorical_draw(any_pos ? r : p, V, seed, P0 + k - 1, e);
-      out[(int64_t)b * K1 + k] = (int32_t)w.idx;
-      if (gaps) gaps[b] = w.gap;
-      done = 1;
-    }
-    if (rc != ORC_OK) break;
-    if (!done) {
-      const int64_t toff = ((int64_t)b * K1 + K) * V;
-      const void* trow = target_bf16
-                             ? (const void*)((const uint16_t*)target + toff)
-                             : (const void*)((const float*)target + toff);
-      orc_winner w;
-      if (greedy) {
-        for (int64_t v = 0; v < V; v++) r[v] = load_elem(trow, target_bf16, v);
-        w = block_argmax(r, V);
-      } else {
-        double sl;
-        target_probs_impl(trow, target_bf16, V, T, top_p[s], p, keep, NULL,
-                          NULL, &sl, e, kv);
-        if (slack) slack[b * K1 + K] = sl;
-        w = categorical_draw(p, V, seed, P0 + K - 1, r);
-      }
-      out[(int64_t)b * K1 + K] = (int32_t)w.idx;
-      if (gaps) gaps[b] = w.gap;
-    }
-    num_acc[b] = n_acc;
-  }
-  free(p);
-  free(q);
-  free(r);
-  free(e);
-  free(keep);
-  free(kv);
   return rc;
+}
+
+/* Host threads the batch entry points use: n > 0 sets it (OpenMP build);
+ * returns the count now in force (1 in the plain build). */
+int orc_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
 }
 
 /* ------------------------------------------------------------------------ */

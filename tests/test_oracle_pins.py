@@ -313,13 +313,106 @@ def test_markov_deterministic_and_teacher_forcing(orc):
     np.testing.assert_array_equal(a[0], f[0])
 
 
+def _torch_bf16_bits(x32):
+    """fp32 -> bf16 bit patterns by torch's own conversion (round to nearest
+    even), a library routine independent of the oracle's bit arithmetic."""
+    torch = pytest.importorskip("torch")
+    t = torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
 def test_bf16_cache_is_rounded_fp32_cache(orc):
+    """The bf16 cache is the fp32 cache rounded by torch's fp32 -> bf16
+    conversion (nearest even), element for element."""
     w = wl.custom(2, 2, 999, 16, seed=5, temperature=[0.75, 1.0])
     _, c32, _ = orc.markov_sample(w.base, w.w1, w.w2, w.anchor, w.req_state_idx,
                                   w.positions, w.temperature, w.seeds)
     _, c16, _ = orc.markov_sample(w.base, w.w1, w.w2, w.anchor, w.req_state_idx,
                                   w.positions, w.temperature, w.seeds, cache_bf16=True)
-    np.testing.assert_array_equal(c16, wl.f32_to_bf16_bits(c32))
+    np.testing.assert_array_equal(c16, _torch_bf16_bits(c32))
+
+
+def _bf16_edge_row():
+    """fp32 values at the edges of the fp32 -> bf16 rounding: halfway cases
+    with an even and an odd kept bit, one bit above and below halfway, fp32
+    subnormals, bf16's largest finite value and the values that round up to
+    infinity, infinities, signed zeros, NaN; then random values."""
+    bits = []
+    for hi in (0x3F80, 0x3F81, 0x4123, 0x4124, 0xC0A0, 0xC0A1, 0x0001, 0x8002, 0x7F7E):
+        for lo in (0x8000, 0x7FFF, 0x8001, 0x0000, 0xFFFF):
+            bits.append((hi << 16) | lo)
+    bits += [0x00000001, 0x80000001, 0x007FFFFF, 0x00400000, 0x00008000, 0x00018000,
+             0x7F7F7FFF, 0x7F7F8000, 0x7F7FFFFF, 0xFF7F8000, 0x7F800000, 0xFF800000,
+             0x00000000, 0x80000000, 0x7FC00000, 0xFFC00001, 0x7F800001]
+    x = np.array(bits, np.uint32).view(np.float32)
+    r = np.random.default_rng(11).standard_normal(1000).astype(np.float32) * np.float32(3)
+    return np.concatenate([x, r])
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_bf16_cache_rounding_edges_match_torch(orc, T):
+    """With markov_w2 = 0 the bias is exactly 0 and the cached value is
+    fp32(fp32(base + 0) / T); its bf16 cache equals torch's nearest-even
+    conversion of that value (ties, subnormals, overflow to infinity, signed
+    zeros), and NaN stays NaN."""
+    row = _bf16_edge_row()
+    V, R = row.size, 64
+    base = row.reshape(1, 1, V)
+    w1 = wl.f32_to_bf16_bits(np.random.default_rng(3).standard_normal((V, R)).astype(np.float32))
+    w2 = np.zeros((V, R), np.uint16)
+    args = (base, w1, w2, np.array([3], np.int32), np.array([0], np.int32),
+            wl.default_positions(1), np.array([T], np.float32), wl.default_seeds(1, 0))
+    with np.errstate(over="ignore", invalid="ignore"):
+        x = ((row + np.float32(0.0)) / np.float32(T)).astype(np.float32)
+    _, c32, _ = orc.markov_sample(*args)
+    _, c16, _ = orc.markov_sample(*args, cache_bf16=True)
+    nan = np.isnan(x)
+    np.testing.assert_array_equal(np.isnan(c32[0, 0]), nan)
+    np.testing.assert_array_equal(c32[0, 0][~nan].view(np.uint32), x[~nan].view(np.uint32))
+    got = c16[0, 0]
+    np.testing.assert_array_equal(np.isnan(wl.bf16_bits_to_f32(got)), nan)
+    np.testing.assert_array_equal(got[~nan], _torch_bf16_bits(x)[~nan])
+
+
+@pytest.mark.parametrize("cache_bf16", [False, True])
+def test_cache_at_temperature_is_scaled_biased_logits(orc, cache_bf16):
+    """The cache holds x = fp32(fp32(base + fp32(bias)) / T) at T = 0.5, 0.7,
+    1.3 and 1 (IEEE division, numpy fp32), and z at T = 0, with the bias a
+    numpy fp64 matmul rounded once; the step's gap and token are those of
+    y = fp32(x + g) with g the separately pinned draft noise at P0 + i - 1
+    (the pages' "processed logits": the scaled logits the draft was drawn
+    from). Teacher forcing fixes each step's previous token."""
+    temps = [0.5, 0.7, 1.3, 1.0, 0.0]
+    B, K, V, R = len(temps), 3, 777, 64
+    w = wl.custom(B, K, V, R, seed=21, temperature=temps)
+    forced = np.random.default_rng(22).integers(0, V, (B, K)).astype(np.int32)
+    tok, cache, gaps = orc.markov_sample(w.base, w.w1, w.w2, w.anchor, w.req_state_idx,
+                                         w.positions, w.temperature, w.seeds,
+                                         cache_bf16=cache_bf16, forced=forced)
+    w2 = wl.bf16_bits_to_f32(w.w2).astype(np.float64)
+    cols = np.arange(V, dtype=np.uint32)
+    for b in range(B):
+        T = np.float32(temps[b])
+        prev = int(w.anchor[b])
+        for i in range(K):
+            bias = (w2 @ wl.bf16_bits_to_f32(w.w1[prev]).astype(np.float64)).astype(np.float32)
+            z = (w.base[b, i] + bias).astype(np.float32)
+            x = (z / T).astype(np.float32) if T > 0 else z
+            got = cache[b, i]
+            if cache_bf16:
+                np.testing.assert_array_equal(got, _torch_bf16_bits(x))
+            else:
+                np.testing.assert_array_equal(got.view(np.uint32), x.view(np.uint32))
+            if T > 0:
+                _, _, g = orc.noise(w.seeds[b], w.positions[b] + i - 1, cols,
+                                    orc.STREAM_DRAFT)
+                y = (x + g).astype(np.float32)
+            else:
+                y = z
+            top2 = np.sort(y.astype(np.float64))[-2:]
+            assert tok[b, i] == int(np.argmax(y))
+            assert gaps[b, i] == top2[1] - top2[0]
+            prev = int(forced[b, i])
 
 
 # ----------------------------------------------------------------------------
@@ -607,6 +700,82 @@ def test_verifier_draws_use_documented_streams_and_positions(orc):
         assert tok == _flat_rule((logp + g).astype(np.float32))
 
 
+def _p64(xt, top_p):
+    """fp64 target distribution of one scaled row with the top-p keep set
+    taken by sorting (logit desc, id asc) and accumulating fp64 probabilities;
+    also the cumulative masses at the kept count n and at n - 1."""
+    pr = _softmax64(xt)
+    if top_p >= 1.0:
+        return pr, None
+    order = sorted(range(xt.size), key=lambda v: (-(xt[v] if not np.isnan(xt[v]) else -np.inf), v))
+    cum = np.cumsum(pr[order])
+    n = int(np.searchsorted(cum, top_p, side="left")) + 1
+    n = min(n, xt.size)
+    keep = np.zeros(xt.size, bool)
+    keep[order[:n]] = True
+    p = np.where(keep, pr, 0.0)
+    p /= p.sum()
+    return p, (cum[n - 1], cum[n - 2] if n >= 2 else 0.0)
+
+
+def test_verifier_exception_gates_against_fp64(orc):
+    """The three numbers that decide which GPU/oracle differences are excused,
+    recomputed directly in fp64 from the pinned noise: the accept margin
+    |u - p(d)/q(d)| of every ratio test made, the top-p boundary slack
+    min(|S_n - p|, |S_(n-1) - p|) of every target row used, and the top-two
+    gap of the draw that produced the last emitted token (residual max(0,
+    p - q), or p for the bonus). A gate that were always 0 (or taken on the
+    wrong row, stream or position) fails here; the oracle's decisions agree
+    with the fp64 ones wherever the fp64 margin or gap is clear of rounding."""
+    B, K, V = 48, 3, 400
+    temps = np.resize(np.array([1.0, 0.8, 1.25], np.float32), B)
+    topps = np.resize(np.array([1.0, 0.9, 0.7, 0.95], np.float32), B)
+    w = wl.custom(B, K, V, 32, seed=31, temperature=temps, top_p=topps, target_noise=0.8)
+    draft, cache, _ = orc.markov_sample(w.base, w.w1, w.w2, w.anchor, w.req_state_idx,
+                                        w.positions, w.temperature, w.seeds)
+    res = orc.rejection_sample(draft, cache, w.target, w.req_state_idx, w.positions,
+                               w.temperature, w.top_p, w.seeds)
+    cols = np.arange(V, dtype=np.uint32)
+    n_margin = n_slack = n_gap = 0
+    for b in range(B):
+        T, tp, seed, P0 = temps[b], float(topps[b]), w.seeds[b], int(w.positions[b])
+        emitted_row, weights = None, None
+        for k in range(K + 1):
+            xt = (w.target[b, k] / T).astype(np.float32)
+            p, cums = _p64(xt, tp)
+            sl = res["slack"][b, k]
+            if cums is not None and not np.isnan(sl):
+                slack64 = min(abs(cums[0] - tp), abs(cums[1] - tp))
+                assert abs(sl - slack64) < 1e-6, (b, k, sl, slack64)
+                n_slack += 1
+            if k == K:
+                emitted_row, weights = k, p
+                break
+            d = int(draft[b, k])
+            q = _softmax64(cache[b, k])
+            _, u, _ = orc.noise(seed, P0 + k - 1, 0, orc.STREAM_ACCEPT)
+            m64 = abs(float(u) - p[d] / q[d])
+            mo = res["margins"][b, k]
+            assert abs(mo - m64) <= 1e-6 + 1e-5 * m64, (b, k, mo, m64)
+            n_margin += 1
+            accepted = res["out_tokens"][b, k] == d and res["num_accepted"][b] > k
+            if m64 > 1e-5:
+                assert accepted == (float(u) * q[d] < p[d]), (b, k)
+            if not accepted:
+                emitted_row, weights = k, np.maximum(p - q, 0.0)
+                break
+        _, _, g = orc.noise(seed, P0 + emitted_row - 1, cols, orc.STREAM_TARGET)
+        with np.errstate(divide="ignore"):
+            y = np.log(weights) + g.astype(np.float64)
+        top2 = np.sort(y)[-2:]
+        gap64 = top2[1] - top2[0]
+        assert abs(res["gaps"][b] - gap64) < 1e-4, (b, res["gaps"][b], gap64)
+        if gap64 > 1e-4:
+            assert res["out_tokens"][b, emitted_row] == int(np.argmax(y))
+        n_gap += 1
+    assert n_margin > 60 and n_slack > 40 and n_gap == B
+
+
 def test_rejection_padding_and_bounds(orc):
     w = wl.custom(3, 2, 100, 8, seed=6, rsi=[1, -1, 0], S=2)
     d = wl.random_drafts(w)
@@ -685,3 +854,28 @@ def test_topk_draws_follow_the_truncated_softmax(orc):
     p = np.exp(z[cand] - z[cand].max())
     counts = [(tok[:, 0] == c).sum() for c in cand]
     assert _chi2_pvalue(counts, p) > 1e-4
+
+
+def test_threaded_oracle_is_the_single_threaded_one():
+    """The OpenMP build of the oracle (requests on several host threads, the
+    CPU baseline's parallel leg) returns exactly what the single-threaded
+    build returns: tokens, cache, gaps, and every verifier output."""
+    import oracle as orc
+    orc.build()
+    if not os.path.exists(orc._OMP_PATH):
+        pytest.skip("gcc without OpenMP")
+    w = wl.custom(12, 3, 3001, 64, seed=41, temperature=[0.9, 1.0, 0.0, 1.2] * 3,
+                  top_p=[1.0, 0.9, 0.8] * 4, S=12)
+    args = (w.base, w.w1, w.w2, w.anchor, w.req_state_idx, w.positions, w.temperature,
+            w.seeds)
+    a = orc.markov_sample(*args)
+    b = orc.markov_sample(*args, threads=4)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    r1 = orc.rejection_sample(a[0], a[1], w.target, w.req_state_idx, w.positions,
+                              w.temperature, w.top_p, w.seeds)
+    r2 = orc.rejection_sample(a[0], a[1], w.target, w.req_state_idx, w.positions,
+                              w.temperature, w.top_p, w.seeds, threads=4)
+    for k in r1:
+        np.testing.assert_array_equal(r1[k], r2[k])
+    assert orc.threads_in_use(4) == 4
