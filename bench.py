@@ -210,8 +210,9 @@ def _subset(w, idx):
     return v
 
 
-def time_oracle(w, n_req: int):
-    """Seconds of the CPU oracle for n_req requests of w (loop + verify)."""
+def time_oracle(w, n_req: int, threads: int = 1):
+    """Seconds of the CPU oracle for the first n_req requests of w (loop,
+    verify), on `threads` host threads (OpenMP over requests when > 1)."""
     import oracle
     oracle.build()
     sub = _subset(w, list(range(n_req)))
@@ -219,12 +220,60 @@ def time_oracle(w, n_req: int):
     tok, cache, _ = oracle.markov_sample(sub.base, sub.w1, sub.w2, sub.anchor,
                                          sub.req_state_idx, sub.positions, sub.temperature,
                                          sub.seeds, cache_rows=w.C, cache_bf16=w.cache_bf16,
-                                         row_map=w.row_map)
+                                         row_map=w.row_map, threads=threads)
     t1 = time.perf_counter()
     oracle.rejection_sample(tok, cache, sub.target, sub.req_state_idx, sub.positions,
-                            sub.temperature, sub.top_p, sub.seeds, row_map=w.row_map)
+                            sub.temperature, sub.top_p, sub.seeds, row_map=w.row_map,
+                            threads=threads)
     t2 = time.perf_counter()
     return t1 - t0, t2 - t1
+
+
+def host_threads() -> int:
+    """The host cores this process may run on (nproc)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_threads() -> int:
+    """Threads the parallel oracle leg uses: every host core, if the OpenMP
+    build of the oracle exists, else 1."""
+    import oracle
+    n = host_threads()
+    try:
+        return oracle.threads_in_use(n)
+    except RuntimeError:
+        return 1
+
+
+def cpu_baseline(w, budget_s: float = 20.0):
+    """The oracle on the host cores: the parallel leg runs as many requests of
+    the batch as fit the time budget (the whole batch if it does) on every
+    core; the single-threaded leg runs request 0 alone, i.e. the workload at
+    batch 1. Both as µs per decode step."""
+    thr = oracle_threads()
+    a1, b1 = time_oracle(w, 1, 1)
+    one = (a1 + b1) * 1e6
+    # requests the parallel leg can afford: about `budget_s` of wall time
+    per_req_wall = (a1 + b1) / max(1, thr)
+    n_req = int(max(1, min(w.B, budget_s / max(per_req_wall, 1e-9))))
+    t0 = time.perf_counter()
+    a, b = time_oracle(w, n_req, thr)
+    wall = time.perf_counter() - t0
+    scale = w.B / n_req
+    return {"value": round((a + b) * scale * 1e6, 1), "unit": "us", "cores": thr,
+            "kind": "oracle", "nproc": host_threads(),
+            "sample": (f"{n_req} of {w.B} requests of one decode step (K-step loop + "
+                       f"verification), OpenMP over requests on {thr} host threads" +
+                       ("" if n_req == w.B else f", scaled by {w.B}/{n_req}")),
+            "measured_wall_s": round(wall, 3), "extrapolation": round(scale, 3),
+            "loop_us": round(a * scale * 1e6, 1), "verify_us": round(b * scale * 1e6, 1),
+            "single_thread": {"value": round(one, 1), "unit": "us", "cores": 1,
+                              "sample": "request 0 alone (the same workload at batch 1): "
+                                        "K-step loop + verification, measured, not scaled",
+                              "loop_us": round(a1 * 1e6, 1), "verify_us": round(b1 * 1e6, 1)}}
 
 
 def build_workload(args):
@@ -246,19 +295,36 @@ def max_over_ranks(value: float, world: int, device: str) -> float:
 
 
 def run_reference(args, rank, world):
-    """--impl reference: the CPU oracle on the host cores."""
+    """--impl reference: the CPU oracle on the host cores (OpenMP over the
+    requests on every core). Each step runs as many requests of the batch as
+    keep the whole --warmup + --steps run within about two minutes -- the
+    whole batch when they fit -- and the line says how many and by what
+    factor the time was scaled."""
     if rank != 0:
         return
     w = build_workload(args)
-    n_req = max(1, min(w.B, args.cpu_requests))
+    thr = oracle_threads()
+    # size the per-step sample from one timed request on all threads
+    a1, b1 = time_oracle(w, min(w.B, thr), thr)
+    per_req = (a1 + b1) / min(w.B, thr)
+    n_steps = max(1, args.steps) + max(0, args.warmup)
+    n_req = int(max(1, min(w.B, 120.0 / n_steps / max(per_req, 1e-9))))
+    for _ in range(max(0, args.warmup)):
+        time_oracle(w, n_req, thr)
     loops, vers = [], []
+    t0 = time.perf_counter()
     for _ in range(max(1, args.steps)):
-        a, b = time_oracle(w, n_req)
+        a, b = time_oracle(w, n_req, thr)
         loops.append(a)
         vers.append(b)
-    loop_us = statistics.median(loops) / n_req * w.B * 1e6
-    ver_us = statistics.median(vers) / n_req * w.B * 1e6
+    wall = time.perf_counter() - t0
+    scale = w.B / n_req
+    loop_us = statistics.mean(loops) * scale * 1e6
+    ver_us = statistics.mean(vers) * scale * 1e6
     val = loop_us + ver_us
+    sample = (f"{n_req} of {w.B} requests per step (K-step loop + verification), OpenMP "
+              f"over requests on {thr} host threads" +
+              ("" if n_req == w.B else f", scaled by {w.B}/{n_req}"))
     line = {
         "impl": "reference", "metric": METRIC, "value": round(val, 1), "unit": "us",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -266,9 +332,10 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": _config(w, args),
         "loop_us": round(loop_us, 1), "verify_us": round(ver_us, 1),
-        "cpu_baseline": {"value": round(val, 1), "unit": "us", "cores": 1, "kind": "oracle",
-                         "sample": f"{n_req} of {w.B} requests per step (whole K-step loop "
-                                   f"+ verification), scaled by {w.B}/{n_req}"},
+        "requests_per_step_measured": n_req, "extrapolation": round(scale, 3),
+        "measured_wall_s_timed_steps": round(wall, 3),
+        "cpu_baseline": {"value": round(val, 1), "unit": "us", "cores": thr, "kind": "oracle",
+                         "nproc": host_threads(), "sample": sample},
         "e2e": {"value": round(val, 1), "unit": "us", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -277,6 +344,7 @@ def run_reference(args, rank, world):
 
 def _config(w, args):
     topk = f", top-{args.draft_topk} Markov candidates" if args.draft_topk else ""
+    topk += ", draft-row statistics recorded by the loop" if args.draft_stats else ""
     return {"workload": f"{w.name}-like drafter: batch {w.B}, K={w.K}, vocab {w.V}, "
                         f"markov_rank {w.R}, {'bf16' if w.base_bf16 else 'fp32'} logits, "
                         f"{'bf16' if w.cache_bf16 else 'fp32'} draft cache{topk}",
@@ -294,7 +362,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     build.build()
     w = build_workload(args)
-    st = DecodeStep(w, draft_topk=args.draft_topk)
+    st = DecodeStep(w, draft_topk=args.draft_topk, draft_stats=args.draft_stats)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
@@ -437,17 +505,13 @@ def run_ours(args, rank, world, local):
                      "verify_frac": round(ver_bytes / (ver_us * 1e-6) / 1e9 / peak, 3)},
         "e2e": {"value": round(e2e_ms * 1e3, 1), "unit": "us", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        # the Markov loop (top-k: selection + loop), verify rows, verify resample
-        "gpu_launches": args.steps * (4 if args.draft_topk else 3),
+        # the Markov loop (top-k: candidate selection + loop) and the one
+        # verification kernel
+        "gpu_launches": args.steps * (3 if args.draft_topk else 2),
         "clocks": clk, "status": status, "wall_s_timed_region": round(wall, 4),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        n_req = max(1, min(w.B, args.cpu_requests))
-        a, b = time_oracle(w, n_req)
-        v = (a + b) / n_req * w.B * 1e6
-        line["cpu_baseline"] = {"value": round(v, 1), "unit": "us", "cores": 1, "kind": "oracle",
-                                "sample": f"{n_req} of {w.B} requests (whole K-step loop + "
-                                          f"verification), scaled by {w.B}/{n_req}"}
+        line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -485,10 +549,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="minimax")
     ap.add_argument("--batch", type=int, default=32)
-    ap.add_argument("--cpu-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--draft-topk", type=int, default=0,
                     help="time the top-k variant of the Markov loop (0: the dense loop)")
+    ap.add_argument("--draft-stats", action="store_true",
+                    help="the Markov loop records each draft row's maximum and exp-mass "
+                         "and the verifier uses them instead of reading the rows")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

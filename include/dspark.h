@@ -78,12 +78,21 @@ typedef enum {
                                    array of dspark_markov_sample_static    */
 } dspark_status;
 
-/* Statistics of one draft-logits cache row (one request, one draft step):
- * m = the maximum of the row's stored values (NaN read as -inf; for a bf16
- * cache the stored bf16 value). Exact, whatever order it is taken in. */
+/* Statistics of one draft-logits cache row (one request, one draft step),
+ * recorded by dspark_markov_sample while it writes the row:
+ *   m     the maximum of the row's stored values (NaN read as -inf; for a
+ *         bf16 cache the stored bf16 value); exact, whatever order it is
+ *         taken in. NaN: not recorded.
+ *   mass  the row's exp-mass sum_v exp(x_v - m) in 64-bit fixed point
+ *         (2^40 per unit): each CTA of the loop sums its part of the row in
+ *         fp32 (a fixed order) and adds it, rescaled to m and rounded to an
+ *         integer, with an integer atomic, so the total does not depend on
+ *         the order of the additions. 0 for a row with no value above -inf.
+ * dspark_rejection_sample uses them in place of reading the row. */
 typedef struct {
   float m;
-  uint32_t scratch; /* used by dspark_markov_sample while it runs */
+  uint32_t scratch;  /* used by dspark_markov_sample while it runs */
+  uint64_t mass;
 } dspark_row_stats;
 
 /* Limits checked on the host. */
@@ -101,7 +110,8 @@ typedef struct {
  *   e      = markov_w1[prev, :]                        (Markov embedding)
  *   bias_v = sum_r markov_w2[v, r] * e[r]              (fp32 accumulation)
  *   z_v    = base_logits[b, i, v] + bias_v             (fp32)
- *   T = temperature[s] > 0:  x_v = z_v / T (IEEE), y_v = x_v + g_v with g the
+ *   T = temperature[s] > 0:  x_v = z_v / T (IEEE division, correctly
+ *       rounded; T = 1 leaves z_v as it is), y_v = x_v + g_v with g the
  *       Gumbel noise of (seeds[s], positions[b] + i - 1, v, draft stream)
  *   otherwise (greedy):      x_v = y_v = z_v
  *   out_tokens[b, i] = lowest-index NaN of y if any, else the lowest index of
@@ -126,11 +136,11 @@ typedef struct {
  *   cache_row_map [S] int32 in [0, C), or NULL for row = slot
  *   out_tokens    [B, K] int32   (written)
  *   draft_stats   [B, K] dspark_row_stats, or NULL: if given (and cache is
- *                 not NULL), the maximum of every cache row the call writes,
- *                 so that dspark_rejection_sample can skip its own pass for
- *                 it (padding requests: zero; B > 64: NaN, "not recorded").
- *                 No counterpart in the pages: the loop has every value of
- *                 the row at hand.
+ *                 not NULL), the maximum and exp-mass of every cache row the
+ *                 call writes, so that dspark_rejection_sample need not read
+ *                 the row (padding requests: zero; B > 64: m = NaN, "not
+ *                 recorded"). No counterpart in the pages: the loop has every
+ *                 value of the row at hand.
  *   B in [0, 256], K in [1, 16], V in [1, 2^22), R a multiple of 64 up to
  *   512, S >= 1, C >= 1 if cache != NULL.
  *   workspace     device scratch of at least dspark_markov_workspace_bytes()
@@ -201,10 +211,14 @@ dspark_status dspark_markov_sample_topk(
  *           on the host with DSPARK_ERR_SCRATCH_LIMIT before anything runs.
  *           32 KiB holds B * K <= 4095: every batch up to 256 requests with up
  *           to 15 draft steps, or up to 255 requests with 16.
- * Set-up.   The first call on a device looks up the array's device address
- *           (cudaGetSymbolAddress, with that device current) and keeps it;
- *           a failure returns DSPARK_ERR_CUDA. Make that first call on each
- *           device before any stream capture begins.
+ * Checks.   The argument checks of dspark_markov_sample come first, in its
+ *           order and with its codes; the scratch limit after them.
+ * Set-up.   Every call looks up the array's address on the current device
+ *           (cudaGetSymbolAddress, with that device current; a failure
+ *           returns DSPARK_ERR_CUDA), so a device reset that reloads the
+ *           library's module elsewhere leaves no stale address behind. The
+ *           first call on a device may load the module: make it before any
+ *           stream capture begins.
  * Sharing.  Every call on a device uses the same array, which keeps what the
  *           last call left there. The part that must start at zero (the
  *           kernel's arrival counter) is cleared on `stream` by each call;
@@ -258,11 +272,12 @@ dspark_status dspark_markov_sample_static(
  *   draft_tokens  [B, K] int32 in [0, V) or -1
  *   draft_cache   [C, K, V] cache_dtype (may be NULL if every slot is greedy)
  *   cache_row_map [S] int32 or NULL (row = slot)
- *   draft_stats   [B, K] dspark_row_stats or NULL: the maxima that
- *                 dspark_markov_sample wrote for these cache rows; each draft
- *                 row with a recorded (non-NaN) maximum is then read once
- *                 (for its mass) instead of twice. They must describe the
- *                 cache passed here.
+ *   draft_stats   [B, K] dspark_row_stats or NULL: the statistics that
+ *                 dspark_markov_sample recorded for these cache rows; a draft
+ *                 row with recorded statistics (m not NaN) is then not read
+ *                 for its distribution: q = exp(x - m) / (fp32(mass) 2^-40),
+ *                 and only the row a residual draw needs is read. They must
+ *                 describe the cache passed here.
  *   target_logits [B, K+1, V] target_dtype
  *   req_state_idx [B], positions [B], temperature [S], top_p [S] fp32,
  *   seeds [S] as for dspark_markov_sample

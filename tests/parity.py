@@ -5,21 +5,36 @@ the oracle's top-two noised-value gap (drafter draws, resample, bonus) or its
 accept margin |u - p/q| is below 1e-5, or where the top-p boundary mass is
 within 1e-6 of p (the pages' own exception for the kept set); such cases are
 counted. fp32 cache values agree within abs 1e-4 + rel 1e-5 with NaN matching
-NaN; a bf16 cache within abs 1e-4 + one bf16 ulp (rel 2^-7 at the bottom
-of a binade).
+NaN; a bf16 cache to one bf16 ulp: both sides round their fp32 value to
+nearest even, and the fp32 values can differ in their last place only
+through the order of the bias sum, which moves a rounding by at most one
+bf16 step.
+
+Every counted exception is recorded in EXCEPTIONS (test, kind, count out of
+how many, the smallest gap or margin among them); the test suite prints the
+table at the end of the run.
 """
 from __future__ import annotations
+
+import os
 
 import numpy as np
 
 import oracle
+
+EXCEPTIONS: list[dict] = []
+
+
+def _record(kind, n_exc, n_total, smallest):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    EXCEPTIONS.append(dict(test=test, kind=kind, exceptions=int(n_exc), total=int(n_total),
+                           smallest=None if smallest is None else float(smallest)))
 
 GAP_TOL = 1e-5
 MARGIN_TOL = 1e-5
 SLACK_TOL = 1e-6
 CACHE_ATOL = 1e-4
 CACHE_RTOL = 1e-5
-BF16_RTOL = 2.0 ** -7
 
 
 def subset(w, idx):
@@ -43,6 +58,13 @@ def check_cache(gpu, ora, bf16, mask_rows=None):
         return _check_cache(gpu, ora, bf16)
 
 
+def bf16_order(bits):
+    """bf16 bit patterns -> integers in value order (-0 and +0 adjacent), so
+    that one rounding step apart is a difference of 1."""
+    b = np.asarray(bits, np.uint16).astype(np.int64)
+    return np.where(b & 0x8000, 0x7FFF - (b & 0x7FFF), 0x8000 + b)
+
+
 def _check_cache(gpu, ora, bf16):
     if bf16:
         gf = (gpu.astype(np.uint32) << 16).view(np.float32)
@@ -50,8 +72,20 @@ def _check_cache(gpu, ora, bf16):
         nan_g, nan_o = np.isnan(gf), np.isnan(of)
         assert (nan_g == nan_o).all(), "NaN positions differ in the bf16 cache"
         fin = ~nan_g
-        # bf16 rounding of the fp32 value: within abs 1e-4 + one bf16 ulp
-        np.testing.assert_allclose(gf[fin], of[fin], atol=CACHE_ATOL, rtol=BF16_RTOL)
+        # both round their fp32 value to nearest even, and the fp32 values
+        # differ only through the order of the bias sum (well below 1e-6):
+        # at most one bf16 step apart, or both within 1e-6 where the values
+        # are so small that one step is finer than that
+        steps = np.abs(bf16_order(gpu[fin]) - bf16_order(ora[fin]))
+        close = np.abs(gf[fin].astype(np.float64) - of[fin].astype(np.float64)) <= 1e-6
+        bad = (steps > 1) & ~close
+        assert not bad.any(), (
+            f"bf16 cache differs by {steps[bad].max()} rounding steps at "
+            f"{gf[fin][bad][:4]} vs {of[fin][bad][:4]}")
+        # only values next to a rounding boundary may land one step apart
+        # (a truncating side would differ on about half of them)
+        if steps.size >= 1000:
+            assert (steps != 0).mean() < 0.01, f"{(steps != 0).mean():.4f} of bf16 values differ"
         d = np.abs(gf[fin].astype(np.float64) - of[fin].astype(np.float64))
         d = d[np.isfinite(d)]
         return float(d.max()) if d.size else 0.0
@@ -81,6 +115,9 @@ def markov_parity(w, gpu_tokens, gpu_cache=None, check_cache_values=True, topk=0
         assert not bad.any(), (
             f"token mismatch beyond the near-tie rule at {np.argwhere(bad)[:5].tolist()}: "
             f"oracle {tok_o[bad][:5]}, gpu {gpu_tokens[bad][:5]}, gaps {gaps[bad][:5]}")
+    live = np.asarray(w.req_state_idx) >= 0
+    _record("draft token (gap < 1e-5)", exc, int(live.sum()) * tok_o.shape[1],
+            float(gaps[diff].min()) if exc else None)
     if gpu_cache is not None and check_cache_values:
         rows = sorted({int(w.row_map[s]) if w.row_map is not None else int(s)
                        for s in w.req_state_idx if s >= 0})
@@ -95,6 +132,7 @@ def verify_parity(w, draft, cache, gpu_out, gpu_nacc, max_exception_frac=0.02):
                                   w.temperature, w.top_p, w.seeds, row_map=w.row_map)
     out_o, nacc_o = res["out_tokens"], res["num_accepted"]
     exceptions = 0
+    smallest = None
     B, K1 = out_o.shape
     for b in range(B):
         if (out_o[b] == gpu_out[b]).all() and nacc_o[b] == gpu_nacc[b]:
@@ -105,16 +143,22 @@ def verify_parity(w, draft, cache, gpu_out, gpu_nacc, max_exception_frac=0.02):
         n = int(nacc_o[b])
         ok = False
         slack = res["slack"][b, j] if j < K1 else np.inf
+        gate = None
         if not np.isnan(slack) and slack < SLACK_TOL:
-            ok = True
+            ok, gate = True, slack
         elif j < n:
             # the oracle accepted draft j, the GPU did not
-            ok = res["margins"][b, j] < MARGIN_TOL
+            gate = res["margins"][b, j]
+            ok = gate < MARGIN_TOL
         elif j == n:
             if gpu_nacc[b] > n:
-                ok = res["margins"][b, j] < MARGIN_TOL   # GPU accepted, oracle rejected
+                gate = res["margins"][b, j]               # GPU accepted, oracle rejected
+                ok = gate < MARGIN_TOL
             else:
-                ok = res["gaps"][b] < GAP_TOL            # same count, different draw
+                gate = res["gaps"][b]                     # same count, different draw
+                ok = gate < GAP_TOL
+        if gate is not None:
+            smallest = gate if smallest is None else min(smallest, gate)
         assert ok, (f"request {b}: oracle {out_o[b].tolist()} (n={n}) vs gpu "
                     f"{gpu_out[b].tolist()} (n={int(gpu_nacc[b])}); margins "
                     f"{res['margins'][b].tolist()}, gap {res['gaps'][b]}, slack "
@@ -125,4 +169,6 @@ def verify_parity(w, draft, cache, gpu_out, gpu_nacc, max_exception_frac=0.02):
         m = int(gpu_nacc[b])
         assert (g[:m + 1] >= 0).all() and (g[:m + 1] < w.V).all() and (g[m + 1:] == -1).all()
     assert exceptions <= max(1, int(max_exception_frac * B)), f"{exceptions} exceptions in {B}"
+    live = int((np.asarray(w.req_state_idx) >= 0).sum())
+    _record("verified request (margin/gap < 1e-5, slack < 1e-6)", exceptions, live, smallest)
     return exceptions, res

@@ -1,5 +1,5 @@
 """The C ABI without a GPU: the library builds for sm_103a, loads, exports
-every function include/dspark.h declares, and its host-side argument checks
+every function include/*.h declares, and its host-side argument checks
 reject bad calls before touching the device."""
 import ctypes
 import os
@@ -11,7 +11,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _declared_functions():
-    src = open(os.path.join(ROOT, "include", "dspark.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc))
+                  if f.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(dspark_[a-z0-9_]+)\s*\(",
                        src, flags=re.M)
@@ -92,6 +94,24 @@ def test_argument_checks_return_before_any_launch(L):
     assert verify(B=0) == 0
     assert L.dspark_noise(fake, fake, fake, fake, null, null, null, -1, null) == -1
     assert L.dspark_noise(null, null, null, null, null, null, null, 0, null) == 0
+
+
+def test_wait_limit_hook_checks_its_knobs(L):
+    """The bounded-wait test hook takes limits from 0.1 ms to 2 s and at most
+    one extra arrival; everything else is checked as dspark_markov_sample."""
+    vp = ctypes.c_void_p
+    fake, null = vp(256), None
+    def hook(limit=1_000_000, extra=1, B=1, R=64, ws=fake):
+        return L.dspark_testing_markov_wait_limit(
+            fake, 0, fake, fake, fake, fake, fake, fake, fake, null, 0, null, fake, B, 1, 10, R,
+            1, 1, ws, 1 << 20, null, null, limit, extra)
+    assert hook(limit=10) == -1
+    assert hook(limit=3_000_000_000) == -1
+    assert hook(extra=2) == -1
+    assert hook(B=300) == -1
+    assert hook(R=100) == -2
+    assert hook(ws=null) == -6
+    assert hook(B=0) == 0
 
 
 def test_missing_library_fails_loudly(tmp_path):

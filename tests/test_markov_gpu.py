@@ -28,6 +28,99 @@ def test_tiny():
     assert markov_parity(w, tok, cache) == 0
 
 
+def _edge_values():
+    """fp32 values at the edges of bf16 rounding (halfway cases with an even
+    and an odd kept bit, one bit either side), fp32 subnormals, values that
+    round up to infinity, infinities and signed zeros."""
+    bits = []
+    for hi in (0x3F80, 0x3F81, 0x4123, 0xC0A1, 0x0001, 0x7F7E):
+        for lo in (0x8000, 0x7FFF, 0x8001):
+            bits.append((hi << 16) | lo)
+    bits += [0x00000001, 0x80000001, 0x007FFFFF, 0x7F7F7FFF, 0x7F7F8000, 0xFF7F8000,
+             0x7F800000, 0xFF800000, 0x00000000, 0x80000000]
+    return np.array(bits, np.uint32).view(np.float32)
+
+
+@pytest.mark.parametrize("base_bf16,cache_bf16", [(False, False), (False, True), (True, True)])
+def test_zero_bias_cache_is_bit_identical(base_bf16, cache_bf16):
+    """markov_w2 = 0 makes the bias exactly 0 on both sides, so the cached
+    value is fp32(base / T) with nothing left to round differently: the GPU
+    cache must equal the oracle's bit for bit at T = 1, 0.5, 0.7, 1.3 and 0
+    (IEEE division, nearest-even bf16), NaN where the oracle has NaN."""
+    temps = [1.0, 0.5, 0.7, 1.3, 0.0]
+    B, K, V, R = len(temps), 3, 4097, 64
+    w = wl.custom(B, K, V, R, seed=77, temperature=temps, base_bf16=False,
+                  cache_bf16=cache_bf16)
+    edge = _edge_values()
+    base = w.base.copy()
+    base[:, :, 1000:1000 + edge.size] = edge
+    base[2, 1, 3000] = np.nan
+    w.base = wl.f32_to_bf16_bits(base) if base_bf16 else base
+    w.w2 = np.zeros_like(w.w2)
+    st, tok, cache = run_markov(w)
+    assert st.status_code() == 0
+    import oracle
+    _, cache_o, _ = oracle.markov_sample(
+        w.base, w.w1, w.w2, w.anchor, w.req_state_idx, w.positions, w.temperature,
+        w.seeds, cache_rows=w.C, cache_bf16=cache_bf16, forced=tok)
+    if cache_bf16:
+        nan_g = np.isnan(wl.bf16_bits_to_f32(cache))
+        nan_o = np.isnan(wl.bf16_bits_to_f32(cache_o))
+    else:
+        nan_g, nan_o = np.isnan(cache), np.isnan(cache_o)
+    np.testing.assert_array_equal(nan_g, nan_o)
+    np.testing.assert_array_equal(cache[~nan_g], cache_o[~nan_o])
+    assert markov_parity(w, tok) <= 1
+
+
+def test_bounded_waits_run_out_and_the_next_call_is_clean():
+    """The grid barrier waits for one arrival more than the grid makes, with
+    every wait limited to 1 ms: each CTA's barrier wait runs out, then the
+    waits of its MMA and copy warps (whose next step never starts); the call
+    must end within a few limits with DSPARK_ERR_TIMEOUT in *status, and the
+    next normal call on the same stream and workspace must give exactly what
+    a fresh run gives (the pages' bounded exchange wait that raises on
+    timeout instead of hanging: vLLM PR #65007, Part 1)."""
+    import time
+    import torch
+    from verify_dspark_markov_step_gb300 import _lib
+    w = wl.make("tiny", with_target=False)
+    st, tok0, cache0 = run_markov(w)
+    assert st.status_code() == 0
+    stream = torch.cuda.Stream()
+    st.status.zero_()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        _lib.markov_sample_wait_limit(st.base, st.w1, st.w2, st.anchor, st.rsi, st.pos,
+                                      st.temperature, st.seeds, st.draft, 1_000_000, 1,
+                                      cache=st.cache, workspace_buf=st.ws_markov,
+                                      status=st.status, stream=stream)
+    stream.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert st.status_code() == -4, st.status_code()   # DSPARK_ERR_TIMEOUT
+    assert elapsed < 1.0, elapsed
+    # the same hook with the barrier left alone completes normally
+    st.status.zero_()
+    with torch.cuda.stream(stream):
+        _lib.markov_sample_wait_limit(st.base, st.w1, st.w2, st.anchor, st.rsi, st.pos,
+                                      st.temperature, st.seeds, st.draft, 1_000_000_000, 0,
+                                      cache=st.cache, workspace_buf=st.ws_markov,
+                                      status=st.status, stream=stream)
+    stream.synchronize()
+    assert st.status_code() == 0
+    np.testing.assert_array_equal(st.draft.cpu().numpy(), tok0)
+    # and the normal entry point after the timeout is bit-identical to before
+    st.draft.fill_(-7)
+    st.cache.zero_()
+    with torch.cuda.stream(stream):
+        st.markov(stream=stream)
+    stream.synchronize()
+    assert st.status_code() == 0
+    np.testing.assert_array_equal(st.draft.cpu().numpy(), tok0)
+    from verify_dspark_markov_step_gb300.step import to_numpy
+    np.testing.assert_array_equal(to_numpy(st.cache), cache0)
+
+
 def test_odd_vocab_nan_and_temperatures():
     w = wl.make("odd", with_target=False)
     st, tok, cache = run_markov(w)

@@ -38,14 +38,21 @@ def test_sizes_beyond_the_fixed_scratch_are_rejected_on_the_host():
     assert _lib.markov_workspace_bytes(256, 16, 200064, 256) > _lib.STATIC_SCRATCH_BYTES
     fake = ctypes.c_void_p(256)  # never dereferenced: every call below fails first
 
-    def call(B, V, K=7, R=256, S=1):
-        return L.dspark_markov_sample_static(fake, 0, fake, fake, fake, fake, fake, fake, fake,
+    def call(B, V, K=7, R=256, S=1, base=fake, bdt=0):
+        return L.dspark_markov_sample_static(base, bdt, fake, fake, fake, fake, fake, fake, fake,
                                              None, 0, None, fake, None, B, K, V, R, S, 1, None,
                                              None)
     assert call(256, 200064, K=16) == -8           # DSPARK_ERR_SCRATCH_LIMIT
     assert _lib.status_string(-8).startswith("sizes need more scratch")
-    assert call(-1, 1000) == -1                    # still an argument error first
+    # every argument check of dspark_markov_sample comes before the limit,
+    # with its own code, also on sizes the scratch could not hold
+    assert call(-1, 1000) == -1
     assert call(4, 1 << 22) == -1
+    assert call(256, 200064, K=16, bdt=7) == -1    # bad dtype
+    assert call(256, 200064, K=16, R=100) == -2    # unsupported markov_rank
+    assert call(256, 200064, K=16, base=None) == -1
+    assert call(256, 200064, K=16, base=ctypes.c_void_p(258)) == -7
+    assert call(0, 200064, K=16) == 0              # empty batch: nothing to do
 
 
 def _reference_and_static(w):

@@ -31,8 +31,10 @@ STATUS = {
     -8: "DSPARK_ERR_SCRATCH_LIMIT",
 }
 
-# Every symbol include/dspark.h declares.
+# Every symbol include/dspark.h and include/dspark_testing.h declare.
 EXPORTS = (
+    "dspark_testing_markov_wait_limit",
+    "dspark_testing_temperature_divide",
     "dspark_markov_workspace_bytes",
     "dspark_markov_sample",
     "dspark_markov_sample_static",
@@ -74,6 +76,12 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.dspark_markov_sample.restype = i32
         L.dspark_markov_sample.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp,
                                            vp, i32, i32, i32, i32, i32, i32, vp, sz, vp, vp]
+        L.dspark_testing_markov_wait_limit.restype = i32
+        L.dspark_testing_markov_wait_limit.argtypes = [
+            vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
+            vp, sz, vp, vp, ctypes.c_uint64, ctypes.c_uint32]
+        L.dspark_testing_temperature_divide.restype = i32
+        L.dspark_testing_temperature_divide.argtypes = [vp, vp, vp, i64, vp]
         L.dspark_markov_sample_static.restype = i32
         L.dspark_markov_sample_static.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                                   vp, vp, vp, i32, i32, i32, i32, i32, i32, vp,
@@ -150,18 +158,28 @@ def verify_workspace_bytes(B, K, V) -> int:
     return int(lib().dspark_verify_workspace_bytes(B, K, V))
 
 
+ROW_STATS_BYTES = 16  # sizeof(dspark_row_stats)
+
+
 def row_stats(B: int, K: int, device=None) -> torch.Tensor:
-    """A device buffer for [B, K] dspark_row_stats (8 bytes each: the row
-    maximum as fp32 in the low half)."""
-    return torch.zeros((B, K), dtype=torch.int64, device=device or "cuda")
+    """A device buffer for [B, K] dspark_row_stats (16 bytes each: the row
+    maximum as fp32 in the low word, a scratch word, the fixed-point mass)."""
+    return torch.zeros((B, K, 2), dtype=torch.int64, device=device or "cuda")
+
+
+def row_stats_fields(t: torch.Tensor):
+    """(m [B,K] fp32, mass [B,K] int64) of a row_stats buffer, on the host."""
+    a = t.cpu()
+    m = a[..., 0].to(torch.int64).bitwise_and(0xFFFFFFFF).to(torch.int32).view(torch.float32)
+    return m, a[..., 1]
 
 
 def _stats(t, B, K, name="draft_stats"):
     if t is None:
         return None
     _dev(t, name)
-    if t.numel() * t.element_size() != B * K * 8:
-        raise ValueError(f"{name} must hold [B, K] 8-byte records")
+    if t.numel() * t.element_size() != B * K * ROW_STATS_BYTES:
+        raise ValueError(f"{name} must hold [B, K] {ROW_STATS_BYTES}-byte records")
     return t
 
 
@@ -213,6 +231,39 @@ def markov_sample(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_id
         _ptr(out_tokens), _ptr(draft_stats), B, K, V, R, S, max(C, 1), _ptr(workspace_buf),
         workspace_buf.numel() * workspace_buf.element_size(), _ptr(status), _stream(stream))
     _check(code, "dspark_markov_sample")
+
+
+def markov_sample_wait_limit(base_logits, markov_w1, markov_w2, anchor_tokens, req_state_idx,
+                             positions, temperature, seeds, out_tokens, wait_limit_ns,
+                             barrier_extra, cache=None, cache_row_map=None, workspace_buf=None,
+                             status=None, stream=None):
+    """dspark_testing_markov_wait_limit (include/dspark_testing.h): the Markov
+    loop with its bounded waits shortened to wait_limit_ns and the grid
+    barrier waiting for barrier_extra arrivals more than the grid makes, so
+    that a test can make the waits run out."""
+    B, K, V = base_logits.shape
+    R = markov_w2.shape[1]
+    S = temperature.shape[0]
+    for t, n in ((base_logits, "base_logits"), (markov_w1, "markov_w1"),
+                 (markov_w2, "markov_w2"), (anchor_tokens, "anchor_tokens"),
+                 (req_state_idx, "req_state_idx"), (positions, "positions"),
+                 (temperature, "temperature"), (seeds, "seeds"), (out_tokens, "out_tokens")):
+        _dev(t, n)
+    C, cache_dt = 0, DSPARK_F32
+    if cache is not None:
+        _dev(cache, "cache", (torch.float32,) + _BF16_LIKE)
+        C, cache_dt = cache.shape[0], _logit_dtype(cache, "cache")
+    if workspace_buf is None:
+        workspace_buf = workspace(markov_workspace_bytes(B, K, V, R), base_logits.device)
+    _dev(status, "status", (torch.int32,))
+    code = lib().dspark_testing_markov_wait_limit(
+        _ptr(base_logits), _logit_dtype(base_logits, "base_logits"), _ptr(markov_w1),
+        _ptr(markov_w2), _ptr(anchor_tokens), _ptr(req_state_idx), _ptr(positions),
+        _ptr(temperature), _ptr(seeds), _ptr(cache), cache_dt, _ptr(cache_row_map),
+        _ptr(out_tokens), B, K, V, R, S, max(C, 1), _ptr(workspace_buf),
+        workspace_buf.numel() * workspace_buf.element_size(), _ptr(status), _stream(stream),
+        int(wait_limit_ns), int(barrier_extra))
+    _check(code, "dspark_testing_markov_wait_limit")
 
 
 # Bytes of the library's fixed scratch array (DSPARK_STATIC_SCRATCH_BYTES).
@@ -353,6 +404,18 @@ def rejection_sample(draft_tokens, draft_cache, target_logits, req_state_idx, po
         _ptr(out_tokens), _ptr(num_accepted), B, K, V, S, max(C, 1), _ptr(workspace_buf),
         workspace_buf.numel() * workspace_buf.element_size(), _ptr(status), _stream(stream))
     _check(code, "dspark_rejection_sample")
+
+
+def temperature_divide(z, T, x, stream=None):
+    """dspark_testing_temperature_divide on 1-D fp32 device tensors."""
+    n = z.numel()
+    for t, name in ((z, "z"), (T, "T"), (x, "x")):
+        _dev(t, name, (torch.float32,))
+        if t.numel() != n:
+            raise ValueError("arrays must have equal length")
+    _check(lib().dspark_testing_temperature_divide(_ptr(z), _ptr(T), _ptr(x), n,
+                                                   _stream(stream)),
+           "dspark_testing_temperature_divide")
 
 
 def noise(seed, pos, col, stream_word, word=None, u=None, g=None, stream=None):

@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "dspark.h"
+#include "dspark_testing.h"
 #include "kernels.h"
 
 namespace {
@@ -40,11 +41,12 @@ struct MarkovWs {
 };
 
 struct VerifyWs {
-  size_t counters, tstats, dstats, keys, anypos, cand, total;
+  size_t ctl, parts, tstats, dstats, keys, anypos, cand, total;
   VerifyWs(int B, int K, int V) {
     const int mc = dspark::verify_max_chunks(V);
-    counters = 0;
-    tstats = align_up(counters + static_cast<size_t>(B) * sizeof(unsigned int));
+    ctl = 0;
+    parts = align_up(ctl + dspark::verify_ctl_bytes(B, K));
+    tstats = align_up(parts + dspark::verify_parts_bytes(B, K, V));
     dstats = align_up(tstats + dspark::verify_tstats_bytes(B, K));
     keys = align_up(dstats + dspark::verify_dstats_bytes(B, K));
     anypos = align_up(keys + static_cast<size_t>(B) * mc * sizeof(unsigned long long));
@@ -70,13 +72,17 @@ size_t dspark_markov_workspace_bytes(int B, int K, int V, int R) {
   return MarkovWs(B, K).total;
 }
 
-dspark_status dspark_markov_sample(
-    const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
-    const uint16_t* markov_w2, const int32_t* anchor_tokens, const int32_t* req_state_idx,
-    const int64_t* positions, const float* temperature, const uint64_t* seeds, void* cache,
-    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens,
-    dspark_row_stats* draft_stats, int B, int K, int V, int R, int S, int C, void* workspace,
-    size_t workspace_bytes, int32_t* status, dspark_stream_t stream) {
+}  // extern "C"
+
+namespace dspark {
+
+dspark_status markov_sample_args(const void* base_logits, dspark_dtype base_dtype,
+                                 const uint16_t* markov_w1, const uint16_t* markov_w2,
+                                 const int32_t* anchor_tokens, const int32_t* req_state_idx,
+                                 const int64_t* positions, const float* temperature,
+                                 const uint64_t* seeds, const void* cache,
+                                 dspark_dtype cache_dtype, const int32_t* out_tokens, int B,
+                                 int K, int V, int R, int S, int C) {
   if (!sizes_ok(B, K, V, S) || R < 1) return DSPARK_ERR_INVALID_ARG;
   if (!valid_dtype(base_dtype) || !valid_dtype(cache_dtype)) return DSPARK_ERR_INVALID_ARG;
   if (R % 64 != 0 || R > 512) return DSPARK_ERR_UNSUPPORTED;
@@ -88,6 +94,27 @@ dspark_status dspark_markov_sample(
   if (!aligned16(base_logits) || !aligned16(markov_w1) || !aligned16(markov_w2) ||
       (cache && !aligned16(cache)))
     return DSPARK_ERR_ALIGNMENT;
+  return DSPARK_OK;
+}
+
+}  // namespace dspark
+
+namespace {
+
+// dspark_markov_sample with the bounded waits' limit and the grid barrier's
+// extra arrivals as parameters (see dspark_testing_markov_wait_limit).
+dspark_status markov_sample_run(
+    const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
+    const uint16_t* markov_w2, const int32_t* anchor_tokens, const int32_t* req_state_idx,
+    const int64_t* positions, const float* temperature, const uint64_t* seeds, void* cache,
+    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens,
+    dspark_row_stats* draft_stats, int B, int K, int V, int R, int S, int C, void* workspace,
+    size_t workspace_bytes, int32_t* status, dspark_stream_t stream,
+    unsigned long long wait_limit_ns, unsigned int barrier_extra) {
+  const dspark_status args = dspark::markov_sample_args(
+      base_logits, base_dtype, markov_w1, markov_w2, anchor_tokens, req_state_idx, positions,
+      temperature, seeds, cache, cache_dtype, out_tokens, B, K, V, R, S, C);
+  if (args != DSPARK_OK || B == 0) return args;
   const MarkovWs ws(B, K);
   if (!workspace || workspace_bytes < ws.total || !aligned16(workspace))
     return DSPARK_ERR_WORKSPACE;
@@ -119,6 +146,8 @@ dspark_status dspark_markov_sample(
   p.counter = reinterpret_cast<unsigned int*>(w + ws.counter);
   p.status = status;
   p.draft_stats = cache != nullptr ? draft_stats : nullptr;
+  p.wait_limit_ns = wait_limit_ns;
+  p.barrier_extra = barrier_extra;
   if (cudaMemsetAsync(w, 0, ws.cleared, st) != cudaSuccess) return DSPARK_ERR_CUDA;
   // the statistics' mass and order-key fields accumulate from zero
   if (p.draft_stats != nullptr &&
@@ -141,6 +170,42 @@ dspark_status dspark_markov_sample(
   if (dspark::launch_markov_loop_tc(p, tmap, bmap, plan, grid, st) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
+}
+
+// The shortest and longest wait limits the test hook accepts.
+constexpr unsigned long long kTestLimitMinNs = 100000ull;      // 0.1 ms
+constexpr unsigned long long kTestLimitMaxNs = dspark::kWaitLimitNs;
+
+}  // namespace
+
+extern "C" {
+
+dspark_status dspark_markov_sample(
+    const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
+    const uint16_t* markov_w2, const int32_t* anchor_tokens, const int32_t* req_state_idx,
+    const int64_t* positions, const float* temperature, const uint64_t* seeds, void* cache,
+    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens,
+    dspark_row_stats* draft_stats, int B, int K, int V, int R, int S, int C, void* workspace,
+    size_t workspace_bytes, int32_t* status, dspark_stream_t stream) {
+  return markov_sample_run(base_logits, base_dtype, markov_w1, markov_w2, anchor_tokens,
+                           req_state_idx, positions, temperature, seeds, cache, cache_dtype,
+                           cache_row_map, out_tokens, draft_stats, B, K, V, R, S, C, workspace,
+                           workspace_bytes, status, stream, dspark::kWaitLimitNs, 0u);
+}
+
+dspark_status dspark_testing_markov_wait_limit(
+    const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
+    const uint16_t* markov_w2, const int32_t* anchor_tokens, const int32_t* req_state_idx,
+    const int64_t* positions, const float* temperature, const uint64_t* seeds, void* cache,
+    dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens, int B, int K,
+    int V, int R, int S, int C, void* workspace, size_t workspace_bytes, int32_t* status,
+    dspark_stream_t stream, uint64_t wait_limit_ns, uint32_t barrier_extra) {
+  if (wait_limit_ns < kTestLimitMinNs || wait_limit_ns > kTestLimitMaxNs || barrier_extra > 1u)
+    return DSPARK_ERR_INVALID_ARG;
+  return markov_sample_run(base_logits, base_dtype, markov_w1, markov_w2, anchor_tokens,
+                           req_state_idx, positions, temperature, seeds, cache, cache_dtype,
+                           cache_row_map, out_tokens, nullptr, B, K, V, R, S, C, workspace,
+                           workspace_bytes, status, stream, wait_limit_ns, barrier_extra);
 }
 
 size_t dspark_markov_topk_workspace_bytes(int B, int K, int V, int R, int topk) {
@@ -231,8 +296,6 @@ dspark_status dspark_rejection_sample(
   const VerifyWs ws(B, K, V);
   if (!workspace || workspace_bytes < ws.total || !aligned16(workspace))
     return DSPARK_ERR_WORKSPACE;
-  int sms = 0;
-  if (num_sms_of_current_device(&sms) != 0) return DSPARK_ERR_CUDA;
   int cluster = 0, slice = 0;
   // fp32 unless both the target and the (present) cache are bf16
   const bool all_bf16 =
@@ -261,16 +324,21 @@ dspark_status dspark_rejection_sample(
   p.V = V;
   p.S = S;
   p.C = C;
-  p.counters = reinterpret_cast<unsigned int*>(w + ws.counters);
+  p.ctl = reinterpret_cast<unsigned int*>(w + ws.ctl);
+  p.parts = w + ws.parts;
+  p.nslice = dspark::verify_nslice(B, K, V);
   p.tstats = w + ws.tstats;
   p.dstats = w + ws.dstats;
   p.keys = reinterpret_cast<unsigned long long*>(w + ws.keys);
   p.anypos = reinterpret_cast<unsigned int*>(w + ws.anypos);
   p.cand = reinterpret_cast<uint2*>(w + ws.cand);
-  p.nchunk = dspark::verify_chunks(B, V, sms);
+  p.kstride = dspark::verify_max_chunks(V);
+  p.stats_items = draft_stats != nullptr && B <= dspark::kRowStatsMaxBatch;
+  p.ndraw = 1;  // chosen at launch from the grid
   p.status = status;
-  // (the draw kernel's per-request counters are zeroed by the row kernel,
-  // which runs before it on the stream)
+  // the work queue and the per-request counters start from zero
+  if (cudaMemsetAsync(w + ws.ctl, 0, dspark::verify_ctl_bytes(B, K), st) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   if (dspark::launch_verify(p, cluster, slice, st) != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
@@ -283,6 +351,17 @@ dspark_status dspark_noise(const uint64_t* seed, const int64_t* pos, const uint3
   if (!seed || !pos || !col || !stream) return DSPARK_ERR_INVALID_ARG;
   if (dspark::launch_noise(seed, pos, col, stream, word, u, g, n,
                            reinterpret_cast<cudaStream_t>(stream_handle)) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_testing_temperature_divide(const float* z, const float* T, float* x,
+                                                int64_t n, dspark_stream_t stream) {
+  if (n < 0) return DSPARK_ERR_INVALID_ARG;
+  if (n == 0) return DSPARK_OK;
+  if (!z || !T || !x) return DSPARK_ERR_INVALID_ARG;
+  if (dspark::launch_temperature_divide(z, T, x, n, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
     return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "dspark.h"
+#include "kernels.h"
 
 namespace dspark {
 
@@ -18,10 +19,6 @@ constexpr uint32_t kStreamAccept = 1u << 29;
 
 // One unit of exp-mass in the 64-bit fixed point of the top-p select.
 constexpr int kFixShift = 40;
-
-// Upper bound of any spin on an mbarrier or flag, in nanoseconds of
-// %globaltimer (about 2 s, like the pages' exchange timeout).
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
@@ -105,6 +102,47 @@ __device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsig
   unsigned long long d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+
+// ---- temperature: x = z / T, correctly rounded ------------------------------
+// For a column with T in [2^-30, 2^30] and r = rn(1/T) (correctly rounded
+// reciprocal), q = rn(z r) is within one ulp of z / T, the residual
+// z - q T is exact in one FMA, and rn(q + (z - q T) r) is the correctly
+// rounded quotient: Markstein's theorem (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990; also the FMA-division chapter of Muller et al.,
+// "Handbook of Floating-Point Arithmetic"). The theorem needs every
+// intermediate to stay normal, which |z| in [2^-60, 2^60] and T in
+// [2^-30, 2^30] guarantee; other z (zeros, infinities, NaN, tiny or huge
+// values) and columns whose T lies outside that range (`slow`) take the IEEE
+// division itself. Two columns at a time, in packed pairs; the bits are
+// those of z / T either way.
+__device__ __forceinline__ bool temp_div_fast_ok(float z) {
+  const float a = fabsf(z);
+  return a >= 0x1p-60f && a <= 0x1p60f;
+}
+__device__ __forceinline__ unsigned long long temp_div2(unsigned long long z,
+                                                        unsigned long long r,
+                                                        unsigned long long neg_t, bool slow) {
+  const unsigned long long q = f2_mul(z, r);
+  const unsigned long long e = f2_fma(q, neg_t, z);  // z - q T, exact
+  unsigned long long x = f2_fma(e, r, q);
+  float z0, z1;
+  f2_unpack(z, z0, z1);
+  const bool bad = slow || !temp_div_fast_ok(z0) || !temp_div_fast_ok(z1);
+  if (bad) {  // rare: this lane takes IEEE divisions
+    float x0, x1, t0, t1;
+    f2_unpack(x, x0, x1);
+    f2_unpack(neg_t, t0, t1);
+    if (slow || !temp_div_fast_ok(z0)) x0 = __fdiv_rn(z0, -t0);
+    if (slow || !temp_div_fast_ok(z1)) x1 = __fdiv_rn(z1, -t1);
+    x = f2_pack(x0, x1);
+  }
+  return x;
+}
+// T in the range where temp_div2's fast form holds.
+__device__ __forceinline__ bool temp_div_t_ok(float T) {
+  return T >= 0x1p-30f && T <= 0x1p30f;
 }
 
 // lg2.approx.f32: log2 with an absolute error of about 2^-22.6 on the
@@ -205,51 +243,6 @@ __device__ __forceinline__ float exp_rel(float x, float m) {
   return ex2_approx(__fmul_rn(__fsub_rn(x, m), kLog2e));
 }
 
-
-// Fixed-point mass rint(e * 2^40) of e in [0, 1], summed as two 32-bit
-// partials: vh = rint(e * 2^20) and f = e * 2^20 - vh (exact: the fraction
-// bits of e * 2^20, |f| <= 1/2), so rint(e * 2^40) = vh * 2^20 +
-// rint(f * 2^20). Both roundings are the add-1.5*2^23 trick inside one FMA
-// (the sum lands in [2^23, 2^24), where the spacing is 1, and the product is
-// exact), read back from the sum's mantissa bits. Neither partial overflows
-// while a thread adds fewer than 2^11 values.
-struct MassAcc {
-  uint32_t hi = 0u;  // sum of the bits of s = vh + magic
-  uint32_t lo = 0u;  // sum of the bits of r = rint(f * 2^20) + magic
-  uint32_t n = 0u;   // values added (each carried one magic)
-  static constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-  static constexpr uint32_t kMagicBits = 0x4B400000u;
-  __device__ __forceinline__ void add(float e) {
-    const float s = __fmaf_rn(e, 0x1p20f, kMagic);
-    const float vh = __fsub_rn(s, kMagic);
-    const float f = __fmaf_rn(e, 0x1p20f, -vh);
-    const float r = __fmaf_rn(f, 0x1p20f, kMagic);
-    hi += __float_as_uint(s);
-    lo += __float_as_uint(r);
-    n += 1u;
-  }
-  // Two values in packed pairs: the same operations lane by lane (-vh is
-  // formed as magic - s, exact like s - magic).
-  __device__ __forceinline__ void add2(unsigned long long e) {
-    const unsigned long long p20 = f2_pack(0x1p20f, 0x1p20f);
-    const unsigned long long mg = f2_pack(kMagic, kMagic);
-    const unsigned long long s = f2_fma(e, p20, mg);
-    const unsigned long long nvh = f2_sub(mg, s);
-    const unsigned long long f = f2_fma(e, p20, nvh);
-    const unsigned long long r = f2_fma(f, p20, mg);
-    hi += static_cast<uint32_t>(s) + static_cast<uint32_t>(s >> 32);
-    lo += static_cast<uint32_t>(r) + static_cast<uint32_t>(r >> 32);
-    n += 2u;
-  }
-  // Modulo 2^32 the magics come off exactly; the true partials fit while a
-  // thread adds fewer than 2^11 values.
-  __device__ __forceinline__ unsigned long long total() const {
-    const uint32_t h = hi - n * kMagicBits;
-    const int32_t l = static_cast<int32_t>(lo - n * kMagicBits);
-    return (static_cast<unsigned long long>(h) << 20) +
-           static_cast<unsigned long long>(static_cast<long long>(l));
-  }
-};
 
 // The same order key without branches: -0 becomes +0 by adding +0, every
 // NaN maps to the largest key.
@@ -389,15 +382,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t phas
 }
 
 // Waits for the phase with parity `phase` to complete. Returns false (and
-// records DSPARK_ERR_TIMEOUT) if it has not completed within kWaitLimitNs.
+// records DSPARK_ERR_TIMEOUT) if it has not completed within limit_ns
+// nanoseconds of %globaltimer.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase,
-                                          int32_t* status) {
+                                          int32_t* status,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, phase)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (;;) {
     for (int i = 0; i < 8; ++i)
       if (mbar_try_wait_sleep(bar, phase, 2000u)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       report(status, DSPARK_ERR_TIMEOUT);
       return false;
     }
@@ -407,6 +402,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase,
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 

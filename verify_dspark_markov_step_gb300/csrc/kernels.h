@@ -10,6 +10,10 @@
 
 namespace dspark {
 
+// Upper bound of any spin on an mbarrier or flag, in nanoseconds of
+// %globaltimer (about 2 s, like the pages' exchange timeout).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
 // The K-step Markov loop.
 struct MarkovStepParams {
   const void* base;
@@ -30,7 +34,28 @@ struct MarkovStepParams {
   dspark_row_stats* draft_stats; // [B][K] statistics of the cache rows written, or null (zeroed)
   unsigned int* counter;         // grid-barrier arrivals (zeroed before the launch)
   int32_t* status;
+  // Bounded waits: each mbarrier wait and the grid barrier give up after
+  // wait_limit_ns; the grid barrier waits for barrier_extra arrivals more
+  // than the grid makes (0 except in the bounded-wait test hook).
+  unsigned long long wait_limit_ns;
+  unsigned int barrier_extra;
 };
+
+// Host-side argument checks of dspark_markov_sample other than the workspace
+// (sizes, dtypes, markov_rank, null pointers, alignment), in its order.
+dspark_status markov_sample_args(const void* base_logits, dspark_dtype base_dtype,
+                                 const uint16_t* markov_w1, const uint16_t* markov_w2,
+                                 const int32_t* anchor_tokens, const int32_t* req_state_idx,
+                                 const int64_t* positions, const float* temperature,
+                                 const uint64_t* seeds, const void* cache,
+                                 dspark_dtype cache_dtype, const int32_t* out_tokens, int B,
+                                 int K, int V, int R, int S, int C);
+
+// The Markov loop records draft-row statistics (maximum and exp-mass) for
+// batches up to this size (8 request columns per epilogue warp, whose
+// running sums fit in registers); above it the statistics read "not
+// recorded" and the verifier reads the rows.
+constexpr int kRowStatsMaxBatch = 32;
 
 // Tensor-core variant (markov_tc.cu).
 struct MarkovTcPlan {
@@ -93,13 +118,27 @@ struct VerifyParams {
   int B, K, V, S, C;
   void* tstats;                  // [B][K+1] target-row statistics
   void* dstats;                  // [B][K] draft-row statistics
-  unsigned long long* keys;      // [B][nchunk] chunk winner keys
-  unsigned int* anypos;          // [B][nchunk] residual had a positive entry
-  unsigned int* counters;        // [B] finished chunks (self-resetting)
+  unsigned long long* keys;      // [B][kstride] winner key of each draw sub-chunk
+  unsigned int* anypos;          // [B][kstride] the sub-chunk had a positive weight
+  unsigned int* ctl;             // per-request and per-row progress, draw jobs (zeroed per call)
   uint2* cand;                   // [kVerifyMaxCtas][kVerifyListCap] top-p candidates (id, x bits)
-  int nchunk;
+  void* parts;                   // [B * (2K + 1)][nslice] per-slice row partials
+  int nslice;                    // slices per row in the flat kernel
+  int kstride;                   // chunk slots per request in keys / anypos
+  int ndraw;                     // draw chunks per request (set at launch)
+  int stats_items;               // draft_stats hold the loop's recorded statistics:
+                                 // a request's draft rows are one item, not read
   int32_t* status;
 };
+
+// VerifyParams::ctl: per request the rows finished and the draw chunks
+// finished, per row the slices finished (32-bit words, zeroed per call),
+// then one draw job per request (verify_draw.cuh).
+size_t verify_ctl_bytes(int B, int K);
+// Slices per row of the flat verification kernel, and the bytes of their
+// partials.
+int verify_nslice(int B, int K, int V);
+size_t verify_parts_bytes(int B, int K, int V);
 
 // Row-statistics CTAs that keep a top-p candidate list in the workspace, and
 // the list's capacity per CTA (a longer candidate set is swept instead).
@@ -109,11 +148,15 @@ constexpr int kVerifyListCap = 512;
 size_t verify_tstats_bytes(int B, int K);
 size_t verify_dstats_bytes(int B, int K);
 int verify_max_chunks(int V);
-int verify_chunks(int B, int V, int num_sms);
 size_t verify_rows_smem_bytes(int W);
 bool verify_rows_plan(int V, int es, int* CL, int* W);
-cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_t stream);
+// The whole verification in one persistent launch of thread-block clusters
+// (row statistics, the accept chain, the draws, the outputs).
 cudaError_t launch_verify(const VerifyParams& p, int CL, int W, cudaStream_t stream);
+
+// The drafter's temperature division on its own (a test hook; verify.cu).
+cudaError_t launch_temperature_divide(const float* z, const float* T, float* x, int64_t n,
+                                      cudaStream_t stream);
 
 // Noise generator on its own (api.cu / verify.cu).
 cudaError_t launch_noise(const uint64_t* seed, const int64_t* pos,

@@ -35,11 +35,14 @@
 //               each tile) and a fixed set of CPW batch columns. Per group of
 //               4 columns: one tcgen05.ld and one Philox block (a lane quad
 //               shares its 4 blocks by a 4x4 butterfly transpose); per pair of
-//               columns, in packed fp32 pairs: Gumbel noise, bias add,
-//               temperature (x = z * (1/T), within 1.5 ulp of z / T) and noise
-//               add; per column: cache store and the running winner -- per
-//               lane in registers across tiles when CPW <= 16, else reduced
-//               per tile with redux.sync.
+//               columns, in packed fp32 pairs: Gumbel noise, bias add and
+//               noise add; temperature x = z / T correctly rounded (an FMA
+//               correction of z * rn(1/T)), compiled into a second version of
+//               the tile loop that only warps holding a column with T other
+//               than 1 run (T = 1 and greedy columns keep x = z); per column:
+//               cache store and the running winner -- per lane in registers
+//               across tiles when CPW <= 16, else reduced per tile with
+//               redux.sync.
 // At the end of a step each CTA folds its winners into the step's global
 // winner keys (64-bit atomicMax), then a grid barrier (an arrival counter,
 // bounded wait) lets every CTA read the step's tokens, gather the next Markov
@@ -48,6 +51,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cfloat>
 #include <type_traits>
 
 #include "common.cuh"
@@ -84,15 +88,16 @@ __host__ __device__ inline size_t base_slot_stride(size_t base_stage) {
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 struct TcLayout {
-  size_t a, e, bases, xs, gs, seed, npos, bptr, cptr, cb0, prev, act, best, wkey, wx, bars, slot,
-      flags, total;
+  size_t a, e, bases, xs, gs, rcp, seed, npos, bptr, cptr, cb0, prev, act, best, wkey, wx, ws,
+      cm, cs, bars, slot, flags, total;
   __host__ __device__ TcLayout(int Npad, int NK, int ns, int nb, size_t base_stage) {
     a = 0;                                                       // markov_w2 ring
     e = a + static_cast<size_t>(ns) * kStageBytes;               // Markov embeddings
     bases = e + static_cast<size_t>(NK) * Npad * 128;            // staged base tiles
     xs = bases + static_cast<size_t>(nb) * base_slot_stride(base_stage);
     gs = xs + static_cast<size_t>(Npad) * 4;
-    seed = gs + static_cast<size_t>(Npad) * 4;                   // per request:
+    rcp = gs + static_cast<size_t>(Npad) * 4;
+    seed = rcp + static_cast<size_t>(Npad) * 4;                  // per request:
     npos = seed + static_cast<size_t>(Npad) * 8;                 //   noise position
     bptr = npos + static_cast<size_t>(Npad) * 8;                 //   base row of the step
     cptr = bptr + static_cast<size_t>(Npad) * 8;                 //   cache row of the step
@@ -101,8 +106,11 @@ struct TcLayout {
     act = prev + static_cast<size_t>(Npad) * 4;
     best = act + static_cast<size_t>(Npad) * 4;
     wkey = best + static_cast<size_t>(Npad) * 8;                 // per lane quarter: winner key,
-    wx = wkey + static_cast<size_t>(4 * Npad) * 8;               //   cache-row maximum key
-    bars = wx + static_cast<size_t>(4 * Npad) * 4;
+    wx = wkey + static_cast<size_t>(4 * Npad) * 8;               //   cache-row maximum key,
+    ws = wx + static_cast<size_t>(4 * Npad) * 4;                 //   its exp-sum
+    cm = ws + static_cast<size_t>(4 * Npad) * 4;                 // per request: the CTA's
+    cs = cm + static_cast<size_t>(Npad) * 4;                     //   row maximum key, exp-sum
+    bars = cs + static_cast<size_t>(Npad) * 4;
     slot = bars + static_cast<size_t>(2 * kMaxStages + 2 * kMaxAcc + 2 * kMaxBaseSlots + 2) * 8;
     flags = slot + 8;
     total = flags + 16 + 1024;  // + slack to align the base to 1024 B
@@ -268,7 +276,10 @@ __device__ __forceinline__ void tmem_load_group(uint32_t taddr, uint32_t (&r)[GW
   }
 }
 
-template <int CPW, bool kBaseBf16, bool kCacheBf16>  // CPW: batch columns per epilogue warp
+// CPW: batch columns per epilogue warp; kStats: record each cache row's
+// maximum and exp-mass (a separate instantiation, so that a loop without
+// them carries none of their registers or instructions)
+template <int CPW, bool kBaseBf16, bool kCacheBf16, bool kStats>
 __global__ void __launch_bounds__(kThreadsTc, 1)
 markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                       const __grid_constant__ CUtensorMap tmap_base, MarkovStepParams P,
@@ -286,22 +297,28 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   unsigned char* e_base = smem + L.e;
   unsigned char* base_s = smem + L.bases;  // nb staged base tiles [B][128]
   const size_t base_stride = base_slot_stride(cfg.base_stage_bytes);
-  float* s_xs = reinterpret_cast<float*>(smem + L.xs);  // x = z * xs: 1/T, or 1 (greedy)
+  float* s_xs = reinterpret_cast<float*>(smem + L.xs);  // x = z / xs: T, or 1 (T = 1, greedy)
   float* s_gs = reinterpret_cast<float*>(smem + L.gs);  // y = x + gs * g: 1, or 0 (greedy)
+  float* s_rcp = reinterpret_cast<float*>(smem + L.rcp);  // rn(1 / xs)
   uint64_t* s_seed = reinterpret_cast<uint64_t*>(smem + L.seed);
   int64_t* s_npos = reinterpret_cast<int64_t*>(smem + L.npos);      // P0 + step - 1
   const unsigned char** s_bptr = reinterpret_cast<const unsigned char**>(smem + L.bptr);
   unsigned char** s_cptr = reinterpret_cast<unsigned char**>(smem + L.cptr);  // null: no store
   unsigned char** s_cb0 = reinterpret_cast<unsigned char**>(smem + L.cb0);
-  // cache-row maxima are recorded by the register-winner epilogue (up to 64
-  // requests); wider batches report them unknown (NaN)
-  const bool want_stats = kRegWinners && P.draft_stats != nullptr;
+  // cache-row statistics are recorded by the register-winner epilogue (up to
+  // kRowStatsMaxBatch requests); wider batches report them unknown (NaN)
+  static_assert(!kStats || 4 * CPW <= kRowStatsMaxBatch, "row statistics batch limit");
+  constexpr bool kRowStats = kStats;
+  const bool want_stats = kStats && P.draft_stats != nullptr;
   int32_t* s_prev = reinterpret_cast<int32_t*>(smem + L.prev);
   int32_t* s_act = reinterpret_cast<int32_t*>(smem + L.act);        // request live
   unsigned long long* best = reinterpret_cast<unsigned long long*>(smem + L.best);
   // register-winner epilogue: one winner per (TMEM lane quarter, request)
   unsigned long long* s_wkey = reinterpret_cast<unsigned long long*>(smem + L.wkey);
   uint32_t* s_wx = reinterpret_cast<uint32_t*>(smem + L.wx);
+  float* s_ws = reinterpret_cast<float*>(smem + L.ws);
+  uint32_t* s_cm = reinterpret_cast<uint32_t*>(smem + L.cm);
+  float* s_cs = reinterpret_cast<float*>(smem + L.cs);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + kMaxStages;
   uint64_t* acc_full = empty + kMaxStages;
@@ -331,7 +348,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
   // ---- prologue: per-request state (thread n < Npad owns column n) -----------
   if (tid < Npad) {
     const int n = tid;
-    float xscale = 1.f, gscale = 0.f;
+    float tdiv = 1.f, gscale = 0.f;
     uint64_t seed = 0;
     int64_t npos = 0;
     const unsigned char* bp = nullptr;
@@ -356,7 +373,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         if (ok) {
           const float T = P.temperature[s];
           if (T > 0.f) {  // sampled; a greedy column keeps x = z and no noise
-            xscale = __frcp_rn(T);
+            tdiv = T;
             gscale = 1.f;
           }
           seed = P.seeds[s];
@@ -369,7 +386,8 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         }
       }
     }
-    s_xs[n] = xscale;
+    s_xs[n] = tdiv;
+    s_rcp[n] = __frcp_rn(tdiv);
     s_gs[n] = gscale;
     s_seed[n] = seed;
     s_npos[n] = npos;
@@ -447,7 +465,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         if (*fail_flag) break;
         const int t = it.t;
         for (int kc = 0; kc < NK; ++kc) {
-          if (!mbar_wait(&empty[stage], ph ^ 1u, P.status)) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u, P.status, P.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -464,7 +482,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       if (!ok) *fail_flag = 1;
       // every copy this CTA issued has landed before the CTA may exit
       for (int s2 = 0; s2 < ns; ++s2)
-        if (issued[s2] != 0xFFFFFFFFu) (void)mbar_wait(&full[s2], issued[s2], P.status);
+        if (issued[s2] != 0xFFFFFFFFu) (void)mbar_wait(&full[s2], issued[s2], P.status, P.wait_limit_ns);
     }
   } else if (warp == kBaseWarp) {
     // ---- TMA producer of the base logits: one [B] x 128 box per tile ------------
@@ -481,7 +499,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         const int t = it.t;
         const int bs = br.slot;
         const uint32_t bph = br.phase;
-        if (!mbar_wait(&bempty[bs], bph ^ 1u, P.status)) {
+        if (!mbar_wait(&bempty[bs], bph ^ 1u, P.status, P.wait_limit_ns)) {
           *fail_flag = 1;
           break;
         }
@@ -491,7 +509,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         last[bs] = bph;
       }
       for (int bs = 0; bs < nb; ++bs)
-        if (last[bs] != 0xFFFFFFFFu) (void)mbar_wait(&bfull[bs], last[bs], P.status);
+        if (last[bs] != 0xFFFFFFFFu) (void)mbar_wait(&bfull[bs], last[bs], P.status, P.wait_limit_ns);
     }
   } else if (warp == 1) {
     // ---- MMA issuer -------------------------------------------------------------
@@ -507,21 +525,21 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       for (int g = 0; g < n_iter && ok; ++g, it.next(), ar.next()) {
         if (*fail_flag) break;
         if (it.first()) {  // first tile of a step: wait for its embeddings
-          if (!mbar_wait(e_ready, static_cast<uint32_t>(it.step) & 1u, P.status)) {
+          if (!mbar_wait(e_ready, static_cast<uint32_t>(it.step) & 1u, P.status, P.wait_limit_ns)) {
             ok = false;
             break;
           }
           tc::fence_after_thread_sync();
         }
         const int ab = ar.slot;
-        if (!mbar_wait(&acc_empty[ab], ar.phase ^ 1u, P.status)) {
+        if (!mbar_wait(&acc_empty[ab], ar.phase ^ 1u, P.status, P.wait_limit_ns)) {
           ok = false;
           break;
         }
         tc::fence_after_thread_sync();
         const uint32_t d = tmem + static_cast<uint32_t>(ab * Npad);
         for (int kc = 0; kc < NK; ++kc) {
-          if (!mbar_wait(&full[stage], ph, P.status)) {
+          if (!mbar_wait(&full[stage], ph, P.status, P.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -545,7 +563,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       if (!ok) *fail_flag = 1;
       // every MMA this thread issued has completed before TMEM is freed
       tc::mma_commit(drain);
-      (void)mbar_wait(drain, 0u, P.status);
+      (void)mbar_wait(drain, 0u, P.status, P.wait_limit_ns);
     }
   } else {
     // ---- epilogue (warps 2..17) -----------------------------------------------
@@ -556,6 +574,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     const int c_live = min(CPW, B - c_begin);  // columns below B (may be <= 0)
     const int r = q * 32 + lane;     // this lane's row of a tile
     float run_xm[kRegWinners ? CPW : 1];  // running maximum of the stored values
+    float run_s[kRowStats ? CPW : 1];     // their sum of exp(x - run_xm), fp32
     uint32_t run_ord[kRegWinners ? CPW : 1];
     uint32_t run_v[kRegWinners ? CPW : 1];
 #pragma unroll
@@ -564,6 +583,9 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       run_v[j] = 0xFFFFFFFFu;
       run_xm[j] = -INFINITY;
     }
+#pragma unroll
+    for (int j = 0; j < (kRowStats ? CPW : 1); ++j) run_s[j] = 0.0f;
+    const unsigned long long l2e2 = f2_pack(kLog2e, kLog2e);
     // base logits straight from global memory (no staged tile)
     auto load_direct = [&](int cb, int v, bool in_range, float (&bv)[GW]) {
 #pragma unroll
@@ -588,6 +610,14 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         quad_transpose(nw + 4 * h);
       }
     };
+    // this warp's columns: does any divide by a temperature other than 1,
+    // and does any such temperature lie outside the fast division's range
+    bool wdiv = false, wslow = false;
+    for (int j = 0; j < CPW; ++j) {
+      const float T = s_xs[c_begin + j];
+      wdiv |= T != 1.f;
+      wslow |= T != 1.f && !temp_div_t_ok(T);
+    }
     bool skip = false;  // set after a failed wait: the warp then only walks the loop
     TileIter it(share, G);
     RingPos ar(na), br(tma_base ? nb : 1);
@@ -623,17 +653,18 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         }
       }
       if (!skip) {
-        bool ok = mbar_wait(&acc_full[ab], aph, P.status);
-        if (ok && tma_base) ok = mbar_wait(&bfull[bs], bph, P.status);
+        bool ok = mbar_wait(&acc_full[ab], aph, P.status, P.wait_limit_ns);
+        if (ok && tma_base) ok = mbar_wait(&bfull[bs], bph, P.status, P.wait_limit_ns);
         if (!ok) {
           *fail_flag = 1;
           skip = true;
         }
       }
       // One tile; kRev = the step walks its tiles backward (ties then go to
-      // the later, lower row).
-      auto tile = [&](auto rev_tag) {
+      // the later, lower row); kDiv = some column divides by T != 1.
+      auto tile = [&](auto rev_tag, auto div_tag) {
         constexpr bool kRev = decltype(rev_tag)::value;
+        constexpr bool kDiv = decltype(div_tag)::value;
         static_cast<void>(kRev);  // only the register winners depend on the order
         const unsigned char* sb = base_s + bs * base_stride;
 #pragma unroll
@@ -663,35 +694,48 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           }
           uint32_t nw[GW];
           noise_group(cb, v, nw);
-          float xsc[GW], gsc[GW];
+          float gsc[GW];
 #pragma unroll
           for (int h = 0; h < GW / 4; ++h) {
-            const float4 x4 = *reinterpret_cast<const float4*>(s_xs + cb + 4 * h);
             const float4 g4 = *reinterpret_cast<const float4*>(s_gs + cb + 4 * h);
-            xsc[4 * h + 0] = x4.x;
-            xsc[4 * h + 1] = x4.y;
-            xsc[4 * h + 2] = x4.z;
-            xsc[4 * h + 3] = x4.w;
             gsc[4 * h + 0] = g4.x;
             gsc[4 * h + 1] = g4.y;
             gsc[4 * h + 2] = g4.z;
             gsc[4 * h + 3] = g4.w;
           }
-          // z = base + bias, x = z / T (greedy: z), y = x + g (greedy: x),
-          // two columns at a time in packed fp32 pairs (fewer instructions and
-          // registers); padding columns (b >= B) compute values that are
-          // neither stored nor folded into a token
+          // z = base + bias, x = z / T (T = 1 and greedy: z), y = x + g
+          // (greedy: x), two columns at a time in packed fp32 pairs (fewer
+          // instructions and registers); padding columns (b >= B) compute
+          // values that are neither stored nor folded into a token
           float gv[GW];
 #pragma unroll
           for (int j = 0; j < GW; j += 2) gumbel_of2(nw[j], nw[j + 1], gv[j], gv[j + 1]);
           tc::tmem_wait_ld();
           float xv[GW], yv[GW];
+          float tq[GW], rq[GW];
+          if constexpr (kDiv) {
+#pragma unroll
+            for (int h = 0; h < GW / 4; ++h) {
+              const float4 t4 = *reinterpret_cast<const float4*>(s_xs + cb + 4 * h);
+              const float4 r4 = *reinterpret_cast<const float4*>(s_rcp + cb + 4 * h);
+              tq[4 * h + 0] = -t4.x;
+              tq[4 * h + 1] = -t4.y;
+              tq[4 * h + 2] = -t4.z;
+              tq[4 * h + 3] = -t4.w;
+              rq[4 * h + 0] = r4.x;
+              rq[4 * h + 1] = r4.y;
+              rq[4 * h + 2] = r4.z;
+              rq[4 * h + 3] = r4.w;
+            }
+          }
 #pragma unroll
           for (int j = 0; j < GW; j += 2) {
-            const unsigned long long z = f2_add(f2_pack(bv[j], bv[j + 1]),
-                                                f2_pack(__uint_as_float(acc[j]),
-                                                        __uint_as_float(acc[j + 1])));
-            const unsigned long long x = f2_mul(z, f2_pack(xsc[j], xsc[j + 1]));
+            unsigned long long x = f2_add(f2_pack(bv[j], bv[j + 1]),
+                                          f2_pack(__uint_as_float(acc[j]),
+                                                  __uint_as_float(acc[j + 1])));
+            // x = z / T (T = 1 and greedy columns: z / 1 = z)
+            if constexpr (kDiv)
+              x = temp_div2(x, f2_pack(rq[j], rq[j + 1]), f2_pack(tq[j], tq[j + 1]), wslow);
             const unsigned long long y =
                 f2_fma(f2_pack(gv[j], gv[j + 1]), f2_pack(gsc[j], gsc[j + 1]), x);
             f2_unpack(x, xv[j], xv[j + 1]);
@@ -712,8 +756,21 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
               st_pred(cp + v, x, cp != nullptr && in_range);
               xr = x;
             }
-            xr = in_range ? xr : -INFINITY;  // fmaxf below skips NaN, read as -inf
-            if constexpr (kRegWinners) run_xm[c + j] = fmaxf(run_xm[c + j], xr);
+            // the stored value, NaN and rows past V read as -inf
+            xr = in_range ? fmaxf(xr, -INFINITY) : -INFINITY;
+            if constexpr (kRowStats) {
+              // running maximum and exp-sum of the cache row's values this
+              // lane stores: both terms rescaled to the new maximum (the
+              // base is finite even for an all -inf start, so every exp of
+              // -inf is 0, never NaN)
+              const float nm = fmaxf(run_xm[c + j], xr);
+              const float base = fmaxf(nm, -FLT_MAX);
+              float ea, eb;
+              f2_unpack(f2_mul(f2_sub(f2_pack(run_xm[c + j], xr), f2_pack(base, base)), l2e2),
+                        ea, eb);
+              run_s[c + j] = __fmaf_rn(run_s[c + j], ex2_approx(ea), ex2_approx(eb));
+              run_xm[c + j] = nm;
+            }
             const uint32_t ord = in_range ? ordered_key(y) : 0u;  // real values map above 0
             if constexpr (kRegWinners) {
               // a lane's rows grow (shrink) across a forward (backward)
@@ -731,13 +788,16 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
       };
       if (!skip) {
         tc::fence_after_thread_sync();
-        if constexpr (kRegWinners) {
-          if (step & 1)
-            tile(std::true_type{});
+        if (wdiv) {
+          if (kRegWinners && (step & 1))
+            tile(std::true_type{}, std::true_type{});
           else
-            tile(std::false_type{});
+            tile(std::false_type{}, std::true_type{});
         } else {
-          tile(std::false_type{});
+          if (kRegWinners && (step & 1))
+            tile(std::true_type{}, std::false_type{});
+          else
+            tile(std::false_type{}, std::false_type{});
         }
         tc::fence_before_thread_sync();
         __syncwarp();
@@ -763,6 +823,23 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
 #pragma unroll
         for (int j = 0; j < CPW; ++j)
           xm[j] = want_stats ? __reduce_max_sync(0xFFFFFFFFu, ordered_key(run_xm[j])) : 0u;
+        // the warp's exp-sum of each column, rescaled to the warp's maximum
+        // (a butterfly of fp32 additions: lane 0's result is the same bits
+        // every run)
+        float xs_w[CPW];
+#pragma unroll
+        for (int j = 0; j < CPW; ++j) {
+          float t = 0.0f;
+          if constexpr (kRowStats) {
+            if (want_stats) {
+            const float mw = fmaxf(key_to_float(xm[j]), -FLT_MAX);
+            t = __fmul_rn(run_s[j], exp_rel(run_xm[j], mw));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xFFFFFFFFu, t, o));
+            }
+          }
+          xs_w[j] = t;
+        }
         if (lane == 0 && !skip) {
 #pragma unroll
           for (int j = 0; j < CPW; ++j) {
@@ -771,7 +848,10 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                   om[j] == 0u ? 0ull
                               : (static_cast<unsigned long long>(om[j]) << 32) |
                                     (0xFFFFFFFFu - vm[j]);
-              s_wx[q * Npad + c_begin + j] = xm[j];
+              if constexpr (kRowStats) {
+                s_wx[q * Npad + c_begin + j] = xm[j];
+                s_ws[q * Npad + c_begin + j] = xs_w[j];
+              }
             }
           }
         }
@@ -780,6 +860,7 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           run_ord[j] = 0u;
           run_v[j] = 0xFFFFFFFFu;
           run_xm[j] = -INFINITY;
+          if constexpr (kRowStats) run_s[j] = 0.0f;
         }
       }
       epi_bar();
@@ -791,16 +872,29 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         if constexpr (kRegWinners) {
           k = umax64(umax64(s_wkey[b], s_wkey[Npad + b]),
                      umax64(s_wkey[2 * Npad + b], s_wkey[3 * Npad + b]));
-          xk = max(max(s_wx[b], s_wx[Npad + b]), max(s_wx[2 * Npad + b], s_wx[3 * Npad + b]));
+          xk = kRowStats ? max(max(s_wx[b], s_wx[Npad + b]),
+                               max(s_wx[2 * Npad + b], s_wx[3 * Npad + b]))
+                         : 0u;
         } else {
           k = best[b];
           best[b] = 0ull;
           xk = 0u;
         }
         if (k != 0ull) atomicMax(keys + b, k);
-        // the cache row's maximum, as an order key in the scratch word
-        if (want_stats && s_cb0[b] != nullptr)
+        // the cache row's maximum, as an order key in the scratch word; the
+        // CTA's exp-sum of the row, rescaled to the CTA's maximum (lane
+        // quarters in a fixed order), kept for after the barrier
+        if (want_stats && s_cb0[b] != nullptr) {
           atomicMax(&P.draft_stats[static_cast<int64_t>(b) * K + step].scratch, xk);
+          const float mc = fmaxf(key_to_float(xk), -FLT_MAX);
+          float sc = 0.0f;
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            sc = __fadd_rn(sc, __fmul_rn(s_ws[qq * Npad + b],
+                                         exp_rel(key_to_float(s_wx[qq * Npad + b]), mc)));
+          s_cm[b] = xk;
+          s_cs[b] = sc;
+        }
       }
       epi_bar();
       if (etid == 0) {
@@ -810,14 +904,16 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           __threadfence();  // the block's key updates before its arrival
           atomicAdd(P.counter, 1u);
         }
-        // the last step's tokens are needed by CTA 0 alone
-        if (!stop && (!last || blockIdx.x == 0)) {
+        // the last step's tokens are needed by CTA 0 alone; its row
+        // maxima (for the exp-sums) by every CTA
+        if (!stop && (!last || blockIdx.x == 0 || want_stats)) {
           const unsigned int target =
-              static_cast<unsigned int>(step + 1) * static_cast<unsigned int>(G);
+              static_cast<unsigned int>(step + 1) * static_cast<unsigned int>(G) +
+              P.barrier_extra;
           const unsigned long long t0 = globaltimer_ns();
           while (ld_acquire_u32(P.counter) < target) {
             __nanosleep(32);
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > P.wait_limit_ns) {
               report(P.status, DSPARK_ERR_TIMEOUT);
               *fail_flag = 1;
               stop = 1;
@@ -829,7 +925,22 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
         *stop_word = stop;
       }
       epi_bar();
-      if (*stop_word || (last && blockIdx.x != 0)) break;  // uniform over the epilogue
+      if (*stop_word) break;  // uniform over the epilogue
+      if (want_stats) {
+        // every CTA has folded its maxima: add this CTA's exp-sum of each
+        // row, rescaled to the row's maximum, in fixed point (2^40 per
+        // unit); integer additions, so the total is the same in any order
+        for (int b = etid; b < B; b += kEpiThreads) {
+          if (s_cb0[b] == nullptr) continue;
+          dspark_row_stats* st = &P.draft_stats[static_cast<int64_t>(b) * K + step];
+          const float mg = fmaxf(key_to_float(__ldcg(&st->scratch)), -FLT_MAX);
+          const float part =
+              __fmul_rn(__fmul_rn(s_cs[b], exp_rel(key_to_float(s_cm[b]), mg)), 0x1p40f);
+          const unsigned long long f = __float2ull_rn(part);
+          if (f != 0ull) atomicAdd(reinterpret_cast<unsigned long long*>(&st->mass), f);
+        }
+      }
+      if (last && blockIdx.x != 0) break;  // uniform over the epilogue
       for (int b = etid; b < Npad; b += kEpiThreads) {
         int32_t tok = -1;
         if (b < B && s_act[b]) {
@@ -878,11 +989,11 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-template <int CPW, bool kBaseBf16, bool kCacheBf16>
+template <int CPW, bool kBaseBf16, bool kCacheBf16, bool kStats>
 cudaError_t launch_tc_cpw(const MarkovStepParams& p, const CUtensorMap& map,
                           const CUtensorMap& bmap, const MarkovTcPlan& plan, int grid,
                           cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(markov_loop_tc_kernel<CPW, kBaseBf16, kCacheBf16>,
+  cudaError_t err = cudaFuncSetAttribute(markov_loop_tc_kernel<CPW, kBaseBf16, kCacheBf16, kStats>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(plan.smem));
   if (err != cudaSuccess) return err;
@@ -905,20 +1016,21 @@ cudaError_t launch_tc_cpw(const MarkovStepParams& p, const CUtensorMap& map,
   attr[0].val.cooperative = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, markov_loop_tc_kernel<CPW, kBaseBf16, kCacheBf16>, map, bmap, p,
+  return cudaLaunchKernelEx(&lc, markov_loop_tc_kernel<CPW, kBaseBf16, kCacheBf16, kStats>, map,
+                            bmap, p,
                             cfg);
 }
 
-template <int CPW>
+template <int CPW, bool kStats>
 cudaError_t launch_tc_dtypes(const MarkovStepParams& p, const CUtensorMap& map,
                              const CUtensorMap& bmap, const MarkovTcPlan& plan, int grid,
                              cudaStream_t stream) {
   if (p.base_bf16) {
-    return p.cache_bf16 ? launch_tc_cpw<CPW, true, true>(p, map, bmap, plan, grid, stream)
-                        : launch_tc_cpw<CPW, true, false>(p, map, bmap, plan, grid, stream);
+    return p.cache_bf16 ? launch_tc_cpw<CPW, true, true, kStats>(p, map, bmap, plan, grid, stream)
+                        : launch_tc_cpw<CPW, true, false, kStats>(p, map, bmap, plan, grid, stream);
   }
-  return p.cache_bf16 ? launch_tc_cpw<CPW, false, true>(p, map, bmap, plan, grid, stream)
-                      : launch_tc_cpw<CPW, false, false>(p, map, bmap, plan, grid, stream);
+  return p.cache_bf16 ? launch_tc_cpw<CPW, false, true, kStats>(p, map, bmap, plan, grid, stream)
+                      : launch_tc_cpw<CPW, false, false, kStats>(p, map, bmap, plan, grid, stream);
 }
 
 }  // namespace
@@ -1027,11 +1139,17 @@ cudaError_t launch_markov_loop_tc(const MarkovStepParams& p, const void* tmap, c
   const CUtensorMap& map = *static_cast<const CUtensorMap*>(tmap);
   const CUtensorMap& bm = *static_cast<const CUtensorMap*>(bmap);
   const int cpw = plan.Npad / 4;
-  if (cpw <= 4) return launch_tc_dtypes<4>(p, map, bm, plan, grid, stream);
-  if (cpw <= 8) return launch_tc_dtypes<8>(p, map, bm, plan, grid, stream);
-  if (cpw <= 16) return launch_tc_dtypes<16>(p, map, bm, plan, grid, stream);
-  if (cpw <= 32) return launch_tc_dtypes<32>(p, map, bm, plan, grid, stream);
-  return launch_tc_dtypes<64>(p, map, bm, plan, grid, stream);
+  // row statistics: asked for, and a batch the register epilogue records
+  const bool stats = p.draft_stats != nullptr && cpw <= kRowStatsMaxBatch / 4;
+  if (cpw <= 4)
+    return stats ? launch_tc_dtypes<4, true>(p, map, bm, plan, grid, stream)
+                 : launch_tc_dtypes<4, false>(p, map, bm, plan, grid, stream);
+  if (cpw <= 8)
+    return stats ? launch_tc_dtypes<8, true>(p, map, bm, plan, grid, stream)
+                 : launch_tc_dtypes<8, false>(p, map, bm, plan, grid, stream);
+  if (cpw <= 16) return launch_tc_dtypes<16, false>(p, map, bm, plan, grid, stream);
+  if (cpw <= 32) return launch_tc_dtypes<32, false>(p, map, bm, plan, grid, stream);
+  return launch_tc_dtypes<64, false>(p, map, bm, plan, grid, stream);
 }
 
 }  // namespace dspark

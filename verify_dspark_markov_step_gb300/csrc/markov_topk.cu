@@ -62,8 +62,12 @@ __global__ void __launch_bounds__(kTopkThreads) markov_topk_loop_kernel(TopkPara
     return;  // the whole cluster leaves: no cluster barrier follows
   }
   const float T = P.temperature[s];
-  const float xs = T > 0.f ? __frcp_rn(T) : 1.f;  // greedy: x = z
-  const float gs = T > 0.f ? 1.f : 0.f;           // greedy: no noise
+  const bool scaled = T > 0.f && T != 1.f;  // x = z / T (IEEE); T = 1 and greedy: x = z
+  const float gs = T > 0.f ? 1.f : 0.f;      // greedy: no noise
+  const float tdiv = scaled ? T : 1.f;
+  const unsigned long long r2 = f2_pack(__frcp_rn(tdiv), __frcp_rn(tdiv));
+  const unsigned long long nt2 = f2_pack(-tdiv, -tdiv);
+  const bool tslow = !temp_div_t_ok(tdiv);
   const uint64_t seed = P.seeds[s];
   const int64_t p0 = P.pos[b];
   const uint32_t neg_inf_key = ordered_key(-INFINITY);
@@ -118,9 +122,11 @@ __global__ void __launch_bounds__(kTopkThreads) markov_topk_loop_kernel(TopkPara
 #pragma unroll
       for (int o = kLanesPerCand / 2; o > 0; o >>= 1)
         acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+      // (every lane computes z and x; lane 0 of a candidate's group keeps them)
+      const float z = __fadd_rn(has ? cval[j] : 0.f, acc);
+      float x, x_unused;
+      f2_unpack(temp_div2(f2_pack(z, z), r2, nt2, tslow), x, x_unused);
       if (has && sl == 0) {
-        const float z = __fadd_rn(cval[j], acc);
-        const float x = __fmul_rn(z, xs);
         const U4 blk = noise_block(seed, p0 + i - 1, static_cast<uint32_t>(v), kStreamDraft);
         const float y =
             __fmaf_rn(gumbel_of(pick_word(blk, static_cast<uint32_t>(v) & 3u)), gs, x);

@@ -8,40 +8,14 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "dspark.h"
+#include "kernels.h"
 
 // The scratch: one per GPU that loads the library, alive until the process
 // exits. Host code must not hand this name to a kernel: on the host it only
 // stands for the symbol, and its device address comes from
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_markov_scratch[DSPARK_STATIC_SCRATCH_BYTES];
-
-namespace {
-
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices] = {};  // device address per device ordinal
-
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and remembered.
-dspark_status scratch_on_current_device(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return DSPARK_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_markov_scratch) != cudaSuccess || p == nullptr)
-      return DSPARK_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
-  return DSPARK_OK;
-}
-
-}  // namespace
 
 extern "C" dspark_status dspark_markov_sample_static(
     const void* base_logits, dspark_dtype base_dtype, const uint16_t* markov_w1,
@@ -50,17 +24,20 @@ extern "C" dspark_status dspark_markov_sample_static(
     dspark_dtype cache_dtype, const int32_t* cache_row_map, int32_t* out_tokens,
     dspark_row_stats* draft_stats, int B, int K, int V, int R, int S, int C, int32_t* status,
     dspark_stream_t stream) {
-  // sizes outside the documented ranges are argument errors, as for
-  // dspark_markov_sample; the scratch limit is checked next, and both before
-  // anything touches the device
-  if (B < 0 || B > DSPARK_MAX_BATCH || K < 1 || K > DSPARK_MAX_STEPS || V < 1 ||
-      V >= DSPARK_MAX_VOCAB || S < 1)
-    return DSPARK_ERR_INVALID_ARG;
+  // the argument checks of dspark_markov_sample, in its order, come first;
+  // then the scratch limit; both before anything touches the device
+  const dspark_status args = dspark::markov_sample_args(
+      base_logits, base_dtype, markov_w1, markov_w2, anchor_tokens, req_state_idx, positions,
+      temperature, seeds, cache, cache_dtype, out_tokens, B, K, V, R, S, C);
+  if (args != DSPARK_OK || B == 0) return args;
   if (dspark_markov_workspace_bytes(B, K, V, R) > DSPARK_STATIC_SCRATCH_BYTES)
     return DSPARK_ERR_SCRATCH_LIMIT;
+  // The array's address on the current device, looked up on every call (a
+  // host-side table lookup once the module is loaded): a cached address would
+  // go stale if the device were reset and the module loaded again elsewhere.
   void* scratch = nullptr;
-  const dspark_status rc = scratch_on_current_device(&scratch);
-  if (rc != DSPARK_OK) return rc;
+  if (cudaGetSymbolAddress(&scratch, g_markov_scratch) != cudaSuccess || scratch == nullptr)
+    return DSPARK_ERR_CUDA;
   // dspark_markov_sample clears the arrival counter on `stream` itself and
   // writes every other scratch word before reading it, so what an earlier
   // call left in the array does not matter.

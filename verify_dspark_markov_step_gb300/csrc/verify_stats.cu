@@ -35,6 +35,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "verify_common.cuh"
+#include "verify_draw.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -72,6 +73,7 @@ struct RowSmem {
   unsigned int c_max[2];         // ordered bits of the CTA maximum (~0: failed)
   unsigned long long c_sum[2];   // fixed-point mass
   unsigned long long c_key[2];   // greedy winner key
+  unsigned long long c_ms[2];    // online (max, sum) of the CTA's slice
   unsigned int w_u32[kRowWarps];
   unsigned long long w_u64[kRowWarps];
   // block-local scratch
@@ -445,12 +447,74 @@ __device__ __forceinline__ void row_sweep_t(RowView rv, uint64_t pol, Fix fix, B
   }
 }
 
-// As row_sweep, with the values of each aligned group of four handed to
-// quad(x[4]) together (for packed pair arithmetic) and the rest to single(x).
-template <int kU, bool kBf16, class Fix, class Quad, class Single>
-__device__ __forceinline__ void row_sweep_quads_t(RowView rv, uint64_t pol, Fix fix, Quad quad,
-                                                  Single single) {
+// ---- rows kept whole: one pass, a deterministic fp32 online softmax sum -----
+// (max m, s = sum of exp(x - m)) of the values a thread saw, in a fixed
+// order; two such pairs combine into the pair of their union. The combine is
+// commutative (fmaxf, and one fp32 addition of two products), so the
+// butterfly reductions below give the same bits in every lane and every run.
+__device__ __forceinline__ unsigned long long ms_pack(float m, float s) {
+  return (static_cast<unsigned long long>(__float_as_uint(s)) << 32) | __float_as_uint(m);
+}
+__device__ __forceinline__ float ms_m(unsigned long long v) {
+  return __uint_as_float(static_cast<uint32_t>(v));
+}
+__device__ __forceinline__ float ms_s(unsigned long long v) {
+  return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+// exp2 of (a - base) * log2(e) with base = 0 when the maximum is -inf (then
+// every term is exp(-inf) = 0 rather than NaN)
+__device__ __forceinline__ float ms_base(float m) { return m == -INFINITY ? 0.0f : m; }
+__device__ __forceinline__ unsigned long long ms_combine(unsigned long long a,
+                                                         unsigned long long b) {
+  const float m = fmaxf(ms_m(a), ms_m(b));
+  const float base = ms_base(m);
+  const float s = __fadd_rn(__fmul_rn(ms_s(a), exp_rel(ms_m(a), base)),
+                            __fmul_rn(ms_s(b), exp_rel(ms_m(b), base)));
+  return ms_pack(m, s);
+}
+
+// One pass over the slice: per thread, chunks of up to kU x 4 values take
+// one rescale of the running sum to the chunk's new maximum and one ex2 per
+// value. known_m: the row maximum is known (recorded by the Markov loop), so
+// no rescale is needed. Returns this thread's (m, s).
+// Thread 0 keeps the slice's next pf_window bytes on their way into L2
+// (cp.async.bulk.prefetch.L2), so that far more of the slice is in flight
+// than the threads' own loads; a window rather than the whole slice keeps
+// the bytes in flight over all CTAs well inside L2.
+struct L2Window {
+  uintptr_t base, end;  // the slice's bytes
+  uintptr_t done;       // prefetched up to here
+  uint32_t window;
+  __device__ L2Window(const void* p, size_t bytes, uint32_t w)
+      : base(reinterpret_cast<uintptr_t>(p)), end(reinterpret_cast<uintptr_t>(p) + bytes),
+        done(reinterpret_cast<uintptr_t>(p) & ~static_cast<uintptr_t>(15)), window(w) {}
+  // the threads have reached byte offset `at` of the slice
+  __device__ __forceinline__ void advance(size_t at) {
+    if (window == 0u) return;
+    uintptr_t want = base + at + window;
+    if (want > end) want = end;
+    want &= ~static_cast<uintptr_t>(15);
+    if (want > done + 4096u || (want == (end & ~static_cast<uintptr_t>(15)) && want > done)) {
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(done),
+                   "r"(static_cast<uint32_t>(want - done))
+                   : "memory");
+      done = want;
+    }
+  }
+};
+
+template <int kU, bool kBf16, class Fix>
+__device__ __forceinline__ unsigned long long slice_online_t(const RowView& rv, uint64_t pol,
+                                                             Fix fix, bool known, float known_m,
+                                                             uint32_t pf_window = 0u) {
   const int tid = threadIdx.x;
+  float m = known ? known_m : -INFINITY;
+  float s0 = 0.0f, s1 = 0.0f;
+  constexpr int kVecBytes = kBf16 ? 8 : 16;
+  L2Window pf(kBf16 ? static_cast<const void*>(rv.h) : static_cast<const void*>(rv.f),
+              static_cast<size_t>(rv.n) * (kBf16 ? 2 : 4), tid == 0 ? pf_window : 0u);
+  pf.advance(0);
+  const unsigned long long l2e = f2_pack(kLog2e, kLog2e);
   auto load4 = [&](int j, float (&v)[4]) {
     if constexpr (kBf16) {
       const uint2 w = ld_hint_u2(rv.h + 4 * j, pol);
@@ -466,58 +530,87 @@ __device__ __forceinline__ void row_sweep_quads_t(RowView rv, uint64_t pol, Fix 
       v[3] = c.w;
     }
   };
+  // the running sums follow the chunk's maximum; returns the subtraction base
+  auto rescale = [&](float cm) -> float {
+    if (known) return ms_base(m);
+    const float mn = fmaxf(m, cm);
+    const float base = ms_base(mn);
+    const float f = exp_rel(m, base);  // 1 if the maximum did not move
+    s0 = __fmul_rn(s0, f);
+    s1 = __fmul_rn(s1, f);
+    m = mn;
+    return base;
+  };
+  auto add4 = [&](const float (&v)[4], float base) {
+    const unsigned long long bb = f2_pack(base, base);
+    float a, b, c, d;
+    f2_unpack(f2_mul(f2_sub(f2_pack(v[0], v[1]), bb), l2e), a, b);
+    f2_unpack(f2_mul(f2_sub(f2_pack(v[2], v[3]), bb), l2e), c, d);
+    s0 = __fadd_rn(s0, ex2_approx(a));
+    s1 = __fadd_rn(s1, ex2_approx(b));
+    s0 = __fadd_rn(s0, ex2_approx(c));
+    s1 = __fadd_rn(s1, ex2_approx(d));
+  };
   int done = 0;
   if (rv.vec) {
     const int n4 = rv.n >> 2;
     int i = tid;
     for (; i + (kU - 1) * kRowThreads < n4; i += kU * kRowThreads) {
+      pf.advance(static_cast<size_t>(i + kU * kRowThreads) * kVecBytes);
       float v[kU][4];
 #pragma unroll
       for (int u = 0; u < kU; ++u) load4(i + u * kRowThreads, v[u]);
+      float cm = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
+      for (int u = 0; u < kU; ++u)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[u][e] = fix(v[u][e]);
-        quad(v[u]);
-      }
+        for (int e = 0; e < 4; ++e) {
+          v[u][e] = fix(v[u][e]);
+          cm = fmaxf(cm, v[u][e]);
+        }
+      const float base = rescale(cm);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) add4(v[u], base);
     }
     for (; i < n4; i += kRowThreads) {
       float v[4];
       load4(i, v);
+      float cm = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = fix(v[e]);
-      quad(v);
+      for (int e = 0; e < 4; ++e) {
+        v[e] = fix(v[e]);
+        cm = fmaxf(cm, v[e]);
+      }
+      add4(v, rescale(cm));
     }
     done = 4 * n4;
   }
   for (int i = done + tid; i < rv.n; i += kRowThreads) {
-    const float c = kBf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol))
-                          : ld_hint_f32(rv.f + i, pol);
-    single(fix(c));
+    const float x = fix(kBf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol))
+                              : ld_hint_f32(rv.f + i, pol));
+    const float base = rescale(x);
+    s0 = __fadd_rn(s0, exp_rel(x, base));
   }
+  return ms_pack(m, __fadd_rn(s0, s1));
 }
 
-// Fixed-point mass of the slice relative to m: exp(x - m) per value, four at
-// a time in packed pairs.
 template <class Fix>
-__device__ __forceinline__ unsigned long long slice_mass(const RowView& rv, uint64_t pol, Fix fix,
-                                                         float m) {
-  MassAcc acc;
-  const unsigned long long mm = f2_pack(m, m);
-  const unsigned long long l2e = f2_pack(kLog2e, kLog2e);
-  auto quad = [&](const float (&x)[4]) {
-    float a, b, c, d;
-    f2_unpack(f2_mul(f2_sub(f2_pack(x[0], x[1]), mm), l2e), a, b);
-    f2_unpack(f2_mul(f2_sub(f2_pack(x[2], x[3]), mm), l2e), c, d);
-    acc.add2(f2_pack(ex2_approx(a), ex2_approx(b)));
-    acc.add2(f2_pack(ex2_approx(c), ex2_approx(d)));
-  };
-  auto single = [&](float x) { acc.add(exp_rel(x, m)); };
-  if (rv.bf16)
-    row_sweep_quads_t<8, true>(rv, pol, fix, quad, single);
-  else
-    row_sweep_quads_t<8, false>(rv, pol, fix, quad, single);
-  return acc.total();
+__device__ __forceinline__ unsigned long long slice_online(const RowView& rv, uint64_t pol,
+                                                           Fix fix, bool known, float known_m,
+                                                           uint32_t pf_window = 0u) {
+  if (rv.bf16) return slice_online_t<4, true>(rv, pol, fix, known, known_m, pf_window);
+  return slice_online_t<4, false>(rv, pol, fix, known, known_m, pf_window);
+}
+
+// The (m, s) pair of the whole row: warps, then the CTA, then the cluster's
+// CTAs (each combine commutative, the order fixed).
+__device__ unsigned long long cluster_online(cg::cluster_group& cl, RowSmem& sm,
+                                             unsigned long long v, int set, int CL) {
+  return cluster_reduce<unsigned long long>(cl, sm, v, &sm.c_ms[set], &sm.bcast_u, CL,
+                                            ms_pack(-INFINITY, 0.0f),
+                                            [](unsigned long long a, unsigned long long b) {
+                                              return ms_combine(a, b);
+                                            });
 }
 
 // One row: statistics written to P.tstats / P.dstats. Every CTA of the
@@ -631,8 +724,16 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
                             ? P.draft_stats[static_cast<int64_t>(b) * K + k].m
                             : __int_as_float(0x7FC00000);
     float m;
-    if (m_rec == m_rec) {  // recorded (NaN: not recorded)
-      m = m_rec;
+    float s_keep = 0.0f;  // rows kept whole: sum of exp(x - m), one pass
+    if (!topp) {
+      // a draft row, or a target row without top-p: one pass from HBM gives
+      // the maximum and the sum together (or the sum alone, when the Markov
+      // loop recorded the maximum)
+      const bool known = m_rec == m_rec;  // NaN: not recorded
+      const unsigned long long ms =
+          cluster_online(cl, sm, slice_online(rv, pol_last_use, fix, known, m_rec), set, CL);
+      m = known ? m_rec : ms_m(ms);
+      s_keep = ms_s(ms);
     } else {
       float lmax = -INFINITY;
       row_sweep(rv, pol_keep, prescale, [&](int, float x) { lmax = fmaxf(lmax, x); });
@@ -659,26 +760,22 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
       return;
     }
 
-    // ---- pass 2 (L2): fixed-point mass (+ first top-p histogram) -----------------
-    if (topp) hist_clear(sm, kRowBins);
-    __syncthreads();
-    unsigned long long F = 0ull;
+    uint32_t kd_thr = 0u;
+    int32_t id_thr = 0;
+    unsigned long long Fk = 0ull;
+    int32_t mode = kModeKeepAll;
     if (topp) {
+      // ---- pass 2 (L2): fixed-point mass and the first top-p histogram ---------
+      hist_clear(sm, kRowBins);
+      __syncthreads();
+      unsigned long long F = 0ull;
       row_sweep<4>(rv, pol_keep, fix, [&](int, float x) {
         const unsigned long long f = fixed_mass(exp_rel(x, m));
         F += f;
         hist_add_mass(sm, adigit0(x, m), f);
       });
-    } else {
-      F = slice_mass(rv, pol_last_use, fix, m);
-    }
-    F = cluster_sum_u64(cl, sm, F, set, CL);
-
-    uint32_t kd_thr = 0u;
-    int32_t id_thr = 0;
-    unsigned long long Fk = F;
-    int32_t mode = kModeKeepAll;
-    if (topp) {
+      F = cluster_sum_u64(cl, sm, F, set, CL);
+      Fk = F;
       mode = kModeThreshold;
       const unsigned long long P32 = topp_scaled(P.top_p[s]);
       const unsigned long long t_lo = P32 * F;
@@ -779,7 +876,9 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
       Fk = above + f.mass;
       kd_thr = kd_of(fix(raw_at(id_thr)));
     }
-    const float D = __fmul_rn(__ull2float_rn(Fk), 0x1p-40f);
+    // the normaliser: the kept fixed-point mass of a top-p row, the fp32 sum
+    // of a row kept whole
+    const float D = topp ? __fmul_rn(__ull2float_rn(Fk), 0x1p-40f) : s_keep;
 
     // ---- outputs (rank 0): p or q at the drafted token, the row statistics --------
     if (rank == 0 && tid == 0) {
@@ -810,9 +909,47 @@ __device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluste
 }
 
 // ---------------------------------------------------------------------------
-// Persistent clusters: cluster c handles rows c, c + nclusters, ...
-__global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyParams P, int W,
-                                                                     int nrows) {
+// Verification, two launches.
+//
+// 1. verify_topp_kernel: persistent thread-block clusters over the target
+//    rows that take a top-p cut (sampled slot, top_p < 1), one cluster per
+//    row: the exact select above (process_row). A batch without such rows
+//    leaves at once.
+// 2. verify_flat_kernel: persistent CTAs (no clusters) over one work queue.
+//    Row items come in request order (request b: target rows 0..K, then
+//    draft rows 0..K-1), each row cut into `nslice` slices, one item per
+//    slice: a slice yields a partial (the online max and exp-sum, or the
+//    greedy winner key) and the CTA that finishes a row's last slice
+//    combines the partials in slice order (the same bits every run) into
+//    the row's statistics. The CTA that finishes a request's last row
+//    replays the request's accept chain (one thread per draft), writes the
+//    request's draw job and publishes `ndraw` draw items: column chunks of
+//    the one categorical the request needs. CTAs take published draw items
+//    before new rows, so a draw runs soon after its rows, beside other
+//    requests' rows; the CTA that finishes a request's last chunk writes the
+//    outputs. Each CTA's scheduler claims its next row at the start of the
+//    current item, so the claim's latency hides behind the item's work.
+//    Every wait is bounded.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const unsigned int* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Is target row (b, k) one the top-p kernel handles? (sampled, top_p < 1)
+__device__ __forceinline__ bool topp_row(const VerifyParams& P, int b) {
+  const int32_t s = P.rsi[b];
+  if (s < 0 || s >= P.S) return false;
+  return P.temperature[s] > 0.0f && P.top_p[s] < 1.0f;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 4) verify_topp_kernel(VerifyParams P, int W) {
   cg::cluster_group cl = cg::this_cluster();
   const int CL = static_cast<int>(cl.num_blocks());
   const int rank = static_cast<int>(cl.block_rank());
@@ -820,18 +957,473 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows_kernel(VerifyParam
   const int nclusters = gridDim.x / CL;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
-  // the draw kernel that follows counts its finished chunks per request here
-  if (blockIdx.x == 0)
-    for (int b = threadIdx.x; b < P.B; b += kRowThreads) P.counters[b] = 0u;
+  // a batch with no top-p row: every CTA sees the same answer and leaves
+  bool any = false;
+  for (int b = threadIdx.x; b < P.B; b += kRowThreads) any |= topp_row(P, b);
+  if (!__syncthreads_or(any)) return;
   int jrow = 0;
-  // odd clusters walk their rows backward: about half the clusters stream a
-  // draft row (one pass) while the others are on a target row (two passes)
-  const int nmine = nrows > cid ? (nrows - cid + nclusters - 1) / nclusters : 0;
-  const int first = (cid & 1) ? cid + (nmine - 1) * nclusters : cid;
-  const int stride = (cid & 1) ? -nclusters : nclusters;
-  for (int row = first; row >= cid && row < nrows; row += stride)
-    process_row(P, W, row, cl, CL, rank, sm, jrow);
+  const int nT = P.B * (P.K + 1);
+  for (int row = cid; row < nT; row += nclusters)
+    if (topp_row(P, row / (P.K + 1))) process_row(P, W, row, cl, CL, rank, sm, jrow);
   cl.sync();  // no CTA exits while another may still read its shared memory
+}
+
+// ---- the flat kernels ------------------------------------------------------
+struct RowPart {
+  float m;                   // online maximum of the slice
+  float s;                   // sum of exp(x - m) over the slice
+  unsigned long long key;    // greedy rows: the slice's winner key
+};
+
+struct CtlView {
+  unsigned int* rows_done;   // [B] rows finished per request
+  unsigned int* draws_done;  // [B] draw chunks finished per request
+  unsigned int* slices_done; // [B * (2K + 1)] slices finished per row
+  DrawJob* jobs;             // [B] what each request's draw needs
+  __device__ CtlView(unsigned int* c, int B, int K)
+      : rows_done(c), draws_done(c + B), slices_done(c + 2 * B),
+        jobs(reinterpret_cast<DrawJob*>(c + jobs_word(B, K))) {}
+  static __host__ __device__ size_t jobs_word(int B, int K) {
+    return (2 * static_cast<size_t>(B) + static_cast<size_t>(B) * (2 * K + 1) + 3) & ~size_t(3);
+  }
+};
+
+struct FlatSmem {
+  unsigned long long w_u64[kRowWarps];
+  int last;          // this CTA finished a row / a request / a draw
+  int bcast_i;
+  int acc[DSPARK_MAX_STEPS];  // the chain replay's per-draft outcome
+};
+
+// Outcome of draft k of request b (thread k of the CTA that finished the
+// request's rows): 1 accepted, 0 rejected, -1 placeholder, -2 out of range.
+__device__ int chain_step(const VerifyParams& P, int b, int k, bool greedy, uint64_t seed,
+                          int64_t P0) {
+  const int K = P.K, V = P.V;
+  const int32_t d = P.draft[static_cast<int64_t>(b) * K + k];
+  if (d == -1) return -1;
+  if (d < -1 || d >= V) return -2;
+  const TgtStats* ts = static_cast<const TgtStats*>(P.tstats) + static_cast<int64_t>(b) * (K + 1) + k;
+  if (greedy) return key_index(__ldcg(&ts->amax_key)) == d ? 1 : 0;
+  const DrfStats* ds = static_cast<const DrfStats*>(P.dstats) + static_cast<int64_t>(b) * K + k;
+  const U4 w = noise_block(seed, P0 + k - 1, 0u, kStreamAccept);
+  return __fmul_rn(uniform_of(w.x), __ldcg(&ds->q_d)) < __ldcg(&ts->p_d) ? 1 : 0;
+}
+
+__device__ __forceinline__ TgtStats ld_tstats(const TgtStats* p) {
+  TgtStats t;
+  t.m = __ldcg(&p->m);
+  t.D = __ldcg(&p->D);
+  t.kd_thr = __ldcg(&p->kd_thr);
+  t.id_thr = __ldcg(&p->id_thr);
+  t.p_d = __ldcg(&p->p_d);
+  t.mode = __ldcg(&p->mode);
+  t.amax_key = __ldcg(&p->amax_key);
+  return t;
+}
+__device__ __forceinline__ DrfStats ld_dstats(const DrfStats* p) {
+  DrfStats d;
+  d.m = __ldcg(&p->m);
+  d.D = __ldcg(&p->D);
+  d.q_d = __ldcg(&p->q_d);
+  d.zero = __ldcg(&p->zero);
+  return d;
+}
+
+// The whole CTA, after it finished a row of request b (that row's
+// statistics written): count the row; the request's last row replays the
+// accept chain (one thread per draft) and writes the request's draw job.
+__device__ void request_row_done(const VerifyParams& P, const CtlView& C, FlatSmem& sm, int b) {
+  const int tid = threadIdx.x, K = P.K;
+  __syncthreads();  // every thread's part of the row is written
+  if (tid == 0) {
+    __threadfence();  // the row's statistics before the count
+    sm.last = atomicAdd(&C.rows_done[b], 1u) + 1u == static_cast<unsigned int>(2 * K + 1);
+    if (sm.last) __threadfence();  // every row's statistics are visible from here on
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  const int32_t s = P.rsi[b];
+  const bool valid_slot = s >= 0 && s < P.S;
+  const float T = valid_slot ? P.temperature[s] : 0.0f;
+  const bool greedy = !(T > 0.0f);
+  const uint64_t seed = valid_slot ? P.seeds[s] : 0ull;
+  const int64_t P0 = P.pos[b];
+  if (valid_slot && tid < K) sm.acc[tid] = chain_step(P, b, tid, greedy, seed, P0);
+  __syncthreads();
+  if (tid == 0) {
+    DrawJob J;
+    J.b = b;
+    J.mode = kDrawNone;
+    J.row = 0;
+    J.invalid = 0;
+    J.crow = 0;
+    J.P0 = P0;
+    J.seed = seed;
+    J.T = T;
+    J.n_acc = 0;
+    J.emit = -1;
+    if (!valid_slot) {
+      J.invalid = 1;
+      if (s >= P.S) report(P.status, DSPARK_ERR_BOUNDS);
+    } else if (!greedy) {
+      if (P.cache == nullptr) {
+        J.invalid = 1;
+        report(P.status, DSPARK_ERR_INVALID_ARG);
+      } else {
+        J.crow = P.row_map ? P.row_map[s] : s;
+        if (J.crow < 0 || J.crow >= P.C) {
+          J.invalid = 1;
+          report(P.status, DSPARK_ERR_BOUNDS);
+        }
+      }
+    }
+    if (!J.invalid) {
+      int k = 0;
+      bool placeholder = false;
+      for (; k < K; ++k) {
+        const int a = sm.acc[k];
+        if (a == -2) {
+          J.invalid = 1;
+          report(P.status, DSPARK_ERR_BOUNDS);
+          break;
+        }
+        if (a == -1) placeholder = true;
+        if (a != 1) break;
+      }
+      if (!J.invalid) {
+        J.n_acc = k;
+        J.row = k;  // the row of the emitted token (K: the bonus row)
+        const TgtStats* tst =
+            static_cast<const TgtStats*>(P.tstats) + static_cast<int64_t>(b) * (K + 1);
+        if (greedy) {
+          J.emit = key_index(__ldcg(&tst[k].amax_key));
+        } else {
+          J.mode = (k < K && !placeholder) ? kDrawResidual : kDrawP;
+          J.ts = ld_tstats(tst + k);
+          if (J.mode == kDrawResidual)
+            J.ds = ld_dstats(static_cast<const DrfStats*>(P.dstats) +
+                             static_cast<int64_t>(b) * K + k);
+        }
+      }
+    }
+    C.jobs[b] = J;  // read by the draw kernel, which runs after this one
+  }
+}
+
+// What a row needs from the flat kernel.
+enum FlatRowKind : int {
+  kFlatNone = 0,       // nothing to compute (padding, greedy draft row, top-p row done before)
+  kFlatGreedy = 1,     // greedy target row: winner key of the raw row
+  kFlatOnline = 2,     // max and exp-sum of the row (sampled target row kept whole, draft row)
+  kFlatRecorded = 3    // draft row whose statistics the Markov loop recorded
+};
+struct FlatRow {
+  int kind;
+  int b, k;
+  bool is_target;
+  bool bf16;
+  float T;           // target rows: the temperature (1: none)
+  int64_t off;       // element offset of the row in its tensor
+  const void* base;
+};
+
+__device__ FlatRow classify_row(const VerifyParams& P, int b, int j) {
+  const int K = P.K;
+  FlatRow r;
+  r.kind = kFlatNone;
+  r.b = b;
+  r.is_target = j <= K;
+  r.k = r.is_target ? j : j - K - 1;
+  r.bf16 = false;
+  r.T = 1.0f;
+  r.off = 0;
+  r.base = nullptr;
+  const int32_t s = P.rsi[b];
+  if (s < 0 || s >= P.S) return r;
+  const float T = P.temperature[s];
+  const bool greedy = !(T > 0.0f);
+  if (r.is_target) {
+    if (!greedy && P.top_p[s] < 1.0f) return r;  // the top-p kernel's row
+    r.kind = greedy ? kFlatGreedy : kFlatOnline;
+    r.T = greedy ? 1.0f : T;
+    r.off = (static_cast<int64_t>(b) * (K + 1) + r.k) * P.V;
+    r.base = P.target;
+    r.bf16 = P.target_bf16 != 0;
+    return r;
+  }
+  if (greedy || P.cache == nullptr) return r;
+  const int64_t crow = P.row_map ? P.row_map[s] : s;
+  if (crow < 0 || crow >= P.C) return r;
+  r.kind = kFlatOnline;
+  if (P.stats_items) {
+    const float mrec = __ldcg(&P.draft_stats[static_cast<int64_t>(b) * K + r.k].m);
+    if (mrec == mrec) r.kind = kFlatRecorded;
+  }
+  r.off = (crow * K + r.k) * P.V;
+  r.base = P.cache;
+  r.bf16 = P.cache_bf16 != 0;
+  return r;
+}
+
+// Bytes of the L2 prefetch window a slice keeps ahead of its loads.
+constexpr uint32_t kSliceWindow = 48u << 10;
+
+// One slice of a row: this CTA's partial in P.parts.
+__device__ void flat_slice(const VerifyParams& P, const FlatRow& R, int s, FlatSmem& sm) {
+  const int V = P.V;
+  int sw = (V + P.nslice - 1) / P.nslice;
+  sw = (sw + 7) & ~7;
+  const int v0 = min(V, s * sw), v1 = min(V, v0 + sw);
+  RowView rv;
+  rv.bf16 = R.bf16;
+  rv.f = static_cast<const float*>(R.base) + R.off + v0;
+  rv.h = static_cast<const uint16_t*>(R.base) + R.off + v0;
+  rv.vec = R.bf16 ? (reinterpret_cast<uintptr_t>(rv.h) & 7u) == 0
+                  : (reinterpret_cast<uintptr_t>(rv.f) & 15u) == 0;
+  rv.n = v1 - v0;
+  // normal priority: a residual draw soon reads the rows of the request's
+  // first rejection again
+  const uint64_t pol = policy_evict_normal();
+  RowPart part;
+  part.m = -INFINITY;
+  part.s = 0.0f;
+  part.key = 0ull;
+  if (R.kind == kFlatGreedy) {
+    unsigned long long key = 0ull;
+    row_sweep(rv, pol, [](float c) { return c; }, [&](int i, float t) {
+      key = umax64(key, winner_key(t, static_cast<uint32_t>(v0 + i)));
+    });
+    part.key = block_reduce<unsigned long long>(
+        key, sm.w_u64, 0ull, [](unsigned long long a, unsigned long long b) { return a > b ? a : b; });
+  } else {
+    unsigned long long ms;
+    if (R.T != 1.0f) {
+      const float T = R.T;
+      ms = slice_online(rv, pol, [T](float c) { return fmaxf(__fdiv_rn(c, T), -INFINITY); }, false,
+                        0.0f, kSliceWindow);
+    } else {
+      ms = slice_online(rv, pol, [](float c) { return fmaxf(c, -INFINITY); }, false, 0.0f,
+                        kSliceWindow);
+    }
+    ms = block_reduce<unsigned long long>(ms, sm.w_u64, ms_pack(-INFINITY, 0.0f),
+                                          [](unsigned long long a, unsigned long long b) {
+                                            return ms_combine(a, b);
+                                          });
+    part.m = ms_m(ms);
+    part.s = ms_s(ms);
+  }
+  if (threadIdx.x == 0) {
+    const int row = R.is_target ? R.b * (P.K + 1) + R.k : P.B * (P.K + 1) + R.b * P.K + R.k;
+    reinterpret_cast<RowPart*>(P.parts)[static_cast<int64_t>(row) * P.nslice + s] = part;
+  }
+}
+
+// Warp 0, after every slice of the row is done: the row's statistics from
+// its partials (lane i holds slice i; a butterfly of commutative combines,
+// the same bits every run).
+__device__ void flat_finish_row(const VerifyParams& P, const FlatRow& R) {
+  const int K = P.K, V = P.V, lane = threadIdx.x & 31;
+  const int row = R.is_target ? R.b * (K + 1) + R.k : P.B * (K + 1) + R.b * K + R.k;
+  const RowPart* parts = reinterpret_cast<const RowPart*>(P.parts) + static_cast<int64_t>(row) * P.nslice;
+  const int32_t d = R.k < K ? P.draft[static_cast<int64_t>(R.b) * K + R.k] : -1;
+  const bool has_d = d >= 0 && d < V;
+  if (R.kind == kFlatGreedy) {
+    unsigned long long key = lane < P.nslice ? __ldcg(&parts[lane].key) : 0ull;
+    key = warp_max64(key);
+    if (lane == 0) {
+      TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(R.b) * (K + 1) + R.k;
+      ts->m = 0.f;
+      ts->D = 1.f;
+      ts->kd_thr = 0u;
+      ts->id_thr = 0;
+      ts->p_d = 0.f;
+      ts->mode = kModeGreedy;
+      ts->amax_key = key;
+    }
+    return;
+  }
+  float m = -INFINITY, s = 0.0f;
+  if (R.kind == kFlatRecorded) {
+    const dspark_row_stats* st = P.draft_stats + static_cast<int64_t>(R.b) * K + R.k;
+    m = __ldcg(&st->m);
+    const unsigned long long mass =
+        __ldcg(reinterpret_cast<const unsigned long long*>(&st->mass));
+    s = __fmul_rn(__ull2float_rn(mass), 0x1p-40f);
+  } else {
+    unsigned long long ms = lane < P.nslice ? ms_pack(__ldcg(&parts[lane].m), __ldcg(&parts[lane].s))
+                                            : ms_pack(-INFINITY, 0.0f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ms = ms_combine(ms, __shfl_xor_sync(0xFFFFFFFFu, ms, o));
+    m = ms_m(ms);
+    s = ms_s(ms);
+  }
+  if (lane != 0) return;
+  // the value at the drafted token, as the row's distribution reads it
+  float x = -INFINITY;
+  if (has_d) {
+    const int64_t o = R.off + d;
+    const float c = R.bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(R.base)[o])
+                           : static_cast<const float*>(R.base)[o];
+    x = R.is_target ? scale_logit(c, R.T) : fmaxf(c, -INFINITY);
+  }
+  if (R.is_target) {
+    TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(R.b) * (K + 1) + R.k;
+    ts->kd_thr = 0u;
+    ts->id_thr = 0;
+    ts->amax_key = 0ull;
+    if (m == -INFINITY) {  // no value above -inf: p is one-hot at column 0
+      ts->m = m;
+      ts->D = 1.0f;
+      ts->p_d = d == 0 ? 1.0f : 0.0f;
+      ts->mode = kModeOneHot;
+    } else {
+      ts->m = m;
+      ts->D = s;
+      ts->p_d = has_d ? __fdiv_rn(exp_rel(x, m), s) : 0.0f;
+      ts->mode = kModeKeepAll;
+    }
+  } else {
+    DrfStats* ds = static_cast<DrfStats*>(P.dstats) + static_cast<int64_t>(R.b) * K + R.k;
+    if (m == -INFINITY) {  // no value above -inf: q = 0
+      ds->m = m;
+      ds->D = 1.0f;
+      ds->q_d = 0.0f;
+      ds->zero = 1;
+    } else {
+      ds->m = m;
+      ds->D = s;
+      ds->q_d = has_d ? __fdiv_rn(exp_rel(x, m), s) : 0.0f;
+      ds->zero = 0;
+    }
+  }
+}
+
+// One row item r = (request, row, slice).
+__device__ void flat_row_item(const VerifyParams& P, const CtlView& C, FlatSmem& sm, int r) {
+  const int per_req = 2 * P.K + 1;
+  const int s = r % P.nslice;
+  const int rr = r / P.nslice;
+  const int b = rr / per_req, j = rr % per_req;
+  const FlatRow R = classify_row(P, b, j);
+  bool row_complete;
+  if (R.kind == kFlatGreedy || R.kind == kFlatOnline) {
+    flat_slice(P, R, s, sm);
+    if (threadIdx.x == 0) {
+      __threadfence();  // the partial before the count
+      const int row = R.is_target ? b * (P.K + 1) + R.k : P.B * (P.K + 1) + b * P.K + R.k;
+      sm.last = atomicAdd(&C.slices_done[row], 1u) + 1u == static_cast<unsigned int>(P.nslice);
+      if (sm.last) __threadfence();
+    }
+    __syncthreads();
+    row_complete = sm.last != 0;
+    if (row_complete && threadIdx.x < 32) flat_finish_row(P, R);
+  } else {
+    // nothing to read (or the recorded statistics): the first slice does it
+    row_complete = s == 0;
+    if (row_complete && R.kind == kFlatRecorded && threadIdx.x < 32) flat_finish_row(P, R);
+  }
+  if (row_complete) request_row_done(P, C, sm, b);
+}
+
+// Row statistics of every row the top-p kernel did not take, and the
+// request's accept chain once its last row is done. Static schedule: CTA i
+// takes row items i, i + grid, ... (request order, a row's slices in turn).
+__global__ void __launch_bounds__(kRowThreads, 4) verify_flat_kernel(VerifyParams P) {
+  __shared__ FlatSmem sm;
+  const CtlView C(P.ctl, P.B, P.K);
+  const int n_items = P.B * (2 * P.K + 1) * P.nslice;
+  for (int r = blockIdx.x; r < n_items; r += gridDim.x) {
+    flat_row_item(P, C, sm, r);
+    __syncthreads();  // sm is reused by the next item
+  }
+  // the draw kernel may start its set-up (it waits for this grid before
+  // reading anything this kernel wrote)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// The draws: CTA (chunk, b) draws columns of chunk `chunk` of request b's
+// categorical; the CTA that finishes the request's last chunk writes its
+// outputs.
+__global__ void __launch_bounds__(kRowThreads) verify_draw_kernel(VerifyParams P) {
+  __shared__ FlatSmem sm;
+  __shared__ DrawJob job;
+  // the row kernel's results (the jobs) are complete once it has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int tid = threadIdx.x;
+  const int b = blockIdx.y, sub = blockIdx.x, nsub = gridDim.x, K = P.K, V = P.V;
+  const CtlView C(P.ctl, P.B, K);
+  static_assert(sizeof(DrawJob) % 8 == 0 && sizeof(DrawJob) / 8 <= kRowThreads, "job copy");
+  if (tid < static_cast<int>(sizeof(DrawJob) / 8))
+    reinterpret_cast<unsigned long long*>(&job)[tid] =
+        __ldcg(reinterpret_cast<const unsigned long long*>(&C.jobs[b]) + tid);
+  __syncthreads();
+  const DrawJob& J = job;
+  int cw = (V + nsub - 1) / nsub;
+  cw = (cw + 3) & ~3;
+  const int c0 = sub * cw, c1 = min(V, c0 + cw);
+  auto umax = [](unsigned long long a, unsigned long long b2) { return a > b2 ? a : b2; };
+  unsigned long long key = 0ull;
+  unsigned int any = 0u;
+  if (!J.invalid && J.mode != kDrawNone && c0 < c1)
+    key = draw_range(P, J, J.mode, c0, c1, kRowThreads, &any);
+  key = block_reduce<unsigned long long>(key, sm.w_u64, 0ull, umax);
+  __syncthreads();
+  const unsigned int anyb = __syncthreads_or(any != 0u) ? 1u : 0u;
+  if (tid == 0) {
+    P.keys[static_cast<int64_t>(b) * P.kstride + sub] = key;
+    P.anypos[static_cast<int64_t>(b) * P.kstride + sub] = anyb;
+    __threadfence();
+    sm.last = atomicAdd(&C.draws_done[b], 1u) == static_cast<unsigned int>(nsub) - 1u;
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  // ---- the request's last chunk: reduce (warp 0, chunks in parallel) --------
+  if (tid < 32) {
+    unsigned long long m = 0ull;
+    unsigned int a = 0u;
+    for (int i = tid; i < nsub; i += 32) {
+      m = umax64(m, __ldcg(P.keys + static_cast<int64_t>(b) * P.kstride + i));
+      a |= __ldcg(P.anypos + static_cast<int64_t>(b) * P.kstride + i);
+    }
+    m = warp_max64(m);
+    a = __any_sync(0xFFFFFFFFu, a != 0u) ? 1u : 0u;
+    if (tid == 0) {
+      int tok = -1;
+      if (!J.invalid) {
+        if (J.mode == kDrawNone)
+          tok = J.emit;
+        else if (J.mode == kDrawResidual && a == 0u)
+          tok = -2;  // r is all zero (fp32 rounding): draw from p
+        else
+          tok = m ? key_index(m) : 0;
+      }
+      sm.bcast_i = tok;
+    }
+  }
+  __syncthreads();
+  int tok = sm.bcast_i;
+  if (tok == -2) {
+    unsigned int dummy = 0u;
+    unsigned long long k3 = draw_range(P, J, kDrawP, 0, V, kRowThreads, &dummy);
+    __syncthreads();
+    k3 = block_reduce<unsigned long long>(k3, sm.w_u64, 0ull, umax);
+    if (tid == 0) sm.bcast_i = k3 ? key_index(k3) : 0;
+    __syncthreads();
+    tok = sm.bcast_i;
+  }
+  for (int k = tid; k <= K; k += kRowThreads) {
+    int32_t o = -1;
+    if (!J.invalid) {
+      if (k < J.n_acc)
+        o = P.draft[static_cast<int64_t>(b) * K + k];
+      else if (k == J.n_acc)
+        o = tok;
+    }
+    P.out_tokens[static_cast<int64_t>(b) * (K + 1) + k] = o;
+  }
+  if (tid == 0) P.num_accepted[b] = J.invalid ? 0 : J.n_acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -1123,47 +1715,108 @@ bool verify_rows_plan(int V, int es, int* CL, int* W) {
   return false;
 }
 
-cudaError_t launch_verify_rows(const VerifyParams& p, int CL, int W, cudaStream_t stream) {
-  const int rows = p.B * (p.K + 1) + p.B * p.K;
-  const size_t smem = verify_rows_smem_bytes(W);
-  cudaError_t err = cudaFuncSetAttribute(verify_rows_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  if (CL > 8) {
-    err = cudaFuncSetAttribute(verify_rows_kernel,
-                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+size_t verify_ctl_bytes(int B, int K) {
+  return CtlView::jobs_word(B, K) * sizeof(unsigned int) + static_cast<size_t>(B) * sizeof(DrawJob);
+}
+
+// Enough slices that about 1024 row items fill the GPU's CTAs, none shorter
+// than 2048 values, at most 32.
+int verify_nslice(int B, int K, int V) {
+  const int rows = B * (2 * K + 1);
+  if (rows <= 0) return 1;
+  int n = (1024 + rows - 1) / rows;
+  const int by_len = V / 2048;
+  if (n > by_len) n = by_len;
+  if (n > 32) n = 32;
+  return n < 1 ? 1 : n;
+}
+
+size_t verify_parts_bytes(int B, int K, int V) {
+  return static_cast<size_t>(B) * (2 * K + 1) * verify_nslice(B, K, V) * sizeof(RowPart);
+}
+
+cudaError_t launch_verify(const VerifyParams& p0, int CL, int W, cudaStream_t stream) {
+  if (p0.B == 0) return cudaSuccess;
+  VerifyParams p = p0;
+  // ---- 1. top-p target rows (thread-block clusters) ---------------------------
+  {
+    const int rows = p.B * (p.K + 1);
+    const size_t smem = verify_rows_smem_bytes(W);
+    cudaError_t err = cudaFuncSetAttribute(verify_topp_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    if (CL > 8) {
+      err = cudaFuncSetAttribute(verify_topp_kernel,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(CL);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many clusters as fit at once, but no more rows in flight than about
+    // 80 MB of L2 holds: a top-p row's later passes read it again from L2
+    cfg.gridDim = dim3(static_cast<unsigned>(rows * CL), 1, 1);
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, verify_topp_kernel, &cfg) != cudaSuccess ||
+        max_clusters < 1) {
+      (void)cudaGetLastError();
+      max_clusters = 1;
+    }
+    const size_t row_bytes = static_cast<size_t>(p.V) * (p.target_bf16 ? 2 : 4);
+    const int l2_rows = static_cast<int>((80ull << 20) / (row_bytes > 0 ? row_bytes : 1));
+    int nclusters = rows < max_clusters ? rows : max_clusters;
+    if (l2_rows >= 1 && nclusters > l2_rows) nclusters = l2_rows;
+    if (nclusters * CL > kVerifyMaxCtas) nclusters = kVerifyMaxCtas / CL;  // one list per CTA
+    if (nclusters < 1) nclusters = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
+    err = cudaLaunchKernelEx(&cfg, verify_topp_kernel, p, W);
     if (err != cudaSuccess) return err;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kRowThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(CL);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // As many clusters as fit on the GPU at once, each looping over rows, but
-  // no more rows in flight than about 80 MB of L2 holds: every pass after
-  // the first reads the row again from L2.
-  cfg.gridDim = dim3(static_cast<unsigned>(rows * CL), 1, 1);
-  int max_clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, verify_rows_kernel, &cfg) != cudaSuccess ||
-      max_clusters < 1) {
+  // ---- 2. every other row, and the chains (persistent CTAs) ------------------
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_flat_kernel, kRowThreads, 0) !=
+          cudaSuccess ||
+      per_sm < 1) {
     (void)cudaGetLastError();
-    max_clusters = 1;
+    sms = 1;
+    per_sm = 1;
   }
-  const size_t row_bytes = static_cast<size_t>(p.V) * (p.target_bf16 ? 2 : 4);
-  const int l2_rows = static_cast<int>((80ull << 20) / (row_bytes > 0 ? row_bytes : 1));
-  int nclusters = rows < max_clusters ? rows : max_clusters;
-  if (l2_rows >= 1 && nclusters > l2_rows) nclusters = l2_rows;
-  if (nclusters * CL > kVerifyMaxCtas) nclusters = kVerifyMaxCtas / CL;  // one list per CTA
-  if (nclusters < 1) nclusters = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
-  return cudaLaunchKernelEx(&cfg, verify_rows_kernel, p, W, rows);
+  const int items = p.B * (2 * p.K + 1) * p.nslice;
+  int ctas = sms * per_sm;
+  if (ctas > items) ctas = items;
+  verify_flat_kernel<<<ctas, kRowThreads, 0, stream>>>(p);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  // ---- 3. the draws: chunks of each request's categorical ----------------------
+  // enough chunks to fill the GPU about twice, none shorter than 1024 columns;
+  // launched as a programmatic dependent of the row kernel, so its CTAs are
+  // set up while that kernel drains
+  int nd = (2 * sms * per_sm + p.B - 1) / p.B;
+  if (nd > p.kstride) nd = p.kstride;
+  if (nd < 1) nd = 1;
+  p.ndraw = nd;
+  cudaLaunchConfig_t dc = {};
+  dc.gridDim = dim3(static_cast<unsigned>(nd), static_cast<unsigned>(p.B), 1);
+  dc.blockDim = dim3(kRowThreads, 1, 1);
+  dc.dynamicSmemBytes = 0;
+  dc.stream = stream;
+  cudaLaunchAttribute da[1];
+  da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  da[0].val.programmaticStreamSerializationAllowed = 1;
+  dc.attrs = da;
+  dc.numAttrs = 1;
+  return cudaLaunchKernelEx(&dc, verify_draw_kernel, p);
 }
 
 cudaError_t launch_topk_rows(const TopkParams& p, int CL, int W, cudaStream_t stream) {
