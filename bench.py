@@ -7,10 +7,12 @@ Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on
 the host cores instead (the slow, obviously-correct restatement), on a
 bounded sample of the same workload.
 
-Timing: CUDA graphs of the two library calls, replayed once per step; CUDA
-events on the launching stream bracket the Markov loop and the verifier in
-every timed step; L2 is flushed (a 512 MiB write) before every step, outside
-the timed events. For N > 1 (torchrun) every rank runs an independent replica
+Timing: one CUDA graph of the two library calls (the Markov loop, then
+verification) replayed once per step, CUDA events on the launching stream
+around each replay; L2 is flushed (a 512 MiB write) before every step,
+outside the timed events. The loop and the verifier are also timed as graphs
+of their own, after the steps, to split the step (each half then pays its own
+graph launch). For N > 1 (torchrun) every rank runs an independent replica
 (no collectives on the data path); the barrier and the max over ranks use the
 process group only for timing.
 """
@@ -366,12 +368,18 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
-    # capture the Markov loop and the verifier as two graphs on one stream
+    # One decode step is one CUDA graph of both library calls (the Markov
+    # loop, then verification, on one stream); the halves are also captured
+    # as graphs of their own, timed after the steps, to split the step.
     with torch.cuda.stream(stream):
         st.run(stream=stream)
     stream.synchronize()
+    g_step = torch.cuda.CUDAGraph()
     g_markov = torch.cuda.CUDAGraph()
     g_verify = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        st.markov(stream=stream)
+        st.verify(stream=stream)
     with torch.cuda.graph(g_markov, stream=stream):
         st.markov(stream=stream)
     with torch.cuda.graph(g_verify, stream=stream):
@@ -382,13 +390,21 @@ def run_ours(args, rank, world, local):
         with torch.cuda.stream(stream):
             flush.fill_(1)
             ev[0].record(stream)
+            g_step.replay()
+            ev[1].record(stream)
+
+    def split_step(ev):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            ev[0].record(stream)
             g_markov.replay()
             ev[1].record(stream)
             g_verify.replay()
             ev[2].record(stream)
 
     for _ in range(args.warmup):
-        one_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+        one_step([torch.cuda.Event(enable_timing=True) for _ in range(2)])
+        split_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
@@ -396,7 +412,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     t0 = time.perf_counter()
     for i in range(args.steps):
         one_step(evs[i])
@@ -404,11 +420,16 @@ def run_ours(args, rank, world, local):
     wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
-    loop_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    ver_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    step_ms = [a + b for a, b in zip(loop_ms, ver_ms)]
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms = max_over_ranks(statistics.mean(step_ms), world, "cuda")
+    # the two halves, each its own graph (each pays its own graph launch)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        split_step(sev[i])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    loop_ms = [e[0].elapsed_time(e[1]) for e in sev]
+    ver_ms = [e[1].elapsed_time(e[2]) for e in sev]
     status = st.status_code()
     nacc = st.num_accepted.float().mean().item()
     tokens = (st.num_accepted + 1).sum().item()
@@ -486,7 +507,10 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": _config(w, args),
+        # the halves timed as graphs of their own (each with its own launch)
         "loop_us": round(loop_us, 2), "verify_us": round(ver_us, 2),
+        "step_us_p10_p90": [round(float(np.percentile(step_ms, 10)) * 1e3, 2),
+                            round(float(np.percentile(step_ms, 90)) * 1e3, 2)],
         "loop_us_p10_p90": [round(float(np.percentile(loop_ms, 10)) * 1e3, 2),
                             round(float(np.percentile(loop_ms, 90)) * 1e3, 2)],
         "verify_us_p10_p90": [round(float(np.percentile(ver_ms, 10)) * 1e3, 2),
@@ -505,9 +529,9 @@ def run_ours(args, rank, world, local):
                      "verify_frac": round(ver_bytes / (ver_us * 1e-6) / 1e9 / peak, 3)},
         "e2e": {"value": round(e2e_ms * 1e3, 1), "unit": "us", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        # the Markov loop (top-k: candidate selection + loop) and the one
-        # verification kernel
-        "gpu_launches": args.steps * (3 if args.draft_topk else 2),
+        # the Markov loop (top-k: candidate selection + loop), and the two
+        # verification kernels (top-p rows; every other row and the draws)
+        "gpu_launches": args.steps * (4 if args.draft_topk else 3),
         "clocks": clk, "status": status, "wall_s_timed_region": round(wall, 4),
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -336,10 +336,10 @@ dspark_status dspark_rejection_sample(
   p.stats_items = draft_stats != nullptr && B <= dspark::kRowStatsMaxBatch;
   p.ndraw = 1;  // chosen at launch from the grid
   p.status = status;
-  // the work queue and the per-request counters start from zero
+  // the progress counters start from zero
   if (cudaMemsetAsync(w + ws.ctl, 0, dspark::verify_ctl_bytes(B, K), st) != cudaSuccess)
     return DSPARK_ERR_CUDA;
-  if (dspark::launch_verify(p, cluster, slice, st) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (dspark::launch_verify(p, st) != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
 

@@ -188,6 +188,45 @@ __device__ __forceinline__ float gumbel_of(uint32_t w) {
   return __fmul_rn(-kLn2, lg2_approx(E));
 }
 
+// E = -ln u of two words at once, the first half of gumbel_of (the same
+// operations lane by lane, in packed pairs): an exponential variate.
+__device__ __forceinline__ void neglog_u2(uint32_t w0, uint32_t w1, float& E0, float& E1) {
+  constexpr float kLn2 = 0.693147180559945309f;
+  const unsigned long long one = f2_pack(1.0f, 1.0f), two = f2_pack(2.0f, 2.0f);
+  const unsigned long long u = f2_add(f2_pack(__uint_as_float(0x3F800000u | (w0 >> 9)),
+                                              __uint_as_float(0x3F800000u | (w1 >> 9))),
+                                      f2_pack(-0x1.fffffep-1f, -0x1.fffffep-1f));
+  const unsigned long long t = f2_sub(one, u);
+  float d0, d1;
+  f2_unpack(f2_sub(two, t), d0, d1);
+  const unsigned long long sr = f2_mul(t, f2_pack(rcp_approx(d0), rcp_approx(d1)));
+  const unsigned long long s2 = f2_mul(sr, sr);
+  unsigned long long p = f2_fma(s2, f2_pack(2.0f / 9.0f, 2.0f / 9.0f), f2_pack(2.0f / 7.0f, 2.0f / 7.0f));
+  p = f2_fma(s2, p, f2_pack(2.0f / 5.0f, 2.0f / 5.0f));
+  p = f2_fma(s2, p, f2_pack(2.0f / 3.0f, 2.0f / 3.0f));
+  p = f2_fma(s2, p, two);
+  const unsigned long long nl2 = f2_pack(-kLn2, -kLn2);
+  float u0, u1, n0, n1, f0, f1;
+  f2_unpack(u, u0, u1);
+  f2_unpack(f2_mul(sr, p), n0, n1);
+  f2_unpack(f2_mul(f2_pack(lg2_approx(u0), lg2_approx(u1)), nl2), f0, f1);
+  E0 = u0 > 0.75f ? n0 : f0;
+  E1 = u1 > 0.75f ? n1 : f1;
+}
+
+// Winner key of a categorical draw in exponential-race form: the Gumbel-max
+// argmax of log w + g, g = -log E, is the argmax of w / E (the same order in
+// exact arithmetic), taken as w * (1/E). Positive ratios only (w > 0, E > 0):
+// the order key of a positive float is its bits with the sign bit set; the
+// column breaks ties, lowest first. 0 is below every real key.
+__device__ __forceinline__ unsigned long long race_key(float w, float E, uint32_t col) {
+  const float ratio = __fmul_rn(w, rcp_approx(E));
+  const uint32_t o = w > 0.0f ? (__float_as_uint(ratio) | 0x80000000u) : 0u;
+  return o == 0u ? 0ull
+                 : (static_cast<unsigned long long>(o) << 32) |
+                       static_cast<unsigned long long>(0xFFFFFFFFu - col);
+}
+
 // gumbel_of of two words at once: the same operations lane by lane, the
 // arithmetic in packed pairs (lg2, rcp and the selection per value).
 __device__ __forceinline__ void gumbel_of2(uint32_t w0, uint32_t w1, float& g0, float& g1) {

@@ -120,7 +120,7 @@ struct VerifyParams {
   void* dstats;                  // [B][K] draft-row statistics
   unsigned long long* keys;      // [B][kstride] winner key of each draw sub-chunk
   unsigned int* anypos;          // [B][kstride] the sub-chunk had a positive weight
-  unsigned int* ctl;             // per-request and per-row progress, draw jobs (zeroed per call)
+  unsigned int* ctl;             // per-request and per-row progress, draw jobs
   uint2* cand;                   // [kVerifyMaxCtas][kVerifyListCap] top-p candidates (id, x bits)
   void* parts;                   // [B * (2K + 1)][nslice] per-slice row partials
   int nslice;                    // slices per row in the flat kernel
@@ -131,9 +131,10 @@ struct VerifyParams {
   int32_t* status;
 };
 
-// VerifyParams::ctl: per request the rows finished and the draw chunks
-// finished, per row the slices finished (32-bit words, zeroed per call),
-// then one draw job per request (verify_draw.cuh).
+// VerifyParams::ctl: the draw queue's two words (on lines of their own), per
+// request the rows finished, the draw chunks finished and the publish list,
+// per row the slices finished (32-bit words, zeroed before each call's
+// kernel), then one draw job per request (verify_draw.cuh).
 size_t verify_ctl_bytes(int B, int K);
 // Slices per row of the flat verification kernel, and the bytes of their
 // partials.
@@ -150,9 +151,9 @@ size_t verify_dstats_bytes(int B, int K);
 int verify_max_chunks(int V);
 size_t verify_rows_smem_bytes(int W);
 bool verify_rows_plan(int V, int es, int* CL, int* W);
-// The whole verification in one persistent launch of thread-block clusters
-// (row statistics, the accept chain, the draws, the outputs).
-cudaError_t launch_verify(const VerifyParams& p, int CL, int W, cudaStream_t stream);
+// The whole verification in one persistent launch (row statistics, the
+// accept chains, the draws, the outputs).
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
 
 // The drafter's temperature division on its own (a test hook; verify.cu).
 cudaError_t launch_temperature_divide(const float* z, const float* T, float* x, int64_t n,

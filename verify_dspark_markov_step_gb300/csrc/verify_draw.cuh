@@ -2,9 +2,10 @@
 // the residual max(0, p - q) at the first rejected draft, p at a -1
 // placeholder, or the bonus row p_K (vLLM PR #65007 Part 2, "Rejection
 // sampling": resample from the normalised residual, bonus token). A draw is
-// the Gumbel-max argmax_v log w_v + g_v with g from the target noise stream
-// at the row's position, under the drafter's winner rule (largest value,
-// lowest column on ties).
+// the Gumbel-max argmax_v log w_v + g_v with g = -log E from the target
+// noise stream at the row's position, under the drafter's winner rule
+// (largest value, lowest column on ties), compared in its exponential-race
+// form w_v / E_v (race_key): the same order without two logarithms.
 #pragma once
 
 #include <stdint.h>
@@ -137,13 +138,13 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const DrawJob& J,
     if (!need) continue;
     any = 1u;
     const U4 r = noise_block(J.seed, npos, static_cast<uint32_t>(g), kStreamTarget);
-    float gn[4];
-    gumbel_of2(r.x, r.y, gn[0], gn[1]);
-    gumbel_of2(r.z, r.w, gn[2], gn[3]);
+    float E[4];
+    neglog_u2(r.x, r.y, E[0], E[1]);
+    neglog_u2(r.z, r.w, E[2], E[3]);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float y = __fadd_rn(ln_approx(w[j]), gn[j]);
-      const uint32_t o = w[j] > 0.0f ? ordered_key(y) : 0u;
+      const float ratio = __fmul_rn(w[j], rcp_approx(E[j]));
+      const uint32_t o = w[j] > 0.0f ? (__float_as_uint(ratio) | 0x80000000u) : 0u;
       if (o > run_o) {
         run_o = o;
         run_c = static_cast<uint32_t>(g + j);
@@ -222,14 +223,12 @@ __device__ unsigned long long draw_range(const VerifyParams& P, const DrawJob& J
     if (!need) continue;
     any = 1u;
     const U4 r = noise_block(J.seed, npos, static_cast<uint32_t>(g), kStreamTarget);
-    const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+    float E[4];
+    neglog_u2(r.x, r.y, E[0], E[1]);
+    neglog_u2(r.z, r.w, E[2], E[3]);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (w[j] > 0.0f) {
-        const float y = __fadd_rn(ln_approx(w[j]), gumbel_of(words[j]));
-        best = umax64(best, winner_key(y, static_cast<uint32_t>(g + j)));
-      }
-    }
+    for (int j = 0; j < 4; ++j)
+      best = umax64(best, race_key(w[j], E[j], static_cast<uint32_t>(g + j)));
   }
   *anypos = any;
   return best;

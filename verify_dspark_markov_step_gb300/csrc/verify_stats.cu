@@ -54,8 +54,6 @@ struct RowSmem {
   unsigned long long red64[kRowWarps];
   float redf[kRowWarps];
   // slots read by the other CTAs of the cluster
-  float x_max;
-  int x_fail;
   int x_pos;
   unsigned long long x_key;
   unsigned long long x_sum;
@@ -70,10 +68,7 @@ struct RowSmem {
   unsigned int list_n;  // top-p candidates this CTA appended to its list
   // per-row reductions: one slot per CTA, two alternating sets (a row's slots
   // are rewritten only after the next row's first cluster barrier)
-  unsigned int c_max[2];         // ordered bits of the CTA maximum (~0: failed)
   unsigned long long c_sum[2];   // fixed-point mass
-  unsigned long long c_key[2];   // greedy winner key
-  unsigned long long c_ms[2];    // online (max, sum) of the CTA's slice
   unsigned int w_u32[kRowWarps];
   unsigned long long w_u64[kRowWarps];
   // block-local scratch
@@ -113,10 +108,6 @@ __device__ unsigned long long block_sum_u64(unsigned long long v, RowSmem& sm) {
 // The CTA reduces its warps through shared memory and thread 0 stores the
 // result in the CTA's slot of the current set; after one cluster barrier warp
 // 0 reads the CL slots of the cluster and broadcasts the result.
-__device__ __forceinline__ float from_ordered(uint32_t o) {
-  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
-}
-
 template <class T, class Op>
 __device__ __forceinline__ T block_reduce(T v, T* wslots, T init, Op op) {
 #pragma unroll
@@ -150,29 +141,11 @@ __device__ __forceinline__ T cluster_reduce(cg::cluster_group& cl, RowSmem& sm, 
   return *bcast;
 }
 
-// Maximum over the cluster; *any_fail = some CTA passed fail = true.
-__device__ float cluster_max_f(cg::cluster_group& cl, RowSmem& sm, float v, bool fail, int set,
-                               int CL, bool* any_fail) {
-  const unsigned int mine = fail ? 0xFFFFFFFFu : ordered_bits(v);
-  const unsigned int o = cluster_reduce<unsigned int>(
-      cl, sm, mine, &sm.c_max[set], reinterpret_cast<unsigned int*>(&sm.bcast_i), CL, 0u,
-      [](unsigned int a, unsigned int b) { return a > b ? a : b; });
-  *any_fail = o == 0xFFFFFFFFu;  // a real maximum is never NaN here (NaN reads as -inf)
-  return from_ordered(o);
-}
-
 __device__ unsigned long long cluster_sum_u64(cg::cluster_group& cl, RowSmem& sm,
                                               unsigned long long v, int set, int CL) {
   return cluster_reduce<unsigned long long>(
       cl, sm, v, &sm.c_sum[set], &sm.bcast_u, CL, 0ull,
       [](unsigned long long a, unsigned long long b) { return a + b; });
-}
-
-__device__ unsigned long long cluster_max_u64(cg::cluster_group& cl, RowSmem& sm,
-                                              unsigned long long v, int set, int CL) {
-  return cluster_reduce<unsigned long long>(
-      cl, sm, v, &sm.c_key[set], &sm.bcast_u, CL, 0ull,
-      [](unsigned long long a, unsigned long long b) { return a > b ? a : b; });
 }
 
 // ---- histograms -------------------------------------------------------------
@@ -182,12 +155,6 @@ __device__ void hist_clear(RowSmem& sm, int nb) {
     sm.hcnt[i] = 0u;
     sm.hid[i] = 0u;
   }
-}
-
-// Adds mass f alone to bin `bin` (the first top-p stage, over every element
-// of the row: its counts are not needed).
-__device__ __forceinline__ void hist_add_mass(RowSmem& sm, int bin, unsigned long long f) {
-  atomicAdd(&sm.hmass[bin], f);
 }
 
 // Adds (mass f, one count, id) to bin `bin` with shared-memory atomics (one
@@ -361,16 +328,15 @@ __device__ __forceinline__ int adigit1(float x, float m, int a0) {
   return static_cast<int>(fminf(__fmul_rn(t, 2048.0f), 2047.0f));
 }
 
-// Reads of one row's slice [v0, v0 + n) straight from global memory. The
-// first pass brings the slice from HBM (L2 evict-last: every later pass of
-// the row reads it again from L2); `fix` maps a raw value to x (temperature,
-// NaN read as -inf). `vec` = the slice start is 16-byte aligned (fp32) or
-// 8-byte aligned (bf16), so it can be read 4 values at a time.
+// Reads of one row's slice [v0, v0 + n) straight from global memory, the
+// eviction priority in L2 chosen by the caller (a top-p row's first passes
+// keep it for the later ones); `fix` maps a raw value to x (temperature,
+// NaN read as -inf). The sweeps read the few elements before the first
+// 16-byte (fp32) or 8-byte (bf16) boundary one at a time, then 4 at a time.
 struct RowView {
   const float* f;
   const uint16_t* h;
   bool bf16;
-  bool vec;
   int n;
 };
 
@@ -386,65 +352,60 @@ __device__ __forceinline__ void row_sweep(const RowView& rv, uint64_t pol, Fix f
     row_sweep_t<kU, false>(rv, pol, fix, body);
 }
 
+// Elements before the slice's first vector-aligned address (16 bytes for
+// fp32, 8 for bf16): a row of an odd-sized vocabulary starts anywhere.
+template <bool kBf16>
+__device__ __forceinline__ int aligned_head(const RowView& rv) {
+  constexpr uintptr_t al = kBf16 ? 8 : 16;
+  const uintptr_t a = kBf16 ? reinterpret_cast<uintptr_t>(rv.h) : reinterpret_cast<uintptr_t>(rv.f);
+  const int head = static_cast<int>(((al - (a & (al - 1))) & (al - 1)) / (kBf16 ? 2 : 4));
+  return head < rv.n ? head : rv.n;
+}
+
 template <int kU, bool kBf16, class Fix, class Body>
 __device__ __forceinline__ void row_sweep_t(RowView rv, uint64_t pol, Fix fix, Body body) {
-  rv.bf16 = kBf16;  // a compile-time constant from here on
   const int tid = threadIdx.x;
-  int done = 0;
-  if (rv.vec) {
-    const int n4 = rv.n >> 2;
-    int i = tid;
-    for (; i + (kU - 1) * kRowThreads < n4; i += kU * kRowThreads) {
-      float v[kU][4];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int j = i + u * kRowThreads;
-        if (rv.bf16) {
-          const uint2 w = ld_hint_u2(rv.h + 4 * j, pol);
-          v[u][0] = bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu));
-          v[u][1] = bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16));
-          v[u][2] = bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu));
-          v[u][3] = bf16_bits_to_float(static_cast<uint16_t>(w.y >> 16));
-        } else {
-          const float4 c = ld_hint_f4(rv.f + 4 * j, pol);
-          v[u][0] = c.x;
-          v[u][1] = c.y;
-          v[u][2] = c.z;
-          v[u][3] = c.w;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int j = 4 * (i + u * kRowThreads);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) body(j + e, fix(v[u][e]));
-      }
+  auto ld1 = [&](int i) -> float {
+    return kBf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol)) : ld_hint_f32(rv.f + i, pol);
+  };
+  auto ld4 = [&](int i, float (&v)[4]) {  // 4 values from aligned element index i
+    if constexpr (kBf16) {
+      const uint2 w = ld_hint_u2(rv.h + i, pol);
+      v[0] = bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu));
+      v[1] = bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16));
+      v[2] = bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu));
+      v[3] = bf16_bits_to_float(static_cast<uint16_t>(w.y >> 16));
+    } else {
+      const float4 c = ld_hint_f4(rv.f + i, pol);
+      v[0] = c.x;
+      v[1] = c.y;
+      v[2] = c.z;
+      v[3] = c.w;
     }
-    for (; i < n4; i += kRowThreads) {
-      float v[4];
-      if (rv.bf16) {
-        const uint2 w = ld_hint_u2(rv.h + 4 * i, pol);
-        v[0] = bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu));
-        v[1] = bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16));
-        v[2] = bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu));
-        v[3] = bf16_bits_to_float(static_cast<uint16_t>(w.y >> 16));
-      } else {
-        const float4 c = ld_hint_f4(rv.f + 4 * i, pol);
-        v[0] = c.x;
-        v[1] = c.y;
-        v[2] = c.z;
-        v[3] = c.w;
-      }
+  };
+  // the few elements before the first aligned address, then 4 at a time
+  const int head = aligned_head<kBf16>(rv);
+  if (tid < head) body(tid, fix(ld1(tid)));
+  const int n4 = (rv.n - head) >> 2;
+  int i = tid;
+  for (; i + (kU - 1) * kRowThreads < n4; i += kU * kRowThreads) {
+    float v[kU][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) body(4 * i + e, fix(v[e]));
+    for (int u = 0; u < kU; ++u) ld4(head + 4 * (i + u * kRowThreads), v[u]);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int j = head + 4 * (i + u * kRowThreads);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) body(j + e, fix(v[u][e]));
     }
-    done = 4 * n4;
   }
-  for (int i = done + tid; i < rv.n; i += kRowThreads) {
-    const float c =
-        rv.bf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol)) : ld_hint_f32(rv.f + i, pol);
-    body(i, fix(c));
+  for (; i < n4; i += kRowThreads) {
+    float v[4];
+    ld4(head + 4 * i, v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) body(head + 4 * i + e, fix(v[e]));
   }
+  for (int t = head + 4 * n4 + tid; t < rv.n; t += kRowThreads) body(t, fix(ld1(t)));
 }
 
 // ---- rows kept whole: one pass, a deterministic fp32 online softmax sum -----
@@ -510,20 +471,28 @@ __device__ __forceinline__ unsigned long long slice_online_t(const RowView& rv, 
   const int tid = threadIdx.x;
   float m = known ? known_m : -INFINITY;
   float s0 = 0.0f, s1 = 0.0f;
-  constexpr int kVecBytes = kBf16 ? 8 : 16;
+  constexpr int kEs = kBf16 ? 2 : 4;
   L2Window pf(kBf16 ? static_cast<const void*>(rv.h) : static_cast<const void*>(rv.f),
-              static_cast<size_t>(rv.n) * (kBf16 ? 2 : 4), tid == 0 ? pf_window : 0u);
+              static_cast<size_t>(rv.n) * kEs, tid == 0 ? pf_window : 0u);
   pf.advance(0);
   const unsigned long long l2e = f2_pack(kLog2e, kLog2e);
-  auto load4 = [&](int j, float (&v)[4]) {
+  // the few elements before the first aligned address, then 4 at a time
+  const int head = aligned_head<kBf16>(rv);
+  const float* af = rv.f + head;
+  const uint16_t* ah = rv.h + head;
+  const int an = rv.n - head;
+  auto ld1 = [&](int i) -> float {  // element i of the slice
+    return kBf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol)) : ld_hint_f32(rv.f + i, pol);
+  };
+  auto load4 = [&](int j, float (&v)[4]) {  // aligned vector j
     if constexpr (kBf16) {
-      const uint2 w = ld_hint_u2(rv.h + 4 * j, pol);
+      const uint2 w = ld_hint_u2(ah + 4 * j, pol);
       v[0] = bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu));
       v[1] = bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16));
       v[2] = bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu));
       v[3] = bf16_bits_to_float(static_cast<uint16_t>(w.y >> 16));
     } else {
-      const float4 c = ld_hint_f4(rv.f + 4 * j, pol);
+      const float4 c = ld_hint_f4(af + 4 * j, pol);
       v[0] = c.x;
       v[1] = c.y;
       v[2] = c.z;
@@ -551,46 +520,42 @@ __device__ __forceinline__ unsigned long long slice_online_t(const RowView& rv, 
     s0 = __fadd_rn(s0, ex2_approx(c));
     s1 = __fadd_rn(s1, ex2_approx(d));
   };
-  int done = 0;
-  if (rv.vec) {
-    const int n4 = rv.n >> 2;
-    int i = tid;
-    for (; i + (kU - 1) * kRowThreads < n4; i += kU * kRowThreads) {
-      pf.advance(static_cast<size_t>(i + kU * kRowThreads) * kVecBytes);
-      float v[kU][4];
+  auto add1 = [&](float x) {
+    const float base = rescale(x);  // before s0 is read: rescale updates it
+    s0 = __fadd_rn(s0, exp_rel(x, base));
+  };
+  if (tid < head) add1(fix(ld1(tid)));
+  const int n4 = an >> 2;
+  int i = tid;
+  for (; i + (kU - 1) * kRowThreads < n4; i += kU * kRowThreads) {
+    pf.advance(static_cast<size_t>(head) * kEs + static_cast<size_t>(i + kU * kRowThreads) * 4 * kEs);
+    float v[kU][4];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) load4(i + u * kRowThreads, v[u]);
-      float cm = -INFINITY;
+    for (int u = 0; u < kU; ++u) load4(i + u * kRowThreads, v[u]);
+    float cm = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kU; ++u)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[u][e] = fix(v[u][e]);
-          cm = fmaxf(cm, v[u][e]);
-        }
-      const float base = rescale(cm);
-#pragma unroll
-      for (int u = 0; u < kU; ++u) add4(v[u], base);
-    }
-    for (; i < n4; i += kRowThreads) {
-      float v[4];
-      load4(i, v);
-      float cm = -INFINITY;
+    for (int u = 0; u < kU; ++u)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        v[e] = fix(v[e]);
-        cm = fmaxf(cm, v[e]);
+        v[u][e] = fix(v[u][e]);
+        cm = fmaxf(cm, v[u][e]);
       }
-      add4(v, rescale(cm));
+    const float base = rescale(cm);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) add4(v[u], base);
+  }
+  for (; i < n4; i += kRowThreads) {
+    float v[4];
+    load4(i, v);
+    float cm = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[e] = fix(v[e]);
+      cm = fmaxf(cm, v[e]);
     }
-    done = 4 * n4;
+    add4(v, rescale(cm));
   }
-  for (int i = done + tid; i < rv.n; i += kRowThreads) {
-    const float x = fix(kBf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol))
-                              : ld_hint_f32(rv.f + i, pol));
-    const float base = rescale(x);
-    s0 = __fadd_rn(s0, exp_rel(x, base));
-  }
+  for (int t = head + 4 * n4 + tid; t < rv.n; t += kRowThreads) add1(fix(ld1(t)));
   return ms_pack(m, __fadd_rn(s0, s1));
 }
 
@@ -600,312 +565,6 @@ __device__ __forceinline__ unsigned long long slice_online(const RowView& rv, ui
                                                            uint32_t pf_window = 0u) {
   if (rv.bf16) return slice_online_t<4, true>(rv, pol, fix, known, known_m, pf_window);
   return slice_online_t<4, false>(rv, pol, fix, known, known_m, pf_window);
-}
-
-// The (m, s) pair of the whole row: warps, then the CTA, then the cluster's
-// CTAs (each combine commutative, the order fixed).
-__device__ unsigned long long cluster_online(cg::cluster_group& cl, RowSmem& sm,
-                                             unsigned long long v, int set, int CL) {
-  return cluster_reduce<unsigned long long>(cl, sm, v, &sm.c_ms[set], &sm.bcast_u, CL,
-                                            ms_pack(-INFINITY, 0.0f),
-                                            [](unsigned long long a, unsigned long long b) {
-                                              return ms_combine(a, b);
-                                            });
-}
-
-// One row: statistics written to P.tstats / P.dstats. Every CTA of the
-// cluster runs the same sequence of cluster barriers (all decisions depend on
-// the row or on cluster-reduced values only).
-__device__ void process_row(const VerifyParams& P, int W, int row_id, cg::cluster_group& cl,
-                            int CL, int rank, RowSmem& sm, int& jrow) {
-  const int tid = threadIdx.x;
-  const int K = P.K, V = P.V;
-  const int nT = P.B * (K + 1);
-  int b, k;
-  bool is_target;
-  if (row_id < nT) {
-    b = row_id / (K + 1);
-    k = row_id % (K + 1);
-    is_target = true;
-  } else {
-    const int r = row_id - nT;
-    b = r / K;
-    k = r % K;
-    is_target = false;
-  }
-  const int32_t s = P.rsi[b];
-  if (s < 0 || s >= P.S) return;
-  const float T = P.temperature[s];
-  const bool greedy = !(T > 0.0f);
-  int64_t crow = 0;
-  if (!is_target) {
-    if (greedy || P.cache == nullptr) return;
-    crow = P.row_map ? P.row_map[s] : s;
-    if (crow < 0 || crow >= P.C) return;
-  }
-  const int set = jrow & 1;
-  ++jrow;
-  const int v0 = rank * W;
-  const int n = max(0, min(W, V - v0));
-  int64_t off;
-  bool bf16;
-  if (is_target) {
-    off = (static_cast<int64_t>(b) * (K + 1) + k) * V;
-    bf16 = P.target_bf16 != 0;
-  } else {
-    off = (crow * K + k) * V;
-    bf16 = P.cache_bf16 != 0;
-  }
-  const void* base = is_target ? P.target : P.cache;
-  RowView rv;
-  rv.bf16 = bf16;
-  rv.f = static_cast<const float*>(base) + off + v0;
-  rv.h = static_cast<const uint16_t*>(base) + off + v0;
-  rv.vec = bf16 ? (reinterpret_cast<uintptr_t>(rv.h) & 7u) == 0
-                : (reinterpret_cast<uintptr_t>(rv.f) & 15u) == 0;
-  rv.n = n;
-  // the slice's first read comes from HBM: start it as one bulk L2 prefetch,
-  // so that the whole slice is in flight at once
-  if (tid == 0) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(bf16 ? static_cast<const void*>(rv.h)
-                                                         : static_cast<const void*>(rv.f));
-    const uintptr_t a16 = (a + 15) & ~static_cast<uintptr_t>(15);
-    const uint32_t bytes = static_cast<uint32_t>(n) * (bf16 ? 2u : 4u);
-    const uint32_t skip = static_cast<uint32_t>(a16 - a);
-    if (bytes > skip + 16) {
-      const uint32_t len = (bytes - skip) & ~15u;
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a16), "r"(len) : "memory");
-    }
-  }
-  const int32_t d = k < K ? P.draft[static_cast<int64_t>(b) * K + k] : -1;
-  TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(b) * (K + 1) + k;
-  DrfStats* ds = static_cast<DrfStats*>(P.dstats) + static_cast<int64_t>(b) * K + (k < K ? k : 0);
-  const uint64_t pol_keep = policy_evict_last();
-  const uint64_t pol_last_use = policy_evict_first();
-  // one element of the row by token id (any CTA may read any element)
-  auto raw_at = [&](int v) -> float {
-    const int64_t o = off + v;
-    return bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(base)[o])
-                : static_cast<const float*>(base)[o];
-  };
-
-  // ---- greedy target row: winner key of the raw row ----------------------------
-  if (is_target && greedy) {
-    unsigned long long key = 0ull;
-    row_sweep(rv, pol_last_use, [](float c) { return c; }, [&](int i, float t) {
-      key = umax64(key, winner_key(t, static_cast<uint32_t>(v0 + i)));
-    });
-    key = cluster_max_u64(cl, sm, key, set, CL);
-    if (rank == 0 && tid == 0) {
-      ts->m = 0.f;
-      ts->D = 1.f;
-      ts->kd_thr = 0u;
-      ts->id_thr = 0;
-      ts->p_d = 0.f;
-      ts->mode = kModeGreedy;
-      ts->amax_key = key;
-    }
-    return;
-  }
-
-  // x: the target row after temperature, the draft row as stored; NaN reads
-  // as -inf. The passes are instantiated for scaled and unscaled rows, so an
-  // unscaled row never evaluates a division.
-  const bool topp = is_target && P.top_p[s] < 1.0f;
-  auto passes = [&](auto prescale) {
-    auto fix = [=](float c) -> float {
-      return fmaxf(prescale(c), -INFINITY);  // fmaxf returns the other operand for NaN
-    };
-
-    // ---- pass 1 (HBM): maximum (fmaxf skips NaN, as if it were -inf) ---------------
-    // A draft row whose maximum the Markov loop recorded skips this pass and
-    // is read once, by pass 2 (every CTA of the cluster decides alike).
-    const float m_rec = (!is_target && P.draft_stats != nullptr)
-                            ? P.draft_stats[static_cast<int64_t>(b) * K + k].m
-                            : __int_as_float(0x7FC00000);
-    float m;
-    float s_keep = 0.0f;  // rows kept whole: sum of exp(x - m), one pass
-    if (!topp) {
-      // a draft row, or a target row without top-p: one pass from HBM gives
-      // the maximum and the sum together (or the sum alone, when the Markov
-      // loop recorded the maximum)
-      const bool known = m_rec == m_rec;  // NaN: not recorded
-      const unsigned long long ms =
-          cluster_online(cl, sm, slice_online(rv, pol_last_use, fix, known, m_rec), set, CL);
-      m = known ? m_rec : ms_m(ms);
-      s_keep = ms_s(ms);
-    } else {
-      float lmax = -INFINITY;
-      row_sweep(rv, pol_keep, prescale, [&](int, float x) { lmax = fmaxf(lmax, x); });
-      bool any_fail = false;
-      m = cluster_max_f(cl, sm, lmax, false, set, CL, &any_fail);
-    }
-    if (m == -INFINITY) {
-      if (rank == 0 && tid == 0) {
-        if (is_target) {
-          ts->m = m;
-          ts->D = 1.0f;
-          ts->kd_thr = 0u;
-          ts->id_thr = 0;
-          ts->p_d = d == 0 ? 1.0f : 0.0f;
-          ts->mode = kModeOneHot;
-          ts->amax_key = 0ull;
-        } else {
-          ds->m = m;
-          ds->D = 1.0f;
-          ds->q_d = 0.0f;
-          ds->zero = 1;
-        }
-      }
-      return;
-    }
-
-    uint32_t kd_thr = 0u;
-    int32_t id_thr = 0;
-    unsigned long long Fk = 0ull;
-    int32_t mode = kModeKeepAll;
-    if (topp) {
-      // ---- pass 2 (L2): fixed-point mass and the first top-p histogram ---------
-      hist_clear(sm, kRowBins);
-      __syncthreads();
-      unsigned long long F = 0ull;
-      row_sweep<4>(rv, pol_keep, fix, [&](int, float x) {
-        const unsigned long long f = fixed_mass(exp_rel(x, m));
-        F += f;
-        hist_add_mass(sm, adigit0(x, m), f);
-      });
-      F = cluster_sum_u64(cl, sm, F, set, CL);
-      Fk = F;
-      mode = kModeThreshold;
-      const unsigned long long P32 = topp_scaled(P.top_p[s]);
-      const unsigned long long t_lo = P32 * F;
-      const unsigned long long t_hi = __umul64hi(P32, F);
-      // stage 0 (its histogram was built in pass 2): distance bins, ascending
-      // (a mass-only histogram: the bin's count is unknown, so stage 1 always runs)
-      Found f = cluster_find(cl, sm, kRowBins, false, 0ull, t_hi, t_lo, CL, rank, 0xFFFFFFFFu,
-                             0u, false);
-      f.cnt = 0u;
-      unsigned long long above = f.before;
-      const int a0 = f.bin;
-      int a1 = -1;
-      int kd_len = 0, id_len = 0;
-      uint32_t kd_pre = 0u, id_pre = 0u;
-      // Stages 1..6 split the boundary bin until it holds one element: the
-      // distance sub-bins, kd bits [31:21], [20:10], [9:0], id bits [21:11],
-      // [10:0]. After the last id stage the bin is a single token. Once the
-      // bin holds a single value, the value stages left are skipped.
-      // Stage 1 also copies its candidates (the elements of bin a0) to this
-      // CTA's list; the later stages read the list instead of the slice
-      // unless it overflowed.
-      uint2* list = P.cand + static_cast<size_t>(blockIdx.x) * kVerifyListCap;
-      unsigned int list_len = 0xFFFFFFFFu;  // not built yet
-      for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
-        const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
-        const uint32_t c_kp = kd_pre, c_ip = id_pre;
-        auto match = [=](float x, uint32_t kd, uint32_t id) {
-          if (adigit0(x, m) != a0) return false;
-          if (c_a1 >= 0 && adigit1(x, m, a0) != c_a1) return false;
-          if (c_kl > 0 && (kd >> (32 - c_kl)) != c_kp) return false;
-          if (c_il > 0 && (id >> (22 - c_il)) != c_ip) return false;
-          return true;
-        };
-        auto digit = [=](float x, uint32_t kd, uint32_t id) -> int {
-          switch (stage) {
-            case 1: return adigit1(x, m, a0);
-            case 2: return static_cast<int>(kd >> 21);
-            case 3: return static_cast<int>((kd >> 10) & 0x7FFu);
-            case 4: return static_cast<int>(kd & 0x3FFu);
-            case 5: return static_cast<int>((id >> 11) & 0x7FFu);
-            default: return static_cast<int>(id & 0x7FFu);
-          }
-        };
-        const int nb = stage == 4 ? 1024 : kRowBins;
-        const bool desc = stage >= 2 && stage <= 4;  // larger kd first; distance and id ascending
-        hist_clear(sm, nb);
-        if (stage == 1 && tid == 0) sm.list_n = 0u;
-        __syncthreads();
-        uint32_t cmin = 0xFFFFFFFFu, cmax = 0u;  // value-key range of the candidates
-        auto visit = [&](uint32_t id, float x, bool append) {
-          const uint32_t kd = kd_of(x);
-          if (match(x, kd, id)) {
-            hist_add(sm, true, digit(x, kd, id), fixed_mass(exp_rel(x, m)), id);
-            cmin = min(cmin, kd);
-            cmax = max(cmax, kd);
-            if (append) {
-              const unsigned int at = atomicAdd(&sm.list_n, 1u);
-              if (at < static_cast<unsigned int>(kVerifyListCap))
-                list[at] = make_uint2(id, __float_as_uint(x));
-            }
-          }
-        };
-        if (list_len <= static_cast<unsigned int>(kVerifyListCap)) {
-          for (unsigned int j = tid; j < list_len; j += kRowThreads) {
-            const uint2 e = __ldcg(list + j);
-            visit(e.x, __uint_as_float(e.y), false);
-          }
-        } else {
-          const bool append = stage == 1;
-          row_sweep<4>(rv, pol_keep, fix, [&](int i, float x) {
-            visit(static_cast<uint32_t>(v0 + i), x, append);
-          });
-        }
-        f = cluster_find(cl, sm, nb, desc, above, t_hi, t_lo, CL, rank, cmin, cmax);
-        if (stage == 1) list_len = sm.list_n;  // complete: cluster_find synchronised the CTA
-        above = f.before;
-        const uint32_t bin = static_cast<uint32_t>(f.bin);
-        if (stage == 1) {
-          a1 = f.bin;
-        } else if (stage <= 4) {
-          kd_pre = (kd_pre << (stage == 4 ? 10 : 11)) | bin;
-          kd_len += stage == 4 ? 10 : 11;
-        } else {
-          id_pre = (id_pre << 11) | bin;
-          id_len += 11;
-        }
-        // every candidate of this stage had one value (ties, e.g. in a bf16
-        // row), so the boundary bin does too: the value stages cannot split
-        // it, go on with the token-id stages
-        if (stage < 5 && f.cnt > 1u && f.kmin == f.kmax) {
-          kd_pre = f.kmin;
-          kd_len = 32;
-          stage = 4;
-        }
-      }
-      // f is the one-element bin at the boundary: its token, mass and logit
-      id_thr = static_cast<int32_t>(f.id);
-      Fk = above + f.mass;
-      kd_thr = kd_of(fix(raw_at(id_thr)));
-    }
-    // the normaliser: the kept fixed-point mass of a top-p row, the fp32 sum
-    // of a row kept whole
-    const float D = topp ? __fmul_rn(__ull2float_rn(Fk), 0x1p-40f) : s_keep;
-
-    // ---- outputs (rank 0): p or q at the drafted token, the row statistics --------
-    if (rank == 0 && tid == 0) {
-      const bool has_d = d >= 0 && d < V;
-      const float x = has_d ? fix(raw_at(d)) : 0.0f;
-      if (is_target) {
-        const uint32_t kd = kd_of(x);
-        const bool keep = mode == kModeKeepAll || kd > kd_thr || (kd == kd_thr && d <= id_thr);
-        ts->p_d = has_d && keep ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
-        ts->m = m;
-        ts->D = D;
-        ts->kd_thr = kd_thr;
-        ts->id_thr = id_thr;
-        ts->mode = mode;
-        ts->amax_key = 0ull;
-      } else {
-        ds->q_d = has_d ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
-        ds->m = m;
-        ds->D = D;
-        ds->zero = 0;
-      }
-    }
-  };
-  if (is_target && T != 1.0f)
-    passes([T](float c) { return __fdiv_rn(c, T); });
-  else
-    passes([](float c) { return c; });
 }
 
 // ---------------------------------------------------------------------------
@@ -936,37 +595,6 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const unsigned int* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Is target row (b, k) one the top-p kernel handles? (sampled, top_p < 1)
-__device__ __forceinline__ bool topp_row(const VerifyParams& P, int b) {
-  const int32_t s = P.rsi[b];
-  if (s < 0 || s >= P.S) return false;
-  return P.temperature[s] > 0.0f && P.top_p[s] < 1.0f;
-}
-
-__global__ void __launch_bounds__(kRowThreads, 4) verify_topp_kernel(VerifyParams P, int W) {
-  cg::cluster_group cl = cg::this_cluster();
-  const int CL = static_cast<int>(cl.num_blocks());
-  const int rank = static_cast<int>(cl.block_rank());
-  const int cid = blockIdx.x / CL;
-  const int nclusters = gridDim.x / CL;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  RowSmem& sm = *reinterpret_cast<RowSmem*>(smem_raw);
-  // a batch with no top-p row: every CTA sees the same answer and leaves
-  bool any = false;
-  for (int b = threadIdx.x; b < P.B; b += kRowThreads) any |= topp_row(P, b);
-  if (!__syncthreads_or(any)) return;
-  int jrow = 0;
-  const int nT = P.B * (P.K + 1);
-  for (int row = cid; row < nT; row += nclusters)
-    if (topp_row(P, row / (P.K + 1))) process_row(P, W, row, cl, CL, rank, sm, jrow);
-  cl.sync();  // no CTA exits while another may still read its shared memory
-}
 
 // ---- the flat kernels ------------------------------------------------------
 struct RowPart {
@@ -976,15 +604,23 @@ struct RowPart {
 };
 
 struct CtlView {
+  unsigned int* draw_head;   // next draw item (its own 128-byte line)
+  unsigned int* ready_count; // requests published (its own line)
+  unsigned int* row_head;    // next row item (its own line)
   unsigned int* rows_done;   // [B] rows finished per request
   unsigned int* draws_done;  // [B] draw chunks finished per request
+  unsigned int* ready;       // [B] request + 1, in publish order
   unsigned int* slices_done; // [B * (2K + 1)] slices finished per row
   DrawJob* jobs;             // [B] what each request's draw needs
+  static constexpr int kHead = 96;  // words of the three queue lines
   __device__ CtlView(unsigned int* c, int B, int K)
-      : rows_done(c), draws_done(c + B), slices_done(c + 2 * B),
+      : draw_head(c), ready_count(c + 32), row_head(c + 64), rows_done(c + kHead),
+        draws_done(c + kHead + B),
+        ready(c + kHead + 2 * B), slices_done(c + kHead + 3 * B),
         jobs(reinterpret_cast<DrawJob*>(c + jobs_word(B, K))) {}
   static __host__ __device__ size_t jobs_word(int B, int K) {
-    return (2 * static_cast<size_t>(B) + static_cast<size_t>(B) * (2 * K + 1) + 3) & ~size_t(3);
+    return (static_cast<size_t>(kHead) + 3 * static_cast<size_t>(B) +
+            static_cast<size_t>(B) * (2 * K + 1) + 3) & ~size_t(3);
   }
 };
 
@@ -993,6 +629,8 @@ struct FlatSmem {
   int last;          // this CTA finished a row / a request / a draw
   int bcast_i;
   int acc[DSPARK_MAX_STEPS];  // the chain replay's per-draft outcome
+  int chunk;         // the draw item taken: its chunk, or -1 (none left)
+  DrawJob job;       // the draw item's request
 };
 
 // Outcome of draft k of request b (thread k of the CTA that finished the
@@ -1107,7 +745,10 @@ __device__ void request_row_done(const VerifyParams& P, const CtlView& C, FlatSm
         }
       }
     }
-    C.jobs[b] = J;  // read by the draw kernel, which runs after this one
+    C.jobs[b] = J;
+    __threadfence();  // the job before the request is listed
+    const unsigned int slot = atomicAdd(C.ready_count, 1u);
+    atomicExch(&C.ready[slot], static_cast<unsigned int>(b + 1));
   }
 }
 
@@ -1116,7 +757,8 @@ enum FlatRowKind : int {
   kFlatNone = 0,       // nothing to compute (padding, greedy draft row, top-p row done before)
   kFlatGreedy = 1,     // greedy target row: winner key of the raw row
   kFlatOnline = 2,     // max and exp-sum of the row (sampled target row kept whole, draft row)
-  kFlatRecorded = 3    // draft row whose statistics the Markov loop recorded
+  kFlatRecorded = 3,   // draft row whose statistics the Markov loop recorded
+  kFlatTopp = 4        // sampled target row with a top-p cut: the exact select, whole
 };
 struct FlatRow {
   int kind;
@@ -1144,8 +786,7 @@ __device__ FlatRow classify_row(const VerifyParams& P, int b, int j) {
   const float T = P.temperature[s];
   const bool greedy = !(T > 0.0f);
   if (r.is_target) {
-    if (!greedy && P.top_p[s] < 1.0f) return r;  // the top-p kernel's row
-    r.kind = greedy ? kFlatGreedy : kFlatOnline;
+    r.kind = greedy ? kFlatGreedy : (P.top_p[s] < 1.0f ? kFlatTopp : kFlatOnline);
     r.T = greedy ? 1.0f : T;
     r.off = (static_cast<int64_t>(b) * (K + 1) + r.k) * P.V;
     r.base = P.target;
@@ -1169,6 +810,319 @@ __device__ FlatRow classify_row(const VerifyParams& P, int b, int j) {
 // Bytes of the L2 prefetch window a slice keeps ahead of its loads.
 constexpr uint32_t kSliceWindow = 48u << 10;
 
+// ---- top-p rows inside the flat kernel: one CTA per row ---------------------
+// The exact select of the cluster version, with every histogram and
+// reduction in one CTA's shared memory: the distance-to-maximum bins (stage
+// 0, during the mass pass), their sub-bins (stage 1, which also lists its
+// candidates), then the ordered logit bits and the token id, each stage
+// splitting the boundary bin until it holds one element.
+struct TopSmem {
+  unsigned long long hmass[kRowBins];
+  unsigned int hcnt[kRowBins];
+  unsigned int hid[kRowBins];
+  unsigned long long red64[kRowWarps];
+  unsigned int red32[2 * kRowWarps];
+  int found_pos;
+  int f_bin;
+  unsigned long long f_before, f_mass;
+  unsigned int f_cnt, f_id, f_kmin, f_kmax;
+  unsigned int list_n;
+  float bcast_f;
+};
+
+struct BFound {
+  int bin;
+  unsigned long long before;  // running mass before the bin
+  unsigned long long mass;
+  unsigned int cnt, id;
+  unsigned int kmin, kmax;    // value-key range of all the stage's candidates
+};
+
+__device__ void top_hist_clear(TopSmem& t, int nb) {
+  for (int i = threadIdx.x; i < nb; i += kRowThreads) {
+    t.hmass[i] = 0ull;
+    t.hcnt[i] = 0u;
+    t.hid[i] = 0u;
+  }
+}
+
+// The first bin, in scan order (descending bin index if desc), whose running
+// mass from `above` reaches the target (t_hi:t_lo): a bin qualifies if it
+// holds an element (counted) or mass (mass-only histogram). Thread t scans a
+// run of nb / 256 bins; an exclusive prefix over the block gives each run's
+// start. Every thread returns the same result.
+__device__ BFound block_find(TopSmem& t, int nb, bool desc, unsigned long long above,
+                             unsigned long long t_hi, unsigned long long t_lo, uint32_t kmin,
+                             uint32_t kmax, bool counted) {
+  const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+  __syncthreads();  // the histogram is complete
+  // the candidates' value-key range
+  {
+    uint32_t lo = kmin, hi = kmax;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
+      hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
+    }
+    if (lane == 0) {
+      t.red32[wp] = lo;
+      t.red32[kRowWarps + wp] = hi;
+    }
+  }
+  const int per = nb / kRowThreads;
+  const int p0 = tid * per;
+  auto bin_at = [&](int pos) { return desc ? nb - 1 - pos : pos; };
+  unsigned long long tsum = 0ull;
+  for (int i = 0; i < per; ++i) tsum += t.hmass[bin_at(p0 + i)];
+  unsigned long long incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long nv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += nv;
+  }
+  if (lane == 31) t.red64[wp] = incl;
+  if (tid == 0) t.found_pos = 0x7FFFFFFF;
+  __syncthreads();
+  unsigned long long woff = 0ull;
+  for (int i = 0; i < wp; ++i) woff += t.red64[i];
+  unsigned long long run = above + woff + incl - tsum;
+  int found = 0x7FFFFFFF;
+  unsigned long long fbefore = 0ull;
+  for (int i = 0; i < per; ++i) {
+    const int bin = bin_at(p0 + i);
+    const unsigned long long mb = t.hmass[bin];
+    if ((counted ? t.hcnt[bin] > 0u : mb > 0ull) && reaches(run + mb, t_hi, t_lo)) {
+      found = p0 + i;
+      fbefore = run;
+      break;
+    }
+    run += mb;
+  }
+  atomicMin(&t.found_pos, found);
+  __syncthreads();
+  if (found != 0x7FFFFFFF && found == t.found_pos) {
+    const int bin = bin_at(found);
+    t.f_bin = bin;
+    t.f_before = fbefore;
+    t.f_mass = t.hmass[bin];
+    t.f_cnt = t.hcnt[bin];
+    t.f_id = t.hid[bin];
+  }
+  if (tid == 0) {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int i = 0; i < kRowWarps; ++i) {
+      lo = min(lo, t.red32[i]);
+      hi = max(hi, t.red32[kRowWarps + i]);
+    }
+    t.f_kmin = lo;
+    t.f_kmax = hi;
+    if (t.found_pos == 0x7FFFFFFF) {  // cannot happen: the stage's set holds the boundary
+      t.f_bin = 0;
+      t.f_before = above;
+      t.f_mass = 0ull;
+      t.f_cnt = 1u;
+      t.f_id = 0u;
+    }
+  }
+  __syncthreads();
+  BFound f;
+  f.bin = t.f_bin;
+  f.before = t.f_before;
+  f.mass = t.f_mass;
+  f.cnt = t.f_cnt;
+  f.id = t.f_id;
+  f.kmin = t.f_kmin;
+  f.kmax = t.f_kmax;
+  __syncthreads();  // the slots may be rewritten by the next stage
+  return f;
+}
+
+__device__ unsigned long long block_sum64(TopSmem& t, unsigned long long v) {
+  v = warp_sum64(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) t.red64[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long s = 0ull;
+  for (int i = 0; i < kRowWarps; ++i) s += t.red64[i];
+  __syncthreads();
+  return s;
+}
+
+// A sampled target row with a top-p cut, whole, by this CTA (vLLM PR #65007
+// Part 2, "Temperature and top-p"): its maximum, fixed-point mass and exact
+// boundary, written to P.tstats with p at the drafted token.
+template <class Fix>
+__device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem& t, Fix fix) {
+  const int tid = threadIdx.x, K = P.K, V = P.V;
+  RowView rv;
+  rv.bf16 = R.bf16;
+  rv.f = static_cast<const float*>(R.base) + R.off;
+  rv.h = static_cast<const uint16_t*>(R.base) + R.off;
+  rv.n = V;
+  const uint64_t pol_keep = policy_evict_last();   // passes 1 and 2: read again
+  const uint64_t pol_last = policy_evict_first();  // stage 1: the last full pass
+  const int32_t d = R.k < K ? P.draft[static_cast<int64_t>(R.b) * K + R.k] : -1;
+  TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(R.b) * (K + 1) + R.k;
+  auto raw_at = [&](int v) -> float {
+    return R.bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(R.base)[R.off + v])
+                  : static_cast<const float*>(R.base)[R.off + v];
+  };
+  // ---- pass 1 (HBM): the maximum ------------------------------------------------
+  unsigned long long ms = slice_online(rv, pol_keep, fix, false, 0.0f, kSliceWindow);
+  {
+    const float lm = ms_m(ms);
+    float v = lm;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    __syncthreads();
+    if ((tid & 31) == 0) t.red32[tid >> 5] = __float_as_uint(v);
+    __syncthreads();
+    if (tid == 0) {
+      float mm = -INFINITY;
+      for (int i = 0; i < kRowWarps; ++i) mm = fmaxf(mm, __uint_as_float(t.red32[i]));
+      t.bcast_f = mm;
+    }
+    __syncthreads();
+  }
+  const float m = t.bcast_f;
+  if (m == -INFINITY) {  // no value above -inf: p is one-hot at column 0
+    if (tid == 0) {
+      ts->m = m;
+      ts->D = 1.0f;
+      ts->kd_thr = 0u;
+      ts->id_thr = 0;
+      ts->p_d = d == 0 ? 1.0f : 0.0f;
+      ts->mode = kModeOneHot;
+      ts->amax_key = 0ull;
+    }
+    return;
+  }
+  // ---- pass 2 (L2): fixed-point mass and the stage-0 histogram -------------------
+  top_hist_clear(t, kRowBins);
+  __syncthreads();
+  unsigned long long F = 0ull;
+  row_sweep<4>(rv, pol_keep, fix, [&](int, float x) {
+    const unsigned long long f = fixed_mass(exp_rel(x, m));
+    F += f;
+    atomicAdd(&t.hmass[adigit0(x, m)], f);
+  });
+  F = block_sum64(t, F);
+  const int32_t s = P.rsi[R.b];
+  const unsigned long long P32 = topp_scaled(P.top_p[s]);
+  const unsigned long long t_lo = P32 * F;
+  const unsigned long long t_hi = __umul64hi(P32, F);
+  // stage 0: distance bins, ascending (mass only: stage 1 always runs)
+  BFound f = block_find(t, kRowBins, false, 0ull, t_hi, t_lo, 0xFFFFFFFFu, 0u, false);
+  f.cnt = 0u;
+  unsigned long long above = f.before;
+  const int a0 = f.bin;
+  int a1 = -1;
+  int kd_len = 0, id_len = 0;
+  uint32_t kd_pre = 0u, id_pre = 0u;
+  uint2* list = P.cand + static_cast<size_t>(blockIdx.x) * kVerifyListCap;
+  unsigned int list_len = 0xFFFFFFFFu;  // not built yet
+  for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
+    const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
+    const uint32_t c_kp = kd_pre, c_ip = id_pre;
+    auto match = [=](float x, uint32_t kd, uint32_t id) {
+      if (adigit0(x, m) != a0) return false;
+      if (c_a1 >= 0 && adigit1(x, m, a0) != c_a1) return false;
+      if (c_kl > 0 && (kd >> (32 - c_kl)) != c_kp) return false;
+      if (c_il > 0 && (id >> (22 - c_il)) != c_ip) return false;
+      return true;
+    };
+    auto digit = [=](float x, uint32_t kd, uint32_t id) -> int {
+      switch (stage) {
+        case 1: return adigit1(x, m, a0);
+        case 2: return static_cast<int>(kd >> 21);
+        case 3: return static_cast<int>((kd >> 10) & 0x7FFu);
+        case 4: return static_cast<int>(kd & 0x3FFu);
+        case 5: return static_cast<int>((id >> 11) & 0x7FFu);
+        default: return static_cast<int>(id & 0x7FFu);
+      }
+    };
+    const int nb = stage == 4 ? 1024 : kRowBins;
+    const bool desc = stage >= 2 && stage <= 4;  // larger kd first; distance and id ascending
+    top_hist_clear(t, nb);
+    if (stage == 1 && tid == 0) t.list_n = 0u;
+    __syncthreads();
+    uint32_t cmin = 0xFFFFFFFFu, cmax = 0u;  // value-key range of the candidates
+    auto visit = [&](uint32_t id, float x, bool append) {
+      const uint32_t kd = kd_of(x);
+      if (match(x, kd, id)) {
+        const int bin = digit(x, kd, id);
+        atomicAdd(&t.hmass[bin], fixed_mass(exp_rel(x, m)));
+        atomicAdd(&t.hcnt[bin], 1u);
+        atomicMax(&t.hid[bin], id);
+        cmin = min(cmin, kd);
+        cmax = max(cmax, kd);
+        if (append) {
+          const unsigned int at = atomicAdd(&t.list_n, 1u);
+          if (at < static_cast<unsigned int>(kVerifyListCap)) list[at] = make_uint2(id, __float_as_uint(x));
+        }
+      }
+    };
+    if (list_len <= static_cast<unsigned int>(kVerifyListCap)) {
+      for (unsigned int j = tid; j < list_len; j += kRowThreads) {
+        const uint2 e = __ldcg(list + j);
+        visit(e.x, __uint_as_float(e.y), false);
+      }
+    } else {
+      const bool append = stage == 1;
+      row_sweep<4>(rv, stage == 1 ? pol_last : pol_keep, fix,
+                   [&](int i, float x) { visit(static_cast<uint32_t>(i), x, append); });
+    }
+    f = block_find(t, nb, desc, above, t_hi, t_lo, cmin, cmax, true);
+    if (stage == 1) list_len = t.list_n;  // complete: block_find synchronised the CTA
+    above = f.before;
+    const uint32_t bin = static_cast<uint32_t>(f.bin);
+    if (stage == 1) {
+      a1 = f.bin;
+    } else if (stage <= 4) {
+      kd_pre = (kd_pre << (stage == 4 ? 10 : 11)) | bin;
+      kd_len += stage == 4 ? 10 : 11;
+    } else {
+      id_pre = (id_pre << 11) | bin;
+      id_len += 11;
+    }
+    // every candidate of this stage had one value (ties, e.g. in a bf16
+    // row), so the boundary bin does too: go on with the token-id stages
+    if (stage < 5 && f.cnt > 1u && f.kmin == f.kmax) {
+      kd_pre = f.kmin;
+      kd_len = 32;
+      stage = 4;
+    }
+  }
+  // f is the one-element bin at the boundary: its token, mass and logit
+  if (tid == 0) {
+    const int32_t id_thr = static_cast<int32_t>(f.id);
+    const unsigned long long Fk = above + f.mass;
+    const uint32_t kd_thr = kd_of(fix(raw_at(id_thr)));
+    const float D = __fmul_rn(__ull2float_rn(Fk), 0x1p-40f);
+    const bool has_d = d >= 0 && d < V;
+    const float x = has_d ? fix(raw_at(d)) : 0.0f;
+    const uint32_t kd = kd_of(x);
+    const bool keep = kd > kd_thr || (kd == kd_thr && d <= id_thr);
+    ts->p_d = has_d && keep ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
+    ts->m = m;
+    ts->D = D;
+    ts->kd_thr = kd_thr;
+    ts->id_thr = id_thr;
+    ts->mode = kModeThreshold;
+    ts->amax_key = 0ull;
+  }
+}
+
+__device__ void flat_topp_row(const VerifyParams& P, const FlatRow& R, TopSmem& t) {
+  if (R.T != 1.0f) {
+    const float T = R.T;
+    flat_topp_row_t(P, R, t, [T](float c) { return fmaxf(__fdiv_rn(c, T), -INFINITY); });
+  } else {
+    flat_topp_row_t(P, R, t, [](float c) { return fmaxf(c, -INFINITY); });
+  }
+}
+
+
 // One slice of a row: this CTA's partial in P.parts.
 __device__ void flat_slice(const VerifyParams& P, const FlatRow& R, int s, FlatSmem& sm) {
   const int V = P.V;
@@ -1179,8 +1133,6 @@ __device__ void flat_slice(const VerifyParams& P, const FlatRow& R, int s, FlatS
   rv.bf16 = R.bf16;
   rv.f = static_cast<const float*>(R.base) + R.off + v0;
   rv.h = static_cast<const uint16_t*>(R.base) + R.off + v0;
-  rv.vec = R.bf16 ? (reinterpret_cast<uintptr_t>(rv.h) & 7u) == 0
-                  : (reinterpret_cast<uintptr_t>(rv.f) & 15u) == 0;
   rv.n = v1 - v0;
   // normal priority: a residual draw soon reads the rows of the request's
   // first rejection again
@@ -1299,8 +1251,14 @@ __device__ void flat_finish_row(const VerifyParams& P, const FlatRow& R) {
   }
 }
 
+struct FlatShared {
+  FlatSmem f;
+  TopSmem t;         // top-p rows
+};
+
 // One row item r = (request, row, slice).
-__device__ void flat_row_item(const VerifyParams& P, const CtlView& C, FlatSmem& sm, int r) {
+__device__ void flat_row_item(const VerifyParams& P, const CtlView& C, FlatSmem& sm, TopSmem& t,
+                              int r) {
   const int per_req = 2 * P.K + 1;
   const int s = r % P.nslice;
   const int rr = r / P.nslice;
@@ -1318,6 +1276,10 @@ __device__ void flat_row_item(const VerifyParams& P, const CtlView& C, FlatSmem&
     __syncthreads();
     row_complete = sm.last != 0;
     if (row_complete && threadIdx.x < 32) flat_finish_row(P, R);
+  } else if (R.kind == kFlatTopp) {
+    // the whole row, by the CTA holding its first slice
+    row_complete = s == 0;
+    if (row_complete) flat_topp_row(P, R, t);
   } else {
     // nothing to read (or the recorded statistics): the first slice does it
     row_complete = s == 0;
@@ -1326,42 +1288,15 @@ __device__ void flat_row_item(const VerifyParams& P, const CtlView& C, FlatSmem&
   if (row_complete) request_row_done(P, C, sm, b);
 }
 
-// Row statistics of every row the top-p kernel did not take, and the
-// request's accept chain once its last row is done. Static schedule: CTA i
-// takes row items i, i + grid, ... (request order, a row's slices in turn).
-__global__ void __launch_bounds__(kRowThreads, 4) verify_flat_kernel(VerifyParams P) {
-  __shared__ FlatSmem sm;
-  const CtlView C(P.ctl, P.B, P.K);
-  const int n_items = P.B * (2 * P.K + 1) * P.nslice;
-  for (int r = blockIdx.x; r < n_items; r += gridDim.x) {
-    flat_row_item(P, C, sm, r);
-    __syncthreads();  // sm is reused by the next item
-  }
-  // the draw kernel may start its set-up (it waits for this grid before
-  // reading anything this kernel wrote)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// The draws: CTA (chunk, b) draws columns of chunk `chunk` of request b's
-// categorical; the CTA that finishes the request's last chunk writes its
-// outputs.
-__global__ void __launch_bounds__(kRowThreads) verify_draw_kernel(VerifyParams P) {
-  __shared__ FlatSmem sm;
-  __shared__ DrawJob job;
-  // the row kernel's results (the jobs) are complete once it has finished
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+// One draw item: chunk `chunk` of request J.b's categorical; the CTA that
+// finishes the request's last chunk writes its outputs.
+__device__ void flat_draw_chunk(const VerifyParams& P, const CtlView& C, FlatSmem& sm,
+                                const DrawJob& J, int chunk) {
   const int tid = threadIdx.x;
-  const int b = blockIdx.y, sub = blockIdx.x, nsub = gridDim.x, K = P.K, V = P.V;
-  const CtlView C(P.ctl, P.B, K);
-  static_assert(sizeof(DrawJob) % 8 == 0 && sizeof(DrawJob) / 8 <= kRowThreads, "job copy");
-  if (tid < static_cast<int>(sizeof(DrawJob) / 8))
-    reinterpret_cast<unsigned long long*>(&job)[tid] =
-        __ldcg(reinterpret_cast<const unsigned long long*>(&C.jobs[b]) + tid);
-  __syncthreads();
-  const DrawJob& J = job;
+  const int b = J.b, nsub = P.ndraw, K = P.K, V = P.V;
   int cw = (V + nsub - 1) / nsub;
   cw = (cw + 3) & ~3;
-  const int c0 = sub * cw, c1 = min(V, c0 + cw);
+  const int c0 = chunk * cw, c1 = min(V, c0 + cw);
   auto umax = [](unsigned long long a, unsigned long long b2) { return a > b2 ? a : b2; };
   unsigned long long key = 0ull;
   unsigned int any = 0u;
@@ -1371,8 +1306,8 @@ __global__ void __launch_bounds__(kRowThreads) verify_draw_kernel(VerifyParams P
   __syncthreads();
   const unsigned int anyb = __syncthreads_or(any != 0u) ? 1u : 0u;
   if (tid == 0) {
-    P.keys[static_cast<int64_t>(b) * P.kstride + sub] = key;
-    P.anypos[static_cast<int64_t>(b) * P.kstride + sub] = anyb;
+    P.keys[static_cast<int64_t>(b) * P.kstride + chunk] = key;
+    P.anypos[static_cast<int64_t>(b) * P.kstride + chunk] = anyb;
     __threadfence();
     sm.last = atomicAdd(&C.draws_done[b], 1u) == static_cast<unsigned int>(nsub) - 1u;
   }
@@ -1424,6 +1359,70 @@ __global__ void __launch_bounds__(kRowThreads) verify_draw_kernel(VerifyParams P
     P.out_tokens[static_cast<int64_t>(b) * (K + 1) + k] = o;
   }
   if (tid == 0) P.num_accepted[b] = J.invalid ? 0 : J.n_acc;
+}
+
+// Thread 0: the next draw item (sm.chunk = -1 when none is left). Items are
+// taken in publish order; item h is chunk h % ndraw of the request listed in
+// slot h / ndraw, which may still be finishing its rows (bounded wait).
+__device__ void take_draw(const VerifyParams& P, const CtlView& C, FlatSmem& sm) {
+  sm.chunk = -1;
+  const unsigned int n_draw = static_cast<unsigned int>(P.B) * P.ndraw;
+  const unsigned int h = atomicAdd(C.draw_head, 1u);
+  if (h >= n_draw) return;
+  const unsigned int slot = h / P.ndraw;
+  unsigned int b1 = ld_acquire_gpu(&C.ready[slot]);
+  if (b1 == 0u) {
+    const unsigned long long t0 = globaltimer_ns();
+    unsigned int nap = 64u;
+    do {
+      __nanosleep(nap);
+      if (nap < 512u) nap <<= 1;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        report(P.status, DSPARK_ERR_TIMEOUT);
+        return;
+      }
+      b1 = ld_acquire_gpu(&C.ready[slot]);
+    } while (b1 == 0u);
+  }
+  // the publisher's job, 8-byte words loaded independently
+  const unsigned long long* src = reinterpret_cast<const unsigned long long*>(&C.jobs[b1 - 1u]);
+  unsigned long long* dst = reinterpret_cast<unsigned long long*>(&sm.job);
+#pragma unroll
+  for (int i = 0; i < static_cast<int>(sizeof(DrawJob) / 8); ++i) dst[i] = __ldcg(src + i);
+  sm.chunk = static_cast<int>(h % P.ndraw);
+}
+
+// Row statistics of every row, the requests' accept chains, and the draws.
+// The rows: each CTA claims the next row item (request order, a row's
+// slices in turn) with an atomic counter, the claim of its next item issued
+// when it starts the current one, so the claim's latency hides behind the
+// item's work; then each CTA takes draw items of the requests published so
+// far.
+__global__ void __launch_bounds__(kRowThreads, 4) verify_flat_kernel(VerifyParams P) {
+  __shared__ FlatShared shared;
+  FlatSmem& sm = shared.f;
+  const CtlView C(P.ctl, P.B, P.K);
+  const unsigned int n_items = static_cast<unsigned int>(P.B) * (2 * P.K + 1) * P.nslice;
+  if (threadIdx.x == 0) sm.chunk = static_cast<int>(atomicAdd(C.row_head, 1u));
+  __syncthreads();
+  for (;;) {
+    const unsigned int r = static_cast<unsigned int>(sm.chunk);
+    if (r >= n_items) break;
+    unsigned int next = 0u;
+    if (threadIdx.x == 0) next = atomicAdd(C.row_head, 1u);  // used after this item
+    __syncthreads();  // every thread has read r
+    flat_row_item(P, C, sm, shared.t, static_cast<int>(r));
+    __syncthreads();  // sm is reused by the next item
+    if (threadIdx.x == 0) sm.chunk = static_cast<int>(next);
+    __syncthreads();
+  }
+  for (;;) {
+    if (threadIdx.x == 0) take_draw(P, C, sm);
+    __syncthreads();
+    if (sm.chunk < 0) break;
+    flat_draw_chunk(P, C, sm, sm.job, sm.chunk);
+    __syncthreads();  // sm.job is rewritten by the next take
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1506,8 +1505,6 @@ __device__ void topk_row(const TopkParams& P, int W, int row_id, cg::cluster_gro
   rv.bf16 = P.base_bf16 != 0;
   rv.f = static_cast<const float*>(P.base) + off + v0;
   rv.h = static_cast<const uint16_t*>(P.base) + off + v0;
-  rv.vec = rv.bf16 ? (reinterpret_cast<uintptr_t>(rv.h) & 7u) == 0
-                   : (reinterpret_cast<uintptr_t>(rv.f) & 15u) == 0;
   rv.n = n;
   const uint64_t pol = policy_evict_last();
   int32_t* cidx = P.cand_idx + static_cast<int64_t>(row_id) * P.k;
@@ -1735,53 +1732,10 @@ size_t verify_parts_bytes(int B, int K, int V) {
   return static_cast<size_t>(B) * (2 * K + 1) * verify_nslice(B, K, V) * sizeof(RowPart);
 }
 
-cudaError_t launch_verify(const VerifyParams& p0, int CL, int W, cudaStream_t stream) {
+cudaError_t launch_verify(const VerifyParams& p0, cudaStream_t stream) {
   if (p0.B == 0) return cudaSuccess;
   VerifyParams p = p0;
-  // ---- 1. top-p target rows (thread-block clusters) ---------------------------
-  {
-    const int rows = p.B * (p.K + 1);
-    const size_t smem = verify_rows_smem_bytes(W);
-    cudaError_t err = cudaFuncSetAttribute(verify_topp_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    if (CL > 8) {
-      err = cudaFuncSetAttribute(verify_topp_kernel,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (err != cudaSuccess) return err;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kRowThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(CL);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // as many clusters as fit at once, but no more rows in flight than about
-    // 80 MB of L2 holds: a top-p row's later passes read it again from L2
-    cfg.gridDim = dim3(static_cast<unsigned>(rows * CL), 1, 1);
-    int max_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, verify_topp_kernel, &cfg) != cudaSuccess ||
-        max_clusters < 1) {
-      (void)cudaGetLastError();
-      max_clusters = 1;
-    }
-    const size_t row_bytes = static_cast<size_t>(p.V) * (p.target_bf16 ? 2 : 4);
-    const int l2_rows = static_cast<int>((80ull << 20) / (row_bytes > 0 ? row_bytes : 1));
-    int nclusters = rows < max_clusters ? rows : max_clusters;
-    if (l2_rows >= 1 && nclusters > l2_rows) nclusters = l2_rows;
-    if (nclusters * CL > kVerifyMaxCtas) nclusters = kVerifyMaxCtas / CL;  // one list per CTA
-    if (nclusters < 1) nclusters = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
-    err = cudaLaunchKernelEx(&cfg, verify_topp_kernel, p, W);
-    if (err != cudaSuccess) return err;
-  }
-  // ---- 2. every other row, and the chains (persistent CTAs) ------------------
+  // ---- every row, the chains, the draws: persistent CTAs ----------------------
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -1792,31 +1746,26 @@ cudaError_t launch_verify(const VerifyParams& p0, int CL, int W, cudaStream_t st
     sms = 1;
     per_sm = 1;
   }
-  const int items = p.B * (2 * p.K + 1) * p.nslice;
-  int ctas = sms * per_sm;
-  if (ctas > items) ctas = items;
-  verify_flat_kernel<<<ctas, kRowThreads, 0, stream>>>(p);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  // ---- 3. the draws: chunks of each request's categorical ----------------------
-  // enough chunks to fill the GPU about twice, none shorter than 1024 columns;
-  // launched as a programmatic dependent of the row kernel, so its CTAs are
-  // set up while that kernel drains
-  int nd = (2 * sms * per_sm + p.B - 1) / p.B;
+  const int ctas = sms * per_sm;
+  // draw chunks per request: about one wave of CTAs over the batch, none
+  // shorter than 1024 columns
+  int nd = (ctas + p.B - 1) / p.B;
   if (nd > p.kstride) nd = p.kstride;
   if (nd < 1) nd = 1;
   p.ndraw = nd;
-  cudaLaunchConfig_t dc = {};
-  dc.gridDim = dim3(static_cast<unsigned>(nd), static_cast<unsigned>(p.B), 1);
-  dc.blockDim = dim3(kRowThreads, 1, 1);
-  dc.dynamicSmemBytes = 0;
-  dc.stream = stream;
-  cudaLaunchAttribute da[1];
-  da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  da[0].val.programmaticStreamSerializationAllowed = 1;
-  dc.attrs = da;
-  dc.numAttrs = 1;
-  return cudaLaunchKernelEx(&dc, verify_draw_kernel, p);
+  // cooperative: every CTA is resident at once, which a CTA waiting for a
+  // request that other CTAs are still finishing relies on
+  cudaLaunchConfig_t fc = {};
+  fc.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  fc.blockDim = dim3(kRowThreads, 1, 1);
+  fc.dynamicSmemBytes = 0;
+  fc.stream = stream;
+  cudaLaunchAttribute fa[1];
+  fa[0].id = cudaLaunchAttributeCooperative;
+  fa[0].val.cooperative = 1;
+  fc.attrs = fa;
+  fc.numAttrs = 1;
+  return cudaLaunchKernelEx(&fc, verify_flat_kernel, p);
 }
 
 cudaError_t launch_topk_rows(const TopkParams& p, int CL, int W, cudaStream_t stream) {
