@@ -355,6 +355,95 @@ def _config(w, args):
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
 
+def _capture(st, stream):
+    """One decode step as one CUDA graph of both library calls (the Markov
+    loop, then verification, on one stream), and each half as a graph of its
+    own (to split the step)."""
+    import torch
+    with torch.cuda.stream(stream):
+        st.run(stream=stream)
+    stream.synchronize()
+    g = {"step": torch.cuda.CUDAGraph(), "markov": torch.cuda.CUDAGraph(),
+         "verify": torch.cuda.CUDAGraph()}
+    with torch.cuda.graph(g["step"], stream=stream):
+        st.markov(stream=stream)
+        st.verify(stream=stream)
+    with torch.cuda.graph(g["markov"], stream=stream):
+        st.markov(stream=stream)
+    with torch.cuda.graph(g["verify"], stream=stream):
+        st.verify(stream=stream)
+    return g
+
+
+def _one_step(g, stream, flush):
+    """L2 flush, then one timed replay of the whole step; returns its events."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        flush.fill_(1)
+        ev[0].record(stream)
+        g["step"].replay()
+        ev[1].record(stream)
+    return ev
+
+
+def _split_step(g, stream, flush):
+    """L2 flush, then the loop's graph and the verifier's, timed apart."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    with torch.cuda.stream(stream):
+        flush.fill_(1)
+        ev[0].record(stream)
+        g["markov"].replay()
+        ev[1].record(stream)
+        g["verify"].replay()
+        ev[2].record(stream)
+    return ev
+
+
+# The workloads timed beside the headline one (same run, same timing rules):
+# the drafter at batch 1 and 4, the verify-heavy bf16 workload, the long-draft
+# stress workload and the odd vocabulary.
+OTHER_CONFIGS = [("minimax", 1), ("minimax", 4), ("qwen", 256), ("long", 128), ("odd", 8)]
+
+
+def other_configs(args, stream, flush, peak):
+    """Each other workload: its step, loop and verifier times and the
+    verifier's fraction of the HBM peak."""
+    import torch
+    from verify_dspark_markov_step_gb300 import workloads as wl
+    from verify_dspark_markov_step_gb300.step import DecodeStep
+    out = []
+    steps = max(3, min(args.steps, 10))
+    for name, batch in OTHER_CONFIGS:
+        if (name, batch) == (args.config, args.batch):
+            continue
+        w = wl.make(name, batch=batch)
+        st = DecodeStep(w, draft_topk=args.draft_topk, draft_stats=args.draft_stats)
+        g = _capture(st, stream)
+        for _ in range(3):
+            _one_step(g, stream, flush)
+            _split_step(g, stream, flush)
+        evs = [_one_step(g, stream, flush) for _ in range(steps)]
+        sev = [_split_step(g, stream, flush) for _ in range(steps)]
+        torch.cuda.synchronize()
+        step_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+        loop_us = statistics.mean(e[0].elapsed_time(e[1]) for e in sev) * 1e3
+        ver_us = statistics.mean(e[1].elapsed_time(e[2]) for e in sev) * 1e3
+        per_step, ver_bytes = algorithmic_bytes(w)
+        out.append({
+            "workload": f"{w.name}: batch {w.B}, K={w.K}, vocab {w.V}, markov_rank {w.R}",
+            "steps": steps, "value": round(step_us, 2), "unit": "us",
+            "loop_us": round(loop_us, 2), "verify_us": round(ver_us, 2),
+            "loop_frac": round(per_step * w.K / (loop_us * 1e-6) / 1e9 / peak, 3),
+            "verify_frac": round(ver_bytes / (ver_us * 1e-6) / 1e9 / peak, 3),
+            "mean_accepted": round(st.num_accepted.float().mean().item(), 3),
+            "status": st.status_code()})
+        del g, st
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, local):
     import torch
     from verify_dspark_markov_step_gb300 import build
@@ -368,43 +457,11 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
 
-    # One decode step is one CUDA graph of both library calls (the Markov
-    # loop, then verification, on one stream); the halves are also captured
-    # as graphs of their own, timed after the steps, to split the step.
-    with torch.cuda.stream(stream):
-        st.run(stream=stream)
-    stream.synchronize()
-    g_step = torch.cuda.CUDAGraph()
-    g_markov = torch.cuda.CUDAGraph()
-    g_verify = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_step, stream=stream):
-        st.markov(stream=stream)
-        st.verify(stream=stream)
-    with torch.cuda.graph(g_markov, stream=stream):
-        st.markov(stream=stream)
-    with torch.cuda.graph(g_verify, stream=stream):
-        st.verify(stream=stream)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
-
-    def one_step(ev):
-        with torch.cuda.stream(stream):
-            flush.fill_(1)
-            ev[0].record(stream)
-            g_step.replay()
-            ev[1].record(stream)
-
-    def split_step(ev):
-        with torch.cuda.stream(stream):
-            flush.fill_(1)
-            ev[0].record(stream)
-            g_markov.replay()
-            ev[1].record(stream)
-            g_verify.replay()
-            ev[2].record(stream)
-
+    graphs = _capture(st, stream)
     for _ in range(args.warmup):
-        one_step([torch.cuda.Event(enable_timing=True) for _ in range(2)])
-        split_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+        _one_step(graphs, stream, flush)
+        _split_step(graphs, stream, flush)
     torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
@@ -412,10 +469,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        one_step(evs[i])
+    evs = [_one_step(graphs, stream, flush) for _ in range(args.steps)]
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     if world > 1:
@@ -423,9 +478,7 @@ def run_ours(args, rank, world, local):
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms = max_over_ranks(statistics.mean(step_ms), world, "cuda")
     # the two halves, each its own graph (each pays its own graph launch)
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        split_step(sev[i])
+    sev = [_split_step(graphs, stream, flush) for _ in range(args.steps)]
     torch.cuda.synchronize()
     clk = clocks.stop()
     loop_ms = [e[0].elapsed_time(e[1]) for e in sev]
@@ -501,7 +554,8 @@ def run_ours(args, rank, world, local):
     loop_us = statistics.mean(loop_ms) * 1e3
     ver_us = statistics.mean(ver_ms) * 1e3
     achieved = per_launch / (loop_us * 1e-6) / 1e9
-    traffic = None if args.draft_topk else _traffic_from_profile(args)
+    traffic = None if args.draft_topk or args.draft_stats else _traffic_from_profile(
+        args, "markov_loop_tc_minimax_b32.md", ("markov_tc.cu", "common.cuh", "tc_ptx.cuh"))
     line = {
         "metric": METRIC, "value": round(ms * 1e3, 2), "unit": "us", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -529,26 +583,37 @@ def run_ours(args, rank, world, local):
                      "verify_frac": round(ver_bytes / (ver_us * 1e-6) / 1e9 / peak, 3)},
         "e2e": {"value": round(e2e_ms * 1e3, 1), "unit": "us", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        # the Markov loop (top-k: candidate selection + loop), and the two
-        # verification kernels (top-p rows; every other row and the draws)
-        "gpu_launches": args.steps * (4 if args.draft_topk else 3),
+        # per step: the Markov loop kernel (top-k: candidate selection, then
+        # the loop) and the one verification kernel; the graph's memset nodes
+        # (the loop's and the verifier's cleared control words) are not kernels
+        "gpu_launches": args.steps * (3 if args.draft_topk else 2),
+        "memset_nodes_per_step": 3 if args.draft_stats else 2,
         "clocks": clk, "status": status, "wall_s_timed_region": round(wall, 4),
     }
+    vt = None if args.draft_topk or args.draft_stats else _traffic_from_profile(
+        args, "verify_flat_minimax_b32.md",
+        ("verify_stats.cu", "verify_draw.cuh", "verify_common.cuh", "common.cuh", "kernels.h"))
+    line["roofline"]["verify_traffic"] = vt
+    if rank == 0 and world == 1 and not args.no_other_configs:
+        del graphs
+        torch.cuda.empty_cache()
+        line["other_configs"] = other_configs(args, stream, flush, peak)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def _traffic_from_profile(args):
-    """DRAM bytes (read + write) per launch of the Markov loop kernel from the
-    committed ncu summary, if it was taken on this workload and on the current
-    kernel sources (its source hash matches); else None."""
+def _traffic_from_profile(args, summary, sources):
+    """DRAM bytes (read + write) per launch of a kernel from its committed ncu
+    summary under profiles/, if it was taken on this workload (MiniMax-like,
+    batch 32) and on the current kernel sources (its source hash matches);
+    else None."""
     import hashlib
     import re
     if args.config != "minimax" or args.batch != 32:
         return None
-    p = os.path.join(ROOT, "profiles", "markov_loop_tc_minimax_b32.md")
+    p = os.path.join(ROOT, "profiles", summary)
     try:
         with open(p) as f:
             txt = f.read()
@@ -557,7 +622,7 @@ def _traffic_from_profile(args):
         if not t or not h:
             return None
         m = hashlib.sha256()
-        for name in ("markov_tc.cu", "common.cuh", "tc_ptx.cuh"):
+        for name in sources:
             with open(os.path.join(ROOT, "verify_dspark_markov_step_gb300", "csrc", name), "rb") as f:
                 m.update(f.read())
         return int(t.group(1)) if m.hexdigest().startswith(h.group(1)) else None
@@ -574,6 +639,8 @@ def main():
     ap.add_argument("--config", default="minimax")
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="time the named workload only (no other_configs block)")
     ap.add_argument("--draft-topk", type=int, default=0,
                     help="time the top-k variant of the Markov loop (0: the dense loop)")
     ap.add_argument("--draft-stats", action="store_true",

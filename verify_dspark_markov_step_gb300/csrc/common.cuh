@@ -103,6 +103,14 @@ __device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsig
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// round toward zero: with 2^23 added to a value in [0, 2^23), the sum holds
+// the value's integer part in its low mantissa bits
+__device__ __forceinline__ unsigned long long f2_add_rz(unsigned long long a,
+                                                        unsigned long long b) {
+  unsigned long long d;
+  asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 
 // ---- temperature: x = z / T, correctly rounded ------------------------------
 // For a column with T in [2^-30, 2^30] and r = rn(1/T) (correctly rounded

@@ -144,7 +144,7 @@ size_t verify_parts_bytes(int B, int K, int V);
 // Row-statistics CTAs that keep a top-p candidate list in the workspace, and
 // the list's capacity per CTA (a longer candidate set is swept instead).
 constexpr int kVerifyMaxCtas = 1024;
-constexpr int kVerifyListCap = 512;
+constexpr int kVerifyListCap = 8192;
 
 size_t verify_tstats_bytes(int B, int K);
 size_t verify_dstats_bytes(int B, int K);

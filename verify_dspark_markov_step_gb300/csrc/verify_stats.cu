@@ -811,24 +811,62 @@ __device__ FlatRow classify_row(const VerifyParams& P, int b, int j) {
 constexpr uint32_t kSliceWindow = 48u << 10;
 
 // ---- top-p rows inside the flat kernel: one CTA per row ---------------------
-// The exact select of the cluster version, with every histogram and
-// reduction in one CTA's shared memory: the distance-to-maximum bins (stage
-// 0, during the mass pass), their sub-bins (stage 1, which also lists its
-// candidates), then the ordered logit bits and the token id, each stage
-// splitting the boundary bin until it holds one element.
+// The keep set of a sampled row with top_p < 1 (vLLM PR #65007 Part 2,
+// "Temperature and top-p"): the smallest prefix, in the order of larger x
+// first and lower token id on ties, whose 2^40 fixed-point mass reaches
+// top_p times the row's total F. Two passes over the row find it in the
+// common case:
+//  1. the maximum m, and a count histogram of the values in bins of 1/128 of
+//     a logit unit around an anchor (the largest of 256 values spread over
+//     the row); the counts, weighted by exp at the bin centres, estimate
+//     where the cumulative mass reaches top_p, and so a window of distance
+//     bins (1/64 unit below m, the bins of the exact select) around the
+//     boundary;
+//  2. the exact F, the exact mass of every element above the window, and a
+//     list (token id, x) of the elements inside it.
+// The exact mass of each window bin then comes from the list, and the
+// boundary bin is the one where the exact running mass first reaches the
+// target; its elements are split further from the list alone (stages 1-6
+// below). When the estimate missed (the boundary lies outside the window)
+// or the list overflowed, the row takes the exact select: a third pass with
+// the full distance-bin mass histogram (stage 0), then the stages, sweeping
+// the row again if the boundary bin's candidates do not fit in the list.
+// Either way the result is the same exact boundary.
 struct TopSmem {
-  unsigned long long hmass[kRowBins];
+  unsigned long long hmass[kRowBins];  // pass 1: the count histogram (kTopFine words)
   unsigned int hcnt[kRowBins];
   unsigned int hid[kRowBins];
-  unsigned long long red64[kRowWarps];
+  unsigned long long red64[2 * kRowWarps];
+  unsigned long long wmass[kRowWarps][8];  // window-bin masses per warp
+  unsigned int wcnt[kRowWarps][8];
+  unsigned int wlen[kRowWarps];            // entries in each warp's list segment
+  unsigned int cand_n;                     // candidates of the boundary bin
   unsigned int red32[2 * kRowWarps];
+  float redf[kRowWarps];
   int found_pos;
   int f_bin;
   unsigned long long f_before, f_mass;
   unsigned int f_cnt, f_id, f_kmin, f_kmax;
   unsigned int list_n;
+  int fast_ok;
   float bcast_f;
 };
+
+// pass-1 histogram: kTopFine bins of 1/128 unit, from kTopFineTop above the
+// anchor down (the first and last bins also take everything beyond)
+constexpr int kTopFine = 4096;
+constexpr float kTopFineTop = 12.0f;
+static_assert(kTopFine * sizeof(unsigned int) <= sizeof(unsigned long long) * kRowBins,
+              "the pass-1 histogram lives in the stage histogram's words");
+// distance bins on each side of the estimated boundary bin kept exact in pass 2
+constexpr int kTopWin = 2;
+static_assert(2 * kTopWin + 1 <= 8, "window bins per warp slot");
+// each warp's share of the CTA's list in pass 2, and the candidates that the
+// boundary bin may hold for the sort below
+constexpr int kTopSeg = kVerifyListCap / kRowWarps;
+constexpr int kTopSort = 1024;
+static_assert(kTopSort * sizeof(unsigned long long) <= sizeof(unsigned long long) * kRowBins,
+              "the sort keys live in the stage histogram's words");
 
 struct BFound {
   int bin;
@@ -937,54 +975,257 @@ __device__ BFound block_find(TopSmem& t, int nb, bool desc, unsigned long long a
   return f;
 }
 
-__device__ unsigned long long block_sum64(TopSmem& t, unsigned long long v) {
-  v = warp_sum64(v);
+// Block sums of two values (every thread gets both).
+__device__ void block_sum64x2(TopSmem& t, unsigned long long& a, unsigned long long& b) {
+  a = warp_sum64(a);
+  b = warp_sum64(b);
   __syncthreads();
-  if ((threadIdx.x & 31) == 0) t.red64[threadIdx.x >> 5] = v;
+  if ((threadIdx.x & 31) == 0) {
+    t.red64[threadIdx.x >> 5] = a;
+    t.red64[kRowWarps + (threadIdx.x >> 5)] = b;
+  }
   __syncthreads();
-  unsigned long long s = 0ull;
-  for (int i = 0; i < kRowWarps; ++i) s += t.red64[i];
+  a = 0ull;
+  b = 0ull;
+  for (int i = 0; i < kRowWarps; ++i) {
+    a += t.red64[i];
+    b += t.red64[kRowWarps + i];
+  }
   __syncthreads();
-  return s;
 }
 
-// A sampled target row with a top-p cut, whole, by this CTA (vLLM PR #65007
-// Part 2, "Temperature and top-p"): its maximum, fixed-point mass and exact
-// boundary, written to P.tstats with p at the drafted token.
-template <class Fix>
-__device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem& t, Fix fix) {
-  const int tid = threadIdx.x, K = P.K, V = P.V;
+__device__ unsigned long long block_sum64(TopSmem& t, unsigned long long v) {
+  unsigned long long z = 0ull;
+  block_sum64x2(t, v, z);
+  return v;
+}
+
+__device__ __forceinline__ float warp_maxf(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// x of a raw target value: divided by the temperature (correctly rounded, by
+// Markstein's FMA form where it holds, as temp_div2), NaN read as -inf.
+template <bool kScale>
+struct TempFix {
+  float T = 1.0f, r = 1.0f;
+  bool slow = false;
+  unsigned long long r2 = 0ull, nt2 = 0ull;
+  __device__ explicit TempFix(float T_) : T(T_) {
+    if constexpr (kScale) {
+      r = __frcp_rn(T);
+      slow = !temp_div_t_ok(T);
+      r2 = f2_pack(r, r);
+      nt2 = f2_pack(-T, -T);
+    }
+  }
+  __device__ __forceinline__ float one(float z) const {
+    if constexpr (!kScale) {
+      return fmaxf(z, -INFINITY);
+    } else {
+      float x;
+      if (slow || !temp_div_fast_ok(z)) {
+        x = __fdiv_rn(z, T);
+      } else {
+        const float q = __fmul_rn(z, r);
+        x = __fmaf_rn(__fmaf_rn(q, -T, z), r, q);
+      }
+      return fmaxf(x, -INFINITY);
+    }
+  }
+  __device__ __forceinline__ void four(const float (&z)[4], float (&x)[4]) const {
+    if constexpr (!kScale) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = fmaxf(z[e], -INFINITY);
+    } else {
+      f2_unpack(temp_div2(f2_pack(z[0], z[1]), r2, nt2, slow), x[0], x[1]);
+      f2_unpack(temp_div2(f2_pack(z[2], z[3]), r2, nt2, slow), x[2], x[3]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = fmaxf(x[e], -INFINITY);
+    }
+  }
+};
+
+// A sweep that hands `body4` the four raw values of each aligned group
+// (element index of the first) and `body1` the single values of the
+// unaligned head and the ragged tail, each with a flag that says whether the
+// values are the row's (false: padding to keep the warp together). Every
+// loop runs the same trip count in all 32 lanes of a warp, so a body may use
+// full-warp votes. Thread 0 keeps pf_window bytes of the row on their way
+// into L2 (L2Window).
+template <int kU, bool kBf16, class Body4, class Body1>
+__device__ __forceinline__ void row_quads_t(const RowView& rv, uint64_t pol, uint32_t pf_window,
+                                            Body4 body4, Body1 body1) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  constexpr int kEs = kBf16 ? 2 : 4;
+  L2Window pf(kBf16 ? static_cast<const void*>(rv.h) : static_cast<const void*>(rv.f),
+              static_cast<size_t>(rv.n) * kEs, tid == 0 ? pf_window : 0u);
+  pf.advance(0);
+  const int head = aligned_head<kBf16>(rv);
+  auto ld1 = [&](int i) -> float {
+    return kBf16 ? bf16_bits_to_float(ld_hint_u16(rv.h + i, pol)) : ld_hint_f32(rv.f + i, pol);
+  };
+  auto load4 = [&](int i, float (&v)[4]) {  // 4 values from aligned element index i
+    if constexpr (kBf16) {
+      const uint2 w = ld_hint_u2(rv.h + i, pol);
+      v[0] = bf16_bits_to_float(static_cast<uint16_t>(w.x & 0xFFFFu));
+      v[1] = bf16_bits_to_float(static_cast<uint16_t>(w.x >> 16));
+      v[2] = bf16_bits_to_float(static_cast<uint16_t>(w.y & 0xFFFFu));
+      v[3] = bf16_bits_to_float(static_cast<uint16_t>(w.y >> 16));
+    } else {
+      const float4 c = ld_hint_f4(rv.f + i, pol);
+      v[0] = c.x;
+      v[1] = c.y;
+      v[2] = c.z;
+      v[3] = c.w;
+    }
+  };
+  const int n4 = (rv.n - head) >> 2;
+  const int tail0 = head + 4 * n4;  // the ragged tail: fewer than 4 values
+  if (tid < 32) {                   // warp 0: the head and the tail, at most 3 values each
+    const bool hv = lane < head;
+    body1(lane, hv ? ld1(lane) : 0.0f, hv);
+    const bool tv = tail0 + lane < rv.n;
+    body1(tail0 + lane, tv ? ld1(tail0 + lane) : 0.0f, tv);
+  }
+  int i = tid;
+  const int w0 = tid - lane;  // this warp's first thread: the loops' bounds are the warp's
+  for (; w0 + (i - tid) + 31 + (kU - 1) * kRowThreads < n4; i += kU * kRowThreads) {
+    pf.advance(static_cast<size_t>(head) * kEs + static_cast<size_t>(i + kU * kRowThreads) * 4 * kEs);
+    float v[kU][4];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) load4(head + 4 * (i + u * kRowThreads), v[u]);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) body4(head + 4 * (i + u * kRowThreads), v[u], true);
+  }
+  for (; w0 + (i - tid) < n4; i += kRowThreads) {
+    const bool ok = i < n4;
+    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (ok) load4(head + 4 * i, v);
+    body4(head + 4 * i, v, ok);
+  }
+}
+
+// The pass-2 sums of one thread. The mass f = rint(e 2^40) of an element
+// is taken in two exact fp32 pieces, h = floor(e 2^20) and l = rint of the
+// rest times 2^20 (f = h 2^20 + l, ties to even as rint), each read from
+// the mantissa of a sum with 2^23; the 32-bit sums of their bit patterns
+// are folded into 64-bit totals every kFold elements, before they could
+// wrap (kFold (2^20 + 1) < 2^31).
+struct MassSums {
+  static constexpr uint32_t kBias = 0x4B000000u;  // bits of 2^23
+  static constexpr uint32_t kFold = 1024u;
+  unsigned long long F = 0ull, A = 0ull;  // all elements; elements above the window
+  uint32_t h = 0u, l = 0u, n = 0u, ha = 0u, la = 0u, na = 0u;
+  __device__ __forceinline__ void add(uint32_t hb, uint32_t lb, bool above) {
+    h += hb;
+    l += lb;
+    ++n;
+    if (above) {
+      ha += hb;
+      la += lb;
+      ++na;
+    }
+  }
+  __device__ __forceinline__ void fold() {
+    F += (static_cast<unsigned long long>(h - n * kBias) << 20) +
+         static_cast<unsigned long long>(l - n * kBias);
+    A += (static_cast<unsigned long long>(ha - na * kBias) << 20) +
+         static_cast<unsigned long long>(la - na * kBias);
+    h = l = n = ha = la = na = 0u;
+  }
+};
+
+// Appends to a warp's own list segment: every lane of the warp calls it
+// with the same `n` (entries so far, kept in a register); no atomics.
+__device__ __forceinline__ void seg_append(uint2* seg, unsigned int& n, bool want, uint32_t id,
+                                           float x) {
+  const unsigned int bal = __ballot_sync(0xFFFFFFFFu, want);
+  const int lane = threadIdx.x & 31;
+  if (want) {
+    const unsigned int at = n + static_cast<unsigned int>(__popc(bal & ((1u << lane) - 1u)));
+    if (at < static_cast<unsigned int>(kTopSeg)) seg[at] = make_uint2(id, __float_as_uint(x));
+  }
+  n += static_cast<unsigned int>(__popc(bal));
+}
+
+// x from its order key (ordered_bits, x not NaN)
+__device__ __forceinline__ float x_of_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+template <bool kBf16, bool kScale>
+__device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem& t) {
+  const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5, K = P.K, V = P.V;
+  const TempFix<kScale> fx(R.T);
+  auto fix = [&](float c) { return fx.one(c); };
   RowView rv;
-  rv.bf16 = R.bf16;
+  rv.bf16 = kBf16;
   rv.f = static_cast<const float*>(R.base) + R.off;
   rv.h = static_cast<const uint16_t*>(R.base) + R.off;
   rv.n = V;
-  const uint64_t pol_keep = policy_evict_last();   // passes 1 and 2: read again
-  const uint64_t pol_last = policy_evict_first();  // stage 1: the last full pass
+  const uint64_t pol_keep = policy_evict_last();   // read again by a later pass
+  const uint64_t pol_last = policy_evict_first();  // the last full pass
   const int32_t d = R.k < K ? P.draft[static_cast<int64_t>(R.b) * K + R.k] : -1;
   TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(R.b) * (K + 1) + R.k;
   auto raw_at = [&](int v) -> float {
-    return R.bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(R.base)[R.off + v])
-                  : static_cast<const float*>(R.base)[R.off + v];
+    return kBf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(R.base)[R.off + v])
+                 : static_cast<const float*>(R.base)[R.off + v];
   };
-  // ---- pass 1 (HBM): the maximum ------------------------------------------------
-  unsigned long long ms = slice_online(rv, pol_keep, fix, false, 0.0f, kSliceWindow);
+  uint2* list = P.cand + static_cast<size_t>(blockIdx.x) * kVerifyListCap;
+  unsigned int* fine = reinterpret_cast<unsigned int*>(t.hmass);
+
+  // ---- the anchor: the largest of 256 values spread over the row ----------------
+  float anchor;
   {
-    const float lm = ms_m(ms);
-    float v = lm;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    const int at = static_cast<int>((static_cast<long long>(tid) * V) / kRowThreads);
+    const float v = warp_maxf(fix(raw_at(at)));
+    for (int i = tid; i < kTopFine; i += kRowThreads) fine[i] = 0u;
+    if (lane == 0) t.red32[wp] = __float_as_uint(v);
     __syncthreads();
-    if ((tid & 31) == 0) t.red32[tid >> 5] = __float_as_uint(v);
-    __syncthreads();
-    if (tid == 0) {
-      float mm = -INFINITY;
-      for (int i = 0; i < kRowWarps; ++i) mm = fmaxf(mm, __uint_as_float(t.red32[i]));
-      t.bcast_f = mm;
-    }
-    __syncthreads();
+    anchor = -INFINITY;
+    for (int i = 0; i < kRowWarps; ++i) anchor = fmaxf(anchor, __uint_as_float(t.red32[i]));
+    if (!(anchor > -INFINITY && anchor < INFINITY)) anchor = 0.0f;  // any anchor is valid
   }
-  const float m = t.bcast_f;
+  // ---- pass 1 (HBM): the maximum and the count histogram ------------------------
+  const float c128 = __fmul_rn(__fadd_rn(anchor, kTopFineTop), 128.0f);
+  float mx = -INFINITY;
+  auto count1 = [&](float x) {
+    // bin = floor((anchor + top - x) 128), clamped to the histogram; v >= 0
+    // keeps the sum with 2^23 in [2^23, inf] and so the index in range
+    const float v = fmaxf(__fmaf_rn(x, -128.0f, c128), 0.0f);
+    const int b = static_cast<int>(__float_as_uint(__fadd_rz(v, 8388608.0f)) - MassSums::kBias);
+    atomicAdd(&fine[min(b, kTopFine - 1)], 1u);
+  };
+  row_quads_t<4, kBf16>(
+      rv, pol_keep, kSliceWindow,
+      [&](int, const float (&z)[4], bool ok) {
+        if (!ok) return;
+        float x[4];
+        fx.four(z, x);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          mx = fmaxf(mx, x[e]);
+          count1(x[e]);
+        }
+      },
+      [&](int, float z, bool ok) {
+        if (!ok) return;
+        const float x = fix(z);
+        mx = fmaxf(mx, x);
+        count1(x);
+      });
+  mx = warp_maxf(mx);
+  if (lane == 0) t.red32[kRowWarps + wp] = __float_as_uint(mx);
+  if (tid == 0) {
+    t.found_pos = 0x7FFFFFFF;
+    t.cand_n = 0u;
+  }
+  __syncthreads();  // the histogram is complete
+  float m = -INFINITY;
+  for (int i = 0; i < kRowWarps; ++i) m = fmaxf(m, __uint_as_float(t.red32[kRowWarps + i]));
   if (m == -INFINITY) {  // no value above -inf: p is one-hot at column 0
     if (tid == 0) {
       ts->m = m;
@@ -997,30 +1238,310 @@ __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem
     }
     return;
   }
-  // ---- pass 2 (L2): fixed-point mass and the stage-0 histogram -------------------
-  top_hist_clear(t, kRowBins);
-  __syncthreads();
-  unsigned long long F = 0ull;
-  row_sweep<4>(rv, pol_keep, fix, [&](int, float x) {
-    const unsigned long long f = fixed_mass(exp_rel(x, m));
-    F += f;
-    atomicAdd(&t.hmass[adigit0(x, m)], f);
-  });
-  F = block_sum64(t, F);
   const int32_t s = P.rsi[R.b];
   const unsigned long long P32 = topp_scaled(P.top_p[s]);
-  const unsigned long long t_lo = P32 * F;
-  const unsigned long long t_hi = __umul64hi(P32, F);
-  // stage 0: distance bins, ascending (mass only: stage 1 always runs)
-  BFound f = block_find(t, kRowBins, false, 0ull, t_hi, t_lo, 0xFFFFFFFFu, 0u, false);
+
+  // ---- the estimated boundary and its window of distance bins -------------------
+  // (every branch below depends on shared values only: uniform over the CTA)
+  bool fast = m < INFINITY;
+  int lo = 0, hi = -1;
+  if (fast) {
+    constexpr int per = kTopFine / kRowThreads;
+    const int j0 = tid * per;
+    const float top = __fadd_rn(anchor, kTopFineTop);
+    auto centre = [&](int j) { return __fsub_rn(top, (static_cast<float>(j) + 0.5f) * 0.0078125f); };
+    float est[per];
+    float sum = 0.0f;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+      const unsigned int c = fine[j0 + q];
+      est[q] = c ? __fmul_rn(static_cast<float>(c), exp_rel(fminf(centre(j0 + q), m), m)) : 0.0f;
+      sum += est[q];
+    }
+    float incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float nv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += nv;
+    }
+    if (lane == 31) t.redf[wp] = incl;
+    __syncthreads();
+    float total = 0.0f, woff = 0.0f;
+    for (int i = 0; i < kRowWarps; ++i) {
+      total += t.redf[i];
+      if (i < wp) woff += t.redf[i];
+    }
+    const float target = __fmul_rn(P.top_p[s], total);
+    float run = woff + incl - sum;
+    int found = 0x7FFFFFFF;
+    for (int q = 0; q < per; ++q) {
+      run += est[q];
+      if (fine[j0 + q] != 0u && run >= target) {
+        found = j0 + q;
+        break;
+      }
+    }
+    atomicMin(&t.found_pos, found);
+    __syncthreads();
+    const int jf = t.found_pos;
+    fast = jf != 0x7FFFFFFF;
+    if (fast) {
+      const float cj = fminf(centre(jf), m);
+      const int g = static_cast<int>(fminf(__fmul_rn(__fsub_rn(m, cj), 64.0f), 2047.0f));
+      lo = max(g - kTopWin, 0);
+      hi = min(g + kTopWin, kRowBins - 1);
+    }
+  }
+
+  // ---- pass 2 (L2): exact F, the exact mass above the window, the window's list -
+  // An element's distance bin is trunc((m - x) 64) (adigit0); with
+  // d = x - m (one rounding, d = -(m - x) exactly) the bin is below lo when
+  // d > -lo / 64 and at most hi when d > -(hi + 1) / 64: the scalings by
+  // powers of two are exact, so the tests on d decide exactly as the bins.
+  unsigned long long F = 0ull, above = 0ull;
+  int a0 = 0;
+  uint2* seg = list + wp * kTopSeg;
+  unsigned int seg_n = 0u;
+  if (fast) {
+    MassSums ms;
+    const unsigned long long mm = f2_pack(m, m), l2e = f2_pack(kLog2e, kLog2e);
+    const unsigned long long p20 = f2_pack(0x1p20f, 0x1p20f), c23 = f2_pack(8388608.0f, 8388608.0f);
+    const float d_lo = -static_cast<float>(lo) * 0.015625f;
+    const float d_hi = hi == kRowBins - 1 ? -INFINITY : -static_cast<float>(hi + 1) * 0.015625f;
+    // two elements: their masses into the sums; returns the in-window bits
+    auto pair = [&](float x0, float x1, bool ok) -> uint32_t {
+      const unsigned long long dd = f2_sub(f2_pack(x0, x1), mm);
+      float t0, t1, d0, d1;
+      f2_unpack(f2_mul(dd, l2e), t0, t1);
+      f2_unpack(dd, d0, d1);
+      const unsigned long long a = f2_mul(f2_pack(ex2_approx(t0), ex2_approx(t1)), p20);
+      const unsigned long long hb = f2_add_rz(a, c23);
+      const unsigned long long lb = f2_fma(f2_sub(a, f2_sub(hb, c23)), p20, c23);
+      if (ok) {
+        ms.add(static_cast<uint32_t>(hb), static_cast<uint32_t>(lb), d0 > d_lo);
+        ms.add(static_cast<uint32_t>(hb >> 32), static_cast<uint32_t>(lb >> 32), d1 > d_lo);
+      }
+      return ok ? ((d0 <= d_lo && d0 > d_hi ? 1u : 0u) | (d1 <= d_lo && d1 > d_hi ? 2u : 0u)) : 0u;
+    };
+    row_quads_t<4, kBf16>(
+        rv, pol_last, kSliceWindow,
+        [&](int j, const float (&z)[4], bool ok) {
+          float x[4];
+          fx.four(z, x);
+          const uint32_t w = pair(x[0], x[1], ok) | (pair(x[2], x[3], ok) << 2);
+          if (__any_sync(0xFFFFFFFFu, w != 0u)) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) seg_append(seg, seg_n, (w >> e) & 1u, j + e, x[e]);
+          }
+          if (ms.n >= MassSums::kFold - 4u) ms.fold();
+        },
+        [&](int j, float z, bool ok) {
+          const float x = fix(z);
+          const float dd = __fsub_rn(x, m);
+          const float a = __fmul_rn(ex2_approx(__fmul_rn(dd, kLog2e)), 0x1p20f);
+          const float hb = __fadd_rz(a, 8388608.0f);
+          const float lb = __fmaf_rn(__fsub_rn(a, __fsub_rn(hb, 8388608.0f)), 0x1p20f, 8388608.0f);
+          if (ok) ms.add(__float_as_uint(hb), __float_as_uint(lb), dd > d_lo);
+          seg_append(seg, seg_n, ok && dd <= d_lo && dd > d_hi, j, x);
+          if (ms.n >= MassSums::kFold - 4u) ms.fold();
+        });
+    ms.fold();
+    F = ms.F;
+    above = ms.A;
+    if (lane == 0) t.wlen[wp] = seg_n;
+    block_sum64x2(t, F, above);  // synchronises: every segment is complete
+    for (int w = 0; w < kRowWarps; ++w) fast = fast && t.wlen[w] <= static_cast<unsigned int>(kTopSeg);
+  }
+  const unsigned long long t_lo = P32 * F, t_hi = __umul64hi(P32, F);
+  BFound f;
   f.cnt = 0u;
-  unsigned long long above = f.before;
-  const int a0 = f.bin;
+  if (fast) {
+    // the exact mass and count of each window bin, each warp from its own
+    // segment; then warp 0 finds the bin where the exact running mass from
+    // `above` first reaches the target
+    constexpr int kW = 2 * kTopWin + 1;
+    unsigned long long mw[kW];
+    unsigned int cw[kW];
+#pragma unroll
+    for (int q = 0; q < kW; ++q) {
+      mw[q] = 0ull;
+      cw[q] = 0u;
+    }
+    unsigned int bad = 0u;
+    for (unsigned int j = lane; j < seg_n; j += 32) {
+      const float x = __uint_as_float(__ldcg(seg + j).y);
+      const int q = adigit0(x, m) - lo;
+      bad |= static_cast<uint32_t>(q) > static_cast<uint32_t>(hi - lo) ? 1u : 0u;
+      const unsigned long long fm = fixed_mass(exp_rel(x, m));
+#pragma unroll
+      for (int k = 0; k < kW; ++k) {
+        mw[k] += q == k ? fm : 0ull;
+        cw[k] += q == k ? 1u : 0u;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kW; ++k) {
+      mw[k] = warp_sum64(mw[k]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cw[k] += __shfl_xor_sync(0xFFFFFFFFu, cw[k], o);
+    }
+    bad = __reduce_or_sync(0xFFFFFFFFu, bad);
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < kW; ++k) {
+        t.wmass[wp][k] = mw[k];
+        t.wcnt[wp][k] = cw[k] | (bad << 31);
+      }
+    }
+    __syncthreads();
+    if (wp == 0) {
+      unsigned long long mb = 0ull;
+      unsigned int cb = 0u, bd = 0u;
+      if (lane <= hi - lo) {
+        for (int w = 0; w < kRowWarps; ++w) {
+          mb += t.wmass[w][lane];
+          cb += t.wcnt[w][lane] & 0x7FFFFFFFu;
+          bd |= t.wcnt[w][lane] >> 31;
+        }
+      }
+      unsigned long long incl = mb;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long nv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += nv;
+      }
+      const unsigned long long run = above + incl - mb;
+      const unsigned int hit =
+          __ballot_sync(0xFFFFFFFFu, lane <= hi - lo && mb > 0ull && reaches(run + mb, t_hi, t_lo));
+      // no bin reaches (the boundary lies below the window), the mass above
+      // the window already reaches (it lies above), a listed element outside
+      // the window, or more candidates than the sort takes: the exact select
+      const int qf = hit ? __ffs(hit) - 1 : 0;
+      const unsigned int cf = __shfl_sync(0xFFFFFFFFu, cb, qf);
+      const bool ok = hit != 0u && !__any_sync(0xFFFFFFFFu, bd != 0u) &&
+                      !reaches(above, t_hi, t_lo) && cf <= static_cast<unsigned int>(kTopSort);
+      if (lane == qf) {
+        t.f_bin = lo + qf;
+        t.f_before = run;
+        t.f_cnt = cb;
+      }
+      if (lane == 0) t.fast_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    fast = t.fast_ok != 0;
+    a0 = t.f_bin;
+    above = t.f_before;
+  }
+  if (fast) {
+    // ---- the boundary bin's candidates, sorted: x descending, id ascending ----
+    unsigned long long* key = reinterpret_cast<unsigned long long*>(t.hmass);
+    const unsigned int nc = t.f_cnt;
+    unsigned int np = kRowThreads;
+    while (np < nc) np <<= 1;
+    for (unsigned int j0 = 0; j0 < seg_n; j0 += 32) {  // the same trip count in every lane
+      const unsigned int j = j0 + static_cast<unsigned int>(lane);
+      bool in = false;
+      uint2 e = make_uint2(0u, 0u);
+      if (j < seg_n) {
+        e = __ldcg(seg + j);
+        in = adigit0(__uint_as_float(e.y), m) == a0;
+      }
+      const unsigned int bal = __ballot_sync(0xFFFFFFFFu, in);
+      if (bal == 0u) continue;
+      unsigned int base = 0u;
+      if (lane == 0) base = atomicAdd(&t.cand_n, static_cast<unsigned int>(__popc(bal)));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      if (in) {
+        const unsigned int at = base + static_cast<unsigned int>(__popc(bal & ((1u << lane) - 1u)));
+        if (at < static_cast<unsigned int>(kTopSort))
+          key[at] = (static_cast<unsigned long long>(kd_of(__uint_as_float(e.y))) << 32) |
+                    static_cast<unsigned long long>(0xFFFFFFFFu - e.x);
+      }
+    }
+    if (tid == 0) {  // found below; a valid token id whatever happens
+      t.f_id = 0u;
+      t.f_mass = 0ull;
+      t.f_before = above;
+    }
+    __syncthreads();
+    for (unsigned int j = nc + tid; j < np; j += kRowThreads) key[j] = 0ull;  // sorts last
+    __syncthreads();
+    // bitonic sort, descending
+    for (unsigned int k = 2; k <= np; k <<= 1) {
+      for (unsigned int jj = k >> 1; jj > 0; jj >>= 1) {
+        for (unsigned int i = tid; i < np; i += kRowThreads) {
+          const unsigned int ixj = i ^ jj;
+          if (ixj > i) {
+            const unsigned long long a = key[i], b = key[ixj];
+            if (((i & k) == 0) ? (a < b) : (a > b)) {
+              key[i] = b;
+              key[ixj] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    // running masses in that order; the element where the running mass from
+    // `above` first reaches the target is the boundary
+    const unsigned int per = np / kRowThreads;
+    const unsigned int i0 = tid * per;
+    unsigned long long mine = 0ull;
+    for (unsigned int q = 0; q < per; ++q)
+      if (i0 + q < nc) mine += fixed_mass(exp_rel(x_of_key(static_cast<uint32_t>(key[i0 + q] >> 32)), m));
+    unsigned long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long nv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += nv;
+    }
+    if (lane == 31) t.red64[wp] = incl;
+    __syncthreads();
+    unsigned long long run = above + incl - mine;
+    for (int i = 0; i < wp; ++i) run += t.red64[i];
+    for (unsigned int q = 0; q < per; ++q) {
+      const unsigned int i = i0 + q;
+      if (i >= nc) break;
+      const unsigned long long kk = key[i];
+      const unsigned long long fm = fixed_mass(exp_rel(x_of_key(static_cast<uint32_t>(kk >> 32)), m));
+      if (fm > 0ull && !reaches(run, t_hi, t_lo) && reaches(run + fm, t_hi, t_lo)) {
+        t.f_id = 0xFFFFFFFFu - static_cast<uint32_t>(kk);
+        t.f_mass = fm;
+        t.f_before = run;
+      }
+      run += fm;
+    }
+    __syncthreads();
+    f.id = t.f_id;
+    f.mass = t.f_mass;
+    above = t.f_before;
+    f.cnt = 1u;
+  }
+
+  // ---- otherwise the exact select: pass 2' (L2), the stage-0 histogram ----------
+  unsigned int list_len = 0xFFFFFFFFu;  // not built yet
+  unsigned long long tt_lo = t_lo, tt_hi = t_hi;
+  if (!fast) {
+    top_hist_clear(t, kRowBins);
+    __syncthreads();
+    unsigned long long Fx = 0ull;
+    row_sweep_t<4, kBf16>(rv, pol_keep, fix, [&](int, float x) {
+      const unsigned long long fm = fixed_mass(exp_rel(x, m));
+      Fx += fm;
+      atomicAdd(&t.hmass[adigit0(x, m)], fm);
+    });
+    F = block_sum64(t, Fx);
+    tt_lo = P32 * F;
+    tt_hi = __umul64hi(P32, F);
+    // stage 0: distance bins, ascending (mass only: stage 1 always runs)
+    f = block_find(t, kRowBins, false, 0ull, tt_hi, tt_lo, 0xFFFFFFFFu, 0u, false);
+    f.cnt = 0u;
+    above = f.before;
+    a0 = f.bin;
+  }
   int a1 = -1;
   int kd_len = 0, id_len = 0;
   uint32_t kd_pre = 0u, id_pre = 0u;
-  uint2* list = P.cand + static_cast<size_t>(blockIdx.x) * kVerifyListCap;
-  unsigned int list_len = 0xFFFFFFFFu;  // not built yet
   for (int stage = 1; f.cnt != 1u && stage <= 6; ++stage) {
     const int c_a1 = a1, c_kl = kd_len, c_il = id_len;
     const uint32_t c_kp = kd_pre, c_ip = id_pre;
@@ -1062,17 +1583,18 @@ __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem
         }
       }
     };
-    if (list_len <= static_cast<unsigned int>(kVerifyListCap)) {
+    const bool from_list = list_len <= static_cast<unsigned int>(kVerifyListCap);
+    if (from_list) {
       for (unsigned int j = tid; j < list_len; j += kRowThreads) {
         const uint2 e = __ldcg(list + j);
         visit(e.x, __uint_as_float(e.y), false);
       }
     } else {
       const bool append = stage == 1;
-      row_sweep<4>(rv, stage == 1 ? pol_last : pol_keep, fix,
-                   [&](int i, float x) { visit(static_cast<uint32_t>(i), x, append); });
+      row_sweep_t<4, kBf16>(rv, stage == 1 ? pol_last : pol_keep, fix,
+                            [&](int i, float x) { visit(static_cast<uint32_t>(i), x, append); });
     }
-    f = block_find(t, nb, desc, above, t_hi, t_lo, cmin, cmax, true);
+    f = block_find(t, nb, desc, above, tt_hi, tt_lo, cmin, cmax, true);
     if (stage == 1) list_len = t.list_n;  // complete: block_find synchronised the CTA
     above = f.before;
     const uint32_t bin = static_cast<uint32_t>(f.bin);
@@ -1114,11 +1636,13 @@ __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem
 }
 
 __device__ void flat_topp_row(const VerifyParams& P, const FlatRow& R, TopSmem& t) {
-  if (R.T != 1.0f) {
-    const float T = R.T;
-    flat_topp_row_t(P, R, t, [T](float c) { return fmaxf(__fdiv_rn(c, T), -INFINITY); });
+  const bool scale = R.T != 1.0f;
+  if (R.bf16) {
+    if (scale) flat_topp_row_t<true, true>(P, R, t);
+    else flat_topp_row_t<true, false>(P, R, t);
   } else {
-    flat_topp_row_t(P, R, t, [](float c) { return fmaxf(c, -INFINITY); });
+    if (scale) flat_topp_row_t<false, true>(P, R, t);
+    else flat_topp_row_t<false, false>(P, R, t);
   }
 }
 
