@@ -138,7 +138,7 @@ typedef struct {
  *   draft_stats   [B, K] dspark_row_stats, or NULL: if given (and cache is
  *                 not NULL), the maximum and exp-mass of every cache row the
  *                 call writes, so that dspark_rejection_sample need not read
- *                 the row (padding requests: zero; B > 64: m = NaN, "not
+ *                 the row (padding requests: zero; B > 32: m = NaN, "not
  *                 recorded"). No counterpart in the pages: the loop has every
  *                 value of the row at hand.
  *   B in [0, 256], K in [1, 16], V in [1, 2^22), R a multiple of 64 up to
@@ -247,11 +247,16 @@ dspark_status dspark_markov_sample_static(
  *     m = max xt; e_v = exp(xt_v - m) (fp32); f_v = rint(e_v * 2^40) (uint64);
  *     if top_p[s] < 1 keep the shortest prefix of the (xt desc, id asc) order
  *     with (sum of f over the prefix) * 2^32 >= rint(top_p * 2^32) * (sum of
- *     all f), else keep all; p_v = e_v / (fp32(sum of kept f) * 2^-40) on the
+ *     all f), and D = fp32(sum of kept f) * 2^-40; else keep all, and D =
+ *     the fp32 sum of e_v in a fixed order (per-slice running sums, each
+ *     rescaled to the slice maximum as it grows, combined in slice order:
+ *     one pass over the row, the same bits every run; it differs from
+ *     fp32(sum of f) * 2^-40 by fp32 rounding only). p_v = e_v / D on the
  *     kept set, 0 elsewhere. A row with no value above -inf is one-hot at 0.
- *   draft row k (k < K): q = the same normalisation of cache[row, k, :] with
- *     no temperature and no top-p (the cache holds scaled logits); a row with
- *     no value above -inf gives q = 0.
+ *   draft row k (k < K): q = exp(c_v - m) / D of c = cache[row, k, :] with
+ *     no temperature and no top-p (the cache holds scaled logits), D the
+ *     fp32 sum as for a target row kept whole (or, with draft_stats, from the
+ *     recorded fixed-point mass); a row with no value above -inf gives q = 0.
  *   for k = 0..K-1, d = draft_tokens[b, k]:
  *     d = -1: emit a draw from p_k and stop;
  *     u = uniform(seeds[s], positions[b] + k - 1, column 0, accept stream);
@@ -282,8 +287,8 @@ dspark_status dspark_markov_sample_static(
  *   req_state_idx [B], positions [B], temperature [S], top_p [S] fp32,
  *   seeds [S] as for dspark_markov_sample
  *   out_tokens    [B, K+1] int32, num_accepted [B] int32 (written)
- *   workspace     at least dspark_verify_workspace_bytes() bytes (a few
- *                 MB: per-request statistics plus a fixed 4 MB area of
+ *   workspace     at least dspark_verify_workspace_bytes() bytes (per-row
+ *                 and per-request statistics plus a fixed 64 MB area of
  *                 top-p candidate lists); no initial contents required
  * Alignment: draft_cache and target_logits must be 16-byte aligned.
  * ------------------------------------------------------------------------ */

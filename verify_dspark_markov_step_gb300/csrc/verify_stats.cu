@@ -1,36 +1,25 @@
-// verify_stats.cu -- per-row statistics of the verifier, one thread-block
-// cluster per row.
+// verify_stats.cu -- the verifier (one persistent launch) and the top-k
+// candidate selection of the top-k Markov loop.
 //
-// vLLM PR #65007 Part 2 ("Temperature and top-p"): the target row after
-// temperature, its maximum and total exp-mass in 64-bit fixed point, and the
-// exact top-p keep set -- the smallest prefix by (logit desc, token id asc)
-// whose mass reaches p, plus the row max. Draft rows (the cache) get their
-// maximum and fixed-point mass. Greedy target rows get their winner key.
+// The verifier follows vLLM PR #65007 Part 2 ("Temperature and top-p" and
+// the rejection sampler): per request, the target rows after temperature
+// (their maximum, exp-mass and, for a sampled row with top_p < 1, the exact
+// keep set -- the smallest prefix by (logit desc, token id asc) whose 64-bit
+// fixed-point mass reaches p, plus the row max), the draft rows' maximum and
+// exp-mass, the accept/reject chain, and one categorical draw (residual,
+// placeholder row or bonus row). Greedy target rows get their winner key.
+// How the work is scheduled is described above verify_flat_kernel; the
+// top-p select above flat_topp_row_t.
 //
-// A row is split over the CL CTAs of a cluster (CL up to 16, slices of at
-// most 32768 values). Each CTA starts its slice as one bulk L2 prefetch,
-// reads it once for the maximum with an L2 evict-last hint, and the later
-// passes (fixed-point mass, the radix stages of the top-p select) read it
-// again from L2; with nothing held in shared memory but histograms, four CTAs
-// share an SM and many rows are in flight (odd clusters take their rows in
-// reverse order, so one-pass draft rows and two-pass target rows overlap).
-// Reductions across the cluster go through distributed shared memory:
-// scalars by each CTA reading the others' slots, histograms by each CTA
-// reducing its own range of bins over the cluster, in place.
-//
-// Top-p select: a radix select in (logit descending, token id ascending)
-// order with histograms of fixed-point mass; each stage finds the first bin at
-// which the running mass reaches P32 * F / 2^32 and the next stage splits
-// that bin, until the bin holds one element. The first two stages bin by the
-// distance to the row maximum (2048 bins of 1/64 over [0, 32), counted during
-// the mass pass, then 2048 sub-bins of the chosen bin, whose elements are
-// also copied to a per-CTA candidate list that the later stages read instead
-// of the slice); then come the ordered bits kd of the logit (11 + 11 + 10
-// bits, skipped once a stage's candidates all share one value) and, for
-// exact ties, the token id (11 + 11 bits).
+// The top-k selection (topk_rows_kernel, at the end of the file) runs one
+// thread-block cluster per base-logit row and reduces through distributed
+// shared memory; the helpers right below (RowSmem, cluster_reduce,
+// cluster_find) serve it.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -568,27 +557,23 @@ __device__ __forceinline__ unsigned long long slice_online(const RowView& rv, ui
 }
 
 // ---------------------------------------------------------------------------
-// Verification, two launches.
-//
-// 1. verify_topp_kernel: persistent thread-block clusters over the target
-//    rows that take a top-p cut (sampled slot, top_p < 1), one cluster per
-//    row: the exact select above (process_row). A batch without such rows
-//    leaves at once.
-// 2. verify_flat_kernel: persistent CTAs (no clusters) over one work queue.
-//    Row items come in request order (request b: target rows 0..K, then
-//    draft rows 0..K-1), each row cut into `nslice` slices, one item per
-//    slice: a slice yields a partial (the online max and exp-sum, or the
-//    greedy winner key) and the CTA that finishes a row's last slice
-//    combines the partials in slice order (the same bits every run) into
-//    the row's statistics. The CTA that finishes a request's last row
-//    replays the request's accept chain (one thread per draft), writes the
-//    request's draw job and publishes `ndraw` draw items: column chunks of
-//    the one categorical the request needs. CTAs take published draw items
-//    before new rows, so a draw runs soon after its rows, beside other
-//    requests' rows; the CTA that finishes a request's last chunk writes the
-//    outputs. Each CTA's scheduler claims its next row at the start of the
-//    current item, so the claim's latency hides behind the item's work.
-//    Every wait is bounded.
+// Verification in one launch: verify_flat_kernel, persistent CTAs (no
+// clusters, four per SM, cooperative so that every CTA is resident) over one
+// work queue. Row items come in request order (request b: target rows 0..K,
+// then draft rows 0..K-1). A row kept whole (or a greedy row) is cut into
+// `nslice` slices, one item per slice: a slice yields a partial (the online
+// maximum and exp-sum, or the greedy winner key) and the CTA that finishes a
+// row's last slice combines the partials in slice order (the same bits every
+// run) into the row's statistics. A sampled target row with a top-p cut is
+// one item, done whole by one CTA (flat_topp_row). The CTA that finishes a
+// request's last row replays the request's accept chain (one thread per
+// draft), writes the request's draw job and publishes `ndraw` draw items:
+// column chunks of the one categorical the request needs. CTAs take
+// published draw items before new rows, so a draw runs soon after its rows,
+// beside other requests' rows; the CTA that finishes a request's last chunk
+// writes the outputs. Each CTA claims its next row at the start of the
+// current item, so the claim's latency hides behind the item's work. Every
+// wait is bounded.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* p) {
   uint32_t v;
@@ -1156,6 +1141,102 @@ __device__ __forceinline__ float x_of_key(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// The boundary element among the boundary bin's nc candidates (order keys
+// in key[0, nc): value key << 32 | ~id): a bitonic sort into descending key
+// order (x descending, id ascending) with E keys per thread in registers --
+// exchanges between threads of a warp by shuffles, between warps through
+// shared memory -- then running masses in that order from `above`; the
+// element where the running mass first reaches the target writes its id,
+// mass and the mass before it to t.f_id, t.f_mass, t.f_before.
+template <int E>
+__device__ void topp_sort_find(TopSmem& t, unsigned long long* key, unsigned int nc, float m,
+                               unsigned long long above, unsigned long long t_hi,
+                               unsigned long long t_lo) {
+  constexpr unsigned int np = kRowThreads * E;
+  const unsigned int tid = threadIdx.x, lane = tid & 31u, wp = tid >> 5;
+  unsigned long long k[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const unsigned int i = tid * E + e;
+    k[e] = i < nc ? key[i] : 0ull;  // 0 sorts last
+  }
+  for (unsigned int ks = 2; ks <= np; ks <<= 1) {
+    for (unsigned int jj = ks >> 1; jj > 0; jj >>= 1) {
+      if (jj < static_cast<unsigned int>(E)) {  // both keys in this thread
+        // (the partner's register index must be a constant: jj is 1 or 2)
+        auto local = [&](auto J) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            constexpr int kJ = decltype(J)::value;
+            const int p = e ^ kJ;
+            if (p > e) {
+              const bool desc = ((tid * E + e) & ks) == 0u;
+              const unsigned long long a = k[e], b = k[p];
+              const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+              k[e] = desc ? hi : lo;
+              k[p] = desc ? lo : hi;
+            }
+          }
+        };
+        if constexpr (E >= 2) {
+          if (jj == 1u) local(std::integral_constant<int, 1>{});
+        }
+        if constexpr (E >= 4) {
+          if (jj == 2u) local(std::integral_constant<int, 2>{});
+        }
+      } else {
+        unsigned long long other[E];
+        if (jj < 32u * E) {  // the partner is in this warp
+#pragma unroll
+          for (int e = 0; e < E; ++e) other[e] = __shfl_xor_sync(0xFFFFFFFFu, k[e], jj / E);
+        } else {             // in another warp
+          __syncthreads();   // the last readers of key[] are done
+#pragma unroll
+          for (int e = 0; e < E; ++e) key[tid * E + e] = k[e];
+          __syncthreads();
+#pragma unroll
+          for (int e = 0; e < E; ++e) other[e] = key[(tid * E + e) ^ jj];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const unsigned int i = tid * E + e;
+          const bool keep_max = (((i & ks) == 0u) == ((i & jj) == 0u));
+          const unsigned long long a = k[e], b = other[e];
+          k[e] = keep_max ? (a > b ? a : b) : (a > b ? b : a);
+        }
+      }
+    }
+  }
+  unsigned long long fm[E];
+  unsigned long long mine = 0ull;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    fm[e] = tid * E + e < nc ? fixed_mass(exp_rel(x_of_key(static_cast<uint32_t>(k[e] >> 32)), m))
+                             : 0ull;
+    mine += fm[e];
+  }
+  unsigned long long incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long nv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= static_cast<unsigned int>(o)) incl += nv;
+  }
+  __syncthreads();  // t.red64 is free
+  if (lane == 31u) t.red64[wp] = incl;
+  __syncthreads();
+  unsigned long long run = above + incl - mine;
+  for (unsigned int i = 0; i < wp; ++i) run += t.red64[i];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if (fm[e] > 0ull && !reaches(run, t_hi, t_lo) && reaches(run + fm[e], t_hi, t_lo)) {
+      t.f_id = 0xFFFFFFFFu - static_cast<uint32_t>(k[e]);
+      t.f_mass = fm[e];
+      t.f_before = run;
+    }
+    run += fm[e];
+  }
+}
+
 template <bool kBf16, bool kScale>
 __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem& t) {
   const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5, K = P.K, V = P.V;
@@ -1190,12 +1271,19 @@ __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem
     if (!(anchor > -INFINITY && anchor < INFINITY)) anchor = 0.0f;  // any anchor is valid
   }
   // ---- pass 1 (HBM): the maximum and the count histogram ------------------------
+  // With a temperature in the range where the division is monotone and
+  // finite (T in [2^-30, 2^30]) the pass reads z itself: the correctly
+  // rounded z / T is non-decreasing in z, so the maximum of x is the
+  // quotient of the maximum of z (NaN read as -inf on both sides), and the
+  // histogram, an estimate only, bins z times an approximate 128 / T.
+  const bool by_z = kScale && temp_div_t_ok(R.T);
   const float c128 = __fmul_rn(__fadd_rn(anchor, kTopFineTop), 128.0f);
+  const float s128 = by_z ? __fmul_rn(128.0f, __frcp_rn(R.T)) : 128.0f;
   float mx = -INFINITY;
-  auto count1 = [&](float x) {
+  auto count1 = [&](float y) {
     // bin = floor((anchor + top - x) 128), clamped to the histogram; v >= 0
     // keeps the sum with 2^23 in [2^23, inf] and so the index in range
-    const float v = fmaxf(__fmaf_rn(x, -128.0f, c128), 0.0f);
+    const float v = fmaxf(__fmaf_rn(y, -s128, c128), 0.0f);
     const int b = static_cast<int>(__float_as_uint(__fadd_rz(v, 8388608.0f)) - MassSums::kBias);
     atomicAdd(&fine[min(b, kTopFine - 1)], 1u);
   };
@@ -1204,7 +1292,12 @@ __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem
       [&](int, const float (&z)[4], bool ok) {
         if (!ok) return;
         float x[4];
-        fx.four(z, x);
+        if (by_z) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = fmaxf(z[e], -INFINITY);
+        } else {
+          fx.four(z, x);
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           mx = fmaxf(mx, x[e]);
@@ -1213,11 +1306,12 @@ __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem
       },
       [&](int, float z, bool ok) {
         if (!ok) return;
-        const float x = fix(z);
+        const float x = by_z ? fmaxf(z, -INFINITY) : fix(z);
         mx = fmaxf(mx, x);
         count1(x);
       });
   mx = warp_maxf(mx);
+  if (by_z) mx = fix(mx);
   if (lane == 0) t.red32[kRowWarps + wp] = __float_as_uint(mx);
   if (tid == 0) {
     t.found_pos = 0x7FFFFFFF;
@@ -1464,53 +1558,9 @@ __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem
       t.f_before = above;
     }
     __syncthreads();
-    for (unsigned int j = nc + tid; j < np; j += kRowThreads) key[j] = 0ull;  // sorts last
-    __syncthreads();
-    // bitonic sort, descending
-    for (unsigned int k = 2; k <= np; k <<= 1) {
-      for (unsigned int jj = k >> 1; jj > 0; jj >>= 1) {
-        for (unsigned int i = tid; i < np; i += kRowThreads) {
-          const unsigned int ixj = i ^ jj;
-          if (ixj > i) {
-            const unsigned long long a = key[i], b = key[ixj];
-            if (((i & k) == 0) ? (a < b) : (a > b)) {
-              key[i] = b;
-              key[ixj] = a;
-            }
-          }
-        }
-        __syncthreads();
-      }
-    }
-    // running masses in that order; the element where the running mass from
-    // `above` first reaches the target is the boundary
-    const unsigned int per = np / kRowThreads;
-    const unsigned int i0 = tid * per;
-    unsigned long long mine = 0ull;
-    for (unsigned int q = 0; q < per; ++q)
-      if (i0 + q < nc) mine += fixed_mass(exp_rel(x_of_key(static_cast<uint32_t>(key[i0 + q] >> 32)), m));
-    unsigned long long incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long nv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += nv;
-    }
-    if (lane == 31) t.red64[wp] = incl;
-    __syncthreads();
-    unsigned long long run = above + incl - mine;
-    for (int i = 0; i < wp; ++i) run += t.red64[i];
-    for (unsigned int q = 0; q < per; ++q) {
-      const unsigned int i = i0 + q;
-      if (i >= nc) break;
-      const unsigned long long kk = key[i];
-      const unsigned long long fm = fixed_mass(exp_rel(x_of_key(static_cast<uint32_t>(kk >> 32)), m));
-      if (fm > 0ull && !reaches(run, t_hi, t_lo) && reaches(run + fm, t_hi, t_lo)) {
-        t.f_id = 0xFFFFFFFFu - static_cast<uint32_t>(kk);
-        t.f_mass = fm;
-        t.f_before = run;
-      }
-      run += fm;
-    }
+    if (np == kRowThreads) topp_sort_find<1>(t, key, nc, m, above, t_hi, t_lo);
+    else if (np == 2 * kRowThreads) topp_sort_find<2>(t, key, nc, m, above, t_hi, t_lo);
+    else topp_sort_find<4>(t, key, nc, m, above, t_hi, t_lo);
     __syncthreads();
     f.id = t.f_id;
     f.mass = t.f_mass;
@@ -1635,7 +1685,9 @@ __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem
   }
 }
 
-__device__ void flat_topp_row(const VerifyParams& P, const FlatRow& R, TopSmem& t) {
+// Out of line: the select's registers and code stay out of the kernel's
+// common path (slices, draws), which runs at the kernel's register limit.
+__device__ __noinline__ void flat_topp_row(const VerifyParams& P, const FlatRow& R, TopSmem& t) {
   const bool scale = R.T != 1.0f;
   if (R.bf16) {
     if (scale) flat_topp_row_t<true, true>(P, R, t);
