@@ -397,6 +397,8 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
     s_prev[n] = prev;
     s_act[n] = prev >= 0;
     best[n] = 0ull;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) s_wkey[qq * Npad + n] = 0ull;
   }
   if (tid == 0) {
     for (int i = 0; i < ns; ++i) {
@@ -780,8 +782,13 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                 run_v[c + j] = static_cast<uint32_t>(v);
               }
             } else {
+              // the warp's winner into its lane quarter's slot of the
+              // column: the warp alone writes it (no atomic)
               const unsigned long long key = warp_winner(ord, static_cast<uint32_t>(v));
-              if (lane == 0 && key != 0ull) atomicMax(&best[b], key);
+              if (lane == 0) {
+                unsigned long long* sl = &s_wkey[q * Npad + b];
+                if (key > *sl) *sl = key;
+              }
             }
           }
         }
@@ -876,8 +883,10 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
                                max(s_wx[2 * Npad + b], s_wx[3 * Npad + b]))
                          : 0u;
         } else {
-          k = best[b];
-          best[b] = 0ull;
+          k = umax64(umax64(s_wkey[b], s_wkey[Npad + b]),
+                     umax64(s_wkey[2 * Npad + b], s_wkey[3 * Npad + b]));
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) s_wkey[qq * Npad + b] = 0ull;
           xk = 0u;
         }
         if (k != 0ull) atomicMax(keys + b, k);
