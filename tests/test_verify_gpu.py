@@ -92,6 +92,28 @@ def test_topp_row_kinds(kind):
     verify_parity(w, draft, cache, out, nacc, max_exception_frac=0.25)
 
 
+@pytest.mark.parametrize("kind", ["coarse_ties", "flat", "lm"])
+def test_topp_long_rows_take_every_select_path(kind):
+    """Rows of 65536 values: with three distinct values (coarse_ties) or all
+    values within a few distance bins (flat), every warp lists thousands of
+    window values, more than its list segment holds, and the row takes the
+    exact select on the whole row; LM-like rows take the two-pass select.
+    Each must give the oracle's keep set (the pages' top-p test matrix at a
+    vocabulary size where the passes span many tiles)."""
+    rng = np.random.default_rng(zlib.crc32(("long-" + kind).encode()))
+    ps = [0.3, 0.9, 0.95, 0.5]
+    B, K, V = len(ps), 1, 65536
+    w = wl.custom(B, K, V, 64, seed=13, top_p=ps, temperature=[1.0] * B)
+    w.target = np.stack([np.stack([_topp_rows(kind, V, rng) for _ in range(K + 1)])
+                         for _ in range(B)]).astype(np.float32)
+    cache = np.stack([np.stack([_topp_rows("lm", V, rng) for _ in range(K)])
+                      for _ in range(B)]).astype(np.float32)
+    draft = wl.random_drafts(w, seed=3)
+    st, out, nacc = run_verify(w, draft, cache)
+    assert st.status_code() == 0
+    verify_parity(w, draft, cache, out, nacc, max_exception_frac=0.25)
+
+
 def test_bf16_target_and_cache():
     w = wl.custom(16, 3, 8192, 64, seed=12, base_bf16=True, cache_bf16=True,
                   target_bf16=True, top_p=0.95, temperature=1.0)

@@ -654,6 +654,18 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           }
         }
       }
+      // the noise of this tile's first column group does not depend on the
+      // step's tokens: with one group per warp (small batches) draw it before
+      // waiting for the accumulator (at a step's first tile the wait covers
+      // the embedding gather and the MMA chain); wider warps draw it in turn
+      constexpr bool kPreNoise = CPW <= GW;
+      float gpre[GW];
+      if (kPreNoise && !skip && c_tile > 0) {
+        uint32_t nw0[GW];
+        noise_group(c_begin, v, nw0);
+#pragma unroll
+        for (int j = 0; j < GW; j += 2) gumbel_of2(nw0[j], nw0[j + 1], gpre[j], gpre[j + 1]);
+      }
       if (!skip) {
         bool ok = mbar_wait(&acc_full[ab], aph, P.status, P.wait_limit_ns);
         if (ok && tma_base) ok = mbar_wait(&bfull[bs], bph, P.status, P.wait_limit_ns);
@@ -694,8 +706,16 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
             for (int j = 0; j < GW; ++j) bv[j] = bnext[j];
             if (c + GW < c_tile) load_direct(cb + GW, v, in_range, bnext);
           }
-          uint32_t nw[GW];
-          noise_group(cb, v, nw);
+          float gv[GW];
+          if (kPreNoise && c == 0) {
+#pragma unroll
+            for (int j = 0; j < GW; ++j) gv[j] = gpre[j];
+          } else {
+            uint32_t nw[GW];
+            noise_group(cb, v, nw);
+#pragma unroll
+            for (int j = 0; j < GW; j += 2) gumbel_of2(nw[j], nw[j + 1], gv[j], gv[j + 1]);
+          }
           float gsc[GW];
 #pragma unroll
           for (int h = 0; h < GW / 4; ++h) {
@@ -709,9 +729,6 @@ markov_loop_tc_kernel(const __grid_constant__ CUtensorMap tmap_w2,
           // (greedy: x), two columns at a time in packed fp32 pairs (fewer
           // instructions and registers); padding columns (b >= B) compute
           // values that are neither stored nor folded into a token
-          float gv[GW];
-#pragma unroll
-          for (int j = 0; j < GW; j += 2) gumbel_of2(nw[j], nw[j + 1], gv[j], gv[j + 1]);
           tc::tmem_wait_ld();
           float xv[GW], yv[GW];
           float tq[GW], rq[GW];
