@@ -23,10 +23,11 @@ def _run(w, topk):
     return st, st.draft.cpu().numpy(), to_numpy(st.cache)
 
 
-@pytest.mark.parametrize("case", ["tiny", "odd", "bf16_rowmap", "ties", "nan_heavy", "k_over_v"])
+@pytest.mark.parametrize("case", ["tiny", "odd", "bf16_rowmap", "ties", "nan_heavy", "k_over_v",
+                                  "coarse_big"])
 def test_topk_loop_and_verify(case):
     k = {"tiny": 7, "odd": 64, "bf16_rowmap": 100, "ties": 33, "nan_heavy": 5,
-         "k_over_v": 5000}[case]
+         "k_over_v": 5000, "coarse_big": 5000}[case]
     if case == "tiny":
         w = wl.make("tiny")
     elif case == "odd":
@@ -45,6 +46,10 @@ def test_topk_loop_and_verify(case):
         w.base = w.base.copy()
         w.base[0, 0, rng.integers(0, 4099, 9)] = np.nan
         w.base[1, 1, [3, 4000]] = np.nan
+    elif case == "coarse_big":  # three values over 65536 columns: the boundary
+        # value holds far more candidates than a list keeps (the radix stages)
+        w = wl.custom(2, 2, 65536, 64, seed=15, temperature=[1.0, 0.9])
+        w.base = np.random.default_rng(2).integers(0, 3, w.base.shape).astype(np.float32)
     else:  # k above V: every column is a candidate (the dense loop)
         w = wl.custom(3, 2, 4099, 128, seed=14, temperature=[1.0, 0.0, 0.8])
     st, tok, cache = _run(w, k)

@@ -2158,6 +2158,170 @@ __device__ void topk_row(const TopkParams& P, int W, int row_id, cg::cluster_gro
   __syncthreads();
   for (int q = tid; q < kRowBins; q += kRowThreads) sm.hmass[q] = sm.hcnt[q];
   Found f = cluster_find(cl, sm, kRowBins, true, 0ull, t_hi, t_lo, CL, rank);
+  // ---- one sweep: the values above the boundary bin (and the NaNs) are
+  // candidates whatever the rest, the boundary bin's values are listed by
+  // their order keys; the cluster's rank 0 sorts those keys (x descending,
+  // id ascending) and takes the top ones. Lists longer than the shared
+  // memory holds take the radix stages below instead.
+  {
+    constexpr unsigned int kCap = kRowBins;  // entries per list (16 KB each)
+    const uint32_t b_star = static_cast<uint32_t>(f.bin);
+    const unsigned int need_b = static_cast<unsigned int>(need - f.before);
+    int2* alist = reinterpret_cast<int2*>(sm.hmass);                  // (id, value bits)
+    unsigned long long* blist = reinterpret_cast<unsigned long long*>(sm.hcnt);  // order keys
+    static_assert(sizeof(unsigned int) * 2 * kRowBins >= sizeof(unsigned long long) * kRowBins,
+                  "the boundary list lives in hcnt and hid");
+    __syncthreads();  // the histograms are read
+    if (tid == 0) {
+      sm.x_pref = 0u;
+      sm.list_n = 0u;
+    }
+    __syncthreads();
+    row_sweep<4>(rv, pol, ident, [&](int j, float x) {
+      const uint32_t id = static_cast<uint32_t>(v0 + j);
+      const uint32_t kd = kd_of(x);
+      const uint32_t dg = kd >> 21;
+      if (x != x || dg > b_star) {
+        const unsigned int at = atomicAdd(&sm.x_pref, 1u);
+        if (at < kCap) alist[at] = make_int2(static_cast<int>(id), __float_as_int(x));
+      } else if (dg == b_star) {
+        const unsigned int at = atomicAdd(&sm.list_n, 1u);
+        if (at < kCap)
+          blist[at] = (static_cast<unsigned long long>(kd) << 32) |
+                      static_cast<unsigned long long>(0xFFFFFFFFu - id);
+      }
+    });
+    __syncthreads();
+    const unsigned int na = sm.x_pref, nbl = sm.list_n;
+    unsigned int a_before, a_total, b_before, b_total, ovf_before, ovf_total;
+    cluster_prefix(cl, sm, na, CL, rank, &a_before, &a_total);
+    cluster_prefix(cl, sm, nbl, CL, rank, &b_before, &b_total);
+    cluster_prefix(cl, sm, (na > kCap || nbl > kCap) ? 1u : 0u, CL, rank, &ovf_before, &ovf_total);
+    if (ovf_total == 0u && b_total <= kCap && b_total >= need_b) {
+      for (unsigned int q = tid; q < na; q += kRowThreads) {
+        const unsigned int at = a_before + q;
+        if (at < static_cast<unsigned int>(k_eff)) {
+          cidx[at] = alist[q].x;
+          cval[at] = __int_as_float(alist[q].y);
+        }
+      }
+      if (rank == 0) {  // the other ranks' boundary lists after this CTA's own
+        unsigned int at = nbl;
+        for (int r = 1; r < CL; ++r) {
+          const unsigned int nr = *cl.map_shared_rank(&sm.list_n, r);
+          const unsigned long long* src = cl.map_shared_rank(blist, r);
+          for (unsigned int q = tid; q < nr; q += kRowThreads) blist[at + q] = src[q];
+          at += nr;
+        }
+      }
+      cl.sync();  // rank 0 has read the other ranks' lists
+      if (rank == 0) {
+        // the top need_b keys of the boundary bin: a count histogram of the
+        // next 11 key bits over the list finds the sub-bin where they end;
+        // every key above it is taken, the sub-bin's keys are sorted
+        unsigned int* cnt = reinterpret_cast<unsigned int*>(sm.hmass);  // 2048 words
+        for (int q = tid; q < kRowBins; q += kRowThreads) cnt[q] = 0u;
+        if (tid == 0) {
+          sm.x_pref = 0u;     // keys taken so far
+          sm.found_pos = -1;  // the boundary sub-bin
+        }
+        __syncthreads();
+        auto sub = [](unsigned long long key) {
+          return static_cast<int>((static_cast<uint32_t>(key >> 32) >> 10) & 0x7FFu);
+        };
+        for (unsigned int q = tid; q < b_total; q += kRowThreads) atomicAdd(&cnt[sub(blist[q])], 1u);
+        __syncthreads();
+        // thread t holds sub-bins 2047 - 8t .. 2040 - 8t (descending); an
+        // exclusive prefix over the block gives the count above each run
+        constexpr int per = kRowBins / kRowThreads;
+        unsigned int run[per], tsum = 0u;
+#pragma unroll
+        for (int i = 0; i < per; ++i) {
+          run[i] = cnt[kRowBins - 1 - (tid * per + i)];
+          tsum += run[i];
+        }
+        unsigned int all_keys;
+        const unsigned int before = block_prefix(sm, tsum, &all_keys);
+        unsigned int acc = before;
+#pragma unroll
+        for (int i = 0; i < per; ++i) {
+          if (acc < need_b && acc + run[i] >= need_b) {
+            sm.found_pos = kRowBins - 1 - (tid * per + i);
+            sm.found_before = acc;
+          }
+          acc += run[i];
+        }
+        __syncthreads();
+        const int sb = sm.found_pos;
+        const unsigned int taken_above = static_cast<unsigned int>(sm.found_before);
+        const unsigned int rest = need_b - taken_above;  // from sub-bin sb
+        // keys above the sub-bin: all taken (order inside does not matter)
+        for (unsigned int q = tid; q < b_total; q += kRowThreads) {
+          const unsigned long long key = blist[q];
+          if (sub(key) > sb) {
+            const unsigned int at = a_total + atomicAdd(&sm.x_pref, 1u);
+            const int32_t id = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+            if (at < static_cast<unsigned int>(k_eff)) {
+              cidx[at] = id;
+              cval[at] = rv.bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(P.base)[off + id])
+                                 : static_cast<const float*>(P.base)[off + id];
+            }
+          }
+        }
+        __syncthreads();
+        // the sub-bin's keys, moved to the front of the list (cnt[sb] of them)
+        // and sorted descending; the first `rest` are taken
+        const unsigned int nsb = cnt[sb];
+        unsigned long long* keys2 = reinterpret_cast<unsigned long long*>(sm.hmass);
+        __syncthreads();  // cnt is read
+        if (tid == 0) sm.list_n = 0u;
+        __syncthreads();
+        for (unsigned int q = tid; q < b_total; q += kRowThreads) {
+          const unsigned long long key = blist[q];
+          if (sub(key) == sb) keys2[atomicAdd(&sm.list_n, 1u)] = key;
+        }
+        unsigned int np = 1u;
+        while (np < nsb) np <<= 1;
+        __syncthreads();
+        for (unsigned int q = nsb + tid; q < np; q += kRowThreads) keys2[q] = 0ull;  // last
+        __syncthreads();
+        for (unsigned int ks = 2; ks <= np; ks <<= 1) {
+          for (unsigned int jj = ks >> 1; jj > 0; jj >>= 1) {
+            for (unsigned int q = tid; q < np; q += kRowThreads) {
+              const unsigned int r2 = q ^ jj;
+              if (r2 > q) {
+                const unsigned long long x0 = keys2[q], x1 = keys2[r2];
+                if (((q & ks) == 0u) ? (x0 < x1) : (x0 > x1)) {
+                  keys2[q] = x1;
+                  keys2[r2] = x0;
+                }
+              }
+            }
+            __syncthreads();
+          }
+        }
+        for (unsigned int q = tid; q < rest; q += kRowThreads) {
+          const unsigned int at = a_total + taken_above + q;
+          if (at < static_cast<unsigned int>(k_eff)) {
+            const int32_t id = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(keys2[q]));
+            cidx[at] = id;
+            cval[at] = rv.bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(P.base)[off + id])
+                               : static_cast<const float*>(P.base)[off + id];
+          }
+        }
+      }
+      return;
+    }
+    // the histograms were overwritten: count pass 1's bins again for the stages
+    hist_clear(sm, kRowBins);
+    __syncthreads();
+    row_sweep(rv, pol, ident, [&](int, float x) {
+      if (x == x) atomicAdd(&sm.hcnt[kd_of(x) >> 21], 1u);
+    });
+    __syncthreads();
+    for (int q = tid; q < kRowBins; q += kRowThreads) sm.hmass[q] = sm.hcnt[q];
+    f = cluster_find(cl, sm, kRowBins, true, 0ull, t_hi, t_lo, CL, rank);
+  }
   unsigned long long above = f.before;
   int kd_len = 11, id_len = 0;
   uint32_t kd_pre = static_cast<uint32_t>(f.bin), id_pre = 0u;
