@@ -2038,6 +2038,47 @@ __device__ void cluster_prefix(cg::cluster_group& cl, RowSmem& sm, unsigned int 
   cl.sync();  // the slots may be rewritten by the next call
 }
 
+// cluster_prefix for three counts at once (one exchange, two cluster barriers).
+__device__ void cluster_prefix3(cg::cluster_group& cl, RowSmem& sm, const unsigned int (&v)[3],
+                                int CL, int rank, unsigned int (&before)[3],
+                                unsigned int (&total)[3]) {
+  if (threadIdx.x == 0) {
+    sm.x_pref = v[0];
+    sm.x_cmin = v[1];
+    sm.x_cmax = v[2];
+  }
+  cl.sync();
+  if (threadIdx.x < 32) {
+    const int r = threadIdx.x;
+    unsigned int x[3] = {0u, 0u, 0u};
+    if (r < CL) {
+      x[0] = *cl.map_shared_rank(&sm.x_pref, r);
+      x[1] = *cl.map_shared_rank(&sm.x_cmin, r);
+      x[2] = *cl.map_shared_rank(&sm.x_cmax, r);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      unsigned int lower = r < rank ? x[j] : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        x[j] += __shfl_xor_sync(0xFFFFFFFFu, x[j], o);
+        lower += __shfl_xor_sync(0xFFFFFFFFu, lower, o);
+      }
+      if (threadIdx.x == 0) {
+        sm.w_u32[2 * j] = lower;
+        sm.w_u32[2 * j + 1] = x[j];
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    before[j] = sm.w_u32[2 * j];
+    total[j] = sm.w_u32[2 * j + 1];
+  }
+  cl.sync();  // the slots may be rewritten by the next call
+}
+
 // Exclusive prefix of a per-thread count over the block, and the block total.
 __device__ unsigned int block_prefix(RowSmem& sm, unsigned int v, unsigned int* total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -2193,10 +2234,10 @@ __device__ void topk_row(const TopkParams& P, int W, int row_id, cg::cluster_gro
     });
     __syncthreads();
     const unsigned int na = sm.x_pref, nbl = sm.list_n;
-    unsigned int a_before, a_total, b_before, b_total, ovf_before, ovf_total;
-    cluster_prefix(cl, sm, na, CL, rank, &a_before, &a_total);
-    cluster_prefix(cl, sm, nbl, CL, rank, &b_before, &b_total);
-    cluster_prefix(cl, sm, (na > kCap || nbl > kCap) ? 1u : 0u, CL, rank, &ovf_before, &ovf_total);
+    const unsigned int counts[3] = {na, nbl, (na > kCap || nbl > kCap) ? 1u : 0u};
+    unsigned int cb[3], ct[3];
+    cluster_prefix3(cl, sm, counts, CL, rank, cb, ct);
+    const unsigned int a_before = cb[0], a_total = ct[0], b_total = ct[1], ovf_total = ct[2];
     if (ovf_total == 0u && b_total <= kCap && b_total >= need_b) {
       for (unsigned int q = tid; q < na; q += kRowThreads) {
         const unsigned int at = a_before + q;
