@@ -92,6 +92,37 @@ def test_topp_row_kinds(kind):
     verify_parity(w, draft, cache, out, nacc, max_exception_frac=0.25)
 
 
+@pytest.mark.parametrize("kind", ["lm", "ties", "ninf", "peaked", "flat", "tiny", "allninf",
+                                  "coarse_ties"])
+def test_topp_bf16_row_kinds(kind):
+    """The top-p row kinds with bf16 target rows at temperature 1, where every
+    value is one of 2^16 and the select counts values exactly: LM-like rows,
+    ties, -inf columns, a spike far above the rest, flat rows, rows of values
+    below 2^-10 in magnitude (with their signed zeros), rows with no finite
+    value, three-valued rows; p from 0.01 to 1 - 1e-7."""
+    rng = np.random.default_rng(zlib.crc32(("bf16-" + kind).encode()))
+    ps = [0.01, 0.3, 0.9, 0.95, 0.9999, 1 - 1e-7, 0.5]
+    B, K, V = len(ps), 2, 20011
+    w = wl.custom(B, K, V, 64, seed=17, top_p=ps, temperature=[1.0] * B)
+
+    def row():
+        if kind == "tiny":
+            x = (rng.standard_normal(V) * 1e-3).astype(np.float32)
+            x[rng.integers(V, size=8)] = 0.0
+            x[rng.integers(V, size=8)] = -0.0
+            return x
+        return _topp_rows(kind, V, rng)
+
+    t32 = np.stack([np.stack([row() for _ in range(K + 1)]) for _ in range(B)])
+    w.target = wl.f32_to_bf16_bits(t32)
+    cache = np.stack([np.stack([_topp_rows("lm", V, rng) for _ in range(K)])
+                      for _ in range(B)]).astype(np.float32)
+    draft = wl.random_drafts(w, seed=4)
+    st, out, nacc = run_verify(w, draft, cache)
+    assert st.status_code() == 0
+    verify_parity(w, draft, cache, out, nacc, max_exception_frac=0.25)
+
+
 @pytest.mark.parametrize("kind", ["coarse_ties", "flat", "lm"])
 def test_topp_long_rows_take_every_select_path(kind):
     """Rows of 65536 values: with three distinct values (coarse_ties) or all

@@ -1237,8 +1237,342 @@ __device__ void topp_sort_find(TopSmem& t, unsigned long long* key, unsigned int
   }
 }
 
+// ---- bf16 rows at temperature 1: the exact top-p from a value histogram -------
+// A bf16 row holds at most 2^16 distinct values. Set apart the few values of
+// magnitude below 2^-10 (listed one by one) and every other value is one bin
+// of a histogram keyed by its order key with the small-magnitude keys removed
+// (the compact key): each bin holds one value, so the fixed-point mass of a
+// bin is its count times that value's mass, exactly. Every value whose mass is
+// not 0 (x > m - 28.5) lies within 4096 compact keys below m, so pass 1 (HBM)
+// takes the maximum and counts the values into 4096 bins below a top set
+// from the anchor; F, the boundary value and the number r of its columns kept
+// follow from the bins; pass 2 (L2) finds the r-th column holding the boundary
+// value, in column order. A row whose maximum is above the bins, whose values
+// below the bins could carry mass, or whose boundary lies among more listed
+// small values than the sort takes is left to the general select.
+constexpr uint32_t kOkNegBig = 0x457Fu;   // order key of -2^-10
+constexpr uint32_t kOkPosBig = 0xBA80u;   // order key of +2^-10
+constexpr uint32_t kTinyKeys = kOkPosBig - kOkNegBig - 1u;
+constexpr uint32_t kCkMax = 0xFF80u - kTinyKeys;  // compact key of +inf
+constexpr int kValBins = 4096;
+
+// order key of bf16 bits (not NaN): larger value, larger key
+__device__ __forceinline__ uint32_t bf16_okey(uint32_t b) {
+  return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+}
+__device__ __forceinline__ uint32_t ckey_of_okey(uint32_t ok) {
+  return ok <= kOkNegBig ? ok : ok - kTinyKeys;
+}
+__device__ __forceinline__ uint32_t bits_of_ckey(uint32_t ck) {
+  const uint32_t ok = ck <= kOkNegBig ? ck : ck + kTinyKeys;
+  return (ok & 0x8000u) ? (ok & 0x7FFFu) : (~ok & 0xFFFFu);
+}
+
+// Returns true when it wrote the row's statistics; false leaves the row to
+// the general select (nothing written).
+__device__ bool topp_bf16_exact(const VerifyParams& P, const FlatRow& R, TopSmem& t) {
+  const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5, K = P.K, V = P.V;
+  const uint16_t* h = static_cast<const uint16_t*>(R.base) + R.off;
+  RowView rv;
+  rv.bf16 = true;
+  rv.f = nullptr;
+  rv.h = h;
+  rv.n = V;
+  unsigned int* cnt = reinterpret_cast<unsigned int*>(t.hmass);  // kValBins words
+  uint2* tiny = P.cand + static_cast<size_t>(blockIdx.x) * kVerifyListCap;
+  const uint64_t pol_keep = policy_evict_last();
+  const uint64_t pol_last = policy_evict_first();
+
+  // ---- the anchor, and the bins' top: 512 compact keys above it ------------------
+  uint32_t top;
+  {
+    const int at = static_cast<int>((static_cast<long long>(tid) * V) / kRowThreads);
+    const uint32_t b = h[at];
+    uint32_t ok = (b & 0x7FFFu) > 0x7F80u ? 0u : bf16_okey(b);
+    ok = __reduce_max_sync(0xFFFFFFFFu, ok);
+    for (int i = tid; i < kValBins; i += kRowThreads) cnt[i] = 0u;
+    if (lane == 0) t.red32[wp] = ok;
+    if (tid == 0) {
+      t.list_n = 0u;
+      t.fast_ok = 0;  // set: a value above the bins
+    }
+    __syncthreads();
+    uint32_t aok = 0u;
+    for (int i = 0; i < kRowWarps; ++i) aok = max(aok, t.red32[i]);
+    const uint32_t ca = aok >= kOkPosBig ? ckey_of_okey(aok) : (aok <= kOkNegBig ? aok : kOkNegBig + 1u);
+    top = min(ca + 512u, kCkMax);
+  }
+  const uint32_t bottom = top >= static_cast<uint32_t>(kValBins - 1) ? top - (kValBins - 1) : 0u;
+
+  // ---- pass 1 (HBM): the maximum, the value counts, the small values -------------
+  uint32_t mok = 0u;  // the largest order key (0: no value but NaN)
+  auto count1 = [&](int j, float z) {
+    const uint32_t b = __float_as_uint(z) >> 16;  // the bf16 bits
+    const uint32_t mag = b & 0x7FFFu;
+    if (mag > 0x7F80u) return;  // NaN
+    const uint32_t ok = bf16_okey(b);
+    mok = max(mok, ok);
+    if (mag < 0x3A80u) {  // |x| < 2^-10: listed
+      const unsigned int at = atomicAdd(&t.list_n, 1u);
+      if (at < static_cast<unsigned int>(kVerifyListCap)) tiny[at] = make_uint2(static_cast<uint32_t>(j), b);
+      return;
+    }
+    const uint32_t ck = ckey_of_okey(ok);
+    if (ck > top) {
+      t.fast_ok = 1;
+    } else if (ck >= bottom) {
+      atomicAdd(&cnt[top - ck], 1u);
+    }
+  };
+  row_quads_t<4, true>(
+      rv, pol_keep, kSliceWindow,
+      [&](int j, const float (&z)[4], bool ok) {
+        if (!ok) return;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) count1(j + e, z[e]);
+      },
+      [&](int j, float z, bool ok) {
+        if (ok) count1(j, z);
+      });
+  mok = __reduce_max_sync(0xFFFFFFFFu, mok);
+  if (lane == 0) t.red32[kRowWarps + wp] = mok;
+  __syncthreads();
+  mok = 0u;
+  for (int i = 0; i < kRowWarps; ++i) mok = max(mok, t.red32[kRowWarps + i]);
+  const unsigned int ntiny = t.list_n;
+  const int32_t d = R.k < K ? P.draft[static_cast<int64_t>(R.b) * K + R.k] : -1;
+  TgtStats* ts = static_cast<TgtStats*>(P.tstats) + static_cast<int64_t>(R.b) * (K + 1) + R.k;
+  if (mok <= 0x007Fu) {  // no value above -inf: p is one-hot at column 0
+    if (tid == 0) {
+      ts->m = -INFINITY;
+      ts->D = 1.0f;
+      ts->kd_thr = 0u;
+      ts->id_thr = 0;
+      ts->p_d = d == 0 ? 1.0f : 0.0f;
+      ts->mode = kModeOneHot;
+      ts->amax_key = 0ull;
+    }
+    return true;
+  }
+  const uint32_t mbits = (mok & 0x8000u) ? (mok & 0x7FFFu) : (~mok & 0xFFFFu);
+  const float m = __uint_as_float(mbits << 16);
+  // left to the general select: a maximum of +inf or of magnitude below 2^-10,
+  // a value above the bins, an overfull list of small values, or values below
+  // the bins that could carry mass
+  if (!(m < INFINITY) || (mbits & 0x7FFFu) < 0x3A80u || t.fast_ok != 0 ||
+      ntiny > static_cast<unsigned int>(kVerifyListCap))
+    return false;
+  if (bottom > 0x007Fu &&
+      fixed_mass(exp_rel(__uint_as_float(bits_of_ckey(bottom - 1u) << 16), m)) != 0ull)
+    return false;
+
+  // ---- F, and the boundary: bins in descending value order, the small values
+  // after the bin of +2^-10 (the last positive one) --------------------------------
+  constexpr int per = kValBins / kRowThreads;
+  const int j0 = tid * per;
+  const int bp = static_cast<int>(top) - static_cast<int>(kOkNegBig + 1u);  // bin of +2^-10
+  unsigned long long tiny_mass = 0ull;
+  for (unsigned int q = tid; q < ntiny; q += kRowThreads) {
+    const uint2 e = __ldcg(tiny + q);
+    tiny_mass += fixed_mass(exp_rel(__uint_as_float(e.y << 16), m));
+  }
+  unsigned long long mine = 0ull;
+#pragma unroll 4
+  for (int q = 0; q < per; ++q) {
+    const unsigned int c = cnt[j0 + q];
+    if (c != 0u) {
+      const float x = __uint_as_float(bits_of_ckey(top - static_cast<uint32_t>(j0 + q)) << 16);
+      mine += static_cast<unsigned long long>(c) * fixed_mass(exp_rel(x, m));
+    }
+  }
+  unsigned long long T = tiny_mass;
+  block_sum64x2(t, mine, T);  // every thread: the bins' total (mine) and the small values'
+  // (bp past the last bin: the small values lie below the bins, and the
+  // check above made their mass 0; bp below 0: m < 0 and there are none)
+  const bool tiny_in = bp >= 0 && bp < kValBins;
+  const unsigned long long Fb = mine;
+  const unsigned long long F = Fb + (tiny_in ? T : 0ull);
+  const unsigned long long P32 = topp_scaled(P.top_p[P.rsi[R.b]]);
+  const unsigned long long t_lo = P32 * F, t_hi = __umul64hi(P32, F);
+  // this thread's run of bins (the small values' mass with the run holding bp)
+  unsigned long long tsum = 0ull;
+  for (int q = 0; q < per; ++q) {
+    const unsigned int c = cnt[j0 + q];
+    if (c != 0u) {
+      const float x = __uint_as_float(bits_of_ckey(top - static_cast<uint32_t>(j0 + q)) << 16);
+      tsum += static_cast<unsigned long long>(c) * fixed_mass(exp_rel(x, m));
+    }
+    if (tiny_in && j0 + q == bp) tsum += T;
+  }
+  unsigned long long incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long nv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += nv;
+  }
+  if (lane == 31) t.red64[wp] = incl;
+  if (tid == 0) t.found_pos = -1;
+  __syncthreads();
+  unsigned long long run = incl - tsum;
+  for (int i = 0; i < wp; ++i) run += t.red64[i];
+  for (int q = 0; q < per; ++q) {
+    const int b = j0 + q;
+    const unsigned int c = cnt[b];
+    if (c != 0u) {
+      const float x = __uint_as_float(bits_of_ckey(top - static_cast<uint32_t>(b)) << 16);
+      const unsigned long long mb = static_cast<unsigned long long>(c) * fixed_mass(exp_rel(x, m));
+      if (mb > 0ull && !reaches(run, t_hi, t_lo) && reaches(run + mb, t_hi, t_lo)) {
+        t.found_pos = b;
+        t.f_before = run;
+      }
+      run += mb;
+    }
+    if (tiny_in && b == bp) {
+      if (T > 0ull && !reaches(run, t_hi, t_lo) && reaches(run + T, t_hi, t_lo)) {
+        t.found_pos = kValBins;  // among the small values
+        t.f_before = run;
+      }
+      run += T;
+    }
+  }
+  __syncthreads();
+  const int fb = t.found_pos;
+  const unsigned long long before = t.f_before;
+  __syncthreads();
+  if (fb < 0) return false;  // cannot happen: the target is at most F
+  uint32_t id_thr, vbits;
+  unsigned long long kept;
+  if (fb == kValBins) {
+    // ---- the boundary among the small values: sort them (value desc, id asc) -----
+    if (ntiny > static_cast<unsigned int>(kTopSort)) return false;
+    unsigned long long* key = reinterpret_cast<unsigned long long*>(t.hmass);
+    for (unsigned int q = tid; q < ntiny; q += kRowThreads) {
+      const uint2 e = __ldcg(tiny + q);
+      key[q] = (static_cast<unsigned long long>(kd_of(__uint_as_float(e.y << 16))) << 32) |
+               static_cast<unsigned long long>(0xFFFFFFFFu - e.x);
+    }
+    unsigned int np = kRowThreads;
+    while (np < ntiny) np <<= 1;
+    if (tid == 0) {
+      t.f_id = 0u;
+      t.f_mass = 0ull;
+      t.f_before = before;
+    }
+    __syncthreads();
+    if (np == kRowThreads) topp_sort_find<1>(t, key, ntiny, m, before, t_hi, t_lo);
+    else if (np == 2 * kRowThreads) topp_sort_find<2>(t, key, ntiny, m, before, t_hi, t_lo);
+    else topp_sort_find<4>(t, key, ntiny, m, before, t_hi, t_lo);
+    __syncthreads();
+    id_thr = t.f_id;
+    kept = t.f_before + t.f_mass;
+    vbits = h[id_thr];
+  } else {
+    // ---- the boundary value: r of its columns are kept, the first r in column
+    // order; pass 2 (L2) counts its columns per run of 2^sh columns ------------------
+    vbits = bits_of_ckey(top - static_cast<uint32_t>(fb));
+    const unsigned long long fv = fixed_mass(exp_rel(__uint_as_float(vbits << 16), m));
+    const unsigned int c = cnt[fb];
+    // r: the fewest columns with before + r fv reaching the target (1 <= r <= c)
+    unsigned int lo_r = 1u, hi_r = c;
+    while (lo_r < hi_r) {
+      const unsigned int mid = (lo_r + hi_r) >> 1;
+      if (reaches(before + static_cast<unsigned long long>(mid) * fv, t_hi, t_lo)) hi_r = mid;
+      else lo_r = mid + 1u;
+    }
+    const unsigned int r = lo_r;
+    kept = before + static_cast<unsigned long long>(r) * fv;
+    int sh = 7;
+    while ((static_cast<long long>(V) >> sh) >= kRowBins) ++sh;
+    unsigned int* runs = t.hcnt;  // kRowBins words
+    __syncthreads();              // cnt (in hmass) is read; runs are cleared next
+    for (int i = tid; i < kRowBins; i += kRowThreads) runs[i] = 0u;
+    __syncthreads();
+    row_quads_t<4, true>(
+        rv, pol_last, kSliceWindow,
+        [&](int j, const float (&z)[4], bool ok) {
+          if (!ok) return;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if ((__float_as_uint(z[e]) >> 16) == vbits) atomicAdd(&runs[(j + e) >> sh], 1u);
+        },
+        [&](int j, float z, bool ok) {
+          if (ok && (__float_as_uint(z) >> 16) == vbits) atomicAdd(&runs[j >> sh], 1u);
+        });
+    __syncthreads();
+    // the run holding the r-th column: a prefix over the runs (8 per thread)
+    constexpr int rper = kRowBins / kRowThreads;
+    unsigned int rs = 0u;
+    for (int q = 0; q < rper; ++q) rs += runs[tid * rper + q];
+    unsigned int rin = rs;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned int nv = __shfl_up_sync(0xFFFFFFFFu, rin, o);
+      if (lane >= o) rin += nv;
+    }
+    if (lane == 31) t.red32[wp] = rin;
+    if (tid == 0) t.found_pos = -1;
+    __syncthreads();
+    unsigned int racc = rin - rs;
+    for (int i = 0; i < wp; ++i) racc += t.red32[i];
+    for (int q = 0; q < rper; ++q) {
+      const unsigned int cq = runs[tid * rper + q];
+      if (racc < r && racc + cq >= r) {
+        t.found_pos = tid * rper + q;
+        t.f_cnt = r - racc;  // the r-th overall is this run's (r - racc)-th
+      }
+      racc += cq;
+    }
+    __syncthreads();
+    const int run_id = t.found_pos;
+    const unsigned int nth = t.f_cnt;
+    if (run_id < 0) return false;  // cannot happen: the value has c >= r columns
+    // warp 0 walks the run's columns in order
+    if (wp == 0) {
+      const int c0 = run_id << sh, c1 = min(V, (run_id + 1) << sh);
+      unsigned int seen = 0u;
+      int found = -1;
+      for (int b0 = c0; b0 < c1 && found < 0; b0 += 32) {
+        const int j = b0 + lane;
+        const bool hit = j < c1 && static_cast<uint32_t>(h[j]) == vbits;
+        const unsigned int bal = __ballot_sync(0xFFFFFFFFu, hit);
+        const unsigned int k = nth - seen;  // 1-based within this chunk
+        if (static_cast<unsigned int>(__popc(bal)) >= k) {
+          // the k-th set bit of bal
+          unsigned int bb = bal;
+          for (unsigned int i = 1u; i < k; ++i) bb &= bb - 1u;
+          found = b0 + __ffs(bb) - 1;
+        }
+        seen += static_cast<unsigned int>(__popc(bal));
+      }
+      if (lane == 0) t.f_id = static_cast<uint32_t>(found < 0 ? 0 : found);
+    }
+    __syncthreads();
+    id_thr = t.f_id;
+  }
+  if (tid == 0) {
+    const float D = __fmul_rn(__ull2float_rn(kept), 0x1p-40f);
+    const uint32_t kd_thr = kd_of(__uint_as_float(vbits << 16));
+    const bool has_d = d >= 0 && d < V;
+    const float x = has_d ? fmaxf(__uint_as_float(static_cast<uint32_t>(h[d]) << 16), -INFINITY) : 0.0f;
+    const uint32_t kd = kd_of(x);
+    const bool keep = kd > kd_thr || (kd == kd_thr && d <= static_cast<int32_t>(id_thr));
+    ts->p_d = has_d && keep ? __fdiv_rn(exp_rel(x, m), D) : 0.0f;
+    ts->m = m;
+    ts->D = D;
+    ts->kd_thr = kd_thr;
+    ts->id_thr = static_cast<int32_t>(id_thr);
+    ts->mode = kModeThreshold;
+    ts->amax_key = 0ull;
+  }
+  return true;
+}
+
 template <bool kBf16, bool kScale>
 __device__ void flat_topp_row_t(const VerifyParams& P, const FlatRow& R, TopSmem& t) {
+  if constexpr (kBf16 && !kScale) {
+    if (topp_bf16_exact(P, R, t)) return;
+    __syncthreads();  // the general select reuses the shared memory
+  }
   const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5, K = P.K, V = P.V;
   const TempFix<kScale> fx(R.T);
   auto fix = [&](float c) { return fx.one(c); };
