@@ -296,12 +296,6 @@ dspark_status dspark_rejection_sample(
   const VerifyWs ws(B, K, V);
   if (!workspace || workspace_bytes < ws.total || !aligned16(workspace))
     return DSPARK_ERR_WORKSPACE;
-  int cluster = 0, slice = 0;
-  // fp32 unless both the target and the (present) cache are bf16
-  const bool all_bf16 =
-      target_dtype == DSPARK_BF16 && (!draft_cache || cache_dtype == DSPARK_BF16);
-  const int es = all_bf16 ? 2 : 4;
-  if (!dspark::verify_rows_plan(V, es, &cluster, &slice)) return DSPARK_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   unsigned char* w = static_cast<unsigned char*>(workspace);
   dspark::VerifyParams p;
