@@ -98,10 +98,8 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const DrawJob& J,
   // keeps the lowest column on ties
   uint32_t run_o = 0u, run_c = 0u;
   unsigned int any = 0u;
-  for (int g = c0 + 4 * static_cast<int>(threadIdx.x); g < c1; g += 4 * nthr) {
-    float t4[4], c4[4];
-    draw_load4(P.target, tbf, toff, g, c1, tvec, t4);
-    if (kResidual) draw_load4(P.cache, cbf, coff, g, c1, cvec, c4);
+  // one 4-column group: weights, and the noise only if a weight is positive
+  auto group = [&](int g, const float (&t4)[4], const float (&c4)[4]) {
     // p = exp(x - m) / D (and q likewise) two columns at a time in packed
     // pairs: the same fp32 operations as exp_rel and the scalar products
     float x4[4], p4[4], q4[4];
@@ -135,7 +133,7 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const DrawJob& J,
       w[j] = g + j < c1 ? pv : 0.0f;
       need |= w[j] > 0.0f;
     }
-    if (!need) continue;
+    if (!need) return;
     any = 1u;
     const U4 r = noise_block(J.seed, npos, static_cast<uint32_t>(g), kStreamTarget);
     float E[4];
@@ -150,6 +148,21 @@ __device__ unsigned long long draw_fast(const VerifyParams& P, const DrawJob& J,
         run_c = static_cast<uint32_t>(g + j);
       }
     }
+  };
+  // two groups per iteration, both loaded before either is used (a group at
+  // or past c1 loads nothing and weighs 0); the thread's columns still come
+  // in increasing order
+  for (int g = c0 + 4 * static_cast<int>(threadIdx.x); g < c1; g += 8 * nthr) {
+    const int g2 = g + 4 * nthr;
+    float t4[4], c4[4] = {0.f, 0.f, 0.f, 0.f}, t4b[4], c4b[4] = {0.f, 0.f, 0.f, 0.f};
+    draw_load4(P.target, tbf, toff, g, c1, tvec, t4);
+    draw_load4(P.target, tbf, toff, g2, c1, tvec, t4b);
+    if (kResidual) {
+      draw_load4(P.cache, cbf, coff, g, c1, cvec, c4);
+      draw_load4(P.cache, cbf, coff, g2, c1, cvec, c4b);
+    }
+    group(g, t4, c4);
+    if (g2 < c1) group(g2, t4b, c4b);
   }
   *anypos = any;
   return run_o == 0u ? 0ull

@@ -568,12 +568,15 @@ __device__ __forceinline__ unsigned long long slice_online(const RowView& rv, ui
 // one item, done whole by one CTA (flat_topp_row). The CTA that finishes a
 // request's last row replays the request's accept chain (one thread per
 // draft), writes the request's draw job and publishes `ndraw` draw items:
-// column chunks of the one categorical the request needs. CTAs take
-// published draw items before new rows, so a draw runs soon after its rows,
-// beside other requests' rows; the CTA that finishes a request's last chunk
-// writes the outputs. Each CTA claims its next row at the start of the
-// current item, so the claim's latency hides behind the item's work. Every
-// wait is bounded.
+// column chunks of the one categorical the request needs. A CTA that finds
+// the row queue empty takes draw items in publish order (two waves of chunks
+// over the CTAs, so that the last requests' draws spread over many CTAs),
+// waiting for a request still finishing its rows; the CTA that finishes a
+// request's last chunk writes the outputs. (Taking published draws between
+// row items was measured slower: requests publish at about the items'
+// boundaries, so the draws ran late and delayed the rows claimed before
+// them.) Each CTA claims its next row at the start of the current item, so
+// the claim's latency hides behind the item's work. Every wait is bounded.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* p) {
   uint32_t v;
@@ -2862,9 +2865,9 @@ cudaError_t launch_verify(const VerifyParams& p0, cudaStream_t stream) {
     per_sm = 1;
   }
   const int ctas = sms * per_sm;
-  // draw chunks per request: about one wave of CTAs over the batch, none
+  // draw chunks per request: about two waves of CTAs over the batch, none
   // shorter than 1024 columns
-  int nd = (ctas + p.B - 1) / p.B;
+  int nd = (2 * ctas + p.B - 1) / p.B;
   if (nd > p.kstride) nd = p.kstride;
   if (nd < 1) nd = 1;
   p.ndraw = nd;
