@@ -569,8 +569,8 @@ __device__ __forceinline__ unsigned long long slice_online(const RowView& rv, ui
 // request's last row replays the request's accept chain (one thread per
 // draft), writes the request's draw job and publishes `ndraw` draw items:
 // column chunks of the one categorical the request needs. A CTA that finds
-// the row queue empty takes draw items in publish order (two waves of chunks
-// over the CTAs, so that the last requests' draws spread over many CTAs),
+// the row queue empty takes draw items in publish order (four waves of
+// chunks over the CTAs, so that the last requests' draws spread over many CTAs),
 // waiting for a request still finishing its rows; the CTA that finishes a
 // request's last chunk writes the outputs. (Taking published draws between
 // row items was measured slower: requests publish at about the items'
@@ -2865,9 +2865,10 @@ cudaError_t launch_verify(const VerifyParams& p0, cudaStream_t stream) {
     per_sm = 1;
   }
   const int ctas = sms * per_sm;
-  // draw chunks per request: about two waves of CTAs over the batch, none
-  // shorter than 1024 columns
-  int nd = (2 * ctas + p.B - 1) / p.B;
+  // draw chunks per request: about four waves of CTAs over the batch (the
+  // last requests' draws then spread over many CTAs), none shorter than 1024
+  // columns
+  int nd = (4 * ctas + p.B - 1) / p.B;
   if (nd > p.kstride) nd = p.kstride;
   if (nd < 1) nd = 1;
   p.ndraw = nd;
